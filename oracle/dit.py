@@ -1,0 +1,340 @@
+"""Plain float64 NumPy definitions of the DiT block forward and the denoise loop (test oracle).
+
+Sources, cited by page title and section:
+
+* [host contract]  "Host contract - RGBA-Image-2.1-Turbo (Core AI port of Qwen-Image-2.1-Turbo)":
+  section 1 (graph I/O, int8lin weights), section 4 (sequence layout and RoPE tables), section 5
+  (latent packing), section 6 (FlowMatch Euler sampler).
+* [gizai:dit]  the "gizai:dit" module reference: ``Block.forward``, ``normedInto``, ``Modulation``,
+  ``Sequence``, ``prepOf``, ``gatedInto``, ``gluRows``, ``weightAt``, ``sinusoids``.
+* [klein]  "944 -> 346 ms: optimizing FLUX.2 klein-4B on one TPU v6e chip": section 2 (cast
+  points), section 4.3 (attention: softmax with 1/sqrt(d) applied in fp32), section 4.4 (qk prep:
+  QK-RMSNorm as mean of squares + eps -> rsqrt).
+
+Readings where the pages are silent (each is listed with its basis in the design notes):
+modulation uses (1 + scale); RMSNorm is x * (mean(x^2) + eps)^-1/2 with eps = 1e-6; RoPE rotates
+adjacent pairs (2i, 2i+1) of the whole head; d = 64 heads use axis widths (8, 28, 28); the block is
+sequential (attention residual lands before the second norm); the final norm of the denoise loop is
+a modulated RMSNorm without an affine weight; no linear has a bias.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "bf16_to_f64", "bf16_rne_bits", "positions", "axis_widths", "rope_tables", "rope_axis_table",
+    "modulated_rmsnorm", "qk_rmsnorm", "rope_apply", "attention", "silu", "swiglu_interleaved",
+    "block_forward", "block_forward_rows", "dequant_int8", "euler_step", "shift_sigmas",
+    "timestep_sinusoids", "time_embedding", "denoise", "pack_latents", "block_weights_f64",
+]
+
+
+# ----------------------------------------------------------------------------------------------
+# number formats
+# ----------------------------------------------------------------------------------------------
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bfloat16 bit patterns (uint16) as float64."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def bf16_rne_bits(x32: np.ndarray) -> np.ndarray:
+    """Round float32 values to nearest bfloat16, ties to even, as uint16 bit patterns (finite inputs)."""
+    u = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep = u >> np.uint64(16)
+    rest = u & np.uint64(0xFFFF)
+    up = (rest > 0x8000) | ((rest == 0x8000) & ((keep & np.uint64(1)) == 1))
+    return (keep + up.astype(np.uint64)).astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------------------------
+# sequence layout and rotary tables  [host contract, section 4]
+# ----------------------------------------------------------------------------------------------
+
+def positions(L: int, h: int, w: int) -> np.ndarray:
+    """3-axis (frame, height, width) positions of the packed [text L | image h*w] sequence.
+
+    Text token i sits at (i, i, i); the image token at row y, column x (index y*w + x) sits at
+    (L, y - (h - h//2), x - (w - w//2)), a grid centred on zero.  [host contract, section 4]"""
+    pos = np.zeros((L + h * w, 3), dtype=np.int64)
+    for i in range(L):
+        pos[i] = (i, i, i)
+    for y in range(h):
+        for x in range(w):
+            pos[L + y * w + x] = (L, y - (h - h // 2), x - (w - w // 2))
+    return pos
+
+
+def axis_widths(head_dim: int) -> tuple:
+    """Rotary widths of the three axes. The contract gives (16, 56, 56) for a 128-wide head
+    [host contract, section 4]; other head sizes scale them by head_dim / 128 (our reading)."""
+    if head_dim == 128:
+        return (16, 56, 56)
+    if (16 * head_dim) % 256 or (56 * head_dim) % 256:
+        raise ValueError("head_dim must scale the (16, 56, 56) widths to even integers")
+    return (16 * head_dim // 128, 56 * head_dim // 128, 56 * head_dim // 128)
+
+
+def _axis_frequencies(width: int, theta: float) -> np.ndarray:
+    # 1 / theta^(arange(0, width, 2) / width)   [host contract, section 4]
+    k = np.arange(0, width, 2, dtype=np.float64)
+    return 1.0 / np.power(float(theta), k / width)
+
+
+def rope_axis_table(width: int, theta: float = 10000.0, first: int = -1024, last: int = 8191):
+    """One axis table as the contract stores it: row p - first holds cos/sin of p * f_k for
+    positions first..last, [rows, width/2], float32.  [host contract, section 4]"""
+    p = np.arange(first, last + 1, dtype=np.float64)
+    ang = np.outer(p, _axis_frequencies(width, theta))
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def rope_tables(pos: np.ndarray, head_dim: int, theta: float = 10000.0):
+    """Per-row cos/sin [R, head_dim/2] float32: the three axes' angle columns concatenated in axis
+    order, angle = position * frequency evaluated in float64 and rounded once to float32.
+    [host contract, section 4]"""
+    cols_c, cols_s = [], []
+    for a, width in enumerate(axis_widths(head_dim)):
+        ang = np.outer(pos[:, a].astype(np.float64), _axis_frequencies(width, theta))
+        cols_c.append(np.cos(ang))
+        cols_s.append(np.sin(ang))
+    return (np.concatenate(cols_c, axis=1).astype(np.float32),
+            np.concatenate(cols_s, axis=1).astype(np.float32))
+
+
+# ----------------------------------------------------------------------------------------------
+# block pieces
+# ----------------------------------------------------------------------------------------------
+
+def modulated_rmsnorm(x, w, shift, scale, eps):
+    """y = x * (mean(x^2) + eps)^-1/2 * w * (1 + scale) + shift, row by row.
+    [gizai:dit, normedInto and Modulation; klein, section 4.4 for mean of squares + eps]"""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    y = x / np.sqrt(ms + eps)
+    if w is not None:
+        y = y * np.asarray(w, dtype=np.float64)
+    return y * (1.0 + np.asarray(scale, dtype=np.float64)) + np.asarray(shift, dtype=np.float64)
+
+
+def qk_rmsnorm(t, w, eps):
+    """Each head vector over its own RMS times the head-norm weight: t [R, heads, d].
+    [gizai:dit, prepOf; klein, section 4.4]"""
+    ms = np.mean(t * t, axis=-1, keepdims=True)
+    y = t / np.sqrt(ms + eps)
+    if w is not None:
+        y = y * np.asarray(w, dtype=np.float64)
+    return y
+
+
+def rope_apply(t, cos, sin):
+    """Rotate the adjacent pairs (2i, 2i+1) of each head by the row's angle i:
+    (a, b) -> (a cos - b sin, a sin + b cos).  t [R, heads, d], cos/sin [R, d/2].
+    [host contract, section 4 (complex pairs, torch.polar); klein, section D3 (-sin even, +sin odd)]"""
+    c = np.asarray(cos, dtype=np.float64)[:, None, :]
+    s = np.asarray(sin, dtype=np.float64)[:, None, :]
+    a = t[..., 0::2]
+    b = t[..., 1::2]
+    out = np.empty_like(t)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def attention(q, k, v, rows: Optional[np.ndarray] = None):
+    """Unmasked softmax attention of every query row over every key row, per head, with scale
+    1/sqrt(d):  o = softmax(q k^T / sqrt(d)) v  (max-subtracted).  q/k/v [R, heads, d].
+    ``rows`` restricts the query rows. Returns [len(rows), heads * d] with column head*d + j.
+    [host contract, section 4 (joint text|image sequence); klein, section 4.3]"""
+    R, nh, d = k.shape
+    qs = q if rows is None else q[rows]
+    out = np.empty((qs.shape[0], nh, d), dtype=np.float64)
+    for n in range(nh):
+        S = (qs[:, n, :] @ k[:, n, :].T) / math.sqrt(d)
+        S = S - S.max(axis=1, keepdims=True)
+        P = np.exp(S)
+        P = P / P.sum(axis=1, keepdims=True)
+        out[:, n, :] = P @ v[:, n, :]
+    return out.reshape(qs.shape[0], nh * d)
+
+
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_interleaved(u):
+    """SwiGLU over interleaved rows: a_j = silu(u_{2j}) * u_{2j+1}.  [gizai:dit, gluRows and Block]"""
+    return silu(u[..., 0::2]) * u[..., 1::2]
+
+
+def block_weights_f64(inp):
+    """The four linears of a bf16 block as float64 matrices [out, in]."""
+    return (bf16_to_f64(inp.wqkv), bf16_to_f64(inp.wout), bf16_to_f64(inp.wup), bf16_to_f64(inp.wdown))
+
+
+def _mod_rows(mod, mod_map, rows):
+    m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)[rows]]
+    return [m[:, i, :] for i in range(6)]
+
+
+def block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
+                       rows: Optional[np.ndarray] = None, norm1=None, norm2=None,
+                       q_norm=None, k_norm=None, eps=1e-6, qk_eps=1e-6):
+    """One AdaLN block over the packed rows x [R, H] (float64 copy returned; x untouched).
+
+    1. h  = modnorm(x; norm1, shift_a, scale_a)
+    2. [q|k|v] = h Wqkv^T (columns all-Q, all-K, all-V, head-major inside each)
+    3. q, k  <- per-head RMS norm times q_norm / k_norm
+    4. rotate q, k pairs by the per-row cos/sin tables
+    5. o = softmax(q k^T / sqrt(d)) v over all rows
+    6. x += gate_a * (o Wout^T)
+    7. h2 = modnorm(x; norm2, shift_m, scale_m)
+    8. a_j = silu(u_{2j}) u_{2j+1}, u = h2 Wup^T
+    9. x += gate_m * (a Wdown^T)
+
+    Steps 1-4 run for every row (keys and values need them); steps 5-9 only for ``rows`` (all by
+    default), which lets tests check sampled rows of large sequences.
+    [gizai:dit, Block.forward, normedInto, weightAt (QKV row order), prepOf, gatedInto, gluRows]"""
+    x = np.asarray(x, dtype=np.float64)
+    R, H = x.shape
+    nh, d = heads, head_dim
+    Wqkv, Wout, Wup, Wdown = weights
+    all_rows = np.arange(R)
+    rows = all_rows if rows is None else np.asarray(rows)
+    sa, ca, ga, _, _, _ = _mod_rows(mod, mod_map, all_rows)
+    h = modulated_rmsnorm(x, norm1, sa, ca, eps)
+    qkv = h @ Wqkv.T
+    q = qkv[:, 0:H].reshape(R, nh, d)
+    k = qkv[:, H:2 * H].reshape(R, nh, d)
+    v = qkv[:, 2 * H:3 * H].reshape(R, nh, d)
+    q = rope_apply(qk_rmsnorm(q, q_norm, qk_eps), cos, sin)
+    k = rope_apply(qk_rmsnorm(k, k_norm, qk_eps), cos, sin)
+    o = attention(q, k, v, rows)
+    _, _, ga_r, sm_r, cm_r, gm_r = _mod_rows(mod, mod_map, rows)
+    xr = x[rows] + ga_r * (o @ Wout.T)
+    h2 = modulated_rmsnorm(xr, norm2, sm_r, cm_r, eps)
+    a = swiglu_interleaved(h2 @ Wup.T)
+    return xr + gm_r * (a @ Wdown.T)
+
+
+def block_forward(inp, weights=None, rows=None):
+    """Block forward on a ``dit_inputs.BlockInputs``: returns (txt_out, img_out) float64 for all rows,
+    or the packed output rows ``rows`` when given. Uses the bf16 weights, or ``weights`` if given."""
+    sh = inp.shape
+    x = np.concatenate([inp.txt, inp.img], axis=0).astype(np.float64)
+    cos, sin = rope_tables(positions(sh.L, sh.grid_h, sh.grid_w), sh.head_dim)
+    W = block_weights_f64(inp) if weights is None else weights
+    y = block_forward_rows(x, W, inp.mod, inp.mod_map, cos, sin, sh.heads, sh.head_dim, rows=rows,
+                           norm1=inp.norm1, norm2=inp.norm2, q_norm=inp.q_norm, k_norm=inp.k_norm,
+                           eps=sh.eps, qk_eps=sh.qk_eps)
+    if rows is not None:
+        return y
+    return y[:sh.L], y[sh.L:]
+
+
+# ----------------------------------------------------------------------------------------------
+# int8lin weights  [host contract, section 1]
+# ----------------------------------------------------------------------------------------------
+
+def dequant_int8(q: np.ndarray, s_bits: np.ndarray) -> np.ndarray:
+    """W[o, i] = bf16_rne(q[o, i] * s[o, i // 32]) as bf16 bit patterns.
+
+    The int8 value times the bf16 scale has at most 16 significant bits, so the product is exact in
+    float64 (and float32) before the one rounding to bfloat16.  [host contract, section 1]"""
+    o, k = q.shape
+    if k % 32:
+        raise ValueError("input dimension must be a multiple of 32")
+    s = bf16_to_f64(s_bits)
+    prod = q.astype(np.float64) * np.repeat(s, 32, axis=1)
+    return bf16_rne_bits(prod.astype(np.float32))  # exact conversion, then one RNE rounding
+
+
+# ----------------------------------------------------------------------------------------------
+# sampler and denoise loop  [host contract, sections 5 and 6; gizai:dit, sinusoids]
+# ----------------------------------------------------------------------------------------------
+
+def euler_step(x: np.ndarray, vel: np.ndarray, sigma: float, sigma_next: float) -> np.ndarray:
+    """x + (sigma_next - sigma) * vel, every operation in float32.  [host contract, section 6]"""
+    x = np.asarray(x, dtype=np.float32)
+    vel = np.asarray(vel, dtype=np.float32)
+    dt = np.float32(sigma_next) - np.float32(sigma)
+    return (x + (dt * vel).astype(np.float32)).astype(np.float32)
+
+
+def shift_sigmas(sigmas, shift: float) -> np.ndarray:
+    """shift * s / (1 + (shift - 1) * s) in float32.  [host contract, section 6]"""
+    s = np.asarray(sigmas, dtype=np.float32)
+    sh = np.float32(shift)
+    return (sh * s / (np.float32(1) + (sh - np.float32(1)) * s)).astype(np.float32)
+
+
+def pack_latents(z: np.ndarray) -> np.ndarray:
+    """Channel-major latent z [C, h, w] to tokens x [h*w, C] with x[y*w + x, c] = z[c, y, x].
+    [host contract, section 5]"""
+    C, h, w = z.shape
+    out = np.empty((h * w, C), dtype=z.dtype)
+    for y in range(h):
+        for xx in range(w):
+            out[y * w + xx, :] = z[:, y, xx]
+    return out
+
+
+def timestep_sinusoids(t: Sequence[float], dim: int = 256) -> np.ndarray:
+    """Rows [cos | sin] of 1000 * t times the dim/2 frequencies 10000^(-i / (dim/2)).
+    [gizai:dit, sinusoids; klein, section 2 (the model sees 1000 t)]"""
+    half = dim // 2
+    f = np.power(10000.0, -np.arange(half, dtype=np.float64) / half)
+    ang = np.outer(1000.0 * np.asarray(t, dtype=np.float64), f)
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)
+
+
+def time_embedding(t, w_t1, w_t2):
+    """temb = W2 silu(W1 sinusoids(t)) (no biases, our reading)."""
+    e = timestep_sinusoids(t, dim=bf16_to_f64(w_t1).shape[1])
+    return silu(e @ bf16_to_f64(w_t1).T) @ bf16_to_f64(w_t2).T
+
+
+def denoise(inp, steps: Optional[int] = None, blocks: Optional[int] = None, trace: Optional[list] = None):
+    """The full loop of the host contract's section 6 with a plain DiT around the blocks:
+
+    for each step i with t = sigma_i:
+        X     = x W_in^T                                  (patch in, image rows)
+        temb  = W2 silu(W1 sinusoids(t))                  (time embedding)
+        rows  = [txt_feats ; X], then every block with its modulation W_ada,b silu(temb), M = 1
+        vel   = modnorm(image rows; shift_f, scale_f) W_proj^T,  [shift_f, scale_f] = W_ada,f silu(temb)
+        x     = x + (sigma_{i+1} - sigma_i) vel            (float32)
+
+    Returns x (float32 [N, C]). ``trace`` collects each step's vel when given."""
+    sh = inp.shape
+    H, L, N = sh.hidden, sh.L, sh.N
+    nsteps = len(inp.steps_sigmas) - 1 if steps is None else steps
+    nblocks = inp.blocks if blocks is None else blocks
+    cos, sin = rope_tables(positions(L, sh.grid_h, sh.grid_w), sh.head_dim)
+    W_in = bf16_to_f64(inp.w_in)
+    W_ada_f = bf16_to_f64(inp.w_ada_f)
+    W_proj = bf16_to_f64(inp.w_out)
+    mod_map = np.zeros(L + N, dtype=np.int32)
+    x = np.asarray(inp.latents, dtype=np.float32).copy()
+    sig = inp.steps_sigmas
+    for i in range(nsteps):
+        t = float(sig[i])
+        temb = time_embedding([t], inp.w_t1, inp.w_t2)[0]
+        st = silu(temb)
+        rows = np.concatenate([inp.txt_feats.astype(np.float64), x.astype(np.float64) @ W_in.T], axis=0)
+        for b in range(nblocks):
+            mod = (bf16_to_f64(inp.w_ada[b]) @ st).reshape(1, 6, H)
+            bw = inp.block_w[b]
+            rows = block_forward_rows(rows, block_weights_f64(bw), mod, mod_map, cos, sin,
+                                      sh.heads, sh.head_dim, eps=sh.eps, qk_eps=sh.qk_eps)
+        fin = W_ada_f @ st
+        shift_f, scale_f = fin[:H], fin[H:]
+        vel = modulated_rmsnorm(rows[L:], None, shift_f, scale_f, sh.eps) @ W_proj.T
+        if trace is not None:
+            trace.append(vel.copy())
+        x = euler_step(x, vel.astype(np.float32), sig[i], sig[i + 1])
+    return x

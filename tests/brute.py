@@ -1,0 +1,78 @@
+"""Scalar brute-force restatement of the block forward, for pinning the oracle on tiny inputs.
+
+Pure Python loops over lists of floats (math.exp, math.sqrt): no NumPy, no shared helpers with
+``oracle/``. It takes the separate Q, K and V projection matrices and the un-interleaved gate/up
+matrices, so the oracle's fused-weight row orders (all-Q, all-K, all-V; gate j at row 2j, up j at
+row 2j + 1) are checked by construction.
+"""
+
+import math
+
+
+def matvec(W, x):
+    return [sum(W[o][i] * x[i] for i in range(len(x))) for o in range(len(W))]
+
+
+def rmsnorm_row(x, eps):
+    ms = sum(v * v for v in x) / len(x)
+    r = 1.0 / math.sqrt(ms + eps)
+    return [v * r for v in x]
+
+
+def block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
+          norm1=None, norm2=None, qn=None, kn=None):
+    """x: list of R rows (lists of H floats). mod_rows[r] = 6 lists of H (shift_a, scale_a, gate_a,
+    shift_m, scale_m, gate_m) for row r. cos/sin: R lists of d/2. Returns new rows."""
+    R, H = len(x), len(x[0])
+    one = lambda n: [1.0] * n
+    n1 = norm1 or one(H)
+    n2 = norm2 or one(H)
+    qn = qn or one(d)
+    kn = kn or one(d)
+
+    def modnorm(row, w, shift, scale):
+        y = rmsnorm_row(row, eps)
+        return [y[i] * w[i] * (1.0 + scale[i]) + shift[i] for i in range(H)]
+
+    Q, K, V = [], [], []
+    for r in range(R):
+        sa, ca = mod_rows[r][0], mod_rows[r][1]
+        h = modnorm(x[r], n1, sa, ca)
+        q, k, v = matvec(Wq, h), matvec(Wk, h), matvec(Wv, h)
+        qh, kh, vh = [], [], []
+        for n in range(heads):
+            for (src, w, dst) in ((q, qn, qh), (k, kn, kh)):
+                seg = rmsnorm_row(src[n * d:(n + 1) * d], qk_eps)
+                seg = [seg[j] * w[j] for j in range(d)]
+                rot = [0.0] * d
+                for i in range(d // 2):
+                    a, b = seg[2 * i], seg[2 * i + 1]
+                    c, s = cos[r][i], sin[r][i]
+                    rot[2 * i] = a * c - b * s
+                    rot[2 * i + 1] = a * s + b * c
+                dst.append(rot)
+            vh.append(v[n * d:(n + 1) * d])
+        Q.append(qh)
+        K.append(kh)
+        V.append(vh)
+
+    out = []
+    for r in range(R):
+        o = []
+        for n in range(heads):
+            scores = [sum(Q[r][n][j] * K[c][n][j] for j in range(d)) / math.sqrt(d) for c in range(R)]
+            m = max(scores)
+            e = [math.exp(s - m) for s in scores]
+            z = sum(e)
+            for j in range(d):
+                o.append(sum(e[c] / z * V[c][n][j] for c in range(R)))
+        att = matvec(Wo, o)
+        ga = mod_rows[r][2]
+        xr = [x[r][i] + ga[i] * att[i] for i in range(H)]
+        sm, cm, gm = mod_rows[r][3], mod_rows[r][4], mod_rows[r][5]
+        h2 = modnorm(xr, n2, sm, cm)
+        g, u = matvec(Wg, h2), matvec(Wu, h2)
+        a = [g[j] / (1.0 + math.exp(-g[j])) * u[j] for j in range(len(g))]
+        mlp = matvec(Wd, a)
+        out.append([xr[i] + gm[i] * mlp[i] for i in range(H)])
+    return out
