@@ -1,0 +1,454 @@
+"""Benchmark of the AdaLN DiT block forward on GB300 (one JSON line on stdout, rank 0).
+
+Workload (a "step"): one whole block forward - modulated norm, QKV linear with QK-norm + RoPE
+epilogue, joint attention, out linear with gated residual, second modulated norm, SwiGLU up
+linear, down linear with gated residual - at the 1024^2 shape: hidden 3072, 24 heads x 128,
+ffn 12288, L = 128 text + N = 4096 image rows (R = 4224), bf16 weights, per-row modulation.
+The same run also times the int8lin block (the same shape) and the 32-block, 4-step denoise loop
+(L = 512, N = 4096) and reports them as sub-objects.
+
+Metric: block TFLOP/s (algorithmic FLOP = 2R(3H^2 + H^2 + 2HF + FH) + 4R^2 H per block) and
+ms per block. Inputs are larger than L2 (302 MB of weights per block), so no flush is needed.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU (torchrun): independent replicas, one block stream per GPU, no collective on the data
+path; value = all ranks' FLOP / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import dit_inputs as DI  # noqa: E402
+
+METRIC = "DiT block ms & TFLOP/s at N=4096 (bf16, int8lin) as % of GB300 tensor peak"
+WORKLOAD = "1024sq"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _dev_bf16(torch, u):
+    return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _block_setup(torch, D, inp, int8=False):
+    sh = inp.shape
+    dims = D.DitDims(sh.hidden, sh.heads, sh.head_dim, sh.ffn, sh.eps, sh.qk_eps)
+    cos = torch.empty(sh.R, sh.head_dim // 2, device="cuda")
+    sin = torch.empty_like(cos)
+    D.dit_rope_tables(sh.L, sh.grid_h, sh.grid_w, sh.head_dim, cos, sin)
+    st = dict(dims=dims, txt=_dev(torch, inp.txt), img=_dev(torch, inp.img),
+              tc=cos[:sh.L].contiguous(), ts=sin[:sh.L].contiguous(), ic=cos[sh.L:].contiguous(),
+              is_=sin[sh.L:].contiguous(), mod=D.Modulation(_dev(torch, inp.mod), _dev(torch, inp.mod_map)),
+              ws=torch.empty(D.dit_workspace_bytes(dims, sh.L, sh.N, int(int8)), dtype=torch.uint8, device="cuda"))
+    if int8:
+        st["w"] = D.Int8BlockWeights([_dev(torch, q) for q in inp.q8], [_dev_bf16(torch, s) for s in inp.s8])
+    else:
+        st["w"] = D.BlockWeights(_dev_bf16(torch, inp.wqkv), _dev_bf16(torch, inp.wout), _dev_bf16(torch, inp.wup),
+                                 _dev_bf16(torch, inp.wdown))
+    return st
+
+
+def _block_call(D, st, int8=False):
+    f = D.dit_block_forward_int8 if int8 else D.dit_block_forward
+    f(st["dims"], st["w"], st["txt"], st["img"], st["tc"], st["ts"], st["ic"], st["is_"], st["mod"], st["ws"])
+
+
+def _time_loop(torch, fn, steps, warmup, dist=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1)  # ms for all steps
+
+
+def _kernel_breakdown(torch, D, st, inp, steps):
+    """Time each step kernel on its own (same stream, CUDA events, back-to-back launches)."""
+    sh = inp.shape
+    dims, R, H, F, nh, d = st["dims"], sh.R, sh.hidden, sh.ffn, sh.heads, sh.head_dim
+    h = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty(nh, R, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty_like(q)
+    vt = torch.zeros(nh, d, D.dit_vt_stride(R), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
+    a = torch.empty(R, F, dtype=torch.bfloat16, device="cuda")
+    w = st["w"].tensors
+    M = inp.mod.shape[0]
+    norm_bytes = R * H * 4 + R * H * 2 + 2 * M * H * 4
+    gated_bytes = lambda K_: R * K_ * 2 + H * K_ * 2 + 2 * R * H * 4 + M * H * 4
+    kernels = [
+        ("modnorm", lambda: D.dit_modnorm(dims, st["txt"], st["img"], None, st["mod"], 0, h), 0.0, norm_bytes),
+        ("gemm_qkv_rope", lambda: D.dit_qkv_rope(dims, h, sh.L, sh.N, w[0], None, None, st["tc"], st["ts"], st["ic"],
+                                                 st["is_"], q, k, vt), 2.0 * R * 3 * H * H,
+         R * H * 2 + 3 * H * H * 2 + 3 * R * H * 2),
+        ("attention", lambda: D.dit_attention(dims, R, q, k, vt, o), 4.0 * R * R * H, 4 * R * H * 2),
+        ("gemm_out_gated", lambda: D.dit_linear_gated(dims, o, sh.L, sh.N, w[1], st["mod"], 0, st["txt"], st["img"]),
+         2.0 * R * H * H, gated_bytes(H)),
+        ("gemm_up_swiglu", lambda: D.dit_linear_swiglu(dims, h, w[2], a), 2.0 * R * 2 * F * H,
+         R * H * 2 + 2 * F * H * 2 + R * F * 2),
+        ("gemm_down_gated", lambda: D.dit_linear_gated(dims, a, sh.L, sh.N, w[3], st["mod"], 1, st["txt"], st["img"]),
+         2.0 * R * F * H, gated_bytes(F)),
+    ]
+    out = {}
+    for name, fn, flops, nbytes in kernels:
+        ms = _time_loop(torch, fn, steps, 2) / steps
+        launches = 2 if name == "modnorm" else 1
+        out[name] = {"ms": ms * launches, "ms_per_launch": ms, "launches_per_block": launches,
+                     "flop_per_launch": flops, "bytes_per_launch": nbytes}
+    D.dit_check()
+    return out
+
+
+def _denoise_bench(torch, D, steps_timed=2):
+    """32-block, 4-step denoise at L=512, N=4096 with seeded random weights drawn on the device."""
+    sh = DI.SHAPES["denoise"]
+    H, F, L, N, C = sh.hidden, sh.ffn, sh.L, sh.N, 64
+    gen = torch.Generator(device="cuda").manual_seed(sh.seed)
+    rnd = lambda *s: (torch.randn(*s, generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+    blocks = [D.BlockWeights(rnd(3 * H, H), rnd(H, H), rnd(2 * F, H), rnd(H, F)) for _ in range(32)]
+    dims = D.DitDims(H, sh.heads, sh.head_dim, F, sh.eps, sh.qk_eps)
+    model = D.DenoiseModel(dims, rnd(H, C), rnd(H, 256), rnd(H, H), rnd(32, 6 * H, H), rnd(2 * H, H), rnd(C, H),
+                           blocks, latent_channels=C)
+    noise = torch.randn(N, C, generator=gen, device="cuda")
+    txt = torch.randn(L, H, generator=gen, device="cuda")
+    cos = torch.empty(L + N, sh.head_dim // 2, device="cuda")
+    sin = torch.empty_like(cos)
+    D.dit_rope_tables(L, sh.grid_h, sh.grid_w, sh.head_dim, cos, sin)
+    tc, ts, ic, is_ = cos[:L].contiguous(), sin[:L].contiguous(), cos[L:].contiguous(), sin[L:].contiguous()
+    sig = [1.0, 0.75, 0.5, 0.25, 0.0]
+    ws = torch.empty(D.dit_denoise_workspace_bytes(model, L, N, 4), dtype=torch.uint8, device="cuda")
+    x = noise.clone()
+
+    def run():
+        x.copy_(noise)
+        D.dit_denoise(model, x, txt, sig, tc, ts, ic, is_, ws)
+
+    ms = _time_loop(torch, run, steps_timed, 1) / steps_timed
+    D.dit_check()
+    R = L + N
+    block_flops = 2.0 * R * (3 * H * H + H * H + 2 * H * F + F * H) + 4.0 * R * R * H
+    glue = 4 * (2.0 * N * C * H * 2) + 2.0 * 4 * (256 * H + H * H + 33 * 6 * H * H)
+    flops = 4 * 32 * block_flops + glue
+    del blocks, model
+    return {"workload": "denoise: 32 blocks of the 1024sq architecture, L=512, N=4096, 4 Euler steps, sigmas "
+                        "[1, .75, .5, .25, 0], weights ~N(0, 0.02) drawn on the device (torch seed 4)",
+            "ms_per_denoise": ms, "tflops": flops / (ms * 1e-3) / 1e12, "flop_per_denoise": flops,
+            "gpu_launches_per_denoise": 5 + 4 * (3 + 32 * 7 + 3)}
+
+
+def _e2e(torch, D, st, inp, steps, warmup):
+    """The block through the C ABI with host buffers: pinned H2D of the step's inputs (residual rows,
+    modulation rows, map, rotary tables), the block forward, D2H of the residual rows."""
+    sh = inp.shape
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_txt, h_img, h_mod, h_map = pin(inp.txt), pin(inp.img), pin(inp.mod), pin(inp.mod_map)
+    h_tc, h_ts, h_ic, h_is = (st[k].cpu().pin_memory() for k in ("tc", "ts", "ic", "is_"))
+    o_txt, o_img = torch.empty_like(h_txt).pin_memory(), torch.empty_like(h_img).pin_memory()
+    mod_rows, mod_map = st["mod"].tensors
+    pairs = [(st["txt"], h_txt), (st["img"], h_img), (mod_rows, h_mod), (mod_map, h_map), (st["tc"], h_tc),
+             (st["ts"], h_ts), (st["ic"], h_ic), (st["is_"], h_is)]
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
+    d2h = o_txt.numel() * 4 + o_img.numel() * 4
+
+    def step():
+        for d_, h_ in pairs:
+            d_.copy_(h_, non_blocking=True)
+        _block_call(D, st)
+        o_txt.copy_(st["txt"], non_blocking=True)
+        o_img.copy_(st["img"], non_blocking=True)
+
+    ms = _time_loop(torch, step, steps, warmup) / steps
+    return ms, h2d, d2h
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as tdist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+    torch.cuda.set_device(local)
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    import diffusion_transformer_gb300 as D
+    D.lib()
+
+    peaks = _peaks()
+    sh = DI.SHAPES[WORKLOAD]
+    inp = DI.block_inputs(sh)
+    st = _block_setup(torch, D, inp)
+    flops = sh.flops()
+
+    with ClockSampler(local) as clk:
+        total_ms = _time_loop(torch, lambda: _block_call(D, st), args.steps, args.warmup, dist)
+    D.dit_check()
+    t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = t.item() / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # per-kernel breakdown and the dominant kernel's roofline
+    kb = _kernel_breakdown(torch, D, st, inp, max(5, args.steps // 2))
+    dom = max(kb, key=lambda k: kb[k]["ms"])
+    dk = kb[dom]
+    if dk["flop_per_launch"] > 0:
+        ach = dk["flop_per_launch"] / (dk["ms_per_launch"] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": f"bf16_tflops burst, {peaks['source']}"}
+    else:
+        ach = dk["bytes_per_launch"] / (dk["ms_per_launch"] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None, "peak_source": f"hbm_gbs, {peaks['source']}"}
+    for k, v in kb.items():
+        if v["flop_per_launch"] > 0:
+            v["tflops"] = v["flop_per_launch"] / (v["ms_per_launch"] * 1e-3) / 1e12
+            v["frac_of_peak"] = v["tflops"] / peaks["bf16_tflops"]
+        else:
+            v["gbs"] = v["bytes_per_launch"] / (v["ms_per_launch"] * 1e-3) / 1e9
+            v["frac_of_peak"] = v["gbs"] / peaks["hbm_gbs"]
+
+    # int8lin block
+    int8 = None
+    if not args.no_int8:
+        del st
+        inp8 = DI.int8_block_inputs("1024sq_int8")
+        st8 = _block_setup(torch, D, inp8, int8=True)
+        ms8 = _time_loop(torch, lambda: _block_call(D, st8, int8=True), args.steps, args.warmup, dist) / args.steps
+        D.dit_check()
+        tf8 = flops / (ms8 * 1e-3) / 1e12
+        int8 = {"workload": "1024sq_int8", "ms_per_block": ms8, "tflops": tf8,
+                "frac_of_peak": tf8 / peaks["bf16_tflops"]}
+        del st8
+        st = _block_setup(torch, D, inp)
+
+    # end to end through host buffers
+    e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
+    D.dit_check()
+
+    den = None
+    if not args.no_denoise:
+        del st
+        torch.cuda.empty_cache()
+        den = _denoise_bench(torch, D)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(args.cpu_rows)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded dit_inputs; random-init weights)",
+            "config": {"workload": "1024sq block: hidden 3072, 24x128 heads, ffn 12288, L=128 + N=4096 (R=4224), "
+                                   "per-row modulation, bf16 weights", "R": sh.R, "hidden": sh.hidden,
+                       "ffn": sh.ffn, "flop_per_block": flops, "l2": "inputs > L2 (302 MB weights per block)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "frac_of_peak": value / world / peaks["bf16_tflops"],
+            "roofline": roof,
+            "kernels": kb,
+            "int8lin": int8,
+            "denoise": den,
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 7 * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+            "peaks": peaks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle: the cpu_baseline leg and the reference arm
+# ------------------------------------------------------------------------------------------------
+_ORACLE_INPUTS = {}
+
+
+def _oracle_sample(rows_n: int, seed: int = 0):
+    """Time the oracle's block forward on the 1024sq workload for a sample of query rows (keys and
+    values for all rows). Returns (seconds, algorithmic FLOP performed, description)."""
+    import oracle as O
+    sh = DI.SHAPES[WORKLOAD]
+    if WORKLOAD not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS[WORKLOAD] = DI.block_inputs(sh)
+    inp = _ORACLE_INPUTS[WORKLOAD]
+    R, H, F = sh.R, sh.hidden, sh.ffn
+    rows = np.sort(np.random.default_rng(seed).choice(R, min(rows_n, R), replace=False))
+    n = len(rows)
+    t0 = time.perf_counter()
+    O.block_forward(inp, rows=rows)
+    dt = time.perf_counter() - t0
+    flop = 2.0 * R * 3 * H * H + 4.0 * n * R * H + 2.0 * n * (H * H + 2 * H * F + F * H)
+    return dt, flop, f"oracle block forward (float64 NumPy) on the 1024sq workload: K/V for all {R} rows, " \
+                     f"outputs for {n} sampled rows"
+
+
+def _cpu_baseline(rows_n):
+    dt, flop, desc = _oracle_sample(rows_n)
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle", "sample": desc,
+            "seconds": dt}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        _oracle_sample(max(16, args.cpu_rows // 8))
+    total_t, total_f, desc = 0.0, 0.0, ""
+    for i in range(args.steps):
+        dt, f, desc = _oracle_sample(args.cpu_rows // 4, seed=i)
+        total_t += dt
+        total_f += f
+    v = total_f / total_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded dit_inputs)",
+            "config": {"workload": "1024sq block: hidden 3072, 24x128 heads, ffn 12288, L=128 + N=4096 (R=4224)"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--no-int8", action="store_true")
+    ap.add_argument("--no-denoise", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

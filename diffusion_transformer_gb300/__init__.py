@@ -1,0 +1,341 @@
+"""GB300 (sm_103a) AdaLN diffusion-transformer block library: thin Python binding of libdit.so.
+
+Every function here only marshals arguments (torch CUDA tensors -> device pointers, the current
+torch stream) and calls the C ABI of the same name declared in ``include/dit.h``; all arithmetic
+runs in the library's CUDA kernels. There is no fallback: if libdit.so is missing or fails to load,
+every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int64, c_size_t, c_void_p
+from typing import List, Optional, Sequence
+
+__all__ = [
+    "DitError", "lib", "library_path", "DitDims", "BlockWeights", "Int8BlockWeights", "Modulation",
+    "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_euler_step", "dit_rope_tables",
+    "dit_denoise", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
+    "dit_vt_stride", "dit_attention", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
+    "dit_dequant_int8", "dit_linear_int8", "dit_check", "dit_status_string", "dit_version",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libdit.so")
+
+DIT_OK, DIT_EINVAL, DIT_EUNSUPPORTED, DIT_EWORKSPACE, DIT_ECUDA, DIT_ETIMEOUT = 0, -1, -2, -3, -4, -5
+
+
+class DitError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({dit_status_string(status)})")
+
+
+# ----------------------------------------------------------------------------------------------
+# C structs (mirror include/dit.h)
+# ----------------------------------------------------------------------------------------------
+class dit_dims(ctypes.Structure):
+    _fields_ = [("hidden", c_int), ("heads", c_int), ("head_dim", c_int), ("ffn", c_int),
+                ("eps", c_float), ("qk_eps", c_float)]
+
+
+class dit_block_w(ctypes.Structure):
+    _fields_ = [("wqkv", c_void_p), ("wout", c_void_p), ("wup", c_void_p), ("wdown", c_void_p),
+                ("norm1", c_void_p), ("norm2", c_void_p), ("q_norm", c_void_p), ("k_norm", c_void_p)]
+
+
+class dit_block_w8(ctypes.Structure):
+    _fields_ = [("q", c_void_p * 4), ("s", c_void_p * 4), ("norm1", c_void_p), ("norm2", c_void_p),
+                ("q_norm", c_void_p), ("k_norm", c_void_p)]
+
+
+class dit_mod(ctypes.Structure):
+    _fields_ = [("rows", c_void_p), ("map", c_void_p), ("M", c_int)]
+
+
+class dit_model(ctypes.Structure):
+    _fields_ = [("dims", dit_dims), ("blocks", c_int), ("latent_channels", c_int), ("w_in", c_void_p),
+                ("w_t1", c_void_p), ("w_t2", c_void_p), ("w_ada", c_void_p), ("w_ada_f", c_void_p),
+                ("w_out", c_void_p), ("block", POINTER(dit_block_w))]
+
+
+_SIGNATURES = {
+    "dit_block_forward": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_int, c_void_p, c_int,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p, c_size_t,
+                                  c_void_p]),
+    "dit_block_forward_int8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8), c_void_p, c_int, c_void_p, c_int,
+                                       c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
+                                       c_size_t, c_void_p]),
+    "dit_euler_step": (c_int, [c_void_p, c_void_p, c_int64, c_float, c_float, c_void_p]),
+    "dit_rope_tables": (c_int, [c_int, c_int, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p]),
+    "dit_denoise": (c_int, [POINTER(dit_model), c_void_p, c_int, c_void_p, c_int, POINTER(c_float), c_int,
+                            c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "dit_workspace_bytes": (c_size_t, [POINTER(dit_dims), c_int, c_int, c_int]),
+    "dit_denoise_workspace_bytes": (c_size_t, [POINTER(dit_model), c_int, c_int, c_int]),
+    "dit_modnorm": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_int, c_void_p, POINTER(dit_mod), c_int,
+                            c_void_p, c_void_p]),
+    "dit_qkv_rope": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dit_vt_stride": (c_int, [c_int]),
+    "dit_attention": (c_int, [POINTER(dit_dims), c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dit_linear_gated": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_int, c_void_p, POINTER(dit_mod), c_int,
+                                 c_void_p, c_void_p, c_void_p]),
+    "dit_linear_swiglu": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
+    "dit_linear": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p]),
+    "dit_dequant_int8": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
+    "dit_linear_int8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
+    "dit_check": (c_int, [c_void_p]),
+    "dit_status_string": (c_char_p, [c_int]),
+    "dit_version": (c_int, []),
+}
+
+_lib = None
+
+
+def lib():
+    """Load libdit.so (built in-tree by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"libdit.so not built ({library_path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def dit_status_string(status: int) -> str:
+    return lib().dit_status_string(int(status)).decode()
+
+
+def dit_version() -> int:
+    return lib().dit_version()
+
+
+def _ok(status: int, where: str):
+    if status != DIT_OK:
+        raise DitError(status, where)
+
+
+# ----------------------------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------------------------
+def _ptr(t, dtype=None, name="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name}: expected dtype {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _bf16():
+    import torch
+    return (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class DitDims:
+    def __init__(self, hidden: int, heads: int, head_dim: int, ffn: int, eps: float = 1e-6, qk_eps: float = 1e-6):
+        self.c = dit_dims(hidden, heads, head_dim, ffn, eps, qk_eps)
+        self.hidden, self.heads, self.head_dim, self.ffn = hidden, heads, head_dim, ffn
+        self.eps, self.qk_eps = eps, qk_eps
+
+
+class BlockWeights:
+    """Device tensors of one bf16 block (kept alive by this object)."""
+
+    def __init__(self, wqkv, wout, wup, wdown, norm1=None, norm2=None, q_norm=None, k_norm=None):
+        import torch
+        bf = _bf16()
+        f32 = torch.float32
+        self.tensors = (wqkv, wout, wup, wdown, norm1, norm2, q_norm, k_norm)
+        self.c = dit_block_w(_ptr(wqkv, bf, "wqkv"), _ptr(wout, bf, "wout"), _ptr(wup, bf, "wup"),
+                             _ptr(wdown, bf, "wdown"), _ptr(norm1, f32, "norm1"), _ptr(norm2, f32, "norm2"),
+                             _ptr(q_norm, f32, "q_norm"), _ptr(k_norm, f32, "k_norm"))
+
+
+class Int8BlockWeights:
+    """Device tensors of one int8lin block: q [4] int8 [out, in], s [4] bf16 [out, in/32]."""
+
+    def __init__(self, q: Sequence, s: Sequence, norm1=None, norm2=None, q_norm=None, k_norm=None):
+        import torch
+        f32 = torch.float32
+        self.tensors = (tuple(q), tuple(s), norm1, norm2, q_norm, k_norm)
+        qp = (c_void_p * 4)(*[_ptr(t, torch.int8, "q") for t in q])
+        sp = (c_void_p * 4)(*[_ptr(t, _bf16(), "s") for t in s])
+        self.c = dit_block_w8(qp, sp, _ptr(norm1, f32, "norm1"), _ptr(norm2, f32, "norm2"),
+                              _ptr(q_norm, f32, "q_norm"), _ptr(k_norm, f32, "k_norm"))
+
+
+class Modulation:
+    """rows [M, 6, H] fp32 device tensor and map [R] int32 (or None)."""
+
+    def __init__(self, rows, map=None):
+        import torch
+        self.tensors = (rows, map)
+        self.c = dit_mod(_ptr(rows, torch.float32, "mod rows"), _ptr(map, torch.int32, "map"), rows.shape[0])
+
+
+class DenoiseModel:
+    def __init__(self, dims: DitDims, w_in, w_t1, w_t2, w_ada, w_ada_f, w_out, blocks: List[BlockWeights],
+                 latent_channels: int = 64):
+        bf = _bf16()
+        self.dims, self.blocks = dims, blocks
+        self.tensors = (w_in, w_t1, w_t2, w_ada, w_ada_f, w_out)
+        self._arr = (dit_block_w * max(1, len(blocks)))(*[b.c for b in blocks])
+        self.c = dit_model(dims.c, len(blocks), latent_channels, _ptr(w_in, bf, "w_in"), _ptr(w_t1, bf, "w_t1"),
+                           _ptr(w_t2, bf, "w_t2"), _ptr(w_ada, bf, "w_ada"), _ptr(w_ada_f, bf, "w_ada_f"),
+                           _ptr(w_out, bf, "w_out"), ctypes.cast(self._arr, POINTER(dit_block_w)))
+
+
+# ----------------------------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ----------------------------------------------------------------------------------------------
+def dit_workspace_bytes(dims: DitDims, L: int, N: int, variant: int = 0) -> int:
+    return lib().dit_workspace_bytes(ctypes.byref(dims.c), L, N, variant)
+
+
+def dit_denoise_workspace_bytes(model: DenoiseModel, L: int, N: int, steps: int) -> int:
+    return lib().dit_denoise_workspace_bytes(ctypes.byref(model.c), L, N, steps)
+
+
+def dit_vt_stride(R: int) -> int:
+    return lib().dit_vt_stride(R)
+
+
+def dit_block_forward(dims: DitDims, w: BlockWeights, txt, img, txt_cos, txt_sin, img_cos, img_sin,
+                      mod: Modulation, ws, stream=None):
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_block_forward(ctypes.byref(dims.c), ctypes.byref(w.c), _ptr(txt, f32, "txt"), L,
+                                _ptr(img, f32, "img"), img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                                _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c), _ptr(ws, None, "ws"),
+                                ws.numel() * ws.element_size(), _stream(stream)), "dit_block_forward")
+
+
+def dit_block_forward_int8(dims: DitDims, w: Int8BlockWeights, txt, img, txt_cos, txt_sin, img_cos, img_sin,
+                           mod: Modulation, ws, stream=None):
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_block_forward_int8(ctypes.byref(dims.c), ctypes.byref(w.c), _ptr(txt, f32, "txt"), L,
+                                     _ptr(img, f32, "img"), img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                                     _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
+                                     _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_block_forward_int8")
+
+
+def dit_euler_step(x, vel, sigma: float, sigma_next: float, stream=None):
+    import torch
+    _ok(lib().dit_euler_step(_ptr(x, torch.float32, "x"), _ptr(vel, torch.float32, "vel"), x.numel(), sigma,
+                             sigma_next, _stream(stream)), "dit_euler_step")
+
+
+def dit_rope_tables(L: int, grid_h: int, grid_w: int, head_dim: int, cos, sin, theta: float = 10000.0,
+                    stream=None):
+    import torch
+    _ok(lib().dit_rope_tables(L, grid_h, grid_w, head_dim, theta, _ptr(cos, torch.float32, "cos"),
+                              _ptr(sin, torch.float32, "sin"), _stream(stream)), "dit_rope_tables")
+
+
+def dit_denoise(model: DenoiseModel, img_tokens, txt_feats, sigmas: Sequence[float], txt_cos, txt_sin, img_cos,
+                img_sin, ws, stream=None):
+    import torch
+    f32 = torch.float32
+    steps = len(sigmas) - 1
+    sig = (c_float * len(sigmas))(*[float(s) for s in sigmas])
+    L = 0 if txt_feats is None else txt_feats.shape[0]
+    _ok(lib().dit_denoise(ctypes.byref(model.c), _ptr(img_tokens, f32, "img_tokens"), img_tokens.shape[0],
+                          _ptr(txt_feats, f32, "txt_feats"), L, sig, steps, _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                          _ptr(img_cos, f32), _ptr(img_sin, f32), _ptr(ws, None, "ws"),
+                          ws.numel() * ws.element_size(), _stream(stream)), "dit_denoise")
+
+
+def dit_modnorm(dims: DitDims, txt, img, w, mod: Modulation, which: int, h, stream=None):
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_modnorm(ctypes.byref(dims.c), _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"), img.shape[0],
+                          _ptr(w, f32, "w"), ctypes.byref(mod.c), which, _ptr(h, _bf16(), "h"), _stream(stream)),
+        "dit_modnorm")
+
+
+def dit_qkv_rope(dims: DitDims, h, L: int, N: int, wqkv, q_norm, k_norm, txt_cos, txt_sin, img_cos, img_sin,
+                 q, k, vt, stream=None):
+    import torch
+    f32, bf = torch.float32, _bf16()
+    _ok(lib().dit_qkv_rope(ctypes.byref(dims.c), _ptr(h, bf, "h"), L, N, _ptr(wqkv, bf, "wqkv"),
+                           _ptr(q_norm, f32), _ptr(k_norm, f32), _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                           _ptr(img_cos, f32), _ptr(img_sin, f32), _ptr(q, bf, "q"), _ptr(k, bf, "k"),
+                           _ptr(vt, bf, "vt"), _stream(stream)), "dit_qkv_rope")
+
+
+def dit_attention(dims: DitDims, R: int, q, k, vt, o, stream=None):
+    bf = _bf16()
+    _ok(lib().dit_attention(ctypes.byref(dims.c), R, _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(vt, bf, "vt"),
+                            _ptr(o, bf, "o"), _stream(stream)), "dit_attention")
+
+
+def dit_linear_gated(dims: DitDims, a, L: int, N: int, w, mod: Modulation, which: int, txt, img, stream=None):
+    import torch
+    bf, f32 = _bf16(), torch.float32
+    _ok(lib().dit_linear_gated(ctypes.byref(dims.c), _ptr(a, bf, "a"), L, N, _ptr(w, bf, "w"), ctypes.byref(mod.c),
+                               which, _ptr(txt, f32, "txt"), _ptr(img, f32, "img"), _stream(stream)),
+        "dit_linear_gated")
+
+
+def dit_linear_swiglu(dims: DitDims, h2, wup, a, stream=None):
+    bf = _bf16()
+    _ok(lib().dit_linear_swiglu(ctypes.byref(dims.c), _ptr(h2, bf, "h2"), h2.shape[0], _ptr(wup, bf, "wup"),
+                                _ptr(a, bf, "a"), _stream(stream)), "dit_linear_swiglu")
+
+
+def dit_linear(a, w, out, stream=None):
+    import torch
+    bf = _bf16()
+    M, K = a.shape
+    N = w.shape[0]
+    out_bf16 = 1 if out.dtype != torch.float32 else 0
+    _ok(lib().dit_linear(_ptr(a, bf, "a"), M, K, _ptr(w, bf, "w"), N, _ptr(out, None, "out"), out_bf16,
+                         _stream(stream)), "dit_linear")
+
+
+def dit_linear_int8(a, wq, wscale, out, stream=None):
+    import torch
+    M, K = a.shape
+    N = wq.shape[0]
+    _ok(lib().dit_linear_int8(_ptr(a, _bf16(), "a"), M, K, _ptr(wq, torch.int8, "wq"), _ptr(wscale, _bf16(), "s"), N,
+                              _ptr(out, torch.float32, "out"), _stream(stream)), "dit_linear_int8")
+
+
+def dit_dequant_int8(q, s, w, stream=None):
+    import torch
+    rows, cols = q.shape
+    _ok(lib().dit_dequant_int8(_ptr(q, torch.int8, "q"), _ptr(s, _bf16(), "s"), rows, cols, _ptr(w, _bf16(), "w"),
+                               _stream(stream)), "dit_dequant_int8")
+
+
+def dit_check(stream=None):
+    _ok(lib().dit_check(_stream(stream)), "dit_check")

@@ -1,0 +1,569 @@
+// C ABI of libdit.so: argument validation, workspace carve-up and launch sequencing on the
+// caller's stream. Every arithmetic step runs in the kernels of gemm.cu, attention.cu and
+// elementwise.cu; this file only checks arguments and orders launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "tmap.h"
+
+namespace dit {
+
+// ------------------------------------------------------------------------------------------
+// per-device state: error word address and SM count
+// ------------------------------------------------------------------------------------------
+static __device__ int g_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices];
+int g_sms[kMaxDevices];
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+int* err_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool dims_ok(const dit_dims* d) {
+  if (!d) return false;
+  if (d->head_dim != 64 && d->head_dim != 128) return false;
+  if (d->heads <= 0 || d->hidden != d->heads * d->head_dim) return false;
+  if (d->hidden % 256 != 0 || d->ffn <= 0 || d->ffn % 128 != 0) return false;
+  if (!(d->eps >= 0.f) || !(d->qk_eps >= 0.f)) return false;
+  return true;
+}
+
+struct BlockWs {
+  uint16_t* h;   // [R, H]  norm outputs (h, then h2)
+  uint16_t* q;   // [nh, R, d]
+  uint16_t* k;   // [nh, R, d]
+  uint16_t* vt;  // [nh, d, Rp]
+  uint16_t* o;   // [R, H]  attention output
+  uint16_t* a;   // [R, F]  SwiGLU output
+  size_t bytes;
+};
+
+int vt_stride(int R) { return int(round_up(size_t(R), 8)); }
+
+BlockWs carve_block_ws(const dit_dims* d, int R, void* base) {
+  BlockWs w{};
+  const size_t H = d->hidden, F = d->ffn, nh = d->heads, hd = d->head_dim;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* r = p ? p + off : nullptr;
+    off += round_up(bytes, 256);
+    return reinterpret_cast<uint16_t*>(r);
+  };
+  w.h = take(size_t(R) * H * 2);
+  w.q = take(nh * size_t(R) * hd * 2);
+  w.k = take(nh * size_t(R) * hd * 2);
+  w.vt = take(nh * hd * size_t(vt_stride(R)) * 2);
+  w.o = take(size_t(R) * H * 2);
+  w.a = take(size_t(R) * F * 2);
+  w.bytes = off;
+  return w;
+}
+
+GemmParams base_params(int M, int N, int K, int* err) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.err = err;
+  return p;
+}
+
+struct ModRef {
+  const float* rows;
+  const int32_t* map;
+  int M;
+};
+
+// One whole block on already-validated arguments. `w8` selects the int8lin path.
+int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, float* txt, int L, float* img, int N,
+              const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod, void* ws,
+              cudaStream_t st) {
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  const int R = L + N, H = d->hidden, F = d->ffn;
+  const BlockWs b = carve_block_ws(d, R, ws);
+  const float* norm1 = w8 ? w8->norm1 : w->norm1;
+  const float* norm2 = w8 ? w8->norm2 : w->norm2;
+  const float* qn = w8 ? w8->q_norm : w->q_norm;
+  const float* kn = w8 ? w8->k_norm : w->k_norm;
+  int rc;
+
+  // 1. h = modnorm(x; norm1, shift_a, scale_a)
+  ModNormParams mp{txt, img, L, R, H, H, H, norm1, mod.rows, mod.rows + H, 6LL * H, mod.map, d->eps, b.h};
+  if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+
+  // 2. q, k, vt = qk-norm + rope epilogue of h Wqkv^T
+  GemmParams g = base_params(R, 3 * H, H, err);
+  g.q = b.q;
+  g.k = b.k;
+  g.vt = b.vt;
+  g.H = H;
+  g.heads = d->heads;
+  g.head_dim = d->head_dim;
+  g.Rp = vt_stride(R);
+  g.L = L;
+  g.txt_cos = tc;
+  g.txt_sin = ts;
+  g.img_cos = ic;
+  g.img_sin = is;
+  g.q_norm = qn;
+  g.k_norm = kn;
+  g.qk_eps = d->qk_eps;
+  GemmInt8B q8;
+  if (w8) q8 = GemmInt8B{w8->q[0], w8->s[0]};
+  if ((rc = gemm_launch(b.h, H, w8 ? nullptr : w->wqkv, w8 ? &q8 : nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
+
+  // 3. o = attention(q, k, v)
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+  if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
+
+  // 4. x += gate_a * (o Wout^T)
+  g = base_params(R, H, H, err);
+  g.txt = txt;
+  g.img = img;
+  g.L = L;
+  g.gate = mod.rows + 2LL * H;
+  g.map = mod.map;
+  g.gate_stride = 6LL * H;
+  if (w8) q8 = GemmInt8B{w8->q[1], w8->s[1]};
+  if ((rc = gemm_launch(b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
+
+  // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
+  mp.w = norm2;
+  mp.shift = mod.rows + 3LL * H;
+  mp.scale = mod.rows + 4LL * H;
+  if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+
+  // 6. a = silu(h2 Wgate^T) * (h2 Wup^T), interleaved rows
+  g = base_params(R, 2 * F, H, err);
+  g.out = b.a;
+  g.ldo = F;
+  if (w8) q8 = GemmInt8B{w8->q[2], w8->s[2]};
+  if ((rc = gemm_launch(b.h, H, w8 ? nullptr : w->wup, w8 ? &q8 : nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
+
+  // 7. x += gate_m * (a Wdown^T)
+  g = base_params(R, H, F, err);
+  g.txt = txt;
+  g.img = img;
+  g.L = L;
+  g.gate = mod.rows + 5LL * H;
+  g.map = mod.map;
+  g.gate_stride = 6LL * H;
+  if (w8) q8 = GemmInt8B{w8->q[3], w8->s[3]};
+  return gemm_launch(b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, kEpiGated, g, st);
+}
+
+int check_block_args(const dit_dims* d, const float* txt, int L, const float* img, int N, const float* tc,
+                     const float* ts, const float* ic, const float* is, const dit_mod* mod, const void* ws,
+                     size_t ws_bytes, int variant) {
+  if (!d || !mod) return DIT_EINVAL;
+  if (!dims_ok(d)) return DIT_EUNSUPPORTED;
+  if (L < 0 || N < 1 || (L > 0 && (!txt || !tc || !ts)) || !img || !ic || !is) return DIT_EINVAL;
+  if (!mod->rows || mod->M < 1) return DIT_EINVAL;
+  if (!al16(txt) || !al16(img) || !al16(mod->rows)) return DIT_EINVAL;
+  if (!ws) return DIT_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DIT_EINVAL;
+  if (ws_bytes < dit_workspace_bytes(d, L, N, variant)) return DIT_EWORKSPACE;
+  return DIT_OK;
+}
+
+}  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+bool smem_attr_once(const void* kernel, unsigned bytes) {
+  const int dev = current_device();
+  if (dev < 0) return false;
+  static const void* done[kMaxDevices][32];
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < 32; ++i) {
+    if (done[dev][i] == kernel) return true;
+    if (!done[dev][i]) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) != cudaSuccess)
+        return false;
+      done[dev][i] = kernel;
+      return true;
+    }
+  }
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) == cudaSuccess;
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+}  // namespace dit
+
+using namespace dit;
+
+extern "C" {
+
+int dit_version(void) { return 100; }
+
+const char* dit_status_string(int s) {
+  switch (s) {
+    case DIT_OK: return "ok";
+    case DIT_EINVAL: return "invalid argument (null, size or alignment)";
+    case DIT_EUNSUPPORTED: return "shape not supported by the kernels";
+    case DIT_EWORKSPACE: return "workspace missing or too small";
+    case DIT_ECUDA: return "CUDA error";
+    case DIT_ETIMEOUT: return "a bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
+  if (!dims_ok(d) || L < 0 || N < 1 || (variant != 0 && variant != 1)) return 0;
+  return carve_block_ws(d, L + N, nullptr).bytes;
+}
+
+int dit_vt_stride(int R) { return R < 0 ? 0 : vt_stride(R); }
+
+int dit_check(dit_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DIT_ECUDA;
+  int* p = err_word();
+  if (!p) return DIT_ECUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DIT_ECUDA;
+  if (v != 0) {
+    const int z = 0;
+    cudaMemcpy(p, &z, sizeof(int), cudaMemcpyHostToDevice);
+    return DIT_ETIMEOUT;
+  }
+  return DIT_OK;
+}
+
+int dit_block_forward(const dit_dims* d, const dit_block_w* w, float* txt, int L, float* img, int N, const float* tc,
+                      const float* ts, const float* ic, const float* is, const dit_mod* mod, void* ws,
+                      size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 0);
+  if (rc != DIT_OK) return rc;
+  if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+  if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  return run_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt, int L, float* img, int N,
+                           const float* tc, const float* ts, const float* ic, const float* is, const dit_mod* mod,
+                           void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 1);
+  if (rc != DIT_OK) return rc;
+  if (!w) return DIT_EINVAL;
+  for (int i = 0; i < 4; ++i)
+    if (!w->q[i] || !w->s[i] || !al16(w->q[i])) return DIT_EINVAL;
+  return run_block(d, nullptr, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_euler_step(float* x, const float* vel, int64_t n, float sigma, float sigma_next, dit_stream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !vel))) return DIT_EINVAL;
+  return euler_launch(x, vel, n, sigma, sigma_next, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_rope_tables(int L, int gh, int gw, int head_dim, float theta, float* cos, float* sin, dit_stream_t stream) {
+  if (L < 0 || gh < 1 || gw < 1 || !cos || !sin || !(theta > 0.f)) return DIT_EINVAL;
+  if (head_dim != 64 && head_dim != 128) return DIT_EUNSUPPORTED;
+  return rope_tables_launch(L, gh, gw, head_dim, theta, cos, sin, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_modnorm(const dit_dims* d, const float* txt, int L, const float* img, int N, const float* w,
+                const dit_mod* mod, int which, uint16_t* h, dit_stream_t stream) {
+  if (!d || !mod || !h || !img || L < 0 || N < 1 || (L > 0 && !txt) || (which != 0 && which != 1)) return DIT_EINVAL;
+  if (d->hidden <= 0 || d->hidden % 4 != 0) return DIT_EUNSUPPORTED;
+  if (!mod->rows || mod->M < 1 || !al16(img) || (txt && !al16(txt)) || !al16(mod->rows) || !al16(h) ||
+      (w && !al16(w)))
+    return DIT_EINVAL;
+  const int H = d->hidden;
+  ModNormParams mp{txt, img, L, L + N, H, H, H, w, mod->rows + 3LL * which * H, mod->rows + (3LL * which + 1) * H,
+                   6LL * H, mod->map, d->eps, h};
+  return modnorm_launch(mp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_qkv_rope(const dit_dims* d, const uint16_t* h, int L, int N, const uint16_t* wqkv, const float* q_norm,
+                 const float* k_norm, const float* tc, const float* ts, const float* ic, const float* is, uint16_t* q,
+                 uint16_t* k, uint16_t* vt, dit_stream_t stream) {
+  if (!d || !h || !wqkv || !q || !k || !vt || L < 0 || N < 1 || !ic || !is || (L > 0 && (!tc || !ts)))
+    return DIT_EINVAL;
+  if (!dims_ok(d)) return DIT_EUNSUPPORTED;
+  if (!al16(h) || !al16(wqkv) || !al16(q) || !al16(k) || !al16(vt)) return DIT_EINVAL;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  const int R = L + N, H = d->hidden;
+  GemmParams g = base_params(R, 3 * H, H, err);
+  g.q = q;
+  g.k = k;
+  g.vt = vt;
+  g.H = H;
+  g.heads = d->heads;
+  g.head_dim = d->head_dim;
+  g.Rp = vt_stride(R);
+  g.L = L;
+  g.txt_cos = tc;
+  g.txt_sin = ts;
+  g.img_cos = ic;
+  g.img_sin = is;
+  g.q_norm = q_norm;
+  g.k_norm = k_norm;
+  g.qk_eps = d->qk_eps;
+  return gemm_launch(h, H, wqkv, nullptr, kEpiQKV, g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_attention(const dit_dims* d, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt, uint16_t* o,
+                  dit_stream_t stream) {
+  if (!d || R < 1 || !q || !k || !vt || !o) return DIT_EINVAL;
+  if (!dims_ok(d)) return DIT_EUNSUPPORTED;
+  if (!al16(q) || !al16(k) || !al16(vt) || !al16(o)) return DIT_EINVAL;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), q, k, vt, o, err};
+  return attention_launch(ap, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_linear_gated(const dit_dims* d, const uint16_t* a, int L, int N, const uint16_t* w, const dit_mod* mod,
+                     int which, float* txt, float* img, dit_stream_t stream) {
+  if (!d || !a || !w || !mod || !mod->rows || mod->M < 1 || !img || L < 0 || N < 1 || (L > 0 && !txt) ||
+      (which != 0 && which != 1))
+    return DIT_EINVAL;
+  if (!dims_ok(d)) return DIT_EUNSUPPORTED;
+  if (!al16(a) || !al16(w) || !al16(img) || (txt && !al16(txt)) || !al16(mod->rows)) return DIT_EINVAL;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  const int H = d->hidden, K = which == 0 ? H : d->ffn;
+  GemmParams g = base_params(L + N, H, K, err);
+  g.txt = txt;
+  g.img = img;
+  g.L = L;
+  g.gate = mod->rows + (which == 0 ? 2LL : 5LL) * H;
+  g.map = mod->map;
+  g.gate_stride = 6LL * H;
+  return gemm_launch(a, K, w, nullptr, kEpiGated, g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_linear_swiglu(const dit_dims* d, const uint16_t* h2, int R, const uint16_t* wup, uint16_t* a,
+                      dit_stream_t stream) {
+  if (!d || !h2 || !wup || !a || R < 1) return DIT_EINVAL;
+  if (!dims_ok(d)) return DIT_EUNSUPPORTED;
+  if (!al16(h2) || !al16(wup) || !al16(a)) return DIT_EINVAL;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  GemmParams g = base_params(R, 2 * d->ffn, d->hidden, err);
+  g.out = a;
+  g.ldo = d->ffn;
+  return gemm_launch(h2, d->hidden, wup, nullptr, kEpiSwiGLU, g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_linear(const uint16_t* a, int M, int K, const uint16_t* w, int N, void* out, int out_bf16,
+               dit_stream_t stream) {
+  if (!a || !w || !out || M < 1 || K < 1 || N < 1) return DIT_EINVAL;
+  if (K % 64 != 0 || N % 64 != 0) return DIT_EUNSUPPORTED;
+  if (!al16(a) || !al16(w) || !al16(out)) return DIT_EINVAL;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  GemmParams g = base_params(M, N, K, err);
+  g.out = out;
+  g.ldo = N;
+  return gemm_launch(a, K, w, nullptr, out_bf16 ? kEpiStoreBF16 : kEpiStoreF32, g,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_linear_int8(const uint16_t* a, int M, int K, const int8_t* wq, const uint16_t* wsc, int N, float* out,
+                    dit_stream_t stream) {
+  if (!a || !wq || !wsc || !out || M < 1 || K < 1 || N < 1) return DIT_EINVAL;
+  if (K % 64 != 0 || N % 128 != 0) return DIT_EUNSUPPORTED;
+  if (!al16(a) || !al16(wq) || !al16(out)) return DIT_EINVAL;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  GemmParams g = base_params(M, N, K, err);
+  g.out = out;
+  g.ldo = N;
+  GemmInt8B b8{wq, wsc};
+  return gemm_launch(a, K, nullptr, &b8, kEpiStoreF32, g, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_dequant_int8(const int8_t* q, const uint16_t* s, int64_t rows, int64_t cols, uint16_t* w,
+                     dit_stream_t stream) {
+  if (!q || !s || !w || rows < 0 || cols < 0) return DIT_EINVAL;
+  if (cols % 32 != 0) return DIT_EUNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(w) % 4) return DIT_EINVAL;
+  return dequant_int8_launch(q, s, w, rows, cols, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------------------------------
+// denoise
+// ------------------------------------------------------------------------------------------
+namespace {
+struct DenoiseWs {
+  float* rows;      // [R, H] fp32: text rows then image rows
+  uint8_t* block;   // block workspace
+  uint16_t* xin;    // [N, C] bf16
+  uint16_t* emb;    // [steps, 256] bf16
+  uint16_t* t1;     // [steps, H] bf16
+  uint16_t* st;     // [steps, H] bf16 = silu(temb)
+  float* mods;      // [steps, blocks * 6H] fp32
+  float* fin;       // [steps, 2H] fp32
+  float* vel;       // [N, C] fp32
+  size_t bytes;
+};
+
+DenoiseWs carve_denoise(const dit_model* m, int L, int N, int steps, void* base) {
+  DenoiseWs w{};
+  const size_t H = m->dims.hidden, C = m->latent_channels, R = size_t(L) + N;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* r = p ? p + off : nullptr;
+    off += round_up(bytes, 256);
+    return r;
+  };
+  w.rows = reinterpret_cast<float*>(take(R * H * 4));
+  w.block = take(carve_block_ws(&m->dims, int(R), nullptr).bytes);
+  w.xin = reinterpret_cast<uint16_t*>(take(size_t(N) * C * 2));
+  w.emb = reinterpret_cast<uint16_t*>(take(size_t(steps) * 256 * 2));
+  w.t1 = reinterpret_cast<uint16_t*>(take(size_t(steps) * H * 2));
+  w.st = reinterpret_cast<uint16_t*>(take(size_t(steps) * H * 2));
+  w.mods = reinterpret_cast<float*>(take(size_t(steps) * m->blocks * 6 * H * 4));
+  w.fin = reinterpret_cast<float*>(take(size_t(steps) * 2 * H * 4));
+  w.vel = reinterpret_cast<float*>(take(size_t(N) * C * 4));
+  w.bytes = off;
+  return w;
+}
+
+bool model_ok(const dit_model* m) {
+  if (!m || !dims_ok(&m->dims) || m->blocks < 0 || m->latent_channels < 64 || m->latent_channels % 64 != 0)
+    return false;
+  return true;
+}
+}  // namespace
+
+size_t dit_denoise_workspace_bytes(const dit_model* m, int L, int N, int steps) {
+  if (!model_ok(m) || L < 0 || N < 1 || steps < 1 || steps > 64) return 0;
+  return carve_denoise(m, L, N, steps, nullptr).bytes;
+}
+
+int dit_denoise(const dit_model* m, float* x, int N, const float* txt_feats, int L, const float* sigmas, int steps,
+                const float* tc, const float* ts, const float* ic, const float* is, void* ws, size_t ws_bytes,
+                dit_stream_t stream) {
+  if (!m || !x || !sigmas || N < 1 || L < 0 || (L > 0 && (!txt_feats || !tc || !ts)) || !ic || !is) return DIT_EINVAL;
+  if (!model_ok(m) || steps < 1 || steps > 64) return DIT_EUNSUPPORTED;
+  if (!m->w_in || !m->w_t1 || !m->w_t2 || !m->w_ada_f || !m->w_out || (m->blocks > 0 && (!m->w_ada || !m->block)))
+    return DIT_EINVAL;
+  for (int b = 0; b < m->blocks; ++b) {
+    const dit_block_w& bw = m->block[b];
+    if (!bw.wqkv || !bw.wout || !bw.wup || !bw.wdown) return DIT_EINVAL;
+    if (!al16(bw.wqkv) || !al16(bw.wout) || !al16(bw.wup) || !al16(bw.wdown)) return DIT_EINVAL;
+  }
+  if (!al16(x) || (txt_feats && !al16(txt_feats)) || !al16(m->w_in) || !al16(m->w_t1) || !al16(m->w_t2) ||
+      (m->w_ada && !al16(m->w_ada)) || !al16(m->w_ada_f) || !al16(m->w_out))
+    return DIT_EINVAL;
+  if (!ws) return DIT_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DIT_EINVAL;
+  if (ws_bytes < dit_denoise_workspace_bytes(m, L, N, steps)) return DIT_EWORKSPACE;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const dit_dims* d = &m->dims;
+  const int H = d->hidden, C = m->latent_channels, R = L + N;
+  const DenoiseWs w = carve_denoise(m, L, N, steps, ws);
+  const long long SB = 6LL * H * m->blocks;
+  int rc;
+
+  // step-invariant work: time embeddings and every modulation row for all steps
+  if ((rc = sinusoid_launch(sigmas, steps, 256, w.emb, st)) != DIT_OK) return rc;
+  GemmParams g = base_params(steps, H, 256, err);
+  g.out = w.t1;
+  g.ldo = H;
+  if ((rc = gemm_launch(w.emb, 256, m->w_t1, nullptr, kEpiSiluBF16, g, st)) != DIT_OK) return rc;
+  g = base_params(steps, H, H, err);
+  g.out = w.st;
+  g.ldo = H;
+  if ((rc = gemm_launch(w.t1, H, m->w_t2, nullptr, kEpiSiluBF16, g, st)) != DIT_OK) return rc;
+  if (m->blocks > 0) {
+    g = base_params(steps, int(SB), H, err);
+    g.out = w.mods;
+    g.ldo = SB;
+    if ((rc = gemm_launch(w.st, H, m->w_ada, nullptr, kEpiStoreF32, g, st)) != DIT_OK) return rc;
+  }
+  g = base_params(steps, 2 * H, H, err);
+  g.out = w.fin;
+  g.ldo = 2 * H;
+  if ((rc = gemm_launch(w.st, H, m->w_ada_f, nullptr, kEpiStoreF32, g, st)) != DIT_OK) return rc;
+
+  float* txt_rows = w.rows;
+  float* img_rows = w.rows + size_t(L) * H;
+  for (int i = 0; i < steps; ++i) {
+    if (L > 0 && cudaMemcpyAsync(txt_rows, txt_feats, size_t(L) * H * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return DIT_ECUDA;
+    if ((rc = f32_to_bf16_launch(x, w.xin, (long long)N * C, st)) != DIT_OK) return rc;
+    g = base_params(N, H, C, err);
+    g.out = img_rows;
+    g.ldo = H;
+    if ((rc = gemm_launch(w.xin, C, m->w_in, nullptr, kEpiStoreF32, g, st)) != DIT_OK) return rc;
+    for (int b = 0; b < m->blocks; ++b) {
+      const ModRef mod{w.mods + i * SB + 6LL * H * b, nullptr, 1};
+      if ((rc = run_block(d, &m->block[b], nullptr, txt_rows, L, img_rows, N, tc, ts, ic, is, mod, w.block, st)) !=
+          DIT_OK)
+        return rc;
+    }
+    const BlockWs bw = carve_block_ws(d, R, w.block);
+    ModNormParams mp{nullptr, img_rows, 0, N, H, H, H, nullptr, w.fin + 2LL * H * i, w.fin + 2LL * H * i + H, 0,
+                     nullptr, d->eps, bw.h};
+    if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+    g = base_params(N, C, H, err);
+    g.out = w.vel;
+    g.ldo = C;
+    if ((rc = gemm_launch(bw.h, H, m->w_out, nullptr, kEpiStoreF32, g, st)) != DIT_OK) return rc;
+    if ((rc = euler_launch(x, w.vel, (long long)N * C, sigmas[i], sigmas[i + 1], st)) != DIT_OK) return rc;
+  }
+  return DIT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,211 @@
+// HBM-bound row and elementwise kernels: modulated RMSNorm, FlowMatch Euler step, rotary tables,
+// timestep sinusoids, fp32 -> bf16 conversion and the int8lin dequantisation used for checking.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dit {
+namespace {
+
+constexpr int kNormThreads = 256;
+
+// Modulated RMSNorm (the gizai:dit reference's normedInto with its Modulation rows):
+//   h[r] = bf16( x[r] * rsqrt(mean(x[r]^2) + eps) * w * (1 + scale[m]) + shift[m] )
+// one CTA per row, float4 loads, fp32 statistics (klein article, section 2: fp32 RMSNorm -> bf16).
+__global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormParams p) {
+  const int r = blockIdx.x;
+  const float* x = r < p.L ? p.txt + size_t(r) * p.ld_txt : p.img + size_t(r - p.L) * p.ld_img;
+  const int m = p.map ? __ldg(p.map + r) : 0;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  const float4* sh4 = reinterpret_cast<const float4*>(p.shift + size_t(m) * p.mod_stride);
+  const float4* sc4 = reinterpret_cast<const float4*>(p.scale + size_t(m) * p.mod_stride);
+  const float4* w4 = reinterpret_cast<const float4*>(p.w);
+  const int n4 = p.H >> 2;
+
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n4; i += kNormThreads) {
+    const float4 v = x4[i];
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  __shared__ float part[kNormThreads / 32];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
+  const float rstd = rsqrtf(tot / float(p.H) + p.eps);
+
+  uint2* out = reinterpret_cast<uint2*>(p.out + size_t(r) * p.H);
+  for (int i = threadIdx.x; i < n4; i += kNormThreads) {
+    const float4 v = x4[i];
+    const float4 sh = __ldg(sh4 + i);
+    const float4 sc = __ldg(sc4 + i);
+    float4 w = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (w4) w = __ldg(w4 + i);
+    const float y0 = fmaf(v.x * rstd * w.x, 1.f + sc.x, sh.x);
+    const float y1 = fmaf(v.y * rstd * w.y, 1.f + sc.y, sh.y);
+    const float y2 = fmaf(v.z * rstd * w.z, 1.f + sc.z, sh.z);
+    const float y3 = fmaf(v.w * rstd * w.w, 1.f + sc.w, sh.w);
+    out[i] = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+  }
+}
+
+// FlowMatch Euler step (host contract, section 6): x + (sigma_next - sigma) * vel, each operation
+// rounded separately in fp32.
+__global__ void euler_kernel(float* __restrict__ x, const float* __restrict__ vel, long long n, float s0, float s1) {
+  const float dt = __fsub_rn(s1, s0);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    x[i] = __fadd_rn(x[i], __fmul_rn(dt, vel[i]));
+}
+
+__global__ void euler_kernel_v4(float4* __restrict__ x, const float4* __restrict__ vel, long long n4, float s0, float s1) {
+  const float dt = __fsub_rn(s1, s0);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 a = x[i];
+    const float4 v = vel[i];
+    a.x = __fadd_rn(a.x, __fmul_rn(dt, v.x));
+    a.y = __fadd_rn(a.y, __fmul_rn(dt, v.y));
+    a.z = __fadd_rn(a.z, __fmul_rn(dt, v.z));
+    a.w = __fadd_rn(a.w, __fmul_rn(dt, v.w));
+    x[i] = a;
+  }
+}
+
+// Rotary tables (host contract, section 4): positions text i -> (i, i, i), image (y, x) ->
+// (L, y - (h - h/2), x - (w - w/2)); axis widths (16, 56, 56) scaled by d / 128; column k of axis a
+// holds pos_a * theta^(-2k / width_a), evaluated in fp64 and rounded once to fp32.
+__global__ void rope_kernel(int L, int gh, int gw, int d, double theta, float* cos_out, float* sin_out, long long total) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int half = d / 2;
+  const int r = int(idx / half);
+  const int col = int(idx % half);
+  const int w0 = 16 * d / 128, w1 = 56 * d / 128;
+  int axis, k, width;
+  if (col < w0 / 2) {
+    axis = 0; k = col; width = w0;
+  } else if (col < w0 / 2 + w1 / 2) {
+    axis = 1; k = col - w0 / 2; width = w1;
+  } else {
+    axis = 2; k = col - w0 / 2 - w1 / 2; width = w1;
+  }
+  int pos;
+  if (r < L) {
+    pos = r;
+  } else {
+    const int t = r - L, y = t / gw, x = t % gw;
+    pos = axis == 0 ? L : (axis == 1 ? y - (gh - gh / 2) : x - (gw - gw / 2));
+  }
+  const double f = 1.0 / pow(theta, double(2 * k) / double(width));
+  const double ang = double(pos) * f;
+  cos_out[idx] = float(cos(ang));
+  sin_out[idx] = float(sin(ang));
+}
+
+struct SigmaList {
+  float s[64];
+};
+
+// Timestep sinusoids (gizai:dit reference, sinusoids): row i = [cos | sin] of 1000 * t_i times
+// 10000^(-k / (dim/2)), fp64 angles, stored bf16 as the time MLP's input.
+__global__ void sinusoid_kernel(SigmaList sig, int steps, int dim, uint16_t* out) {
+  const int i = blockIdx.x;
+  const int half = dim / 2;
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const double f = pow(10000.0, -double(k) / double(half));
+    const double ang = 1000.0 * double(sig.s[i]) * f;
+    __nv_bfloat16 c = __double2bfloat16(cos(ang));
+    __nv_bfloat16 s = __double2bfloat16(sin(ang));
+    out[size_t(i) * dim + k] = *reinterpret_cast<uint16_t*>(&c);
+    out[size_t(i) * dim + half + k] = *reinterpret_cast<uint16_t*>(&s);
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ in, uint16_t* __restrict__ out, long long n) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    __nv_bfloat16 b = __float2bfloat16_rn(in[i]);
+    out[i] = *reinterpret_cast<uint16_t*>(&b);
+  }
+}
+
+// w[o, i] = bf16_rne(q[o, i] * s[o, i / 32]) with the same instructions as the GEMM converters.
+__global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ s, uint16_t* __restrict__ w,
+                               long long rows, long long cols) {
+  const long long pairs = rows * cols / 2;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
+    const long long e = 2 * i;
+    const long long o = e / cols, c = e % cols;
+    const uint32_t sc = s[o * (cols / 32) + c / 32];
+    const uint32_t b = uint32_t(uint8_t(q[e])) | (uint32_t(uint8_t(q[e + 1])) << 8);
+    const uint32_t v = bf16x2_mul_rn(i8x2_to_bf16x2(b), sc | (sc << 16));
+    reinterpret_cast<uint32_t*>(w)[i] = v;
+  }
+}
+
+int grid_for(long long n, int threads) {
+  long long g = (n + threads - 1) / threads;
+  const long long cap = 8LL * num_sms();
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : int(g);
+}
+
+}  // namespace
+
+int modnorm_launch(const ModNormParams& p, cudaStream_t stream) {
+  if (p.R <= 0) return DIT_OK;
+  modnorm_kernel<<<p.R, kNormThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int euler_launch(float* x, const float* vel, long long n, float sigma, float sigma_next, cudaStream_t stream) {
+  if (n <= 0) return DIT_OK;
+  if (n % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(vel) % 16 == 0) {
+    euler_kernel_v4<<<grid_for(n / 4, 256), 256, 0, stream>>>(reinterpret_cast<float4*>(x),
+                                                              reinterpret_cast<const float4*>(vel), n / 4, sigma,
+                                                              sigma_next);
+  } else {
+    euler_kernel<<<grid_for(n, 256), 256, 0, stream>>>(x, vel, n, sigma, sigma_next);
+  }
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int rope_tables_launch(int L, int gh, int gw, int head_dim, float theta, float* cos, float* sin, cudaStream_t stream) {
+  const long long total = (long long)(L + gh * gw) * (head_dim / 2);
+  if (total <= 0) return DIT_OK;
+  rope_kernel<<<int((total + 255) / 256), 256, 0, stream>>>(L, gh, gw, head_dim, double(theta), cos, sin, total);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int sinusoid_launch(const float* sigmas, int steps, int dim, uint16_t* out, cudaStream_t stream) {
+  if (steps <= 0 || steps > 64) return DIT_EUNSUPPORTED;
+  SigmaList sl{};
+  for (int i = 0; i < steps; ++i) sl.s[i] = sigmas[i];
+  sinusoid_kernel<<<steps, 128, 0, stream>>>(sl, steps, dim, out);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t stream) {
+  if (n <= 0) return DIT_OK;
+  f32_to_bf16_kernel<<<grid_for(n, 256), 256, 0, stream>>>(in, out, n);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long long rows, long long cols,
+                        cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return DIT_OK;
+  dequant_kernel<<<grid_for(rows * cols / 2, 256), 256, 0, stream>>>(q, s, w, rows, cols);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+}  // namespace dit

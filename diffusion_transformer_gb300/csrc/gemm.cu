@@ -1,0 +1,453 @@
+// Persistent warp-specialised tcgen05 GEMM for sm_103a with fused epilogues.
+//
+//   C[M, N] = A[M, K] * B[N, K]^T     A, B bf16 K-major, fp32 accumulators in TMEM
+//
+// One CTA per SM walks output tiles (128 x BN) in a static round-robin order. Warp 0 issues TMA
+// loads of A and B k-blocks (64 wide, 128-byte swizzle) into a STAGES-deep shared-memory ring;
+// warp 1 issues tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators; warps 2-5 drain
+// the other accumulator through the epilogue, so a tile's epilogue overlaps the next tile's
+// mainloop. For int8lin weights (B8 = true) warps 6-9 convert each int8 k-block of B with its bf16
+// block-32 scales into the bf16 swizzled tile the MMA reads: w = bf16_rne(q * s) (the host
+// contract's int8lin scheme, section 1) - the dequantisation sits inside the mainloop.
+//
+// Epilogues (the gizai:dit reference's linearInto / gatedInto / gluRows / prepOf):
+//   kEpiStoreF32 / kEpiStoreBF16 / kEpiSiluBF16   plain stores
+//   kEpiGated   x += gate[map[r]] * acc            (out and down linears)
+//   kEpiSwiGLU  a_j = silu(acc_2j) * acc_2j+1      (up linear, interleaved rows)
+//   kEpiQKV     per-head RMS norm * weight, rotary pairs (2i, 2i+1), head-major q/k stores and a
+//               transposed v store for the attention kernel (klein article, section 4.4)
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace dit {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+
+template <int BN, bool B8>
+struct GemmCfg {
+  static constexpr int kStages = B8 ? (BN == 256 ? 4 : 6) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
+  static constexpr uint32_t kABytes = BM * BK * 2;
+  static constexpr uint32_t kBBytes = BN * BK * 2;   // bf16 tile the MMA reads
+  static constexpr uint32_t kB8Bytes = BN * BK;      // int8 tile TMA writes (B8 only)
+  static constexpr int kConvStages = 2;              // bf16 B tiles produced by the converters
+  static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int kThreads = B8 ? 320 : 192;
+  // smem: [A ring][B ring (bf16, or int8 for B8)][B8: converted bf16 ring][barriers][tmem slot]
+  static constexpr uint32_t kRingBytes = kStages * (kABytes + (B8 ? kB8Bytes : kBBytes));
+  static constexpr uint32_t kConvBytes = B8 ? kConvStages * kBBytes : 0;
+  static constexpr uint32_t kBarBytes = 8 * (2 * kStages + 4 + 2 * kConvStages + 2) + 16;
+  static constexpr uint32_t kSmemBytes = 1024 + kRingBytes + kConvBytes + kBarBytes;
+};
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+    u.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+    u.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+    u.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+    d[c] = u;
+  }
+}
+
+// ----------------------------------------------------------------------------------------------
+// epilogues: one thread owns one output row of the tile; taddr points at (its lane, column n0).
+// tcgen05.ld is warp-collective, so every lane loads even when its row is out of range.
+// ----------------------------------------------------------------------------------------------
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, int row, int n0) {
+  const bool row_ok = row < p.M;
+  if constexpr (EPI == kEpiQKV) {
+    const int d = p.head_dim;
+    const int H = p.H;
+    const int R = p.M;
+    for (int hh = 0; hh < BN / d; ++hh) {
+      const int col0 = n0 + hh * d;
+      const int which = col0 / H;              // 0 = q, 1 = k, 2 = v
+      const int head = (col0 - which * H) / d;
+      const uint32_t ta = taddr + hh * d;
+      if (which == 2) {
+        for (int c = 0; c < d / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(ta + c * 32, v);
+          tmem_ld_wait();
+          if (row_ok) {
+            uint16_t* dst = p.vt + (size_t(head) * d + c * 32) * p.Rp + row;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
+              dst[size_t(j) * p.Rp] = *reinterpret_cast<uint16_t*>(&b);
+            }
+          }
+        }
+        continue;
+      }
+      // pass 1: sum of squares of the head
+      float ss = 0.f;
+      for (int c = 0; c < d / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(ta + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float f = __uint_as_float(v[j]);
+          ss = fmaf(f, f, ss);
+        }
+      }
+      const float rstd = rsqrtf(ss / float(d) + p.qk_eps);
+      const float* wn = which == 0 ? p.q_norm : p.k_norm;
+      const int half = d / 2;
+      const float* cs = row < p.L ? p.txt_cos + size_t(row) * half : p.img_cos + size_t(row - p.L) * half;
+      const float* sn = row < p.L ? p.txt_sin + size_t(row) * half : p.img_sin + size_t(row - p.L) * half;
+      uint16_t* dst = (which == 0 ? p.q : p.k) + (size_t(head) * R + row) * d;
+      // pass 2: normalise, weight, rotate adjacent pairs, store
+      for (int c = 0; c < d / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(ta + c * 32, v);
+        tmem_ld_wait();
+        if (!row_ok) continue;
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float f = __uint_as_float(v[j]) * rstd;
+          if (wn) f *= __ldg(wn + c * 32 + j);
+          y[j] = f;
+        }
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float ci = __ldg(cs + c * 16 + i);
+          const float si = __ldg(sn + c * 16 + i);
+          const float a = y[2 * i], b = y[2 * i + 1];
+          o[2 * i] = a * ci - b * si;
+          o[2 * i + 1] = a * si + b * ci;
+        }
+        store_bf16x32(dst + c * 32, o);
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(taddr + c * 32, v);
+      tmem_ld_wait();
+      if (!row_ok) continue;
+      const int n = n0 + c * 32;
+      if constexpr (EPI == kEpiStoreF32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + size_t(row) * p.ldo + n);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      } else if constexpr (EPI == kEpiStoreBF16 || EPI == kEpiSiluBF16) {
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          f[j] = __uint_as_float(v[j]);
+          if constexpr (EPI == kEpiSiluBF16) f[j] = silu_f(f[j]);
+        }
+        store_bf16x32(static_cast<uint16_t*>(p.out) + size_t(row) * p.ldo + n, f);
+      } else if constexpr (EPI == kEpiSwiGLU) {
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float a0 = silu_f(__uint_as_float(v[4 * j + 0])) * __uint_as_float(v[4 * j + 1]);
+          const float a1 = silu_f(__uint_as_float(v[4 * j + 2])) * __uint_as_float(v[4 * j + 3]);
+          w[j] = pack_bf16x2(a0, a1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + size_t(row) * p.ldo + n / 2);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else if constexpr (EPI == kEpiGated) {
+        float* x = row < p.L ? p.txt + size_t(row) * p.N : p.img + size_t(row - p.L) * p.N;
+        const int m = p.map ? __ldg(p.map + row) : 0;
+        const float4* g = reinterpret_cast<const float4*>(p.gate + size_t(m) * p.gate_stride + n);
+        float4* xv = reinterpret_cast<float4*>(x + n);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 gq = __ldg(g + q);
+          float4 xq = xv[q];
+          xq.x = fmaf(gq.x, __uint_as_float(v[4 * q + 0]), xq.x);
+          xq.y = fmaf(gq.y, __uint_as_float(v[4 * q + 1]), xq.y);
+          xq.z = fmaf(gq.z, __uint_as_float(v[4 * q + 2]), xq.z);
+          xq.w = fmaf(gq.w, __uint_as_float(v[4 * q + 3]), xq.w);
+          xv[q] = xq;
+        }
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------------------------
+// int8 -> bf16 conversion of one k-block of B: int8 tile [BN rows x 64] (row = 64 bytes, unswizzled)
+// into the bf16 128-byte-swizzled tile [BN rows x 64]. Thread t of the 128 converter threads handles
+// rows t, t + 128, ...; per row: 64 int8 values, two bf16 scales (k-block = 2 groups of 32).
+// Each value: q as bf16 is exact (|q| <= 127 has at most 7 significant bits); bf16 x bf16 product
+// rounded once to bf16 (fma.rn.bf16x2 with -0 addend) = bf16_rne(q * s).
+// ----------------------------------------------------------------------------------------------
+// Work item i of the 128 converter threads = (row i / 4, 16-byte chunk i % 4 of that row's int8
+// values): a warp reads 512 consecutive bytes of the int8 tile (no bank conflicts) and writes the
+// two swizzled 16-byte bf16 chunks of its 16 values.
+template <int BN>
+__device__ __forceinline__ void convert_kblock(const uint8_t* src8, uint8_t* dst16, const uint16_t* scales,
+                                               long long scale_ld, int n_row0, int kb, int N, int ct) {
+#pragma unroll 2
+  for (int i = ct; i < BN * 4; i += 128) {
+    const int r = i >> 2, q = i & 3;
+    const int n = n_row0 + r;
+    const uint32_t s = n < N ? uint32_t(__ldg(scales + size_t(n) * scale_ld + 2 * kb + (q >> 1))) : 0u;
+    const uint32_t sx2 = s | (s << 16);
+    const uint4 u = *reinterpret_cast<const uint4*>(src8 + r * 64 + q * 16);
+    const uint32_t words[4] = {u.x, u.y, u.z, u.w};
+    uint32_t outw[8];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      outw[2 * w] = bf16x2_mul_rn(i8x2_to_bf16x2(words[w] & 0xffff), sx2);
+      outw[2 * w + 1] = bf16x2_mul_rn(i8x2_to_bf16x2(words[w] >> 16), sx2);
+    }
+    *reinterpret_cast<uint4*>(dst16 + sw128_offset(r, 2 * q)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+    *reinterpret_cast<uint4*>(dst16 + sw128_offset(r, 2 * q + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+  }
+}
+
+template <int BN, int EPI, bool B8>
+__global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p, const uint16_t* __restrict__ b8_scales) {
+  using Cfg = GemmCfg<BN, B8>;
+  constexpr int S = Cfg::kStages;
+  constexpr int CS = Cfg::kConvStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * Cfg::kABytes;                              // bf16 ring, or int8 ring when B8
+  uint8_t* sC = sB + S * (B8 ? Cfg::kB8Bytes : Cfg::kBBytes);       // B8: converted bf16 ring
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + Cfg::kConvBytes);
+  uint64_t* full = bars;                 // [S] TMA landed
+  uint64_t* empty = bars + S;            // [S] stage free (MMA done; B8: also converter done)
+  uint64_t* tfull = bars + 2 * S;        // [2] accumulator ready
+  uint64_t* tempty = bars + 2 * S + 2;   // [2] accumulator drained
+  uint64_t* cfull = bars + 2 * S + 4;    // [CS] converted B tile ready (B8)
+  uint64_t* cempty = cfull + CS;         // [CS] converted B tile consumed (B8)
+  uint64_t* drain = cempty + CS;         // [1] final MMA completion
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = lane_id();
+  const int num_m = (p.M + BM - 1) / BM;
+  const int num_n = p.N / BN;
+  const int tiles = num_m * num_n;
+  const int KB = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), B8 ? 129 : 1);  // B8: MMA commit + 128 converter threads
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), 128);
+    }
+    for (int c = 0; c < CS; ++c) {
+      mbar_init(smem_u32(&cfull[c]), 128);
+      mbar_init(smem_u32(&cempty[c]), 1);
+    }
+    mbar_init(smem_u32(drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- TMA producer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, last_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        const int mb = tile % num_m, nb = tile / num_m;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, kErrTimeoutProducer)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, Cfg::kABytes + (B8 ? Cfg::kB8Bytes : Cfg::kBBytes));
+          tma_load_2d(smem_u32(sA + stage * Cfg::kABytes), &tmA, fb, kb * BK, mb * BM);
+          if constexpr (B8)
+            tma_load_2d(smem_u32(sB + stage * Cfg::kB8Bytes), &tmB, fb, kb * BK, nb * BN);
+          else
+            tma_load_2d(smem_u32(sB + stage * Cfg::kBBytes), &tmB, fb, kb * BK, nb * BN);
+          issued_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+      }
+      // every issued copy must have landed before the CTA exits
+      for (int s = 0; s < S; ++s)
+        if (issued_mask & (1u << s))
+          mbar_wait(smem_u32(&full[s]), (last_parity >> s) & 1u, p.err, kErrTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int stage = 0, cstage = 0;
+      uint32_t phase = 0, cphase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, p.err, kErrTimeoutMma)) { ok = false; break; }
+          uint32_t b_addr;
+          if constexpr (B8) {
+            if (!mbar_wait(smem_u32(&cfull[cstage]), cphase, p.err, kErrTimeoutMma)) { ok = false; break; }
+            b_addr = smem_u32(sC + cstage * Cfg::kBBytes);
+          } else {
+            b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+          }
+          tc_fence_after();
+          const uint64_t adesc = sw128_desc(smem_u32(sA + stage * Cfg::kABytes));
+          const uint64_t bdesc = sw128_desc(b_addr);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes per K=16 step inside the swizzle atom
+            umma_bf16(d, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc, (kb | kk) != 0);
+          umma_commit(smem_u32(&empty[stage]));
+          if constexpr (B8) {
+            umma_commit(smem_u32(&cempty[cstage]));
+            if (++cstage == CS) { cstage = 0; cphase ^= 1; }
+          }
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[acc]));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      umma_commit(smem_u32(drain));
+      mbar_wait(smem_u32(drain), 0, p.err, kErrTimeoutDrain);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------- epilogue warps 2..5
+    const int quad = warp & 3;  // TMEM lanes this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      const int mb = tile % num_m, nb = tile / num_m;
+      if (!mbar_wait_warp(smem_u32(&tfull[acc]), acc_phase, p.err, kErrTimeoutEpilogue)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
+      epilogue_tile<BN, EPI>(p, taddr, mb * BM + quad * 32 + lane, nb * BN);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tempty[acc]));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  } else if constexpr (B8) {
+    // ------------------------------------------------------------- int8 -> bf16 converters 6..9
+    const int ct = threadIdx.x - 192;
+    int stage = 0, cstage = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      const int nb = tile / num_m;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(smem_u32(&full[stage]), phase, p.err, kErrTimeoutConverter)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&cempty[cstage]), cphase ^ 1, p.err, kErrTimeoutConverter)) { ok = false; break; }
+        convert_kblock<BN>(sB + stage * Cfg::kB8Bytes, sC + cstage * Cfg::kBBytes, b8_scales, p.K / 32, nb * BN,
+                           kb, p.N, ct);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&cfull[cstage]));
+        mbar_arrive(smem_u32(&empty[stage]));  // this thread is done reading the int8 stage
+        if (++cstage == CS) { cstage = 0; cphase ^= 1; }
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+template <int BN, int EPI, bool B8>
+int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, const uint16_t* scales,
+               cudaStream_t stream) {
+  using Cfg = GemmCfg<BN, B8>;
+  static_assert(Cfg::kSmemBytes <= 227 * 1024, "shared memory budget");
+  auto kern = gemm_kernel<BN, EPI, B8>;
+  if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
+  const int tiles = ((p.M + BM - 1) / BM) * (p.N / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, p, scales);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+template <int BN, bool B8>
+int dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                 const uint16_t* scales, cudaStream_t stream) {
+  switch (epi) {
+    case kEpiStoreF32: return launch_one<BN, kEpiStoreF32, B8>(ta, tb, p, scales, stream);
+    case kEpiStoreBF16: return launch_one<BN, kEpiStoreBF16, B8>(ta, tb, p, scales, stream);
+    case kEpiSiluBF16: return launch_one<BN, kEpiSiluBF16, B8>(ta, tb, p, scales, stream);
+    case kEpiGated: return launch_one<BN, kEpiGated, B8>(ta, tb, p, scales, stream);
+    case kEpiSwiGLU: return launch_one<BN, kEpiSwiGLU, B8>(ta, tb, p, scales, stream);
+    case kEpiQKV: return launch_one<BN, kEpiQKV, B8>(ta, tb, p, scales, stream);
+    default: return DIT_EINVAL;
+  }
+}
+
+}  // namespace
+
+int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmInt8B* b8, int epi,
+                const GemmParams& p, cudaStream_t stream) {
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return DIT_EINVAL;
+  if (p.K % BK != 0 || p.N % 64 != 0) return DIT_EUNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(a) % 16 || (lda * 2) % 16) return DIT_EINVAL;
+  // tile width: 256 where it divides N (fewer A re-reads), else 128, else 64
+  int BN = (p.N % 256 == 0) ? 256 : (p.N % 128 == 0 ? 128 : 64);
+  if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K, p.M, lda * 2, BK, BM, true)) return DIT_ECUDA;
+  if (b8) {
+    if (p.K % 32 != 0 || reinterpret_cast<uintptr_t>(b8->q) % 16) return DIT_EINVAL;
+    if (BN == 64) return DIT_EUNSUPPORTED;
+    if (!make_tmap_2d(&tb, b8->q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.K, p.N, p.K, BK, BN, false)) return DIT_ECUDA;
+    return BN == 256 ? dispatch_epi<256, true>(epi, ta, tb, p, b8->s, stream)
+                     : dispatch_epi<128, true>(epi, ta, tb, p, b8->s, stream);
+  }
+  if (reinterpret_cast<uintptr_t>(b) % 16) return DIT_EINVAL;
+  if (!make_tmap_2d(&tb, b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K, p.N, (long long)p.K * 2, BK, BN, true))
+    return DIT_ECUDA;
+  switch (BN) {
+    case 256: return dispatch_epi<256, false>(epi, ta, tb, p, nullptr, stream);
+    case 128: return dispatch_epi<128, false>(epi, ta, tb, p, nullptr, stream);
+    default: return dispatch_epi<64, false>(epi, ta, tb, p, nullptr, stream);
+  }
+}
+
+}  // namespace dit

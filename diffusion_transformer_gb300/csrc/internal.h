@@ -1,0 +1,102 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dit.h"
+
+namespace dit {
+
+// ------------------------------------------------------------------------------------------
+// GEMM: C[M, N] = A[M, K] * B[N, K]^T, A and B bf16 K-major (row-major [rows, K]), fp32 accumulation
+// in TMEM, one of several fused epilogues.
+// ------------------------------------------------------------------------------------------
+enum GemmEpilogue : int {
+  kEpiStoreF32 = 0,     // out fp32 [M, N] (row stride ldo)
+  kEpiStoreBF16 = 1,    // out bf16 [M, N]
+  kEpiSiluBF16 = 2,     // out bf16 silu(acc)
+  kEpiGated = 3,        // x[r, n] += gate[map[r]][n] * acc; x rows < L in txt, others in img (fp32, stride N)
+  kEpiSwiGLU = 4,       // out bf16 [M, N/2]: a_j = silu(acc_{2j}) * acc_{2j+1}
+  kEpiQKV = 5,          // QK-RMSNorm + RoPE on q/k columns -> q, k [heads, R, d]; v -> vt [heads, d, Rp]
+};
+
+struct GemmParams {
+  int M, N, K;
+  int* err;  // device error word
+  // plain stores / swiglu
+  void* out;
+  long long ldo;
+  // gated residual
+  float* txt;
+  float* img;
+  int L;
+  const float* gate;
+  const int32_t* map;  // may be null: gate row 0 for every row
+  long long gate_stride;
+  // qkv epilogue
+  uint16_t* q;
+  uint16_t* k;
+  uint16_t* vt;
+  int H, heads, head_dim, Rp;
+  const float *txt_cos, *txt_sin, *img_cos, *img_sin;  // [L, d/2], [R-L, d/2]
+  const float *q_norm, *k_norm;                         // [d] or null
+  float qk_eps;
+};
+
+// B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights).
+struct GemmInt8B {
+  const int8_t* q;     // [N, K]
+  const uint16_t* s;   // [N, K/32] bf16 bits
+};
+
+// Launch the GEMM. `a` is bf16 [M, K] (row stride lda elements), `b` bf16 [N, K] (stride K) unless
+// `b8` is given. Returns a DIT_* status; checks shapes the kernels support.
+int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmInt8B* b8, int epi,
+                const GemmParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// attention
+// ------------------------------------------------------------------------------------------
+struct AttnParams {
+  int R, heads, head_dim, Rp;
+  const uint16_t *q, *k, *vt;  // [heads, R, d], [heads, R, d], [heads, d, Rp]
+  uint16_t* o;                 // [R, heads * d]
+  int* err;
+};
+int attention_launch(const AttnParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// elementwise / row kernels
+// ------------------------------------------------------------------------------------------
+// h[r] = bf16( x[r] * rsqrt(mean(x[r]^2) + eps) * w * (1 + scale[m]) + shift[m] ), m = map[r] (or 0)
+struct ModNormParams {
+  const float* txt;
+  const float* img;
+  int L, R, H;
+  long long ld_txt, ld_img;  // row strides (elements)
+  const float* w;            // [H] or null
+  const float* shift;        // row m at shift + m * mod_stride
+  const float* scale;
+  long long mod_stride;
+  const int32_t* map;        // [R] or null (row 0)
+  float eps;
+  uint16_t* out;             // [R, H] bf16
+};
+int modnorm_launch(const ModNormParams& p, cudaStream_t stream);
+
+int euler_launch(float* x, const float* vel, long long n, float sigma, float sigma_next, cudaStream_t stream);
+int rope_tables_launch(int L, int gh, int gw, int head_dim, float theta, float* cos, float* sin,
+                       cudaStream_t stream);
+int sinusoid_launch(const float* sigmas, int steps, int dim, uint16_t* out, cudaStream_t stream);
+int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t stream);
+int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long long rows, long long cols,
+                        cudaStream_t stream);
+
+int num_sms();
+
+// Raise a kernel's dynamic shared-memory limit on the current device (once per kernel and device).
+bool smem_attr_once(const void* kernel, unsigned bytes);
+
+}  // namespace dit

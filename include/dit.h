@@ -1,0 +1,248 @@
+/*
+ * dit.h - C ABI of the GB300 (sm_103a) AdaLN diffusion-transformer block library (libdit.so).
+ *
+ * The library computes the forward of one AdaLN DiT block over a packed [text L | image N]
+ * sequence, its int8lin-weight variant, the FlowMatch Euler step and a stacked-block denoise loop,
+ * entirely in CUDA kernels on the caller's stream.
+ *
+ * Sources, cited by page title and section:
+ *   [host contract]  "Host contract - RGBA-Image-2.1-Turbo (Core AI port of Qwen-Image-2.1-Turbo)",
+ *                    sections 1 (DiT graph I/O, int8lin weights), 4 (sequence layout, RoPE tables),
+ *                    5 (latent packing), 6 (FlowMatch Euler sampler).
+ *   [gizai:dit]      the "gizai:dit" module reference: Block.forward, normedInto, linearInto,
+ *                    gatedInto, prepOf, gluRows, weightAt, sinusoids, Modulation, Sequence.
+ *   [klein]          "944 -> 346 ms: optimizing FLUX.2 klein-4B on one TPU v6e chip", sections 2
+ *                    (cast points), 4.3 (flash attention, 1/sqrt(d) in fp32), 4.4 (fused qk prep).
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns every buffer. The
+ *     library allocates nothing on these paths (a one-time 4-byte error word per device aside).
+ *   - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16).
+ *   - Matrices are row-major and densely packed unless a stride is given. Weights are [out, in].
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     Validation happens before any launch: a call that returns an error launched nothing and left
+ *     every output untouched.
+ *   - Calls that share a workspace must not overlap on the device.
+ *   - Device-side waits are bounded: a stuck pipeline sets the device error word, the kernel frees
+ *     what it holds and returns. dit_check() reports it as DIT_ETIMEOUT.
+ */
+#ifndef DIT_H_
+#define DIT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DIT_API __attribute__((visibility("default")))
+#else
+#define DIT_API
+#endif
+
+typedef struct CUstream_st* dit_stream_t; /* same type as cudaStream_t */
+
+/* Status codes. */
+#define DIT_OK 0
+#define DIT_EINVAL (-1)       /* null pointer, bad size, misaligned pointer (16 bytes for TMA operands) */
+#define DIT_EUNSUPPORTED (-2) /* shape outside what the kernels implement (see each call) */
+#define DIT_EWORKSPACE (-3)   /* workspace null or smaller than dit_workspace_bytes() */
+#define DIT_ECUDA (-4)        /* a CUDA launch or runtime call failed */
+#define DIT_ETIMEOUT (-5)     /* a bounded device wait gave up (reported by dit_check) */
+
+/* Block dimensions. hidden H, heads nh, head_dim d = H / nh, ffn F.
+ * Supported: d in {64, 128}; H % 256 == 0; F % 128 == 0. [gizai:dit, Arch] */
+typedef struct {
+  int hidden;
+  int heads;
+  int head_dim;
+  int ffn;
+  float eps;    /* modulated RMSNorm epsilon (1e-6 in every workload) */
+  float qk_eps; /* per-head query/key RMSNorm epsilon */
+} dit_dims;
+
+/* bf16 weights of one block. [gizai:dit, Block (indexes QKV, OUT, UP, DOWN, NORM1, NORM2, Q_NORM, K_NORM)]
+ *   wqkv  [3H, H]: rows all queries, then all keys, then all values; head-major inside each
+ *                  [gizai:dit, weightAt]
+ *   wout  [H, H]
+ *   wup   [2F, H]: gate row j at 2j, up row j at 2j + 1 [gizai:dit, gluRows]
+ *   wdown [H, F]
+ *   norm1, norm2 [H] fp32 affine weights of the two modulated norms, or NULL for ones
+ *   q_norm, k_norm [d] fp32 head-norm weights, or NULL for ones
+ * Weight pointers must be 16-byte aligned. */
+typedef struct {
+  const uint16_t* wqkv;
+  const uint16_t* wout;
+  const uint16_t* wup;
+  const uint16_t* wdown;
+  const float* norm1;
+  const float* norm2;
+  const float* q_norm;
+  const float* k_norm;
+} dit_block_w;
+
+/* int8lin weights of one block [host contract, section 1]: each linear (0 qkv, 1 out, 2 up, 3 down)
+ * as symmetric int8 values q [out, in] and one bf16 scale per 32 consecutive input elements
+ * s [out, in / 32]; the weight is W[o, i] = bf16_rne(q[o, i] * s[o, i / 32]). Row orders as in
+ * dit_block_w. Norm weights as in dit_block_w. */
+typedef struct {
+  const int8_t* q[4];
+  const uint16_t* s[4];
+  const float* norm1;
+  const float* norm2;
+  const float* q_norm;
+  const float* k_norm;
+} dit_block_w8;
+
+/* Modulation rows [gizai:dit, Modulation and Sequence.map]: rows [M, 6, H] fp32 holding, for each
+ * modulation row, shift_a, scale_a, gate_a (attention) then shift_m, scale_m, gate_m (MLP).
+ * map [L + N] int32 gives each packed row's modulation row (0 <= map[r] < M); NULL means row 0. */
+typedef struct {
+  const float* rows;
+  const int32_t* map;
+  int M;
+} dit_mod;
+
+/* ---------------------------------------------------------------------------------------------
+ * Whole-block forward [gizai:dit, Block.forward]. For packed rows r = 0..L+N-1 (row r < L is
+ * txt[r], else img[r - L]) and m = map[r]:
+ *   h  = modnorm(x; norm1, shift_a, scale_a)      x * rsqrt(mean(x^2) + eps) * w * (1 + scale) + shift
+ *   q,k,v = h Wqkv^T; per head q,k <- rmsnorm(.) * q_norm/k_norm, then rotated in adjacent pairs
+ *           (2i, 2i+1) by the row's angle i (cos/sin tables) [host contract, section 4]
+ *   o  = softmax(q k^T / sqrt(d)) v over all L+N rows, per head (no mask) [klein, section 4.3]
+ *   x += gate_a * (o Wout^T)                      [gizai:dit, gatedInto]
+ *   h2 = modnorm(x; norm2, shift_m, scale_m)
+ *   x += gate_m * ((silu(h2 Wup_gate^T) * (h2 Wup_up^T)) Wdown^T)
+ * txt [L, H] and img [N, H] fp32 are the residual stream, updated in place. L >= 0, N >= 1.
+ * txt_cos/txt_sin [L, d/2] and img_cos/img_sin [N, d/2] fp32 are the per-row rotary tables
+ * (dit_rope_tables builds them). GEMM operands are bf16 with fp32 accumulation; norms, softmax and
+ * residual updates are fp32. ws: device workspace of at least dit_workspace_bytes(dims, L, N, 0)
+ * bytes, 256-byte aligned. Errors: DIT_EINVAL, DIT_EUNSUPPORTED, DIT_EWORKSPACE, DIT_ECUDA.
+ * ------------------------------------------------------------------------------------------- */
+DIT_API int dit_block_forward(const dit_dims* dims, const dit_block_w* w, float* txt, int L, float* img, int N,
+                      const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
+                      const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* The same block with int8lin weights [host contract, section 1]: each linear's weight tile is
+ * dequantized to bf16_rne(q * s) inside the GEMM (the MMA then runs in bf16). Requires
+ * in % 32 == 0 for every linear. Workspace: dit_workspace_bytes(dims, L, N, 1). */
+DIT_API int dit_block_forward_int8(const dit_dims* dims, const dit_block_w8* w, float* txt, int L, float* img, int N,
+                           const float* txt_cos, const float* txt_sin, const float* img_cos,
+                           const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                           dit_stream_t stream);
+
+/* FlowMatch Euler step [host contract, section 6]: x[i] <- x[i] + (sigma_next - sigma) * vel[i],
+ * each operation rounded separately in fp32 (no fused multiply-add). n >= 0. */
+DIT_API int dit_euler_step(float* x, const float* vel, int64_t n, float sigma, float sigma_next, dit_stream_t stream);
+
+/* Per-row rotary tables [host contract, section 4] for the packed sequence of L text tokens and an
+ * h x w image grid: text token i at position (i, i, i), image token (y, x) at
+ * (L, y - (h - h/2), x - (w - w/2)). Axis widths (16, 56, 56) for d = 128, (8, 28, 28) for d = 64;
+ * column k of axis a holds the angle pos_a * theta^(-2k / width_a), evaluated in fp64 and rounded
+ * once to fp32. cos, sin: device [L + h*w, d/2] fp32 (text rows first). */
+DIT_API int dit_rope_tables(int L, int grid_h, int grid_w, int head_dim, float theta, float* cos, float* sin,
+                    dit_stream_t stream);
+
+/* Denoise model: the 32 (or `blocks`) stacked blocks plus the plain DiT around them.
+ *   w_in   [H, C] bf16    patch-in of the packed latent tokens (C = latent_channels)
+ *   w_t1   [H, 256] bf16  time MLP first linear;  w_t2 [H, H] bf16 second linear
+ *   w_ada  [blocks, 6H, H] bf16  per-block modulation linear (shift_a, scale_a, gate_a, shift_m,
+ *                                scale_m, gate_m); w_ada_f [2H, H] final norm (shift, scale)
+ *   w_out  [C, H] bf16    patch-out to velocity
+ *   block  [blocks]       the blocks' linears and norm weights (host array of device pointers)
+ * No biases. Time embedding: temb = w_t2 silu(w_t1 [cos | sin](1000 t f_k)), f_k = 10000^(-k/128)
+ * [gizai:dit, sinusoids]; every modulation is computed from silu(temb) with M = 1. */
+typedef struct {
+  dit_dims dims;
+  int blocks;
+  int latent_channels;
+  const uint16_t* w_in;
+  const uint16_t* w_t1;
+  const uint16_t* w_t2;
+  const uint16_t* w_ada;
+  const uint16_t* w_ada_f;
+  const uint16_t* w_out;
+  const dit_block_w* block; /* HOST array of `blocks` descriptors */
+} dit_model;
+
+/* Full denoise loop [host contract, section 6] for `steps` Euler steps over sigmas[0..steps]
+ * (HOST array, fp32): for each step i with t = sigmas[i], rows = [txt_feats ; x w_in^T] go through
+ * every block, vel = modnorm(image rows; shift_f, scale_f) w_out^T, then
+ * x <- x + (sigmas[i+1] - sigmas[i]) vel in fp32. x (img_tokens [N, C] fp32, device) holds the
+ * packed noise on entry and the result on return. txt_feats [L, H] fp32. Rotary tables as in
+ * dit_block_forward. The step-invariant work (time embeddings and every block's modulation for all
+ * steps) is computed once up front. Workspace: dit_denoise_workspace_bytes(). */
+DIT_API int dit_denoise(const dit_model* model, float* img_tokens, int N, const float* txt_feats, int L,
+                const float* sigmas, int steps, const float* txt_cos, const float* txt_sin,
+                const float* img_cos, const float* img_sin, void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block. Returns 0 for unsupported dims. */
+DIT_API size_t dit_workspace_bytes(const dit_dims* dims, int L, int N, int variant);
+DIT_API size_t dit_denoise_workspace_bytes(const dit_model* model, int L, int N, int steps);
+
+/* Step-level entry points: each runs one step of the block forward on its own. The whole-block
+ * calls above are sequences of these. ------------------------------------------------------ */
+
+/* Modulated RMSNorm [gizai:dit, normedInto]: h[r] = bf16(x[r] * rsqrt(mean(x[r]^2) + eps) * w *
+ * (1 + scale) + shift) with shift/scale the attention (which = 0) or MLP (which = 1) pair of
+ * modulation row map[r]. h [L + N, H] bf16. w [H] or NULL. */
+DIT_API int dit_modnorm(const dit_dims* dims, const float* txt, int L, const float* img, int N, const float* w,
+                const dit_mod* mod, int which, uint16_t* h, dit_stream_t stream);
+
+/* QKV linear with its fused epilogue [gizai:dit, prepOf; klein, section 4.4]: qkv = h Wqkv^T;
+ * q and k heads RMS-normed (times q_norm / k_norm, NULL = ones) then rotated by the tables;
+ * stored bf16 as q, k [heads, R, d] (R = L + N) and v transposed as vt [heads, d, Rp] with
+ * Rp = dit_vt_stride(R) (columns >= R unused). h [R, H] bf16. */
+DIT_API int dit_qkv_rope(const dit_dims* dims, const uint16_t* h, int L, int N, const uint16_t* wqkv,
+                 const float* q_norm, const float* k_norm, const float* txt_cos, const float* txt_sin,
+                 const float* img_cos, const float* img_sin, uint16_t* q, uint16_t* k, uint16_t* vt,
+                 dit_stream_t stream);
+DIT_API int dit_vt_stride(int R);
+
+/* Joint attention [klein, section 4.3]: o[r, n*d + j] = sum_c softmax_c(q_n[r] . k_n[c] / sqrt(d))
+ * vt_n[j, c] over all R rows, bf16 out [R, heads * d]. Layouts as dit_qkv_rope writes them. */
+DIT_API int dit_attention(const dit_dims* dims, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
+                  uint16_t* o, dit_stream_t stream);
+
+/* Linear with gated residual [gizai:dit, gatedInto]: x[r] += gate[map[r]] * (a[r] W^T) for the
+ * attention (which = 0, W = wout [H, H], a [R, H]) or the MLP (which = 1, W = wdown [H, F],
+ * a [R, F]) gate of the modulation rows. x rows < L in txt, others in img. */
+DIT_API int dit_linear_gated(const dit_dims* dims, const uint16_t* a, int L, int N, const uint16_t* w,
+                     const dit_mod* mod, int which, float* txt, float* img, dit_stream_t stream);
+
+/* Up linear with SwiGLU epilogue [gizai:dit, gluRows]: u = h2 Wup^T [R, 2F];
+ * a[r, j] = bf16(silu(u[r, 2j]) * u[r, 2j+1]) [R, F]. */
+DIT_API int dit_linear_swiglu(const dit_dims* dims, const uint16_t* h2, int R, const uint16_t* wup, uint16_t* a,
+                      dit_stream_t stream);
+
+/* Plain linear: out = a W^T with a [M, K] bf16, W [N, K] bf16; out fp32 (out_bf16 = 0) or bf16
+ * (out_bf16 = 1), [M, N]. Supports K % 64 == 0 and N % 64 == 0. */
+DIT_API int dit_linear(const uint16_t* a, int M, int K, const uint16_t* w, int N, void* out, int out_bf16,
+               dit_stream_t stream);
+
+/* int8lin dequantisation [host contract, section 1]: w[o, i] = bf16_rne(q[o, i] * s[o, i/32]),
+ * the same arithmetic the int8 GEMM mainloop performs. cols % 32 == 0. */
+DIT_API int dit_dequant_int8(const int8_t* q, const uint16_t* s, int64_t rows, int64_t cols, uint16_t* w,
+                     dit_stream_t stream);
+
+/* Plain linear with int8lin weights: out fp32 [M, N] = a W^T with W dequantized in the mainloop. */
+DIT_API int dit_linear_int8(const uint16_t* a, int M, int K, const int8_t* wq, const uint16_t* ws_scales, int N,
+                    float* out, dit_stream_t stream);
+
+/* Synchronize `stream` and read (then clear) the device error word of the current device:
+ * DIT_OK, DIT_ETIMEOUT, or DIT_ECUDA if the stream reported an error. */
+DIT_API int dit_check(dit_stream_t stream);
+
+/* Static description of a status code. */
+DIT_API const char* dit_status_string(int status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+DIT_API int dit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIT_H_ */

@@ -1,0 +1,149 @@
+"""Whole-block parity of the CUDA path (dit_block_forward / dit_block_forward_int8 through the C ABI)
+against the float64 oracle on the same seeded inputs.
+
+Gates (written here, derived in the design notes):
+* the stated bar: max |out_gpu - out_ref| <= 2e-2 * RMS(out_ref);
+* a stricter gate on the block's own contribution delta = out - in (the residual input dominates
+  RMS(out), so the first gate alone would let a wrong branch through):
+  RMS(delta_gpu - delta_ref) <= 1e-2 * RMS(delta_ref) and max |.| <= 8e-2 * RMS(delta_ref).
+  The GPU rounds every GEMM operand (h, q, k, v, P, o, h2, a) to bf16 (relative 2^-9 each);
+  with about eight such roundings feeding each output the relative RMS error of delta is a few
+  times 2^-9 ~ 4e-3, and the maximum over ~10^7 outputs sits near 5 standard deviations.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import dit_inputs as DI
+import diffusion_transformer_gb300 as D
+import oracle as O
+from tests.gpu_util import (block_weights_dev, dev, dev_bf16, dims_of, int8_weights_dev, max_abs, modulation_dev,
+                            rms, rope_dev, run_block_gpu, workspace)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(got, ref, x_in, label):
+    d_got, d_ref = got - x_in, ref - x_in
+    e_out = max_abs(got, ref) / rms(ref)
+    e_rms = rms(d_got - d_ref) / rms(d_ref)
+    e_max = max_abs(d_got, d_ref) / rms(d_ref)
+    print(f"{label}: max|out err|/RMS(out) = {e_out:.3e}; delta: RMS err {e_rms:.3e}, max err {e_max:.3e}")
+    assert e_out <= 2e-2, label
+    assert e_rms <= 1e-2, label
+    assert e_max <= 8e-2, label
+
+
+@pytest.mark.parametrize("M,nw", [(None, False), (2, True), (1, False)])
+def test_tiny_block_all_rows(M, nw):
+    inp = DI.block_inputs("tiny", M=M, norm_weights=nw)
+    t, i = run_block_gpu(inp)
+    rt, ri = O.block_forward(inp)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)
+    _check(np.concatenate([t, i]), np.concatenate([rt, ri]), x_in, f"tiny M={M} norm_weights={nw}")
+
+
+def test_zero_gates_leave_residual_bitwise():
+    inp = DI.block_inputs("512sq")
+    inp.mod[:, 2, :] = 0.0
+    inp.mod[:, 5, :] = 0.0
+    t, i = run_block_gpu(inp)
+    assert np.array_equal(t, inp.txt.astype(np.float64)) and np.array_equal(i, inp.img.astype(np.float64))
+
+
+def _sample_rows(sh, n=48, seed=0):
+    g = np.random.default_rng(seed)
+    R = sh.R
+    must = [0, sh.L - 1, sh.L, R - 1, R - 2] + list(range((R // 128) * 128, R))[:8]
+    rows = np.unique(np.concatenate([np.array([r for r in must if 0 <= r < R]), g.choice(R, n, replace=False)]))
+    return rows
+
+
+@pytest.mark.parametrize("shape", ["512sq", "1024sq"])
+def test_block_sampled_rows(shape):
+    inp = DI.block_inputs(shape)
+    sh = inp.shape
+    t, i = run_block_gpu(inp)
+    got = np.concatenate([t, i])
+    rows = _sample_rows(sh)
+    ref = O.block_forward(inp, rows=rows)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)[rows]
+    _check(got[rows], ref, x_in, f"{shape} sampled rows")
+
+
+def test_block_deterministic():
+    inp = DI.block_inputs("512sq")
+    a = run_block_gpu(inp)
+    b = run_block_gpu(inp)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_int8_block_tiny_vs_oracle():
+    inp = DI.int8_block_inputs(DI.SHAPES["tiny"], seed=3)
+    t, i = run_block_gpu(inp, int8=True)
+    W = tuple(O.bf16_to_f64(O.dequant_int8(q, s)) for q, s in zip(inp.q8, inp.s8))
+    rt, ri = O.block_forward(inp, weights=W)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)
+    _check(np.concatenate([t, i]), np.concatenate([rt, ri]), x_in, "tiny int8")
+
+
+@pytest.mark.parametrize("shape", ["tiny", "512sq"])
+def test_int8_block_bitwise_equals_bf16_block_on_dequantized_weights(shape):
+    inp = DI.int8_block_inputs(DI.SHAPES[shape], seed=3)
+    t8, i8 = run_block_gpu(inp, int8=True)
+    sh = inp.shape
+    deq = []
+    for q, s in zip(inp.q8, inp.s8):
+        w = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+        D.dit_dequant_int8(dev(q), dev_bf16(s), w)
+        deq.append(w)
+    dims = dims_of(sh)
+    txt, img = dev(inp.txt), dev(inp.img)
+    tc, ts, ic, is_ = rope_dev(sh)
+    ws = workspace(D.dit_workspace_bytes(dims, sh.L, sh.N, 0))
+    D.dit_block_forward(dims, D.BlockWeights(*deq), txt, img, tc, ts, ic, is_, modulation_dev(inp), ws)
+    D.dit_check()
+    assert np.array_equal(t8, txt.cpu().numpy().astype(np.float64))
+    assert np.array_equal(i8, img.cpu().numpy().astype(np.float64))
+
+
+def test_int8_block_full_size_sampled_rows():
+    inp = DI.int8_block_inputs("1024sq_int8")
+    sh = inp.shape
+    t, i = run_block_gpu(inp, int8=True)
+    got = np.concatenate([t, i])
+    rows = _sample_rows(sh, seed=1)
+    W = tuple(O.bf16_to_f64(O.dequant_int8(q, s)) for q, s in zip(inp.q8, inp.s8))
+    ref = O.block_forward(inp, weights=W, rows=rows)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)[rows]
+    _check(got[rows], ref, x_in, "1024sq int8 sampled rows")
+
+
+def test_block_no_text_rows():
+    sh = DI.BlockShape("img_only", 256, 4, 64, 768, 0, 9, 9, seed=7)
+    inp = DI.block_inputs(sh)
+    t, i = run_block_gpu(inp)
+    _, ri = O.block_forward(inp)
+    _check(i, ri, inp.img.astype(np.float64), "no text rows, N=81")
+
+
+def test_abi_rejects_bad_arguments_without_touching_outputs():
+    inp = DI.block_inputs("tiny")
+    sh = inp.shape
+    dims = dims_of(sh)
+    txt, img = dev(inp.txt), dev(inp.img)
+    tc, ts, ic, is_ = rope_dev(sh)
+    w = block_weights_dev(inp)
+    mod = modulation_dev(inp)
+    need = D.dit_workspace_bytes(dims, sh.L, sh.N, 0)
+    small = workspace(need - 256)
+    with pytest.raises(D.DitError) as e:
+        D.dit_block_forward(dims, w, txt, img, tc, ts, ic, is_, mod, small)
+    assert e.value.status == D.DIT_EWORKSPACE
+    bad = D.DitDims(sh.hidden, sh.heads, 96, sh.ffn)
+    with pytest.raises(D.DitError) as e:
+        D.dit_block_forward(bad, w, txt, img, tc, ts, ic, is_, mod, workspace(need))
+    assert e.value.status == D.DIT_EUNSUPPORTED
+    D.dit_check()
+    assert np.array_equal(txt.cpu().numpy(), inp.txt) and np.array_equal(img.cpu().numpy(), inp.img)

@@ -1,0 +1,274 @@
+"""Step-level parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerances, derived from the arithmetic of each kernel:
+* fp32-accumulated bf16 products over K terms: |err| <= 4e-5 * sum_k |a_k w_k| (well above the
+  typical sqrt(K) * 2^-24 and far below any structural mistake);
+* a bf16-rounded output adds half a bf16 ulp: rtol 2^-8;
+* attention rounds P to bf16 (relative 2^-9 per weight) and the output to bf16:
+  |err| <= 2^-8 * max|v| + 2^-8 |o|;
+* bit-exact where both sides perform the same IEEE operations: Euler step (separately rounded
+  fp32), int8lin dequantisation (one rounding of an exact product), rotary tables (fp64 angle,
+  one rounding to fp32).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import dit_inputs as DI
+import diffusion_transformer_gb300 as D
+import oracle as O
+from tests.gpu_util import (bf16_bits, bf16_f64, dev, dev_bf16, dims_of, max_abs, rope_dev, workspace)
+
+pytestmark = pytest.mark.gpu
+
+GEMM_RTOL = 4e-5
+
+
+def _bf16_rand(g, shape, std):
+    return DI.bf16_bits_from_f32(g.standard_normal(shape, dtype=np.float32) * np.float32(std))
+
+
+def _gemm_bound(A, W):
+    return np.abs(A) @ np.abs(W).T
+
+
+# ---------------------------------------------------------------------------------- Euler
+
+@pytest.mark.parametrize("n", [1, 7, 4096 * 64, 4096 * 64 + 3])
+def test_euler_bit_exact(n):
+    g = np.random.default_rng(n)
+    sig = [1.0, 0.978453, 0.95418, 0.926626, 0.89508, 0.845148, 0.704534, 0.414568, 0.0]
+    x = g.standard_normal(n).astype(np.float32)
+    v = g.standard_normal(n).astype(np.float32)
+    xd, vd = dev(x), dev(v)
+    for i in range(8):
+        D.dit_euler_step(xd, vd, sig[i], sig[i + 1])
+        x = O.euler_step(x, v, np.float32(sig[i]), np.float32(sig[i + 1]))
+    D.dit_check()
+    assert np.array_equal(xd.cpu().numpy().view(np.uint32), x.view(np.uint32))
+
+
+def test_euler_empty_is_noop():
+    D.dit_euler_step(torch.empty(0, device="cuda"), torch.empty(0, device="cuda"), 1.0, 0.5)
+    D.dit_check()
+
+
+# ---------------------------------------------------------------------------------- rotary tables
+
+@pytest.mark.parametrize("shape", ["tiny", "512sq", "1024sq", "denoise"])
+def test_rope_tables_match_oracle(shape):
+    sh = DI.SHAPES[shape]
+    tc, ts, ic, is_ = rope_dev(sh)
+    cos, sin = O.rope_tables(O.positions(sh.L, sh.grid_h, sh.grid_w), sh.head_dim)
+    got_c = np.concatenate([tc.cpu().numpy(), ic.cpu().numpy()])
+    got_s = np.concatenate([ts.cpu().numpy(), is_.cpu().numpy()])
+    # fp64 angle rounded once to fp32 on both sides: equal unless the two fp64 libm results straddle
+    # an fp32 rounding boundary (then one fp32 ulp)
+    diff_c = np.abs(got_c.view(np.int32).astype(np.int64) - cos.view(np.int32).astype(np.int64))
+    diff_s = np.abs(got_s.view(np.int32).astype(np.int64) - sin.view(np.int32).astype(np.int64))
+    assert diff_c.max() <= 1 and diff_s.max() <= 1
+    assert (diff_c > 0).mean() < 1e-4 and (diff_s > 0).mean() < 1e-4
+
+
+# ---------------------------------------------------------------------------------- modulated norm
+
+@pytest.mark.parametrize("shape,M,nw", [("tiny", None, False), ("tiny", 2, True), ("tiny", 1, False),
+                                        ("512sq", None, True)])
+@pytest.mark.parametrize("which", [0, 1])
+def test_modnorm(shape, M, nw, which):
+    inp = DI.block_inputs(shape, M=M, norm_weights=nw)
+    sh = inp.shape
+    dims = dims_of(sh)
+    h = torch.empty(sh.R, sh.hidden, dtype=torch.bfloat16, device="cuda")
+    w = inp.norm1 if which == 0 else inp.norm2
+    D.dit_modnorm(dims, dev(inp.txt), dev(inp.img), None if w is None else dev(w),
+                  D.Modulation(dev(inp.mod), dev(inp.mod_map)), which, h)
+    D.dit_check()
+    x = np.concatenate([inp.txt, inp.img]).astype(np.float64)
+    m = inp.mod[inp.mod_map]
+    ref = O.modulated_rmsnorm(x, w, m[:, 3 * which], m[:, 3 * which + 1], sh.eps)
+    np.testing.assert_allclose(bf16_f64(h), ref, rtol=2 ** -8, atol=1e-5)
+
+
+def test_modnorm_no_text_rows():
+    inp = DI.block_inputs("tiny")
+    sh = inp.shape
+    h = torch.empty(sh.N, sh.hidden, dtype=torch.bfloat16, device="cuda")
+    mod = inp.mod[sh.L:]
+    D.dit_modnorm(dims_of(sh), None, dev(inp.img), None, D.Modulation(dev(mod), dev(np.arange(sh.N, dtype=np.int32))),
+                  0, h)
+    D.dit_check()
+    ref = O.modulated_rmsnorm(inp.img.astype(np.float64), None, mod[:, 0], mod[:, 1], sh.eps)
+    np.testing.assert_allclose(bf16_f64(h), ref, rtol=2 ** -8, atol=1e-5)
+
+
+# ---------------------------------------------------------------------------------- int8 dequant
+
+def test_dequant_bit_exact():
+    g = np.random.default_rng(3)
+    q = g.integers(-127, 128, size=(96, 4096), dtype=np.int8)
+    q[0, :255] = np.arange(-127, 128, dtype=np.int8)       # every code value
+    s = DI.bf16_bits_from_f32((DI.INT8_S0 * (0.75 + 0.5 * g.random((96, 128)))).astype(np.float32))
+    s[1, :] = DI.bf16_bits_from_f32(np.float32(1.0 + 2 ** -7) * np.ones(128, np.float32))  # ties appear
+    w = torch.empty(96, 4096, dtype=torch.bfloat16, device="cuda")
+    D.dit_dequant_int8(dev(q), dev_bf16(s), w)
+    D.dit_check()
+    assert np.array_equal(bf16_bits(w), O.dequant_int8(q, s))
+
+
+# ---------------------------------------------------------------------------------- plain GEMM
+
+@pytest.mark.parametrize("M,N,K", [(72, 256, 256), (128, 128, 64), (200, 64, 128), (1088, 768, 3072),
+                                   (4, 3072, 256), (333, 512, 1024), (4224, 256, 3072)])
+def test_linear_f32(M, N, K):
+    g = np.random.default_rng(M + N + K)
+    A = _bf16_rand(g, (M, K), 1.0)
+    W = _bf16_rand(g, (N, K), 0.02)
+    out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    D.dit_linear(dev_bf16(A), dev_bf16(W), out)
+    D.dit_check()
+    Af, Wf = O.bf16_to_f64(A), O.bf16_to_f64(W)
+    ref = Af @ Wf.T
+    err = np.abs(out.cpu().numpy() - ref)
+    assert np.all(err <= GEMM_RTOL * _gemm_bound(Af, Wf) + 1e-30), float(err.max())
+
+
+def test_linear_bf16_out_and_identity_exact():
+    g = np.random.default_rng(11)
+    M, K = 300, 256
+    A = _bf16_rand(g, (M, K), 1.0)
+    I = DI.bf16_bits_from_f32(np.eye(K, dtype=np.float32))
+    out = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    D.dit_linear(dev_bf16(A), dev_bf16(I), out)
+    out32 = torch.empty(M, K, dtype=torch.float32, device="cuda")
+    D.dit_linear(dev_bf16(A), dev_bf16(I), out32)
+    D.dit_check()
+    assert np.array_equal(bf16_bits(out), A)                       # A I = A exactly
+    assert np.array_equal(out32.cpu().numpy(), O.bf16_to_f64(A).astype(np.float32))
+
+
+@pytest.mark.parametrize("M,N,K", [(72, 256, 256), (1088, 384, 3072), (130, 128, 12288)])
+def test_linear_int8_vs_oracle_and_bitwise_vs_dequant(M, N, K):
+    g = np.random.default_rng(M * 7 + N)
+    A = _bf16_rand(g, (M, K), 1.0)
+    q = g.integers(-127, 128, size=(N, K), dtype=np.int8)
+    s = DI.bf16_bits_from_f32((DI.INT8_S0 * (0.75 + 0.5 * g.random((N, K // 32)))).astype(np.float32))
+    out8 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    D.dit_linear_int8(dev_bf16(A), dev(q), dev_bf16(s), out8)
+    wd = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+    D.dit_dequant_int8(dev(q), dev_bf16(s), wd)
+    out16 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    D.dit_linear(dev_bf16(A), wd, out16)
+    D.dit_check()
+    # the int8 mainloop feeds the MMA the same bf16 tile as dequant + bf16 GEMM: bitwise equal
+    assert torch.equal(out8, out16)
+    Af, Wf = O.bf16_to_f64(A), O.bf16_to_f64(O.dequant_int8(q, s))
+    err = np.abs(out8.cpu().numpy() - Af @ Wf.T)
+    assert np.all(err <= GEMM_RTOL * _gemm_bound(Af, Wf) + 1e-30), float(err.max())
+
+
+# ---------------------------------------------------------------------------------- fused epilogues
+
+@pytest.mark.parametrize("shape,R", [("tiny", 72), ("512sq", 1088), ("512sq", 200)])
+def test_swiglu_epilogue(shape, R):
+    sh = DI.SHAPES[shape]
+    g = np.random.default_rng(R)
+    H, F = sh.hidden, sh.ffn
+    h2 = _bf16_rand(g, (R, H), 1.0)
+    wup = _bf16_rand(g, (2 * F, H), 0.02)
+    a = torch.empty(R, F, dtype=torch.bfloat16, device="cuda")
+    D.dit_linear_swiglu(dims_of(sh), dev_bf16(h2), dev_bf16(wup), a)
+    D.dit_check()
+    u = O.bf16_to_f64(h2) @ O.bf16_to_f64(wup).T
+    ref = O.swiglu_interleaved(u)
+    np.testing.assert_allclose(bf16_f64(a), ref, rtol=2 ** -8, atol=2e-4)
+
+
+@pytest.mark.parametrize("shape,M,which", [("tiny", None, 0), ("tiny", 2, 1), ("512sq", None, 0), ("512sq", 1, 1)])
+def test_gated_epilogue(shape, M, which):
+    inp = DI.block_inputs(shape, M=M)
+    sh = inp.shape
+    g = np.random.default_rng(5)
+    K = sh.hidden if which == 0 else sh.ffn
+    A = _bf16_rand(g, (sh.R, K), 1.0)
+    W = inp.wout if which == 0 else inp.wdown
+    txt, img = dev(inp.txt), dev(inp.img)
+    D.dit_linear_gated(dims_of(sh), dev_bf16(A), sh.L, sh.N, dev_bf16(W), D.Modulation(dev(inp.mod), dev(inp.mod_map)),
+                       which, txt, img)
+    D.dit_check()
+    Af, Wf = O.bf16_to_f64(A), O.bf16_to_f64(W)
+    gate = inp.mod[inp.mod_map, 2 if which == 0 else 5].astype(np.float64)
+    x = np.concatenate([inp.txt, inp.img]).astype(np.float64)
+    ref = x + gate * (Af @ Wf.T)
+    got = np.concatenate([txt.cpu().numpy(), img.cpu().numpy()]).astype(np.float64)
+    tol = GEMM_RTOL * np.abs(gate) * _gemm_bound(Af, Wf) + 2 ** -23 * np.abs(ref) + 1e-30
+    assert np.all(np.abs(got - ref) <= tol), float(np.abs(got - ref).max())
+
+
+@pytest.mark.parametrize("shape,nw", [("tiny", False), ("tiny", True), ("512sq", True)])
+def test_qkv_rope_epilogue(shape, nw):
+    inp = DI.block_inputs(shape, norm_weights=nw)
+    sh = inp.shape
+    R, H, nh, d = sh.R, sh.hidden, sh.heads, sh.head_dim
+    g = np.random.default_rng(8)
+    h = _bf16_rand(g, (R, H), 1.0)
+    q = torch.empty(nh, R, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty_like(q)
+    Rp = D.dit_vt_stride(R)
+    vt = torch.zeros(nh, d, Rp, dtype=torch.bfloat16, device="cuda")
+    tc, ts, ic, is_ = rope_dev(sh)
+    qn = None if inp.q_norm is None else dev(inp.q_norm)
+    kn = None if inp.k_norm is None else dev(inp.k_norm)
+    D.dit_qkv_rope(dims_of(sh), dev_bf16(h), sh.L, sh.N, dev_bf16(inp.wqkv), qn, kn, tc, ts, ic, is_, q, k, vt)
+    D.dit_check()
+    qkv = O.bf16_to_f64(h) @ O.bf16_to_f64(inp.wqkv).T
+    cos, sin = O.rope_tables(O.positions(sh.L, sh.grid_h, sh.grid_w), d)
+    rq = O.rope_apply(O.qk_rmsnorm(qkv[:, :H].reshape(R, nh, d), inp.q_norm, sh.qk_eps), cos, sin)
+    rk = O.rope_apply(O.qk_rmsnorm(qkv[:, H:2 * H].reshape(R, nh, d), inp.k_norm, sh.qk_eps), cos, sin)
+    rv = qkv[:, 2 * H:].reshape(R, nh, d)
+    np.testing.assert_allclose(bf16_f64(q), rq.transpose(1, 0, 2), rtol=2 ** -8, atol=1e-3)
+    np.testing.assert_allclose(bf16_f64(k), rk.transpose(1, 0, 2), rtol=2 ** -8, atol=1e-3)
+    np.testing.assert_allclose(bf16_f64(vt)[:, :, :R], rv.transpose(1, 2, 0), rtol=2 ** -8, atol=1e-4)
+
+
+# ---------------------------------------------------------------------------------- attention
+
+def _attn_case(R, nh, d, seed, qscale=1.0):
+    g = np.random.default_rng(seed)
+    q = _bf16_rand(g, (nh, R, d), qscale)
+    k = _bf16_rand(g, (nh, R, d), 1.0)
+    v = _bf16_rand(g, (nh, R, d), 1.0)
+    return q, k, v
+
+
+@pytest.mark.parametrize("R,nh,d", [(72, 4, 64), (128, 2, 128), (200, 2, 128), (1088, 2, 128), (257, 4, 64),
+                                    (4224, 2, 128)])
+@pytest.mark.parametrize("qscale", [1.0, 0.05])
+def test_attention_vs_oracle(R, nh, d, qscale):
+    q, k, v = _attn_case(R, nh, d, R + nh, qscale)
+    Rp = D.dit_vt_stride(R)
+    vt = np.zeros((nh, d, Rp), np.uint16)
+    vt[:, :, :R] = v.transpose(0, 2, 1)
+    o = torch.empty(R, nh * d, dtype=torch.bfloat16, device="cuda")
+    D.dit_attention(D.DitDims(nh * d, nh, d, 256), R, dev_bf16(q), dev_bf16(k), dev_bf16(vt), o)
+    D.dit_check()
+    f = lambda a: O.bf16_to_f64(a).transpose(1, 0, 2)
+    ref = O.attention(f(q), f(k), f(v))
+    got = bf16_f64(o)
+    vmax = np.abs(O.bf16_to_f64(v)).max()
+    assert np.all(np.abs(got - ref) <= 2 ** -8 * vmax + 2 ** -8 * np.abs(ref)), max_abs(got, ref)
+
+
+def test_attention_zero_query_gives_mean_value():
+    R, nh, d = 300, 2, 128
+    q, k, v = _attn_case(R, nh, d, 1)
+    q[:] = 0
+    vt = np.zeros((nh, d, D.dit_vt_stride(R)), np.uint16)
+    vt[:, :, :R] = v.transpose(0, 2, 1)
+    o = torch.empty(R, nh * d, dtype=torch.bfloat16, device="cuda")
+    D.dit_attention(D.DitDims(nh * d, nh, d, 256), R, dev_bf16(q), dev_bf16(k), dev_bf16(vt), o)
+    D.dit_check()
+    mean_v = O.bf16_to_f64(v).mean(axis=1).reshape(1, nh * d)
+    got = bf16_f64(o)
+    assert np.all(np.abs(got - mean_v) <= 2 ** -8 * np.abs(O.bf16_to_f64(v)).max())
