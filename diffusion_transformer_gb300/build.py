@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdit.so")
 
-SOURCES = ["api.cu", "gemm.cu", "attention.cu", "elementwise.cu"]
+SOURCES = ["api.cu", "gemm.cu", "attention.cu", "elementwise.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE]

@@ -231,6 +231,28 @@ DIT_API int dit_dequant_int8(const int8_t* q, const uint16_t* s, int64_t rows, i
 DIT_API int dit_linear_int8(const uint16_t* a, int M, int K, const int8_t* wq, const uint16_t* ws_scales, int N,
                     float* out, dit_stream_t stream);
 
+/* The whole-block forward for callers that cannot allocate device memory (no counterpart on the
+ * pages: this entry point exists for callers, not for the method). A plugin running inside a host
+ * application whose allocator owns the device memory, or a latency-bound loop where an allocation's
+ * implicit device synchronisation is not allowed, cannot call cudaMalloc; such a caller passes only
+ * inputs and outputs, exactly as for dit_block_forward, and the scratch lives in a static device
+ * array of dit_block_noalloc_max_bytes() bytes (64 MiB) that every GPU loading the library holds
+ * until the process exits. The call allocates nothing (no cudaMalloc/cudaFree, no allocating
+ * library routine).
+ *   - Limit: shapes whose dit_workspace_bytes(dims, L, N, 0) exceeds the array are rejected with
+ *     DIT_EWORKSPACE before any launch (the 512x512 block, hidden 3072 / ffn 12288 / 1088 rows, fits;
+ *     the 1024x1024 block does not).
+ *   - Set-up: the first call on a device (with that device current) looks up the array's device
+ *     address with cudaGetSymbolAddress; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents; nothing in it needs to
+ *     start at zero (each call writes every scratch byte before reading it). Calls that overlap on
+ *     the GPU (other streams, other host threads) race on the array: serialise them.
+ * Other arguments, results and errors as dit_block_forward. */
+DIT_API int dit_block_forward_noalloc(const dit_dims* dims, const dit_block_w* w, float* txt, int L, float* img,
+                                      int N, const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                      const float* img_sin, const dit_mod* mod, dit_stream_t stream);
+DIT_API size_t dit_block_noalloc_max_bytes(void);
+
 /* Synchronize `stream` and read (then clear) the device error word of the current device:
  * DIT_OK, DIT_ETIMEOUT, or DIT_ECUDA if the stream reported an error. */
 DIT_API int dit_check(dit_stream_t stream);
