@@ -433,7 +433,7 @@ int dit_dequant_int8(const int8_t* q, const uint16_t* s, int64_t rows, int64_t c
                      dit_stream_t stream) {
   if (!q || !s || !w || rows < 0 || cols < 0) return DIT_EINVAL;
   if (cols % 32 != 0) return DIT_EUNSUPPORTED;
-  if (reinterpret_cast<uintptr_t>(w) % 4) return DIT_EINVAL;
+  if (reinterpret_cast<uintptr_t>(w) % 16 || reinterpret_cast<uintptr_t>(q) % 16) return DIT_EINVAL;
   return dequant_int8_launch(q, s, w, rows, cols, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -138,18 +138,22 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, uint16_t* __res
   }
 }
 
-// w[o, i] = bf16_rne(q[o, i] * s[o, i / 32]) with the same instructions as the GEMM converters.
+// w[o, i] = bf16_rne(q[o, i] * s[o, i / 32]) with the same instructions as the GEMM converters:
+// one thread per 16 consecutive values (cols % 32 == 0, so a chunk never straddles two scales).
 __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ s, uint16_t* __restrict__ w,
                                long long rows, long long cols) {
-  const long long pairs = rows * cols / 2;
+  const long long chunks = rows * cols / 16;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
-    const long long e = 2 * i;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks; i += stride) {
+    const long long e = 16 * i;
     const long long o = e / cols, c = e % cols;
     const uint32_t sc = s[o * (cols / 32) + c / 32];
-    const uint32_t b = uint32_t(uint8_t(q[e])) | (uint32_t(uint8_t(q[e + 1])) << 8);
-    const uint32_t v = bf16x2_mul_rn(i8x2_to_bf16x2(b), sc | (sc << 16));
-    reinterpret_cast<uint32_t*>(w)[i] = v;
+    const uint4 q16 = *reinterpret_cast<const uint4*>(q + e);
+    uint32_t out[8];
+    dequant16(q16, sc, out);
+    uint4* dst = reinterpret_cast<uint4*>(w + e);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
   }
 }
 
@@ -204,7 +208,7 @@ int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t
 int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long long rows, long long cols,
                         cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return DIT_OK;
-  dequant_kernel<<<grid_for(rows * cols / 2, 256), 256, 0, stream>>>(q, s, w, rows, cols);
+  dequant_kernel<<<grid_for(rows * cols / 16, 256), 256, 0, stream>>>(q, s, w, rows, cols);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 

@@ -248,4 +248,48 @@ __device__ __forceinline__ uint32_t bf16x2_mul_rn(uint32_t a, uint32_t b) {
   return d;
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_fma_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Dequantise 16 signed int8 values (one uint4) that share the bf16 scale s into 8 bf16 pairs,
+// out = bf16_rne(q * s), without int->float conversions (a quarter-rate instruction):
+//   u = q + 128 = 128 h + m with h the top bit of u (not the sign of q) and m the low 7 bits of q;
+//   x = bf16 bits 0x4300 | m is exactly 128 + m;
+//   c = -256 s when h = 0 and -128 s when h = 1 (the bits of -256 s with the exponent lowered by h);
+//   q s = x s + c, and fma.rn.bf16x2 rounds that exact value once.
+// Positive scales whose 128 s and 256 s are normal bf16 numbers take this route; the rest (zero,
+// negative - where q = 0 must give -0 - and extreme exponents) take the exact int -> float route.
+__device__ __forceinline__ void dequant16(const uint4 q16, uint32_t s_bits, uint32_t (&out)[8]) {
+  const uint32_t words[4] = {q16.x, q16.y, q16.z, q16.w};
+  const uint32_t e = (s_bits >> 7) & 0xffu;
+  const uint32_t s2 = s_bits | (s_bits << 16);
+  if (e >= 1u && e <= 0xf6u && (s_bits & 0x8000u) == 0u) {
+    const uint32_t cl = ((s_bits + 0x400u) ^ 0x8000u) & 0xffffu;  // bits of -256 s
+    const uint32_t c2 = cl | (cl << 16);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t xa = words[w] & 0x7f7f7f7fu;     // m: low 7 bits of q + 128 = low 7 bits of q
+      const uint32_t hw = ~words[w] & 0x80808080u;    // h: top bit of q + 128 = not the sign of q
+      // bytes 0, 1 (then 2, 3) into the low byte of each 16-bit lane; 0x43 above m gives 128 + m
+      out[2 * w] = bf16x2_fma_rn(prmt(xa, 0x43434343u, 0x4140u), s2, c2 - prmt(hw, 0u, 0x4140u));
+      out[2 * w + 1] = bf16x2_fma_rn(prmt(xa, 0x43434343u, 0x4342u), s2, c2 - prmt(hw, 0u, 0x4342u));
+    }
+  } else {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      out[2 * w] = bf16x2_mul_rn(i8x2_to_bf16x2(words[w] & 0xffffu), s2);
+      out[2 * w + 1] = bf16x2_mul_rn(i8x2_to_bf16x2(words[w] >> 16), s2);
+    }
+  }
+}
+
 }  // namespace dit

@@ -111,6 +111,11 @@ def test_dequant_bit_exact():
     q[0, :255] = np.arange(-127, 128, dtype=np.int8)       # every code value
     s = DI.bf16_bits_from_f32((DI.INT8_S0 * (0.75 + 0.5 * g.random((96, 128)))).astype(np.float32))
     s[1, :] = DI.bf16_bits_from_f32(np.float32(1.0 + 2 ** -7) * np.ones(128, np.float32))  # ties appear
+    s[2, :] = s[0, :] | np.uint16(0x8000)          # negative scales (q = 0 must give -0)
+    s[3, :] = 0                                    # zero scales
+    s[4, :64] = np.uint16(0x0001)                  # subnormal scales
+    s[4, 64:] = np.uint16(0x7F00)                  # huge scales (256 s overflows bf16)
+    q[2:5, :255] = np.arange(-127, 128, dtype=np.int8)
     w = torch.empty(96, 4096, dtype=torch.bfloat16, device="cuda")
     D.dit_dequant_int8(dev(q), dev_bf16(s), w)
     D.dit_check()
