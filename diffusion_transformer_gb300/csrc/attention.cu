@@ -6,13 +6,20 @@
 // through on-chip memory and keep a running row max m and sum l, rescaling the accumulator by
 // exp(m_old - m_new) ("online softmax", exact up to rounding order), applying 1/sqrt(d) in fp32.
 //
-// GB300 mapping: one CTA per (128-query tile, head). Warp 0 loads Q once and K/V tiles (128 keys)
-// with TMA into a 2-deep ring; warp 1 issues S = Q K^T (M=128, N=128, K=d) into one of two TMEM
-// S buffers and O += P V (M=128, N=d, K=128) into a TMEM O accumulator; warps 2-5 own one query
-// row per thread: they read S from TMEM, do the online softmax in registers (exp2 in the log2
-// domain), rescale O in TMEM when the max moves, and write P as bf16 into a swizzled shared tile
-// the next MMA reads. S of tile j+1 is computed while the softmax of tile j runs.
-// V arrives transposed ([d, keys]) from the QKV epilogue so both MMAs take K-major operands.
+// GB300 mapping. One CTA per (pair of 128-query tiles, head). Warp 0 loads Q0, Q1 once and the
+// K/V tiles (128 keys) with TMA into a 2-deep ring; warp 1 issues every MMA; warps 2-5 run the
+// softmax of query tile 0 and warps 6-9 that of tile 1, one query row per thread. While one
+// softmax group works, the tensor core runs the other tile's S = Q K^T and O += P V, so the
+// exponentials and the MMAs of the two tiles overlap. Tensor memory (512 columns):
+//   [0, 128) S0, overwritten by P0   [128, 256) S1 / P1   [256, 256 + d) O0   [256 + d, 256 + 2d) O1
+// The softmax reads S from TMEM, writes P (bf16, two keys per 32-bit column) back over the columns
+// it has consumed, and the P V MMA reads A straight from TMEM. MMAs issued by one thread complete
+// in order, so S(j+1) is issued right after P V(j) reads P(j) from the same columns, and the
+// completion of S(j+1) also tells the softmax that P V(j) is done with O and P.
+// The running max m only moves when a row's max exceeds it by more than 8 (log2 units), so the
+// rescale of O in TMEM is rare; until then the weights exp2(s - m) stay below 2^8, and the final
+// O / l is the same softmax.
+// V arrives transposed ([d, keys]) from the QKV epilogue so the P V MMA takes a K-major B operand.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -26,47 +33,48 @@
 namespace dit {
 namespace {
 
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
 template <int D>
 struct AttnCfg {
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;                  // producer, MMA, 2 x 4 softmax warps
   static constexpr uint32_t kAtom = 128 * 128;          // one [128 rows x 64 bf16] swizzled atom
-  static constexpr uint32_t kQBytes = 128 * D * 2;      // D/64 atoms
+  static constexpr uint32_t kQBytes = 128 * D * 2;      // one query tile, D/64 atoms
   static constexpr uint32_t kKBytes = 128 * D * 2;      // per stage, D/64 atoms
   static constexpr uint32_t kVAtom = D * 128;           // [D rows x 64 keys]
   static constexpr uint32_t kVBytes = 2 * kVAtom;       // per stage (128 keys)
-  static constexpr uint32_t kPBytes = 2 * kAtom;        // [128 rows x 128 keys]
-  static constexpr uint32_t kBarBytes = 8 * 16;
-  static constexpr uint32_t kSmemNeed = 1024 + kQBytes + 2 * kKBytes + 2 * kVBytes + kPBytes + kBarBytes + 16;
+  static constexpr uint32_t kBarBytes = 8 * 24;
+  static constexpr uint32_t kSmemNeed = 1024 + 2 * kQBytes + 2 * kKBytes + 2 * kVBytes + kBarBytes + 16;
   // at least 116 KB so that two CTAs never share an SM (each allocates all 512 TMEM columns)
   static constexpr uint32_t kSmemBytes = kSmemNeed > 116 * 1024 ? kSmemNeed : 116 * 1024;
-  static constexpr uint32_t kTmemCols = 512;            // S0 [0,128), S1 [128,256), O [256, 256+D)
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnParams p, float scale_log2) {
   using Cfg = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + Cfg::kQBytes;
-  uint8_t* sV = sK + 2 * Cfg::kKBytes;
-  uint8_t* sP = sV + 2 * Cfg::kVBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + Cfg::kPBytes);
+  uint8_t* sQ = smem;                          // Q0, Q1
+  uint8_t* sK = sQ + 2 * Cfg::kQBytes;         // 2 stages
+  uint8_t* sV = sK + 2 * Cfg::kKBytes;         // 2 stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * Cfg::kVBytes);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;     // [2]
+  uint64_t* k_full = bars + 1;     // [2] per stage
   uint64_t* v_full = bars + 3;     // [2]
-  uint64_t* kv_empty = bars + 5;   // [2]
-  uint64_t* s_full = bars + 7;     // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* k_empty = bars + 5;    // [2]
+  uint64_t* v_empty = bars + 7;    // [2]
+  uint64_t* s_full = bars + 9;     // [2] per query tile
+  uint64_t* p_full = bars + 11;    // [2] per query tile
+  uint64_t* o_done = bars + 13;    // [2] per query tile (last P V)
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = lane_id();
-  const int qt = blockIdx.x;
+  const int qp = blockIdx.x;  // query tiles 2 qp, 2 qp + 1
   const int head = blockIdx.y;
   const int R = p.R;
   const int nkv = (R + 127) / 128;
@@ -76,11 +84,12 @@ __global__ void __launch_bounds__(192, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&v_full[s]), 1);
-      mbar_init(smem_u32(&kv_empty[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
       mbar_init(smem_u32(&s_full[s]), 1);
+      mbar_init(smem_u32(&p_full[s]), 128);
+      mbar_init(smem_u32(&o_done[s]), 1);
     }
-    mbar_init(smem_u32(p_full), 128);
-    mbar_init(smem_u32(o_done), 1);
     mbar_init(smem_u32(drain), 1);
     fence_mbar_init();
   }
@@ -97,34 +106,38 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tmem_o = tmem_base + 256;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (elect_one()) {
       const uint32_t qb = smem_u32(q_full);
-      mbar_arrive_expect_tx(qb, Cfg::kQBytes);
-      for (int a = 0; a < D / 64; ++a) tma_load_3d(smem_u32(sQ + a * Cfg::kAtom), &tmQ, qb, a * 64, qt * 128, head);
-      int issued = 0;
+      mbar_arrive_expect_tx(qb, 2 * Cfg::kQBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(smem_u32(sQ + t * Cfg::kQBytes + a * Cfg::kAtom), &tmQ, qb, a * 64, (2 * qp + t) * 128, head);
+      int nk = 0, nv = 0;  // K and V tiles issued
       for (int j = 0; j < nkv; ++j) {
         const int s = j & 1;
-        if (!mbar_wait(smem_u32(&kv_empty[s]), ((j >> 1) & 1) ^ 1, p.err, kErrTimeoutProducer)) break;
+        const uint32_t par = ((j >> 1) & 1) ^ 1;
+        if (!mbar_wait(smem_u32(&k_empty[s]), par, p.err, kErrTimeoutProducer)) break;
         const uint32_t kb = smem_u32(&k_full[s]);
         mbar_arrive_expect_tx(kb, Cfg::kKBytes);
         for (int a = 0; a < D / 64; ++a)
           tma_load_3d(smem_u32(sK + s * Cfg::kKBytes + a * Cfg::kAtom), &tmK, kb, a * 64, j * 128, head);
+        nk = j + 1;
+        if (!mbar_wait(smem_u32(&v_empty[s]), par, p.err, kErrTimeoutProducer)) break;
         const uint32_t vb = smem_u32(&v_full[s]);
         mbar_arrive_expect_tx(vb, Cfg::kVBytes);
         for (int b = 0; b < 2; ++b)
           tma_load_3d(smem_u32(sV + s * Cfg::kVBytes + b * Cfg::kVAtom), &tmV, vb, j * 128 + b * 64, 0, head);
-        issued = j + 1;
+        nv = j + 1;
       }
       // every issued copy lands before the CTA exits
       mbar_wait(qb, 0, p.err, kErrTimeoutDrain);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
+      for (int j = nk - 2 < 0 ? 0 : nk - 2; j < nk; ++j)
         mbar_wait(smem_u32(&k_full[j & 1]), (j >> 1) & 1, p.err, kErrTimeoutDrain);
+      for (int j = nv - 2 < 0 ? 0 : nv - 2; j < nv; ++j)
         mbar_wait(smem_u32(&v_full[j & 1]), (j >> 1) & 1, p.err, kErrTimeoutDrain);
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -132,120 +145,138 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128);
       constexpr uint32_t idesc_o = idesc_bf16(128, D);
       bool ok = mbar_wait(smem_u32(q_full), 0, p.err, kErrTimeoutMma);
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T into columns [128 t, 128 t + 128)
         const int s = j & 1;
-        if (!mbar_wait(smem_u32(&k_full[s]), (j >> 1) & 1, p.err, kErrTimeoutMma)) return false;
-        tc_fence_after();
-        const uint32_t dS = tmem_base + uint32_t(s * 128);
+        const uint32_t dS = tmem_base + uint32_t(t * 128);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t a = kk >> 2, off = uint32_t(2 * (kk & 3));
-          const uint64_t ad = sw128_desc(smem_u32(sQ + a * Cfg::kAtom)) + off;
+          const uint64_t ad = sw128_desc(smem_u32(sQ + t * Cfg::kQBytes + a * Cfg::kAtom)) + off;
           const uint64_t bd = sw128_desc(smem_u32(sK + s * Cfg::kKBytes + a * Cfg::kAtom)) + off;
           umma_bf16(dS, ad, bd, idesc_s, kk != 0);
         }
-        umma_commit(smem_u32(&s_full[s]));
-        return true;
+        umma_commit(smem_u32(&s_full[t]));
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < nkv && ok; ++j) {
-        if (j + 1 < nkv && !issue_s(j + 1)) break;
+      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t from TMEM columns [128 t, 128 t + 64)
         const int s = j & 1;
-        if (!mbar_wait(smem_u32(p_full), j & 1, p.err, kErrTimeoutMma)) break;
-        if (!mbar_wait(smem_u32(&v_full[s]), (j >> 1) & 1, p.err, kErrTimeoutMma)) break;
-        tc_fence_after();
+        const uint32_t dO = tmem_base + 256u + uint32_t(t * D);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t b = kk >> 2, off = uint32_t(2 * (kk & 3));
-          const uint64_t ad = sw128_desc(smem_u32(sP + b * Cfg::kAtom)) + off;
           const uint64_t bd = sw128_desc(smem_u32(sV + s * Cfg::kVBytes + b * Cfg::kVAtom)) + off;
-          umma_bf16(tmem_o, ad, bd, idesc_o, (j | kk) != 0);
+          umma_bf16_ts(dO, tmem_base + uint32_t(t * 128 + kk * 8), bd, idesc_o, (j | kk) != 0);
         }
-        umma_commit(smem_u32(o_done));
-        umma_commit(smem_u32(&kv_empty[s]));
+      };
+      if (ok) ok = mbar_wait(smem_u32(&k_full[0]), 0, p.err, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        umma_commit(smem_u32(&k_empty[0]));
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int s = j & 1;
+        const bool last = j + 1 == nkv;
+        if (!mbar_wait(smem_u32(&v_full[s]), (j >> 1) & 1, p.err, kErrTimeoutMma)) break;
+        // tile 0: P V(j), then S(j+1) over the same columns
+        if (!mbar_wait(smem_u32(&p_full[0]), j & 1, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (last) umma_commit(smem_u32(&o_done[0]));
+        if (!last) {
+          if (!mbar_wait(smem_u32(&k_full[(j + 1) & 1]), ((j + 1) >> 1) & 1, p.err, kErrTimeoutMma)) break;
+          tc_fence_after();
+          issue_s(0, j + 1);
+        }
+        // tile 1
+        if (!mbar_wait(smem_u32(&p_full[1]), j & 1, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        if (last) umma_commit(smem_u32(&o_done[1]));
+        umma_commit(smem_u32(&v_empty[s]));
+        if (!last) {
+          issue_s(1, j + 1);
+          umma_commit(smem_u32(&k_empty[(j + 1) & 1]));
+        }
       }
       umma_commit(smem_u32(drain));
       mbar_wait(smem_u32(drain), 0, p.err, kErrTimeoutDrain);
     }
   } else {
-    // ------------------------------------------------------------------ softmax warps 2..5
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;  // query row within the tile
+    // ------------------------------------------------------------------ softmax warps 2..9
+    const int t = (warp - 2) >> 2;               // query tile of this warp group
+    const int quad = warp & 3;                   // TMEM lanes this warp may access
+    const int row = quad * 32 + lane;            // query row within the tile
     const uint32_t lane_off = uint32_t(quad * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off + uint32_t(t * 128);
+    const uint32_t tO = tmem_base + lane_off + 256u + uint32_t(t * D);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait_warp(smem_u32(&s_full[s]), (j >> 1) & 1, p.err, kErrTimeoutSoftmax)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&s_full[t]), j & 1, p.err, kErrTimeoutSoftmax)) { ok = false; break; }
       tc_fence_after();
-      float sv[128];
+      const int valid = R - j * 128;  // keys of this tile that exist
+      // pass 1: row max of the scaled scores
+      float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem_base + lane_off + uint32_t(s * 128 + c * 32), r);
+        tmem_ld32(tS + uint32_t(c * 32), r);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i)
+          if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(r[i]));
       }
-      const int valid = R - j * 128;
-      if (valid < 128) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= valid) sv[i] = -INFINITY;
+      mx *= scale_log2;
+      float alpha = 1.f;
+      if (mx > m + kRescaleThreshold) {  // also true on the first tile (m = -inf)
+        alpha = ex2_approx(m - mx);
+        m = mx;
       }
-      float mx = sv[0];
-#pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
-      const float m_new = fmaxf(m, mx * scale_log2);
-      const float alpha = ex2_approx(m - m_new);
+      // pass 2: P = exp2(s * scale - m) as bf16 pairs into the consumed S columns; row sum in fp32
       float rowsum = 0.f;
-      uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2_approx(fmaf(sv[2 * i], scale_log2, -m_new));
-        const float p1 = ex2_approx(fmaf(sv[2 * i + 1], scale_log2, -m_new));
-        rowsum += p0 + p1;
-        pk[i] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + uint32_t(c * 32), r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = c * 32 + 2 * i;
+          const float p0 = k0 < valid ? ex2_approx(fmaf(__uint_as_float(r[2 * i]), scale_log2, -m)) : 0.f;
+          const float p1 = k0 + 1 < valid ? ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), scale_log2, -m)) : 0.f;
+          rowsum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + uint32_t(c * 16), pk);
       }
       l = fmaf(l, alpha, rowsum);
-      m = m_new;
-      if (j > 0) {
-        // PV of the previous tile must finish before O is rescaled and P is overwritten
-        if (!mbar_wait_warp(smem_u32(o_done), (j - 1) & 1, p.err, kErrTimeoutSoftmax)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha < 1.0f)) {
+      if (j > 0 && __any_sync(0xffffffffu, alpha < 1.0f)) {
+        // the wait on S(j) above also covers P V(j-1): O is stable here
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            const uint32_t ta = tmem_o + lane_off + uint32_t(c * 32);
-            tmem_ld32(ta, r);
-            tmem_ld_wait();
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + uint32_t(c * 32), r);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(ta, r);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(tO + uint32_t(c * 32), r);
         }
       }
-#pragma unroll
-      for (int k8 = 0; k8 < 16; ++k8) {
-        uint8_t* atom = sP + (k8 >> 3) * Cfg::kAtom;
-        *reinterpret_cast<uint4*>(atom + sw128_offset(uint32_t(row), uint32_t(k8 & 7))) =
-            make_uint4(pk[4 * k8], pk[4 * k8 + 1], pk[4 * k8 + 2], pk[4 * k8 + 3]);
-      }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(p_full));
+      mbar_arrive(smem_u32(&p_full[t]));
     }
-    if (ok && mbar_wait_warp(smem_u32(o_done), (nkv - 1) & 1, p.err, kErrTimeoutSoftmax)) {
+    if (ok && mbar_wait_warp(smem_u32(&o_done[t]), 0, p.err, kErrTimeoutSoftmax)) {
       tc_fence_after();
-      const int grow = qt * 128 + row;
+      const int grow = (2 * qp + t) * 128 + row;
       const float inv_l = 1.0f / l;
       const int H = p.heads * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem_o + lane_off + uint32_t(c * 32), r);
+        tmem_ld32(tO + uint32_t(c * 32), r);
         tmem_ld_wait();
         if (grow < R) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + size_t(grow) * H + head * D + c * 32);
@@ -278,7 +309,7 @@ int launch_d(const AttnParams& p, cudaStream_t stream) {
   auto kern = attn_kernel<D>;
   if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
   const float scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
-  dim3 grid((p.R + 127) / 128, p.heads);
+  dim3 grid((p.R + 255) / 256, p.heads);
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p, scale_log2);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
