@@ -46,15 +46,22 @@ struct GemmCfg {
   static constexpr uint32_t kBBytes = BN * BK * 2;   // bf16 tile the MMA reads
   static constexpr uint32_t kB8Bytes = BN * BK;      // int8 tile TMA writes (B8 only)
   static constexpr uint32_t kSBytes = BN * 16;       // B8: scale tile [BN rows x 8 bf16] (4 k-blocks)
-  static constexpr int kConvStages = BN == 256 ? 2 : 3;  // bf16 B tiles produced by the converters
+  static constexpr int kConvStages = 2;              // bf16 B tiles produced by the converters
   static constexpr int kConvThreads = 128;           // B8: converter warps 6..9, one per SM sub-partition
   static constexpr uint32_t kTmemCols = (kAccBufs * kMH * BN < 32) ? 32 : kAccBufs * kMH * BN;
-  static constexpr int kThreads = B8 ? 192 + kConvThreads : 192;
+  // epilogue warps: one per TMEM lane quadrant (two per quadrant, each taking half of the columns,
+  // measured no faster)
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kEpiCols = BN / (kEpiWarps / 4);   // columns per epilogue warp
+  static constexpr int kConvWarp0 = 2 + kEpiWarps;         // first converter warp (B8)
+  static constexpr int kThreads = 64 + kEpiThreads + (B8 ? kConvThreads : 0);
   // smem: [A ring][B ring (bf16, or int8 + scales for B8)][B8: converted bf16 ring][barriers][tmem slot]
   static constexpr uint32_t kRingBytes = kStages * (kABytes + (B8 ? kB8Bytes + kSBytes : kBBytes));
   static constexpr uint32_t kConvBytes = B8 ? kConvStages * kBBytes : 0;
+  static constexpr uint32_t kEpiBytes = kEpiWarps * 2048;   // epilogue staging, 2 KB per epilogue warp
   static constexpr uint32_t kBarBytes = 8 * (2 * kStages + 4 + 2 * kConvStages + 2) + 16;
-  static constexpr uint32_t kSmemBytes = 1024 + kRingBytes + kConvBytes + kBarBytes;
+  static constexpr uint32_t kSmemBytes = 1024 + kRingBytes + kConvBytes + kEpiBytes + kBarBytes;
 };
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
@@ -73,33 +80,66 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
 }
 
 // ----------------------------------------------------------------------------------------------
-// epilogues: one thread owns one output row of the tile; taddr points at (its lane, column n0).
-// tcgen05.ld is warp-collective, so every lane loads even when its row is out of range.
+// epilogues: thread `lane` of epilogue warp `quad` owns TMEM lane quad * 32 + lane, i.e. output row
+// row0 + lane of the warp's 32-row slab; taddr points at (its lane, column n0). tcgen05.ld is
+// warp-collective, so every lane loads even when its row is out of range. `stage` is this warp's
+// 2 KB shared-memory scratch (the transposed v store). BN here is the warp's column count.
 // ----------------------------------------------------------------------------------------------
 template <int BN, int EPI>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, int row, int n0) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0,
+                                              uint8_t* stage) {
+  const int row = row0 + lane;
   const bool row_ok = row < p.M;
   if constexpr (EPI == kEpiQKV) {
     const int d = p.head_dim;
     const int H = p.H;
     const int R = p.M;
+    const int half = d / 2;
     for (int hh = 0; hh < BN / d; ++hh) {
       const int col0 = n0 + hh * d;
       const int which = col0 / H;              // 0 = q, 1 = k, 2 = v
       const int head = (col0 - which * H) / d;
       const uint32_t ta = taddr + hh * d;
       if (which == 2) {
+        // v, transposed: vt[head*d + j][row]. Stage the warp's 32 rows x 32 values as bf16 (64 B
+        // per row, 16-byte chunks XOR-swizzled by (row >> 1) & 3), then lane j writes value j of
+        // all 32 rows as 64 contiguous bytes.
+        uint32_t* st32 = reinterpret_cast<uint32_t*>(stage);
         for (int c = 0; c < d / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(ta + c * 32, v);
           tmem_ld_wait();
-          if (row_ok) {
-            uint16_t* dst = p.vt + (size_t(head) * d + c * 32) * p.Rp + row;
+          __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
-              dst[size_t(j) * p.Rp] = *reinterpret_cast<uint16_t*>(&b);
-            }
+          for (int q = 0; q < 4; ++q) {
+            const int slot = q ^ ((lane >> 1) & 3);
+            *reinterpret_cast<uint4*>(stage + lane * 64 + slot * 16) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+          }
+          __syncwarp();
+          const int j = lane;  // value index within the chunk
+          uint32_t col[16];
+#pragma unroll
+          for (int r = 0; r < 32; r += 2) {
+            const int o0 = r * 64 + (((j >> 3) ^ ((r >> 1) & 3)) << 4) + (j & 7) * 2;
+            const int o1 = (r + 1) * 64 + (((j >> 3) ^ (((r + 1) >> 1) & 3)) << 4) + (j & 7) * 2;
+            const uint32_t lo = *reinterpret_cast<const uint16_t*>(stage + o0);
+            const uint32_t hi = *reinterpret_cast<const uint16_t*>(stage + o1);
+            col[r >> 1] = lo | (hi << 16);
+          }
+          (void)st32;
+          uint16_t* dst = p.vt + (size_t(head) * d + c * 32 + j) * p.Rp + row0;
+          if (row0 + 32 <= R) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);  // row0 % 32 == 0 and Rp % 8 == 0: 16-byte aligned
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d4[q] = make_uint4(col[4 * q], col[4 * q + 1], col[4 * q + 2], col[4 * q + 3]);
+          } else {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              if (row0 + r < R) dst[r] = uint16_t(r & 1 ? col[r >> 1] >> 16 : col[r >> 1] & 0xffffu);
           }
         }
         continue;
@@ -118,9 +158,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
       }
       const float rstd = rsqrtf(ss / float(d) + p.qk_eps);
       const float* wn = which == 0 ? p.q_norm : p.k_norm;
-      const int half = d / 2;
-      const float* cs = row < p.L ? p.txt_cos + size_t(row) * half : p.img_cos + size_t(row - p.L) * half;
-      const float* sn = row < p.L ? p.txt_sin + size_t(row) * half : p.img_sin + size_t(row - p.L) * half;
+      const float4* cs = reinterpret_cast<const float4*>(row < p.L ? p.txt_cos + size_t(row) * half
+                                                                     : p.img_cos + size_t(row - p.L) * half);
+      const float4* sn = reinterpret_cast<const float4*>(row < p.L ? p.txt_sin + size_t(row) * half
+                                                                     : p.img_sin + size_t(row - p.L) * half);
       uint16_t* dst = (which == 0 ? p.q : p.k) + (size_t(head) * R + row) * d;
       // pass 2: normalise, weight, rotate adjacent pairs, store
       for (int c = 0; c < d / 32; ++c) {
@@ -135,16 +176,58 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
           if (wn) f *= __ldg(wn + c * 32 + j);
           y[j] = f;
         }
+        float cf[16], sf[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 c4 = __ldg(cs + c * 4 + q);
+          const float4 s4 = __ldg(sn + c * 4 + q);
+          cf[4 * q] = c4.x; cf[4 * q + 1] = c4.y; cf[4 * q + 2] = c4.z; cf[4 * q + 3] = c4.w;
+          sf[4 * q] = s4.x; sf[4 * q + 1] = s4.y; sf[4 * q + 2] = s4.z; sf[4 * q + 3] = s4.w;
+        }
         float o[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float ci = __ldg(cs + c * 16 + i);
-          const float si = __ldg(sn + c * 16 + i);
           const float a = y[2 * i], b = y[2 * i + 1];
-          o[2 * i] = a * ci - b * si;
-          o[2 * i + 1] = a * si + b * ci;
+          o[2 * i] = a * cf[i] - b * sf[i];
+          o[2 * i + 1] = a * sf[i] + b * cf[i];
         }
         store_bf16x32(dst + c * 32, o);
+      }
+    }
+  } else if constexpr (EPI == kEpiGated) {
+    // x[r, n] += gate[map[r], n] * acc, one row per thread (the row's segments were prefetched to L2).
+    // Every lane runs every tcgen05.ld (warp-collective); only the global accesses are predicated.
+    const int grow = row_ok ? row : 0;
+    float* x = grow < p.L ? p.txt + size_t(grow) * p.N : p.img + size_t(grow - p.L) * p.N;
+    const int m = (p.map && row_ok) ? __ldg(p.map + grow) : 0;
+    const float* g = p.gate + size_t(m) * p.gate_stride;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(taddr + c * 32, v);
+      const int n = n0 + c * 32;
+      float4 xq[8], gq[8];
+      const float4* xv = reinterpret_cast<const float4*>(x + n);
+      const float4* gv = reinterpret_cast<const float4*>(g + n);
+      if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          xq[q] = xv[q];
+          gq[q] = __ldg(gv + q);
+        }
+      }
+      tmem_ld_wait();
+      if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          xq[q].x = fmaf(gq[q].x, __uint_as_float(v[4 * q + 0]), xq[q].x);
+          xq[q].y = fmaf(gq[q].y, __uint_as_float(v[4 * q + 1]), xq[q].y);
+          xq[q].z = fmaf(gq[q].z, __uint_as_float(v[4 * q + 2]), xq[q].z);
+          xq[q].w = fmaf(gq[q].w, __uint_as_float(v[4 * q + 3]), xq[q].w);
+        }
+        float4* xo = reinterpret_cast<float4*>(x + n);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xo[q] = xq[q];
       }
     }
   } else {
@@ -180,21 +263,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + size_t(row) * p.ldo + n / 2);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      } else if constexpr (EPI == kEpiGated) {
-        float* x = row < p.L ? p.txt + size_t(row) * p.N : p.img + size_t(row - p.L) * p.N;
-        const int m = p.map ? __ldg(p.map + row) : 0;
-        const float4* g = reinterpret_cast<const float4*>(p.gate + size_t(m) * p.gate_stride + n);
-        float4* xv = reinterpret_cast<float4*>(x + n);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 gq = __ldg(g + q);
-          float4 xq = xv[q];
-          xq.x = fmaf(gq.x, __uint_as_float(v[4 * q + 0]), xq.x);
-          xq.y = fmaf(gq.y, __uint_as_float(v[4 * q + 1]), xq.y);
-          xq.z = fmaf(gq.z, __uint_as_float(v[4 * q + 2]), xq.z);
-          xq.w = fmaf(gq.w, __uint_as_float(v[4 * q + 3]), xq.w);
-          xv[q] = xq;
-        }
       }
     }
   }
@@ -246,7 +314,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
   uint8_t* sB = sA + S * Cfg::kABytes;                              // bf16 ring, or int8 ring when B8
   uint8_t* sSc = sB + S * (B8 ? Cfg::kB8Bytes : Cfg::kBBytes);      // B8: scale-tile ring
   uint8_t* sC = sSc + (B8 ? S * Cfg::kSBytes : 0);                  // B8: converted bf16 ring
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + Cfg::kConvBytes);
+  uint8_t* sE = sC + Cfg::kConvBytes;                               // epilogue staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + Cfg::kEpiBytes);
   uint64_t* full = bars;                 // [S] TMA landed
   uint64_t* empty = bars + S;            // [S] stage free (MMA done; B8: also converter done)
   uint64_t* tfull = bars + 2 * S;        // [2] accumulator ready
@@ -260,6 +329,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
   const int lane = lane_id();
   const int num_m = (p.M + Cfg::kTileM - 1) / Cfg::kTileM;
   const int num_n = p.N / BN;
+  // Tile order: consecutive tiles share the smaller operand's panel set, so the CTAs running at
+  // once keep it in L2 and the larger operand streams from DRAM once. m fastest (A resident) when A
+  // is the smaller operand, n fastest (B resident) otherwise.
+  const bool n_fast = 2LL * p.M > (long long)p.N * (B8 ? 1 : 2);  // A bytes > B bytes (per k)
+  auto tile_mn = [&](int tile, int& mb, int& nb) {
+    if (n_fast) {
+      mb = tile / num_n;
+      nb = tile % num_n;
+    } else {
+      mb = tile % num_m;
+      nb = tile / num_m;
+    }
+  };
   const int tiles = num_m * num_n;
   const int KB = p.K / BK;
 
@@ -270,7 +352,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), 128);
+      mbar_init(smem_u32(&tempty[a]), Cfg::kEpiThreads);
     }
     for (int c = 0; c < CS; ++c) {
       mbar_init(smem_u32(&cfull[c]), Cfg::kConvThreads);
@@ -301,7 +383,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
       uint32_t issued_mask = 0, last_parity = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        const int mb = tile % num_m, nb = tile / num_m;
+        int mb, nb;
+        tile_mn(tile, mb, nb);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, kErrTimeoutProducer)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
@@ -373,27 +456,32 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
       umma_commit(smem_u32(drain));
       mbar_wait(smem_u32(drain), 0, p.err, kErrTimeoutDrain);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------- epilogue warps 2..5
-    const int quad = warp & 3;  // TMEM lanes this warp may access
+  } else if (warp < Cfg::kConvWarp0) {
+    // ------------------------------------------------------------- epilogue warps
+    const int quad = warp & 3;                       // TMEM lanes this warp may access
+    const int col0 = ((warp - 2) >> 2) * Cfg::kEpiCols;  // its columns of the tile
+    uint8_t* stage = sE + (warp - 2) * 2048;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-      const int mb = tile % num_m, nb = tile / num_m;
+      int mb, nb;
+      tile_mn(tile, mb, nb);
       if (!mbar_wait_warp(smem_u32(&tfull[acc]), acc_phase, p.err, kErrTimeoutEpilogue)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int h = 0; h < Cfg::kMH; ++h) {
-        const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t((acc * Cfg::kMH + h) * BN);
-        epilogue_tile<BN, EPI>(p, taddr, mb * Cfg::kTileM + h * BM + quad * 32 + lane, nb * BN);
+        const uint32_t taddr =
+            tmem_base + (uint32_t(quad * 32) << 16) + uint32_t((acc * Cfg::kMH + h) * BN + col0);
+        epilogue_tile<Cfg::kEpiCols, EPI>(p, taddr, mb * Cfg::kTileM + h * BM + quad * 32, lane, nb * BN + col0,
+                                          stage);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));
       if (++acc == Cfg::kAccBufs) { acc = 0; acc_phase ^= 1; }
     }
   } else if constexpr (B8) {
-    // ------------------------------------------------------------- int8 -> bf16 converters 6..9
-    const int ct = threadIdx.x - 192;
+    // ------------------------------------------------------------- int8 -> bf16 converters
+    const int ct = threadIdx.x - 32 * Cfg::kConvWarp0;
     int stage = 0, cstage = 0;
     uint32_t phase = 0, cphase = 0;
     bool ok = true;
@@ -455,6 +543,7 @@ int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmI
   if (reinterpret_cast<uintptr_t>(a) % 16 || (lda * 2) % 16) return DIT_EINVAL;
   // tile width: 256 where it divides N (fewer A re-reads), else 128, else 64
   int BN = (p.N % 256 == 0) ? 256 : (p.N % 128 == 0 ? 128 : 64);
+  // QKV epilogue: a tile never straddles q/k/v and holds whole heads
   if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K, p.M, lda * 2, BK, BM, true)) return DIT_ECUDA;
