@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int j = 0; j < nkv; ++j) {
       if (!mbar_wait_warp(smem_u32(&s_full[t]), j & 1, p.err, kErrTimeoutSoftmax)) { ok = false; break; }
       tc_fence_after();
-      const int valid = R - j * 128;  // keys of this tile that exist
+      const int valid = R - j * 128;  // keys of this tile that exist (same for the whole CTA)
+      const bool full = valid >= 128;
       // pass 1: row max of the scaled scores
       float mx = -INFINITY;
 #pragma unroll
@@ -223,9 +224,14 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t r[32];
         tmem_ld32(tS + uint32_t(c * 32), r);
         tmem_ld_wait();
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(r[i]));
+          for (int i = 0; i < 32; i += 2) mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(r[i]));
+        }
       }
       mx *= scale_log2;
       float alpha = 1.f;
@@ -234,7 +240,9 @@ __global__ void __launch_bounds__(320, 1)
         m = mx;
       }
       // pass 2: P = exp2(s * scale - m) as bf16 pairs into the consumed S columns; row sum in fp32
-      float rowsum = 0.f;
+      const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+      const uint64_t negm2 = f2_pack(-m, -m);
+      uint64_t sum2 = 0;  // two fp32 partial sums
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
@@ -243,14 +251,20 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int k0 = c * 32 + 2 * i;
-          const float p0 = k0 < valid ? ex2_approx(fmaf(__uint_as_float(r[2 * i]), scale_log2, -m)) : 0.f;
-          const float p1 = k0 + 1 < valid ? ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), scale_log2, -m)) : 0.f;
-          rowsum += p0 + p1;
+          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), scale2, negm2);
+          float p0 = ex2_approx(f2_lo(x2));
+          float p1 = ex2_approx(f2_hi(x2));
+          if (!full) {
+            const int k0 = c * 32 + 2 * i;
+            if (k0 >= valid) p0 = 0.f;
+            if (k0 + 1 >= valid) p1 = 0.f;
+          }
+          sum2 = f2_add(sum2, f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + uint32_t(c * 16), pk);
       }
+      const float rowsum = f2_lo(sum2) + f2_hi(sum2);
       l = fmaf(l, alpha, rowsum);
       if (j > 0 && __any_sync(0xffffffffu, alpha < 1.0f)) {
         // the wait on S(j) above also covers P V(j-1): O is stable here
