@@ -18,7 +18,7 @@ __all__ = [
     "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_euler_step", "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
     "dit_vt_stride", "dit_attention", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
-    "dit_dequant_int8", "dit_linear_int8", "dit_check", "dit_status_string", "dit_version",
+    "dit_dequant_int8", "dit_linear_int8", "dit_linear_int8_workspace_bytes", "dit_check", "dit_status_string", "dit_version",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -88,7 +88,9 @@ _SIGNATURES = {
     "dit_linear_swiglu": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
     "dit_linear": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p]),
     "dit_dequant_int8": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
-    "dit_linear_int8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
+    "dit_linear_int8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t,
+                                c_void_p]),
+    "dit_linear_int8_workspace_bytes": (c_size_t, [c_int, c_int]),
     "dit_check": (c_int, [c_void_p]),
     "dit_status_string": (c_char_p, [c_int]),
     "dit_version": (c_int, []),
@@ -341,12 +343,17 @@ def dit_linear(a, w, out, stream=None):
                          _stream(stream)), "dit_linear")
 
 
-def dit_linear_int8(a, wq, wscale, out, stream=None):
+def dit_linear_int8_workspace_bytes(N: int, K: int) -> int:
+    return lib().dit_linear_int8_workspace_bytes(N, K)
+
+
+def dit_linear_int8(a, wq, wscale, out, ws, stream=None):
     import torch
     M, K = a.shape
     N = wq.shape[0]
     _ok(lib().dit_linear_int8(_ptr(a, _bf16(), "a"), M, K, _ptr(wq, torch.int8, "wq"), _ptr(wscale, _bf16(), "s"), N,
-                              _ptr(out, torch.float32, "out"), _stream(stream)), "dit_linear_int8")
+                              _ptr(out, torch.float32, "out"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                              _stream(stream)), "dit_linear_int8")
 
 
 def dit_dequant_int8(q, s, w, stream=None):

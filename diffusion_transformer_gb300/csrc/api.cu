@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -88,6 +89,15 @@ BlockWs carve_block_ws(const dit_dims* d, int R, void* base) {
   return w;
 }
 
+// int8lin scratch of a block: the dequantised weight of its largest linear
+size_t int8_scratch_bytes(const dit_dims* d) {
+  const int H = d->hidden, F = d->ffn;
+  const int shapes[4][2] = {{3 * H, H}, {H, H}, {2 * F, H}, {H, F}};
+  size_t tl = 0;
+  for (auto& s : shapes) tl = std::max(tl, gemm_int8_scratch_bytes(s[0], s[1]));
+  return tl;
+}
+
 GemmParams base_params(int M, int N, int K, int* err) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -112,6 +122,8 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
   const BlockWs b = carve_block_ws(d, R, ws);
+  // int8lin scratch after the block workspace: one dequantised weight at a time
+  uint16_t* i8_tiles = w8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
   const float* norm1 = w8 ? w8->norm1 : w->norm1;
   const float* norm2 = w8 ? w8->norm2 : w->norm2;
   const float* qn = w8 ? w8->q_norm : w->q_norm;
@@ -140,7 +152,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.k_norm = kn;
   g.qk_eps = d->qk_eps;
   GemmInt8B q8;
-  if (w8) q8 = GemmInt8B{w8->q[0], w8->s[0]};
+  if (w8) q8 = GemmInt8B{w8->q[0], w8->s[0], i8_tiles};
   if ((rc = gemm_launch(b.h, H, w8 ? nullptr : w->wqkv, w8 ? &q8 : nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
 
   // 3. o = attention(q, k, v)
@@ -155,7 +167,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.gate = mod.rows + 2LL * H;
   g.map = mod.map;
   g.gate_stride = 6LL * H;
-  if (w8) q8 = GemmInt8B{w8->q[1], w8->s[1]};
+  if (w8) q8 = GemmInt8B{w8->q[1], w8->s[1], i8_tiles};
   if ((rc = gemm_launch(b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
 
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
@@ -168,7 +180,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g = base_params(R, 2 * F, H, err);
   g.out = b.a;
   g.ldo = F;
-  if (w8) q8 = GemmInt8B{w8->q[2], w8->s[2]};
+  if (w8) q8 = GemmInt8B{w8->q[2], w8->s[2], i8_tiles};
   if ((rc = gemm_launch(b.h, H, w8 ? nullptr : w->wup, w8 ? &q8 : nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
 
   // 7. x += gate_m * (a Wdown^T)
@@ -179,7 +191,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.gate = mod.rows + 5LL * H;
   g.map = mod.map;
   g.gate_stride = 6LL * H;
-  if (w8) q8 = GemmInt8B{w8->q[3], w8->s[3]};
+  if (w8) q8 = GemmInt8B{w8->q[3], w8->s[3], i8_tiles};
   return gemm_launch(b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, kEpiGated, g, st);
 }
 
@@ -262,7 +274,9 @@ const char* dit_status_string(int s) {
 
 size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
   if (!dims_ok(d) || L < 0 || N < 1 || (variant != 0 && variant != 1)) return 0;
-  return carve_block_ws(d, L + N, nullptr).bytes;
+  size_t bytes = carve_block_ws(d, L + N, nullptr).bytes;
+  if (variant == 1) bytes += int8_scratch_bytes(d);
+  return bytes;
 }
 
 int dit_vt_stride(int R) { return R < 0 ? 0 : vt_stride(R); }
@@ -298,8 +312,9 @@ int dit_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt,
   int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 1);
   if (rc != DIT_OK) return rc;
   if (!w) return DIT_EINVAL;
+  if (d->hidden % 256 != 0 || d->ffn % 256 != 0) return DIT_EUNSUPPORTED;  // int8lin: every K % 256 == 0
   for (int i = 0; i < 4; ++i)
-    if (!w->q[i] || !w->s[i] || !al16(w->q[i])) return DIT_EINVAL;
+    if (!w->q[i] || !w->s[i] || !al16(w->q[i]) || !al16(w->s[i])) return DIT_EINVAL;
   return run_block(d, nullptr, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                    reinterpret_cast<cudaStream_t>(stream));
 }
@@ -415,17 +430,25 @@ int dit_linear(const uint16_t* a, int M, int K, const uint16_t* w, int N, void* 
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t dit_linear_int8_workspace_bytes(int N, int K) {
+  if (N < 1 || K < 1) return 0;
+  return gemm_int8_scratch_bytes(N, K);
+}
+
 int dit_linear_int8(const uint16_t* a, int M, int K, const int8_t* wq, const uint16_t* wsc, int N, float* out,
-                    dit_stream_t stream) {
+                    void* ws, size_t ws_bytes, dit_stream_t stream) {
   if (!a || !wq || !wsc || !out || M < 1 || K < 1 || N < 1) return DIT_EINVAL;
-  if (K % 64 != 0 || N % 128 != 0) return DIT_EUNSUPPORTED;
-  if (!al16(a) || !al16(wq) || !al16(out)) return DIT_EINVAL;
+  if (K % 256 != 0 || N % 128 != 0) return DIT_EUNSUPPORTED;
+  if (!al16(a) || !al16(wq) || !al16(wsc) || !al16(out)) return DIT_EINVAL;
+  if (!ws) return DIT_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DIT_EINVAL;
+  if (ws_bytes < dit_linear_int8_workspace_bytes(N, K)) return DIT_EWORKSPACE;
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   GemmParams g = base_params(M, N, K, err);
   g.out = out;
   g.ldo = N;
-  GemmInt8B b8{wq, wsc};
+  GemmInt8B b8{wq, wsc, static_cast<uint16_t*>(ws)};
   return gemm_launch(a, K, nullptr, &b8, kEpiStoreF32, g, reinterpret_cast<cudaStream_t>(stream));
 }
 

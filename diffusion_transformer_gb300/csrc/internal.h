@@ -45,11 +45,17 @@ struct GemmParams {
   float qk_eps;
 };
 
-// B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights).
+// B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row
+// counts above kInt8MainloopMaxM the weight is first dequantised once into the caller's scratch
+// (bf16 [N, K]) by the HBM-bound dequant kernel and the bf16 mainloop runs on it; below, the
+// converter warps dequantise each k-block inside the mainloop (no scratch used).
 struct GemmInt8B {
   const int8_t* q;     // [N, K]
   const uint16_t* s;   // [N, K/32] bf16 bits
+  uint16_t* wbf;       // scratch [N, K] bf16 (may be null when M <= kInt8MainloopMaxM)
 };
+constexpr int kInt8MainloopMaxM = 512;
+inline size_t gemm_int8_scratch_bytes(int N, int K) { return ((size_t(N) * K * 2) + 255) / 256 * 256; }
 
 // Launch the GEMM. `a` is bf16 [M, K] (row stride lda elements), `b` bf16 [N, K] (stride K) unless
 // `b8` is given. Returns a DIT_* status; checks shapes the kernels support.

@@ -125,9 +125,13 @@ DIT_API int dit_block_forward(const dit_dims* dims, const dit_block_w* w, float*
                       const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
                       const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream);
 
-/* The same block with int8lin weights [host contract, section 1]: each linear's weight tile is
- * dequantized to bf16_rne(q * s) inside the GEMM (the MMA then runs in bf16). Requires
- * in % 32 == 0 for every linear. Workspace: dit_workspace_bytes(dims, L, N, 1). */
+/* The same block with int8lin weights [host contract, section 1]: W = bf16_rne(q * s), then the
+ * bf16 MMA. With at most 512 rows the GEMM's converter warps dequantize each weight k-block inside
+ * the mainloop; with more rows (many M tiles per weight tile) each linear's weight is dequantized
+ * once into the workspace by an HBM-bound kernel with the same arithmetic and the bf16 mainloop
+ * runs on it (bitwise the same result). Requires in % 256 == 0 for every linear.
+ * Workspace: dit_workspace_bytes(dims, L, N, 1) (the bf16 block workspace plus the dequantized
+ * weight of the largest linear). */
 DIT_API int dit_block_forward_int8(const dit_dims* dims, const dit_block_w8* w, float* txt, int L, float* img, int N,
                            const float* txt_cos, const float* txt_sin, const float* img_cos,
                            const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
@@ -227,9 +231,12 @@ DIT_API int dit_linear(const uint16_t* a, int M, int K, const uint16_t* w, int N
 DIT_API int dit_dequant_int8(const int8_t* q, const uint16_t* s, int64_t rows, int64_t cols, uint16_t* w,
                      dit_stream_t stream);
 
-/* Plain linear with int8lin weights: out fp32 [M, N] = a W^T with W dequantized in the mainloop. */
-DIT_API int dit_linear_int8(const uint16_t* a, int M, int K, const int8_t* wq, const uint16_t* ws_scales, int N,
-                    float* out, dit_stream_t stream);
+/* Plain linear with int8lin weights: out fp32 [M, N] = a W^T, W = bf16_rne(q * s) dequantized in
+ * the mainloop (M <= 512) or once into the workspace (M > 512). K % 256 == 0, N % 128 == 0.
+ * ws: dit_linear_int8_workspace_bytes(N, K) bytes, 256-byte aligned. */
+DIT_API int dit_linear_int8(const uint16_t* a, int M, int K, const int8_t* wq, const uint16_t* w_scales, int N,
+                            float* out, void* ws, size_t ws_bytes, dit_stream_t stream);
+DIT_API size_t dit_linear_int8_workspace_bytes(int N, int K);
 
 /* The whole-block forward for callers that cannot allocate device memory (no counterpart on the
  * pages: this entry point exists for callers, not for the method). A plugin running inside a host

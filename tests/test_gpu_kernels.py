@@ -153,21 +153,25 @@ def test_linear_bf16_out_and_identity_exact():
     assert np.array_equal(out32.cpu().numpy(), O.bf16_to_f64(A).astype(np.float32))
 
 
-@pytest.mark.parametrize("M,N,K", [(72, 256, 256), (1088, 384, 3072), (130, 128, 12288)])
+@pytest.mark.parametrize("M,N,K", [(72, 256, 256), (1088, 384, 3072), (130, 128, 12288), (4224, 512, 768)])
 def test_linear_int8_vs_oracle_and_bitwise_vs_dequant(M, N, K):
     g = np.random.default_rng(M * 7 + N)
     A = _bf16_rand(g, (M, K), 1.0)
     q = g.integers(-127, 128, size=(N, K), dtype=np.int8)
     s = DI.bf16_bits_from_f32((DI.INT8_S0 * (0.75 + 0.5 * g.random((N, K // 32)))).astype(np.float32))
     out8 = torch.empty(M, N, dtype=torch.float32, device="cuda")
-    D.dit_linear_int8(dev_bf16(A), dev(q), dev_bf16(s), out8)
+    ws = workspace(D.dit_linear_int8_workspace_bytes(N, K))
+    ws.fill_(0xAB)  # the call must not depend on the scratch's previous contents
+    D.dit_linear_int8(dev_bf16(A), dev(q), dev_bf16(s), out8, ws)
+    out8b = torch.empty_like(out8)
+    D.dit_linear_int8(dev_bf16(A), dev(q), dev_bf16(s), out8b, ws)  # again, over the previous call's scratch
     wd = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
     D.dit_dequant_int8(dev(q), dev_bf16(s), wd)
     out16 = torch.empty(M, N, dtype=torch.float32, device="cuda")
     D.dit_linear(dev_bf16(A), wd, out16)
     D.dit_check()
     # the int8 mainloop feeds the MMA the same bf16 tile as dequant + bf16 GEMM: bitwise equal
-    assert torch.equal(out8, out16)
+    assert torch.equal(out8, out16) and torch.equal(out8b, out16)
     Af, Wf = O.bf16_to_f64(A), O.bf16_to_f64(O.dequant_int8(q, s))
     err = np.abs(out8.cpu().numpy() - Af @ Wf.T)
     assert np.all(err <= GEMM_RTOL * _gemm_bound(Af, Wf) + 1e-30), float(err.max())
