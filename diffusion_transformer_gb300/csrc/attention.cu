@@ -217,21 +217,30 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int valid = R - j * 128;  // keys of this tile that exist (same for the whole CTA)
       const bool full = valid >= 128;
-      // pass 1: row max of the scaled scores
+      // the whole S row in registers: four loads in flight, one wait
+      uint32_t r[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + uint32_t(c * 32), *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+      tmem_ld_wait();
+      // row max of the scaled scores (independent chains)
       float mx = -INFINITY;
+      if (full) {
+        float m8[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + uint32_t(c * 32), r);
-        tmem_ld_wait();
-        if (full) {
+        for (int u = 0; u < 8; ++u) m8[u] = fmax3(__uint_as_float(r[u]), __uint_as_float(r[u + 8]), __uint_as_float(r[u + 16]));
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-        } else {
+        for (int k = 24; k < 128; k += 16) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(r[i]));
+          for (int u = 0; u < 8; ++u) m8[u] = fmax3(m8[u], __uint_as_float(r[k + u]), __uint_as_float(r[k + 8 + u]));
         }
+        // k = 24..119 covered in steps of 16 with two values each; the last 8 values (120..127)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m8[u] = fmaxf(m8[u], __uint_as_float(r[120 + u]));
+        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i < valid) mx = fmaxf(mx, __uint_as_float(r[i]));
       }
       mx *= scale_log2;
       float alpha = 1.f;
@@ -239,32 +248,31 @@ __global__ void __launch_bounds__(320, 1)
         alpha = ex2_approx(m - mx);
         m = mx;
       }
-      // pass 2: P = exp2(s * scale - m) as bf16 pairs into the consumed S columns; row sum in fp32
+      // P = exp2(s * scale - m) as bf16 pairs into the consumed S columns; row sum in fp32
       const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
       const uint64_t negm2 = f2_pack(-m, -m);
-      uint64_t sum2 = 0;  // two fp32 partial sums
+      uint64_t sum2[4] = {0, 0, 0, 0};  // eight fp32 partial sums (four packed pairs)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + uint32_t(c * 32), r);
-        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), scale2, negm2);
+          const int k0 = c * 32 + 2 * i;
+          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[k0]), __uint_as_float(r[k0 + 1])), scale2, negm2);
           float p0 = ex2_approx(f2_lo(x2));
           float p1 = ex2_approx(f2_hi(x2));
           if (!full) {
-            const int k0 = c * 32 + 2 * i;
             if (k0 >= valid) p0 = 0.f;
             if (k0 + 1 >= valid) p1 = 0.f;
           }
-          sum2 = f2_add(sum2, f2_pack(p0, p1));
+          sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + uint32_t(c * 16), pk);
       }
-      const float rowsum = f2_lo(sum2) + f2_hi(sum2);
+      const uint64_t s01 = f2_add(sum2[0], sum2[1]), s23 = f2_add(sum2[2], sum2[3]);
+      const uint64_t s4 = f2_add(s01, s23);
+      const float rowsum = f2_lo(s4) + f2_hi(s4);
       l = fmaf(l, alpha, rowsum);
       if (j > 0 && __any_sync(0xffffffffu, alpha < 1.0f)) {
         // the wait on S(j) above also covers P V(j-1): O is stable here
