@@ -37,6 +37,22 @@ import dit_inputs as DI  # noqa: E402
 METRIC = "DiT block ms & TFLOP/s at N=4096 (bf16, int8lin) as % of GB300 tensor peak"
 WORKLOAD = "1024sq"
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a kernel, from one ncu
+# capture of this workload, with the SHA-256 of the CUDA sources that kernel is built from. The
+# figure is reported only while those sources are unchanged (otherwise the counters no longer
+# describe the kernel and `traffic` is null). Captures: profiles/ncu_gemm_up_swiglu_1024sq.md.
+KERNEL_SOURCES = {
+    "gemm": ["gemm.cu", "ptx.cuh", "tmap.h", "internal.h"],
+    "attention": ["attention.cu", "ptx.cuh", "tmap.h", "internal.h"],
+    "modnorm": ["elementwise.cu", "ptx.cuh", "internal.h"],
+}
+KERNEL_FAMILY = {"modnorm": "modnorm", "attention": "attention", "gemm_qkv_rope": "gemm", "gemm_out_gated": "gemm",
+                 "gemm_up_swiglu": "gemm", "gemm_down_gated": "gemm"}
+NCU_TRAFFIC = {
+    # kernel: (bytes per launch, sha256 of its sources at capture)
+    "gemm_up_swiglu": (259_788_800, "89d8a0bd5aced9f54655d7bb00bb8bbd9d7ae5093b03c5a4aee3ab4b1d0b3342"),
+}
+
 
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -48,6 +64,23 @@ def _peaks():
                 "source": "measured"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _sources_hash(family):
+    import hashlib
+    d = os.path.join(ROOT, "diffusion_transformer_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[family]:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def _traffic(kernel):
+    t = NCU_TRAFFIC.get(kernel)
+    if t and t[1] == _sources_hash(KERNEL_FAMILY[kernel]):
+        return t[0]
+    return None
 
 
 def _cores():
@@ -146,6 +179,21 @@ def _block_setup(torch, D, inp, int8=False):
 def _block_call(D, st, int8=False):
     f = D.dit_block_forward_int8 if int8 else D.dit_block_forward
     f(st["dims"], st["w"], st["txt"], st["img"], st["tc"], st["ts"], st["ic"], st["is_"], st["mod"], st["ws"])
+
+
+def max_over_ranks(value: float, dist=None, device: str = "cpu") -> float:
+    """The slowest rank's time (the job's time): all-reduce MAX across ranks; identity without dist."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flop_per_step: float, ms_per_step: float) -> float:
+    """Aggregate throughput of `world` replicas that each ran one step per ms_per_step."""
+    return world * flop_per_step / (ms_per_step * 1e-3) / 1e12
 
 
 def _time_loop(torch, fn, steps, warmup, dist=None):
@@ -296,11 +344,8 @@ def run_ours(args):
     clk = ClockSampler(local).__enter__()
     total_ms = _time_loop(torch, lambda: _block_call(D, st), args.steps, args.warmup, dist)
     D.dit_check()
-    t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = t.item() / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    ms_step = max_over_ranks(total_ms, dist, "cuda") / args.steps
+    value = whole_job_tflops(world, flops, ms_step)
 
     # per-kernel breakdown and the dominant kernel's roofline
     kb = _kernel_breakdown(torch, D, st, inp, max(5, args.steps // 2))
@@ -309,12 +354,12 @@ def run_ours(args):
     if dk["flop_per_launch"] > 0:
         ach = dk["flop_per_launch"] / (dk["ms_per_launch"] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                "frac": ach / peaks["bf16_tflops"], "traffic": _traffic(dom),
                 "peak_source": f"bf16_tflops burst, {peaks['source']}"}
     else:
         ach = dk["bytes_per_launch"] / (dk["ms_per_launch"] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": None, "peak_source": f"hbm_gbs, {peaks['source']}"}
+                "frac": ach / peaks["hbm_gbs"], "traffic": _traffic(dom), "peak_source": f"hbm_gbs, {peaks['source']}"}
     for k, v in kb.items():
         if v["flop_per_launch"] > 0:
             v["tflops"] = v["flop_per_launch"] / (v["ms_per_launch"] * 1e-3) / 1e12
@@ -332,8 +377,21 @@ def run_ours(args):
         ms8 = _time_loop(torch, lambda: _block_call(D, st8, int8=True), args.steps, args.warmup, dist) / args.steps
         D.dit_check()
         tf8 = flops / (ms8 * 1e-3) / 1e12
+        # the once-per-call dequantisation of each linear (HBM-bound): q + s read, bf16 written
+        deq = {}
+        wq, wsc = st8["w"].tensors[0], st8["w"].tensors[1]
+        for name, q, sc in zip(("qkv", "out", "up", "down"), wq, wsc):
+            wbf = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+            msd = _time_loop(torch, lambda: D.dit_dequant_int8(q, sc, wbf), max(5, args.steps // 2), 2) / max(5, args.steps // 2)
+            nbytes = q.numel() + sc.numel() * 2 + q.numel() * 2
+            deq[name] = {"us": msd * 1e3, "bytes": nbytes, "gbs": nbytes / (msd * 1e-3) / 1e9,
+                         "frac_of_hbm_peak": nbytes / (msd * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+            del wbf
+        D.dit_check()
         int8 = {"workload": "1024sq_int8", "ms_per_block": ms8, "tflops": tf8,
-                "frac_of_peak": tf8 / peaks["bf16_tflops"]}
+                "frac_of_peak": tf8 / peaks["bf16_tflops"], "dequant": deq,
+                "path": "rows > 512: each linear's weight dequantised once per call (HBM-bound kernel), then "
+                        "the bf16 tcgen05 mainloop; rows <= 512: dequantised inside the GEMM mainloop"}
         del st8
         st = _block_setup(torch, D, inp)
 
