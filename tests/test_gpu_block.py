@@ -147,3 +147,38 @@ def test_abi_rejects_bad_arguments_without_touching_outputs():
     assert e.value.status == D.DIT_EUNSUPPORTED
     D.dit_check()
     assert np.array_equal(txt.cpu().numpy(), inp.txt) and np.array_equal(img.cpu().numpy(), inp.img)
+
+
+def test_int8_block_mainloop_path_full_width():
+    # 320 rows (<= 512): the int8lin GEMMs dequantise inside the mainloop at hidden 3072 / ffn 12288
+    sh = DI.BlockShape("int8_mainloop", 3072, 24, 128, 12288, 64, 16, 16, seed=9)
+    inp = DI.int8_block_inputs(sh)
+    t, i = run_block_gpu(inp, int8=True)
+    rows = _sample_rows(sh, n=40, seed=3)
+    W = tuple(O.bf16_to_f64(O.dequant_int8(q, s)) for q, s in zip(inp.q8, inp.s8))
+    ref = O.block_forward(inp, weights=W, rows=rows)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)[rows]
+    _check(np.concatenate([t, i])[rows], ref, x_in, "int8 in-mainloop path, 320 rows")
+
+
+@pytest.mark.parametrize("L,gh,gw", [(8, 16, 20), (13, 9, 10), (1, 5, 7)])
+def test_head64_ragged_multi_tile(L, gh, gw):
+    # d = 64, several 128-row tiles with a ragged tail (R = 328); R = 13 + 90 = 103 and R = 36 are
+    # not multiples of 8 (padded transposed-v stride)
+    sh = DI.BlockShape(f"d64_{L}_{gh}x{gw}", 256, 4, 64, 768, L, gh, gw, seed=L + gh)
+    inp = DI.block_inputs(sh, M=2, norm_weights=True)
+    t, i = run_block_gpu(inp)
+    rt, ri = O.block_forward(inp)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)
+    _check(np.concatenate([t, i]), np.concatenate([rt, ri]), x_in, f"d=64 L={L} grid {gh}x{gw}")
+
+
+def test_denoise_shape_block_sampled_rows():
+    # the block at the denoise sequence (L = 512 + N = 4096) with one modulation row (M = 1)
+    inp = DI.block_inputs("denoise", M=1)
+    sh = inp.shape
+    t, i = run_block_gpu(inp)
+    rows = _sample_rows(sh, n=32, seed=5)
+    ref = O.block_forward(inp, rows=rows)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)[rows]
+    _check(np.concatenate([t, i])[rows], ref, x_in, "denoise-shape block, M=1, sampled rows")
