@@ -13,7 +13,11 @@ constexpr int kNormThreads = 256;
 
 // Modulated RMSNorm (the gizai:dit reference's normedInto with its Modulation rows):
 //   h[r] = bf16( x[r] * rsqrt(mean(x[r]^2) + eps) * w * (1 + scale[m]) + shift[m] )
-// one CTA per row, float4 loads, fp32 statistics (klein article, section 2: fp32 RMSNorm -> bf16).
+// one CTA per row, fp32 statistics (klein article, section 2: fp32 RMSNorm -> bf16). Every load of
+// the row (x, shift, scale, w) is issued before the reduction, so one pass over global memory
+// serves both the statistics and the output. NC = float4 chunks per thread (H = NC * 4 * 256);
+// NC = 0 is the generic two-pass form for other widths.
+template <int NC>
 __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormParams p) {
   const int r = blockIdx.x;
   const float* x = r < p.L ? p.txt + size_t(r) * p.ld_txt : p.img + size_t(r - p.L) * p.ld_img;
@@ -23,37 +27,73 @@ __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormPara
   const float4* sc4 = reinterpret_cast<const float4*>(p.scale + size_t(m) * p.mod_stride);
   const float4* w4 = reinterpret_cast<const float4*>(p.w);
   const int n4 = p.H >> 2;
-
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < n4; i += kNormThreads) {
-    const float4 v = x4[i];
-    ss = fmaf(v.x, v.x, ss);
-    ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss);
-    ss = fmaf(v.w, v.w, ss);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   __shared__ float part[kNormThreads / 32];
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
-#pragma unroll
-  for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
-  const float rstd = rsqrtf(tot / float(p.H) + p.eps);
 
-  uint2* out = reinterpret_cast<uint2*>(p.out + size_t(r) * p.H);
-  for (int i = threadIdx.x; i < n4; i += kNormThreads) {
-    const float4 v = x4[i];
-    const float4 sh = __ldg(sh4 + i);
-    const float4 sc = __ldg(sc4 + i);
-    float4 w = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (w4) w = __ldg(w4 + i);
-    const float y0 = fmaf(v.x * rstd * w.x, 1.f + sc.x, sh.x);
-    const float y1 = fmaf(v.y * rstd * w.y, 1.f + sc.y, sh.y);
-    const float y2 = fmaf(v.z * rstd * w.z, 1.f + sc.z, sh.z);
-    const float y3 = fmaf(v.w * rstd * w.w, 1.f + sc.w, sh.w);
-    out[i] = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+  if constexpr (NC > 0) {
+    float4 xv[NC], sh[NC], sc[NC], wv[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      const int i = threadIdx.x + k * kNormThreads;
+      xv[k] = x4[i];
+      sh[k] = __ldg(sh4 + i);
+      sc[k] = __ldg(sc4 + i);
+      wv[k] = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      ss = fmaf(xv[k].x, xv[k].x, ss);
+      ss = fmaf(xv[k].y, xv[k].y, ss);
+      ss = fmaf(xv[k].z, xv[k].z, ss);
+      ss = fmaf(xv[k].w, xv[k].w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
+    const float rstd = rsqrtf(tot / float(p.H) + p.eps);
+    uint2* out = reinterpret_cast<uint2*>(p.out + size_t(r) * p.H);
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      const float y0 = fmaf(xv[k].x * rstd * wv[k].x, 1.f + sc[k].x, sh[k].x);
+      const float y1 = fmaf(xv[k].y * rstd * wv[k].y, 1.f + sc[k].y, sh[k].y);
+      const float y2 = fmaf(xv[k].z * rstd * wv[k].z, 1.f + sc[k].z, sh[k].z);
+      const float y3 = fmaf(xv[k].w * rstd * wv[k].w, 1.f + sc[k].w, sh[k].w);
+      out[threadIdx.x + k * kNormThreads] = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+    }
+  } else {
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < n4; i += kNormThreads) {
+      const float4 v = x4[i];
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
+    const float rstd = rsqrtf(tot / float(p.H) + p.eps);
+    uint2* out = reinterpret_cast<uint2*>(p.out + size_t(r) * p.H);
+    for (int i = threadIdx.x; i < n4; i += kNormThreads) {
+      const float4 v = x4[i];
+      const float4 shv = __ldg(sh4 + i);
+      const float4 scv = __ldg(sc4 + i);
+      float4 w = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (w4) w = __ldg(w4 + i);
+      const float y0 = fmaf(v.x * rstd * w.x, 1.f + scv.x, shv.x);
+      const float y1 = fmaf(v.y * rstd * w.y, 1.f + scv.y, shv.y);
+      const float y2 = fmaf(v.z * rstd * w.z, 1.f + scv.z, shv.z);
+      const float y3 = fmaf(v.w * rstd * w.w, 1.f + scv.w, shv.w);
+      out[i] = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+    }
   }
 }
 
@@ -139,21 +179,37 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, uint16_t* __res
 }
 
 // w[o, i] = bf16_rne(q[o, i] * s[o, i / 32]) with the same instructions as the GEMM converters:
-// one thread per 16 consecutive values (cols % 32 == 0, so a chunk never straddles two scales).
+// 16 consecutive values per chunk (cols % 32 == 0, so a chunk never straddles two scales); each
+// thread keeps four chunks' loads in flight per iteration.
 __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ s, uint16_t* __restrict__ w,
                                long long rows, long long cols) {
+  constexpr int kU = 4;
   const long long chunks = rows * cols / 16;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks; i += stride) {
-    const long long e = 16 * i;
-    const long long o = e / cols, c = e % cols;
-    const uint32_t sc = s[o * (cols / 32) + c / 32];
-    const uint4 q16 = *reinterpret_cast<const uint4*>(q + e);
-    uint32_t out[8];
-    dequant16(q16, sc, out);
-    uint4* dst = reinterpret_cast<uint4*>(w + e);
-    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (long long base = t; base < chunks; base += kU * nthreads) {
+    uint4 q16[kU];
+    uint32_t sc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long i = base + u * nthreads;
+      if (i < chunks) {
+        const long long e = 16 * i;
+        q16[u] = *reinterpret_cast<const uint4*>(q + e);
+        sc[u] = s[(e / cols) * (cols / 32) + (e % cols) / 32];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const long long i = base + u * nthreads;
+      if (i < chunks) {
+        uint32_t out[8];
+        dequant16(q16[u], sc[u], out);
+        uint4* dst = reinterpret_cast<uint4*>(w + 16 * i);
+        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+      }
+    }
   }
 }
 
@@ -168,7 +224,14 @@ int grid_for(long long n, int threads) {
 
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream) {
   if (p.R <= 0) return DIT_OK;
-  modnorm_kernel<<<p.R, kNormThreads, 0, stream>>>(p);
+  const int chunks = p.H % (4 * kNormThreads) == 0 ? p.H / (4 * kNormThreads) : 0;
+  switch (chunks) {
+    case 1: modnorm_kernel<1><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    case 2: modnorm_kernel<2><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    case 3: modnorm_kernel<3><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    case 4: modnorm_kernel<4><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    default: modnorm_kernel<0><<<p.R, kNormThreads, 0, stream>>>(p); break;
+  }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
