@@ -290,28 +290,60 @@ def _denoise_bench(torch, D, steps_timed=2):
 
 
 def _e2e(torch, D, st, inp, steps, warmup):
-    """The block through the C ABI with host buffers: pinned H2D of the step's inputs (residual rows,
-    modulation rows, map, rotary tables), the block forward, D2H of the residual rows."""
+    """The block through the C ABI with host buffers, as a serving loop runs it: every step uploads
+    its inputs (residual rows, modulation rows, map, rotary tables) from pinned host memory, runs
+    the block and reads the residual rows back. Uploads of step k+1 overlap the block of step k
+    (two device input sets, a copy stream and the compute stream); all copies are in the timed
+    region."""
     sh = inp.shape
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_txt, h_img, h_mod, h_map = pin(inp.txt), pin(inp.img), pin(inp.mod), pin(inp.mod_map)
-    h_tc, h_ts, h_ic, h_is = (st[k].cpu().pin_memory() for k in ("tc", "ts", "ic", "is_"))
-    o_txt, o_img = torch.empty_like(h_txt).pin_memory(), torch.empty_like(h_img).pin_memory()
-    mod_rows, mod_map = st["mod"].tensors
-    pairs = [(st["txt"], h_txt), (st["img"], h_img), (mod_rows, h_mod), (mod_map, h_map), (st["tc"], h_tc),
-             (st["ts"], h_ts), (st["ic"], h_ic), (st["is_"], h_is)]
-    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
-    d2h = o_txt.numel() * 4 + o_img.numel() * 4
+    host = [pin(inp.txt), pin(inp.img), pin(inp.mod), pin(inp.mod_map)] + \
+        [st[k].cpu().pin_memory() for k in ("tc", "ts", "ic", "is_")]
+    outs = [(torch.empty_like(host[0]).pin_memory(), torch.empty_like(host[1]).pin_memory()) for _ in range(2)]
+    sets = []
+    for _ in range(2):
+        dv = [torch.empty(h.shape, dtype=h.dtype, device="cuda") for h in host]
+        sets.append(dict(dev=dv, mod=D.Modulation(dv[2], dv[3])))
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = host[0].numel() * 4 + host[1].numel() * 4
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for d_, h_ in pairs:
-            d_.copy_(h_, non_blocking=True)
-        _block_call(D, st)
-        o_txt.copy_(st["txt"], non_blocking=True)
-        o_img.copy_(st["img"], non_blocking=True)
+    def upload(k):
+        b = k % 2
+        with torch.cuda.stream(copy):
+            copy.wait_event(consumed[b])  # the previous user of this input set has read it back
+            for d_, h_ in zip(sets[b]["dev"], host):
+                d_.copy_(h_, non_blocking=True)
+            uploaded[b].record(copy)
 
-    ms = _time_loop(torch, step, steps, warmup) / steps
-    return ms, h2d, d2h
+    def run(k):
+        b = k % 2
+        dv = sets[b]["dev"]
+        comp.wait_event(uploaded[b])
+        D.dit_block_forward(st["dims"], st["w"], dv[0], dv[1], dv[4], dv[5], dv[6], dv[7], sets[b]["mod"], st["ws"])
+        outs[b][0].copy_(dv[0], non_blocking=True)
+        outs[b][1].copy_(dv[1], non_blocking=True)
+        consumed[b].record(comp)
+
+    def loop(n):
+        upload(0)
+        for k in range(n):
+            if k + 1 < n:
+                upload(k + 1)
+            run(k)
+
+    loop(warmup)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    copy.wait_event(e0)
+    loop(steps)
+    e1.record(comp)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
 def run_ours(args):
@@ -425,7 +457,9 @@ def run_ours(args):
             "int8lin": int8,
             "denoise": den,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": "dit_block_forward on inputs uploaded from pinned host memory each step, residual rows "
+                           "read back each step; uploads of step k+1 overlap the block of step k"},
             "gpu_launches": 7 * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
