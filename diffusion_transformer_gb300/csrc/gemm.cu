@@ -59,7 +59,7 @@ struct GemmCfg {
   // smem: [A ring][B ring (bf16, or int8 + scales for B8)][B8: converted bf16 ring][barriers][tmem slot]
   static constexpr uint32_t kRingBytes = kStages * (kABytes + (B8 ? kB8Bytes + kSBytes : kBBytes));
   static constexpr uint32_t kConvBytes = B8 ? kConvStages * kBBytes : 0;
-  static constexpr uint32_t kEpiBytes = kEpiWarps * 2048;   // epilogue staging, 2 KB per epilogue warp
+  static constexpr uint32_t kEpiBytes = kEpiWarps * 4096;   // epilogue staging, 4 KB per epilogue warp
   static constexpr uint32_t kBarBytes = 8 * (2 * kStages + 4 + 2 * kConvStages + 2) + 16;
   static constexpr uint32_t kSmemBytes = 1024 + kRingBytes + kConvBytes + kEpiBytes + kBarBytes;
 };
@@ -83,9 +83,10 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
 // epilogues: thread `lane` of epilogue warp `quad` owns TMEM lane quad * 32 + lane, i.e. output row
 // row0 + lane of the warp's 32-row slab; taddr points at (its lane, column n0). tcgen05.ld is
 // warp-collective, so every lane loads even when its row is out of range. `stage` is this warp's
-// 2 KB shared-memory scratch (the transposed v store). BN here is the warp's column count.
+// 4 KB shared-memory scratch (the transposed v store, the gated residual's transpose). BN here is
+// the warp's column count.
 // ----------------------------------------------------------------------------------------------
-template <int BN, int EPI>
+template <int BN, int EPI, bool kRowPerThread>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0,
                                               uint8_t* stage) {
   const int row = row0 + lane;
@@ -194,9 +195,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
         store_bf16x32(dst + c * 32, o);
       }
     }
-  } else if constexpr (EPI == kEpiGated) {
-    // x[r, n] += gate[map[r], n] * acc, one row per thread (the row's segments were prefetched to L2).
-    // Every lane runs every tcgen05.ld (warp-collective); only the global accesses are predicated.
+  } else if constexpr (EPI == kEpiGated && kRowPerThread) {
+    // x[r, n] += gate[map[r], n] * acc, one row per thread: the form for the int8 in-mainloop
+    // kernel, whose 320 threads leave 168 registers each (the coalesced form below would spill).
     const int grow = row_ok ? row : 0;
     float* x = grow < p.L ? p.txt + size_t(grow) * p.N : p.img + size_t(grow - p.L) * p.N;
     const int m = (p.map && row_ok) ? __ldg(p.map + grow) : 0;
@@ -228,6 +229,66 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
         float4* xo = reinterpret_cast<float4*>(x + n);
 #pragma unroll
         for (int q = 0; q < 8; ++q) xo[q] = xq[q];
+      }
+    }
+  } else if constexpr (EPI == kEpiGated) {
+    // x[r, n] += gate[map[r], n] * acc. The accumulator chunk (32 rows x 32 columns, thread = row)
+    // goes through the warp's 4 KB shared tile (16-byte chunks XOR-swizzled by row & 7), so the
+    // global accesses are coalesced: lane handles rows (lane >> 3) + 4 i, i = 0..7, 16-byte column
+    // chunk lane & 7, and every warp instruction moves four whole 128-byte lines of x or the gate.
+    // The loads of chunk c + 1 are issued as soon as chunk c is stored. Every lane runs every
+    // tcgen05.ld (warp-collective); only the global accesses are predicated.
+    (void)row_ok;
+    const int cq = lane & 7;
+    float* xr[8];
+    const float* gr[8];
+    bool ok[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = row0 + (lane >> 3) + 4 * i;
+      ok[i] = r < p.M;
+      const int rr = ok[i] ? r : 0;
+      xr[i] = (rr < p.L ? p.txt + size_t(rr) * p.N : p.img + size_t(rr - p.L) * p.N) + n0 + cq * 4;
+      gr[i] = p.gate + size_t(p.map ? __ldg(p.map + rr) : 0) * p.gate_stride + n0 + cq * 4;
+    }
+    float4 xq[8], gq[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (ok[i]) {
+        xq[i] = *reinterpret_cast<const float4*>(xr[i]);
+        gq[i] = __ldg(reinterpret_cast<const float4*>(gr[i]));
+      }
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(taddr + c * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(stage + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+            make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rl = (lane >> 3) + 4 * i;
+        const float4 a = *reinterpret_cast<const float4*>(stage + rl * 128 + ((cq ^ (rl & 7)) << 4));
+        if (ok[i]) {
+          float4 o;
+          o.x = fmaf(gq[i].x, a.x, xq[i].x);
+          o.y = fmaf(gq[i].y, a.y, xq[i].y);
+          o.z = fmaf(gq[i].z, a.z, xq[i].z);
+          o.w = fmaf(gq[i].w, a.w, xq[i].w);
+          *reinterpret_cast<float4*>(xr[i] + c * 32) = o;
+        }
+      }
+      __syncwarp();
+      if (c + 1 < BN / 32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (ok[i]) {
+            xq[i] = *reinterpret_cast<const float4*>(xr[i] + (c + 1) * 32);
+            gq[i] = __ldg(reinterpret_cast<const float4*>(gr[i] + (c + 1) * 32));
+          }
       }
     }
   } else {
@@ -460,7 +521,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     // ------------------------------------------------------------- epilogue warps
     const int quad = warp & 3;                       // TMEM lanes this warp may access
     const int col0 = ((warp - 2) >> 2) * Cfg::kEpiCols;  // its columns of the tile
-    uint8_t* stage = sE + (warp - 2) * 2048;
+    uint8_t* stage = sE + (warp - 2) * 4096;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -472,7 +533,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
       for (int h = 0; h < Cfg::kMH; ++h) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + uint32_t((acc * Cfg::kMH + h) * BN + col0);
-        epilogue_tile<Cfg::kEpiCols, EPI>(p, taddr, mb * Cfg::kTileM + h * BM + quad * 32, lane, nb * BN + col0,
+        epilogue_tile<Cfg::kEpiCols, EPI, B8>(p, taddr, mb * Cfg::kTileM + h * BM + quad * 32, lane, nb * BN + col0,
                                           stage);
       }
       tc_fence_before();
