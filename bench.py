@@ -225,6 +225,8 @@ def _kernel_breakdown(torch, D, st, inp, steps):
     vt = torch.zeros(nh, d, D.dit_vt_stride(R), dtype=torch.bfloat16, device="cuda")
     o = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
     a = torch.empty(R, F, dtype=torch.bfloat16, device="cuda")
+    # scratch for the K-split of the gated GEMMs' last wave, as the block gives them
+    split_ws = torch.empty(((R + 127) // 128 * 128) * H * 12 + 4096, dtype=torch.uint8, device="cuda")
     w = st["w"].tensors
     M = inp.mod.shape[0]
     norm_bytes = R * H * 4 + R * H * 2 + 2 * M * H * 4
@@ -235,11 +237,13 @@ def _kernel_breakdown(torch, D, st, inp, steps):
                                                  st["is_"], q, k, vt), 2.0 * R * 3 * H * H,
          R * H * 2 + 3 * H * H * 2 + 3 * R * H * 2),
         ("attention", lambda: D.dit_attention(dims, R, q, k, vt, o), 4.0 * R * R * H, 4 * R * H * 2),
-        ("gemm_out_gated", lambda: D.dit_linear_gated(dims, o, sh.L, sh.N, w[1], st["mod"], 0, st["txt"], st["img"]),
+        ("gemm_out_gated", lambda: D.dit_linear_gated(dims, o, sh.L, sh.N, w[1], st["mod"], 0, st["txt"], st["img"],
+                                                  split_ws),
          2.0 * R * H * H, gated_bytes(H)),
         ("gemm_up_swiglu", lambda: D.dit_linear_swiglu(dims, h, w[2], a), 2.0 * R * 2 * F * H,
          R * H * 2 + 2 * F * H * 2 + R * F * 2),
-        ("gemm_down_gated", lambda: D.dit_linear_gated(dims, a, sh.L, sh.N, w[3], st["mod"], 1, st["txt"], st["img"]),
+        ("gemm_down_gated", lambda: D.dit_linear_gated(dims, a, sh.L, sh.N, w[3], st["mod"], 1, st["txt"], st["img"],
+                                                   split_ws),
          2.0 * R * F * H, gated_bytes(F)),
     ]
     out = {}

@@ -84,7 +84,7 @@ _SIGNATURES = {
     "dit_vt_stride": (c_int, [c_int]),
     "dit_attention": (c_int, [POINTER(dit_dims), c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dit_linear_gated": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_int, c_void_p, POINTER(dit_mod), c_int,
-                                 c_void_p, c_void_p, c_void_p]),
+                                 c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "dit_linear_swiglu": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
     "dit_linear": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p]),
     "dit_dequant_int8": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
@@ -319,11 +319,14 @@ def dit_attention(dims: DitDims, R: int, q, k, vt, o, stream=None):
                             _ptr(o, bf, "o"), _stream(stream)), "dit_attention")
 
 
-def dit_linear_gated(dims: DitDims, a, L: int, N: int, w, mod: Modulation, which: int, txt, img, stream=None):
+def dit_linear_gated(dims: DitDims, a, L: int, N: int, w, mod: Modulation, which: int, txt, img, ws=None,
+                     stream=None):
     import torch
     bf, f32 = _bf16(), torch.float32
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _ok(lib().dit_linear_gated(ctypes.byref(dims.c), _ptr(a, bf, "a"), L, N, _ptr(w, bf, "w"), ctypes.byref(mod.c),
-                               which, _ptr(txt, f32, "txt"), _ptr(img, f32, "img"), _stream(stream)),
+                               which, _ptr(txt, f32, "txt"), _ptr(img, f32, "img"), _ptr(ws), ws_bytes,
+                               _stream(stream)),
         "dit_linear_gated")
 
 

@@ -167,6 +167,9 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.gate = mod.rows + 2LL * H;
   g.map = mod.map;
   g.gate_stride = 6LL * H;
+  // scratch for the K-split of the last wave: the SwiGLU buffer, not yet written
+  g.split_ws = b.a;
+  g.split_ws_bytes = size_t(R) * F * 2;
   if (w8) q8 = GemmInt8B{w8->q[1], w8->s[1], i8_tiles};
   if ((rc = gemm_launch(b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
 
@@ -191,6 +194,9 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.gate = mod.rows + 5LL * H;
   g.map = mod.map;
   g.gate_stride = 6LL * H;
+  // scratch for the K-split of the last wave: h, q, k, vt and o, all consumed by now
+  g.split_ws = b.h;
+  g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
   if (w8) q8 = GemmInt8B{w8->q[3], w8->s[3], i8_tiles};
   return gemm_launch(b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, kEpiGated, g, st);
 }
@@ -384,12 +390,13 @@ int dit_attention(const dit_dims* d, int R, const uint16_t* q, const uint16_t* k
 }
 
 int dit_linear_gated(const dit_dims* d, const uint16_t* a, int L, int N, const uint16_t* w, const dit_mod* mod,
-                     int which, float* txt, float* img, dit_stream_t stream) {
+                     int which, float* txt, float* img, void* ws, size_t ws_bytes, dit_stream_t stream) {
   if (!d || !a || !w || !mod || !mod->rows || mod->M < 1 || !img || L < 0 || N < 1 || (L > 0 && !txt) ||
       (which != 0 && which != 1))
     return DIT_EINVAL;
   if (!dims_ok(d)) return DIT_EUNSUPPORTED;
   if (!al16(a) || !al16(w) || !al16(img) || (txt && !al16(txt)) || !al16(mod->rows)) return DIT_EINVAL;
+  if (ws && reinterpret_cast<uintptr_t>(ws) % 256 != 0) return DIT_EINVAL;
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int H = d->hidden, K = which == 0 ? H : d->ffn;
@@ -400,6 +407,8 @@ int dit_linear_gated(const dit_dims* d, const uint16_t* a, int L, int N, const u
   g.gate = mod->rows + (which == 0 ? 2LL : 5LL) * H;
   g.map = mod->map;
   g.gate_stride = 6LL * H;
+  g.split_ws = ws_bytes ? ws : nullptr;
+  g.split_ws_bytes = ws ? ws_bytes : 0;
   return gemm_launch(a, K, w, nullptr, kEpiGated, g, reinterpret_cast<cudaStream_t>(stream));
 }
 

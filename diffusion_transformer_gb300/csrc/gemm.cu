@@ -362,6 +362,98 @@ __device__ __forceinline__ void convert_kblock(const uint8_t* src8, const uint16
   }
 }
 
+// ----------------------------------------------------------------------------------------------
+// Work items of the persistent loop. With p.split > 1, the tiles from p.sk_first on (as many as
+// the last, partial wave would hold) are each cut into p.split equal K-ranges, and these parts come
+// first: they spread that wave's work over all SMs, and each split tile is finished while whole
+// tiles still run, so the kernel ends on ordinary tiles. Then come the whole tiles 0 .. sk_first-1.
+// ----------------------------------------------------------------------------------------------
+struct WorkItem {
+  int tile, k0, k1, part;  // part < 0: the whole tile
+};
+__device__ __forceinline__ WorkItem work_item(const GemmParams& p, int it, int tiles, int KB) {
+  if (p.split <= 1) return WorkItem{it, 0, KB, -1};
+  const int n_parts = (tiles - p.sk_first) * p.split;
+  if (it >= n_parts) return WorkItem{it - n_parts, 0, KB, -1};
+  const int part = it % p.split, kl = KB / p.split;
+  return WorkItem{p.sk_first + it / p.split, part * kl, (part + 1) * kl, part};
+}
+
+// Gated residual of a K-split tile, part 1: the warp's 32 rows of its partial accumulator go to
+// their slot (fp32, row stride BN) through the shared transpose, as whole 128-byte lines.
+template <int BN>
+__device__ __forceinline__ void split_store(uint32_t taddr, float* slot, int lane, uint8_t* stage) {
+  const int cq = lane & 7;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<uint4*>(stage + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+          make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rl = (lane >> 3) + 4 * i;
+      const float4 a = *reinterpret_cast<const float4*>(stage + rl * 128 + ((cq ^ (rl & 7)) << 4));
+      __stcg(reinterpret_cast<float4*>(slot + rl * BN + c * 32 + cq * 4), a);
+    }
+    __syncwarp();
+  }
+}
+
+// Part 2, run by the warp that delivered a quadrant's last partial: acc = ((p0 + p1) + p2) ...
+// in part order (the same sum whichever warp finishes last), then x += gate * acc. Every load of a
+// group of four rows is issued before the first add.
+template <int BN, int S>
+__device__ __forceinline__ void split_finish(const GemmParams& p, const float* parts, int row0, int n0, int lane) {
+  const int cq = lane & 7;
+  constexpr size_t kSlot = size_t(BM) * BN;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+#pragma unroll
+    for (int ih = 0; ih < 2; ++ih) {
+      float4 v[4][S], xq[4], gq[4];
+      float* xr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int rl = (lane >> 3) + 4 * (4 * ih + u), r = row0 + rl;
+        const float* src = parts + rl * BN + c * 32 + cq * 4;
+#pragma unroll
+        for (int q = 0; q < S; ++q) v[u][q] = __ldcg(reinterpret_cast<const float4*>(src + q * kSlot));
+        xr[u] = nullptr;
+        if (r < p.M) {
+          xr[u] = (r < p.L ? p.txt + size_t(r) * p.N : p.img + size_t(r - p.L) * p.N) + n0 + c * 32 + cq * 4;
+          xq[u] = *reinterpret_cast<const float4*>(xr[u]);
+          gq[u] = __ldg(reinterpret_cast<const float4*>(p.gate + size_t(p.map ? __ldg(p.map + r) : 0) * p.gate_stride +
+                                                        n0 + c * 32 + cq * 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float4 a = v[u][0];
+#pragma unroll
+        for (int q = 1; q < S; ++q) {
+          a.x += v[u][q].x;
+          a.y += v[u][q].y;
+          a.z += v[u][q].z;
+          a.w += v[u][q].w;
+        }
+        if (xr[u]) {
+          float4 o;
+          o.x = fmaf(gq[u].x, a.x, xq[u].x);
+          o.y = fmaf(gq[u].y, a.y, xq[u].y);
+          o.z = fmaf(gq[u].z, a.z, xq[u].z);
+          o.w = fmaf(gq[u].w, a.w, xq[u].w);
+          *reinterpret_cast<float4*>(xr[u]) = o;
+        }
+      }
+    }
+  }
+}
+
 template <int BN, int EPI, bool B8>
 __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -405,6 +497,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
   };
   const int tiles = num_m * num_n;
   const int KB = p.K / BK;
+  const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -443,10 +536,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const WorkItem w = work_item(p, it, tiles, KB);
         int mb, nb;
-        tile_mn(tile, mb, nb);
-        for (int kb = 0; kb < KB; ++kb) {
+        tile_mn(w.tile, mb, nb);
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, kErrTimeoutProducer)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, Cfg::kABytes + (B8 ? Cfg::kB8Bytes + Cfg::kSBytes : Cfg::kBBytes));
@@ -479,11 +573,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const WorkItem w = work_item(p, it, tiles, KB);
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, kErrTimeoutMma)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * Cfg::kMH * BN);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait(smem_u32(&full[stage]), phase, p.err, kErrTimeoutMma)) { ok = false; break; }
           uint32_t b_addr;
           if constexpr (B8) {
@@ -500,7 +595,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes per K=16 step inside the swizzle atom
               umma_bf16(d + uint32_t(h * BN), adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc,
-                        (kb | kk) != 0);
+                        kb != w.k0 || kk != 0);
           }
           umma_commit(smem_u32(&empty[stage]));
           if constexpr (B8) {
@@ -524,11 +619,36 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     uint8_t* stage = sE + (warp - 2) * 4096;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+      const WorkItem w = work_item(p, it, tiles, KB);
       int mb, nb;
-      tile_mn(tile, mb, nb);
+      tile_mn(w.tile, mb, nb);
       if (!mbar_wait_warp(smem_u32(&tfull[acc]), acc_phase, p.err, kErrTimeoutEpilogue)) break;
       tc_fence_after();
+      if constexpr (EPI == kEpiGated && !B8) {
+        if (w.part >= 0) {
+          // K-split tile: publish this part, release the accumulator, and let the warp that
+          // delivers the quadrant's last part apply the residual update
+          const int ti = w.tile - p.sk_first;
+          float* parts = p.split_part + size_t(ti) * p.split * BM * BN + size_t(quad) * 32 * BN;
+          const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
+          split_store<BN>(taddr, parts + size_t(w.part) * BM * BN, lane, stage);
+          tc_fence_before();
+          mbar_arrive(smem_u32(&tempty[acc]));
+          if (++acc == Cfg::kAccBufs) { acc = 0; acc_phase ^= 1; }
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) last = atomicAdd(p.split_cnt + ti * 4 + quad, 1) == p.split - 1;
+          if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence();
+            const int r0 = mb * BM + quad * 32, n0 = nb * BN;
+            if (p.split == 2) split_finish<BN, 2>(p, parts, r0, n0, lane);
+            else split_finish<BN, 3>(p, parts, r0, n0, lane);
+          }
+          continue;
+        }
+      }
 #pragma unroll 1
       for (int h = 0; h < Cfg::kMH; ++h) {
         const uint32_t taddr =
@@ -546,8 +666,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     int stage = 0, cstage = 0;
     uint32_t phase = 0, cphase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb) {
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      const WorkItem w = work_item(p, it, tiles, KB);
+      for (int kb = w.k0; kb < w.k1; ++kb) {
         if (!mbar_wait(smem_u32(&full[stage]), phase, p.err, kErrTimeoutConverter)) { ok = false; break; }
         if (!mbar_wait(smem_u32(&cempty[cstage]), cphase ^ 1, p.err, kErrTimeoutConverter)) { ok = false; break; }
         convert_kblock<BN, Cfg::kConvThreads>(sB + stage * Cfg::kB8Bytes,
@@ -576,7 +697,8 @@ int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
   auto kern = gemm_kernel<BN, EPI, B8>;
   if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
   const int tiles = ((p.M + Cfg::kTileM - 1) / Cfg::kTileM) * (p.N / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
+  const int grid = items < num_sms() ? items : num_sms();
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, ts, p);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
@@ -635,10 +757,44 @@ int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmI
   if (reinterpret_cast<uintptr_t>(b) % 16) return DIT_EINVAL;
   if (!make_tmap_2d(&tb, b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K, p.N, (long long)p.K * 2, BK, BN, true))
     return DIT_ECUDA;
+  GemmParams q = p;
+  q.split = 1;
+  if (epi == kEpiGated && p.split_ws) {
+    // The last wave holds tail < SMs tiles: cut each into s = 2 or 3 K-ranges (s divides K/64)
+    // when that shortens the critical path, counted in tile-times: waves + ceil(tail s / SMs) / s
+    // (e.g. 396 tiles on 152 SMs: 3 tile-times whole, 2.67 with s = 3). Each part keeps at least 32
+    // k-blocks: finishing a split tile reads s partials besides x and the gate, and only a long
+    // mainloop hides that (measured at 4224 rows, hidden 3072: K = 12288 222 -> 209 us with s = 3,
+    // K = 3072 71 -> 127 us). The partial slots and the arrival counters live in the caller's
+    // scratch; the counters start at zero.
+    const int T = ((p.M + BM - 1) / BM) * (p.N / BN), P = num_sms(), KB = p.K / BK;
+    if (T > P && T % P != 0) {
+      const int waves = T / P, tail = T - waves * P;
+      double best = waves + 1.0;
+      size_t slot_bytes = 0;
+      for (int sp : {2, 3}) {
+        if (KB % sp != 0 || KB / sp < 32) continue;
+        const size_t sb = (size_t(tail) * sp * BM * BN * 4 + 255) / 256 * 256;
+        if (sb + size_t(tail) * 4 * sizeof(int) > p.split_ws_bytes) continue;
+        const double c = waves + double((tail * sp + P - 1) / P) / sp;
+        if (c < best - 1e-9) {
+          best = c;
+          q.split = sp;
+          slot_bytes = sb;
+        }
+      }
+      if (q.split > 1) {
+        q.sk_first = waves * P;
+        q.split_part = static_cast<float*>(p.split_ws);
+        q.split_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(p.split_ws) + slot_bytes);
+        if (cudaMemsetAsync(q.split_cnt, 0, size_t(tail) * 4 * sizeof(int), stream) != cudaSuccess) return DIT_ECUDA;
+      }
+    }
+  }
   switch (BN) {
-    case 256: return dispatch_epi<256, false>(epi, ta, tb, tb, p, stream);
-    case 128: return dispatch_epi<128, false>(epi, ta, tb, tb, p, stream);
-    default: return dispatch_epi<64, false>(epi, ta, tb, tb, p, stream);
+    case 256: return dispatch_epi<256, false>(epi, ta, tb, tb, q, stream);
+    case 128: return dispatch_epi<128, false>(epi, ta, tb, tb, q, stream);
+    default: return dispatch_epi<64, false>(epi, ta, tb, tb, q, stream);
   }
 }
 

@@ -43,6 +43,13 @@ struct GemmParams {
   const float *txt_cos, *txt_sin, *img_cos, *img_sin;  // [L, d/2], [R-L, d/2]
   const float *q_norm, *k_norm;                         // [d] or null
   float qk_eps;
+  // gated residual, bf16 weights: scratch for the K-split of the last, partial wave of tiles (may be
+  // null: no split). Set by gemm_launch: split ways, first split tile, partial slots and counters.
+  void* split_ws;
+  size_t split_ws_bytes;
+  int split, sk_first;
+  float* split_part;   // [tail tiles][split][128][BN] fp32
+  int* split_cnt;      // [tail tiles][4] arrivals per 32-row quadrant
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row

@@ -212,9 +212,15 @@ DIT_API int dit_attention(const dit_dims* dims, int R, const uint16_t* q, const 
 
 /* Linear with gated residual [gizai:dit, gatedInto]: x[r] += gate[map[r]] * (a[r] W^T) for the
  * attention (which = 0, W = wout [H, H], a [R, H]) or the MLP (which = 1, W = wdown [H, F],
- * a [R, F]) gate of the modulation rows. x rows < L in txt, others in img. */
+ * a [R, F]) gate of the modulation rows. x rows < L in txt, others in img.
+ * ws / ws_bytes: optional device scratch (NULL / 0 allowed; 256-byte aligned). When the output
+ * tiles do not fill a whole number of waves over the SMs, the tiles of the last wave are split
+ * along K into partial sums that fit in the scratch and added in a fixed order (the result does
+ * not depend on timing); ((R + 127) / 128 * 128) * H * 12 + 4096 bytes always suffice. Without
+ * scratch every tile is computed whole. */
 DIT_API int dit_linear_gated(const dit_dims* dims, const uint16_t* a, int L, int N, const uint16_t* w,
-                     const dit_mod* mod, int which, float* txt, float* img, dit_stream_t stream);
+                     const dit_mod* mod, int which, float* txt, float* img, void* ws, size_t ws_bytes,
+                     dit_stream_t stream);
 
 /* Up linear with SwiGLU epilogue [gizai:dit, gluRows]: u = h2 Wup^T [R, 2F];
  * a[r, j] = bf16(silu(u[r, 2j]) * u[r, 2j+1]) [R, F]. */
