@@ -34,6 +34,7 @@ __all__ = [
     "bf16_bits_from_f32",
     "block_inputs",
     "int8_block_inputs",
+    "parallel_block_inputs",
     "denoise_inputs",
 ]
 
@@ -153,6 +154,17 @@ def block_inputs(shape: BlockShape | str, M: Optional[int] = None, norm_weights:
         out.norm2 = (1 + 0.02 * g.standard_normal(H)).astype(np.float32)
         out.q_norm = (1 + 0.02 * g.standard_normal(d)).astype(np.float32)
         out.k_norm = (1 + 0.02 * g.standard_normal(d)).astype(np.float32)
+    return out
+
+
+def parallel_block_inputs(shape: BlockShape | str, M: Optional[int] = None, norm_weights: bool = False,
+                          seed: Optional[int] = None) -> BlockInputs:
+    """Inputs of one parallel (single-stream) block: the weights and rows of ``block_inputs`` and
+    its own modulation rows [M, 3, H] (shift, scale, gate), N(0, 0.1). Only ``norm1`` is used."""
+    out = block_inputs(shape, M=M, norm_weights=norm_weights, seed=seed)
+    s = out.shape.seed if seed is None else seed
+    Mr = out.mod.shape[0]
+    out.mod = _rng(s, 4).standard_normal((Mr, 3, out.shape.hidden), dtype=np.float32) * np.float32(0.1)
     return out
 
 

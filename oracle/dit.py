@@ -30,6 +30,7 @@ __all__ = [
     "modulated_rmsnorm", "qk_rmsnorm", "rope_apply", "attention", "silu", "swiglu_interleaved",
     "block_forward", "block_forward_rows", "dequant_int8", "euler_step", "shift_sigmas",
     "timestep_sinusoids", "time_embedding", "denoise", "pack_latents", "block_weights_f64",
+    "modulated_layernorm", "parallel_block_forward", "parallel_block_forward_rows",
 ]
 
 
@@ -232,6 +233,70 @@ def block_forward(inp, weights=None, rows=None):
     y = block_forward_rows(x, W, inp.mod, inp.mod_map, cos, sin, sh.heads, sh.head_dim, rows=rows,
                            norm1=inp.norm1, norm2=inp.norm2, q_norm=inp.q_norm, k_norm=inp.k_norm,
                            eps=sh.eps, qk_eps=sh.qk_eps)
+    if rows is not None:
+        return y
+    return y[:sh.L], y[sh.L:]
+
+
+# ----------------------------------------------------------------------------------------------
+# parallel (single-stream) block  [gizai:dit, Block.parallel]
+# ----------------------------------------------------------------------------------------------
+
+def modulated_layernorm(x, w, shift, scale, eps):
+    """y = (x - mean(x)) * (var(x) + eps)^-1/2 * w * (1 + scale) + shift, row by row, var the mean
+    of squared deviations (biased). w None means ones. Float64.
+
+    The parallel block names a modulated LayerNorm (gizai:dit, Block.parallel); the pages give no
+    formula, so this is the textbook LayerNorm with the block's shift/scale modulation and eps."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    dev = x - mu
+    var = (dev * dev).mean(axis=-1, keepdims=True)
+    y = dev / np.sqrt(var + eps)
+    if w is not None:
+        y = y * np.asarray(w, dtype=np.float64)
+    return y * (1.0 + np.asarray(scale, dtype=np.float64)) + np.asarray(shift, dtype=np.float64)
+
+
+def parallel_block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
+                                rows: Optional[np.ndarray] = None, norm=None, q_norm=None, k_norm=None,
+                                eps=1e-6, qk_eps=1e-6):
+    """The parallel block over the packed rows x [R, H]: both branches read one modulated norm.
+
+    1. h = modulated LayerNorm(x; norm, shift, scale)         mod rows [M, 3, H] = shift, scale, gate
+    2. [q|k|v] = h Wqkv^T; q, k per-head RMS norm, rotated    (as in the sequential block)
+    3. o = softmax(q k^T / sqrt(d)) v
+    4. a_j = silu(u_{2j}) u_{2j+1}, u = h Wup^T               (gate/up rows interleaved)
+    5. x + gate * (o Wout^T + a Wdown^T)
+
+    Steps 1-2 run for every row, 3-5 for ``rows`` (all by default).
+    [gizai:dit, Block.parallel; weightAt, prepOf and gluRows for the shared pieces]"""
+    x = np.asarray(x, dtype=np.float64)
+    R, H = x.shape
+    nh, d = heads, head_dim
+    Wqkv, Wout, Wup, Wdown = weights
+    rows = np.arange(R) if rows is None else np.asarray(rows)
+    m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)]
+    h = modulated_layernorm(x, norm, m[:, 0], m[:, 1], eps)
+    qkv = h @ Wqkv.T
+    q = rope_apply(qk_rmsnorm(qkv[:, 0:H].reshape(R, nh, d), q_norm, qk_eps), cos, sin)
+    k = rope_apply(qk_rmsnorm(qkv[:, H:2 * H].reshape(R, nh, d), k_norm, qk_eps), cos, sin)
+    v = qkv[:, 2 * H:3 * H].reshape(R, nh, d)
+    o = attention(q, k, v, rows)
+    a = swiglu_interleaved(h[rows] @ Wup.T)
+    return x[rows] + m[rows, 2] * (o @ Wout.T + a @ Wdown.T)
+
+
+def parallel_block_forward(inp, weights=None, rows=None):
+    """Parallel block on ``dit_inputs.parallel_block_inputs``: (txt_out, img_out) float64, or the
+    packed output rows ``rows`` when given."""
+    sh = inp.shape
+    x = np.concatenate([inp.txt, inp.img], axis=0).astype(np.float64)
+    cos, sin = rope_tables(positions(sh.L, sh.grid_h, sh.grid_w), sh.head_dim)
+    W = block_weights_f64(inp) if weights is None else weights
+    y = parallel_block_forward_rows(x, W, inp.mod, inp.mod_map, cos, sin, sh.heads, sh.head_dim, rows=rows,
+                                    norm=inp.norm1, q_norm=inp.q_norm, k_norm=inp.k_norm, eps=sh.eps,
+                                    qk_eps=sh.qk_eps)
     if rows is not None:
         return y
     return y[:sh.L], y[sh.L:]

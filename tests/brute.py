@@ -76,3 +76,61 @@ def block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_e
         mlp = matvec(Wd, a)
         out.append([xr[i] + gm[i] * mlp[i] for i in range(H)])
     return out
+
+
+def layernorm_row(x, eps):
+    mu = sum(x) / len(x)
+    var = sum((v - mu) * (v - mu) for v in x) / len(x)
+    r = 1.0 / math.sqrt(var + eps)
+    return [(v - mu) * r for v in x]
+
+
+def parallel_block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
+                   norm=None, qn=None, kn=None):
+    """The parallel block: x + gate * (attention + SwiGLU MLP), both branches reading one modulated
+    LayerNorm. mod_rows[r] = 3 lists of H (shift, scale, gate) for row r. Returns new rows."""
+    R, H = len(x), len(x[0])
+    one = lambda n: [1.0] * n
+    w = norm or one(H)
+    qn = qn or one(d)
+    kn = kn or one(d)
+    hs, Q, K, V = [], [], [], []
+    for r in range(R):
+        shift, scale = mod_rows[r][0], mod_rows[r][1]
+        y = layernorm_row(x[r], eps)
+        h = [y[i] * w[i] * (1.0 + scale[i]) + shift[i] for i in range(H)]
+        hs.append(h)
+        q, k, v = matvec(Wq, h), matvec(Wk, h), matvec(Wv, h)
+        qh, kh, vh = [], [], []
+        for n in range(heads):
+            for (src, wt, dst) in ((q, qn, qh), (k, kn, kh)):
+                seg = rmsnorm_row(src[n * d:(n + 1) * d], qk_eps)
+                seg = [seg[j] * wt[j] for j in range(d)]
+                rot = [0.0] * d
+                for i in range(d // 2):
+                    a, b = seg[2 * i], seg[2 * i + 1]
+                    c, s = cos[r][i], sin[r][i]
+                    rot[2 * i] = a * c - b * s
+                    rot[2 * i + 1] = a * s + b * c
+                dst.append(rot)
+            vh.append(v[n * d:(n + 1) * d])
+        Q.append(qh)
+        K.append(kh)
+        V.append(vh)
+    out = []
+    for r in range(R):
+        o = []
+        for n in range(heads):
+            scores = [sum(Q[r][n][j] * K[c][n][j] for j in range(d)) / math.sqrt(d) for c in range(R)]
+            m = max(scores)
+            e = [math.exp(s - m) for s in scores]
+            z = sum(e)
+            for j in range(d):
+                o.append(sum(e[c] / z * V[c][n][j] for c in range(R)))
+        att = matvec(Wo, o)
+        g, u = matvec(Wg, hs[r]), matvec(Wu, hs[r])
+        a = [g[j] / (1.0 + math.exp(-g[j])) * u[j] for j in range(len(g))]
+        mlp = matvec(Wd, a)
+        gate = mod_rows[r][2]
+        out.append([x[r][i] + gate[i] * (att[i] + mlp[i]) for i in range(H)])
+    return out
