@@ -201,6 +201,65 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   return gemm_launch(b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, kEpiGated, g, st);
 }
 
+// The parallel (single-stream) block [gizai:dit, Block.parallel]: one modulated LayerNorm feeds
+// both branches; mod rows [M, 3, H] = shift, scale, gate. Four launches: the norm, one GEMM over
+// [Wqkv ; Wup] with the QKV epilogue on its first 3H columns and SwiGLU on the rest, the attention,
+// and one GEMM over [o | a] [Wout | Wdown]^T with the gated residual.
+int run_parallel_block(const dit_dims* d, const dit_block_w* w, float* txt, int L, float* img, int N,
+                       const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod,
+                       void* ws, cudaStream_t st) {
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  const int R = L + N, H = d->hidden, F = d->ffn;
+  const BlockWs b = carve_block_ws(d, R, ws);
+  int rc;
+
+  // 1. h = LayerNorm(x) * norm * (1 + scale) + shift
+  ModNormParams mp{txt, img, L, R, H, H, H, w->norm1, mod.rows, mod.rows + H, 3LL * H, mod.map, d->eps, b.h};
+  mp.layernorm = 1;
+  if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+
+  // 2. q, k, vt (QK-norm + rope epilogue) and a (SwiGLU epilogue) from h [Wqkv ; Wup]^T
+  GemmParams g = base_params(R, 3 * H + 2 * F, H, err);
+  g.q = b.q;
+  g.k = b.k;
+  g.vt = b.vt;
+  g.H = H;
+  g.heads = d->heads;
+  g.head_dim = d->head_dim;
+  g.Rp = vt_stride(R);
+  g.L = L;
+  g.txt_cos = tc;
+  g.txt_sin = ts;
+  g.img_cos = ic;
+  g.img_sin = is;
+  g.q_norm = w->q_norm;
+  g.k_norm = w->k_norm;
+  g.qk_eps = d->qk_eps;
+  g.out = b.a;
+  g.ldo = F;
+  g.n_split = 3 * H;
+  if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, w->wqkv, H, w->wup, H, kEpiQKVSwiGLU, g, st)) != DIT_OK) return rc;
+
+  // 3. o = attention(q, k, v)
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+  if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
+
+  // 4. x += gate * ([o | a] [Wout | Wdown]^T)
+  g = base_params(R, H, H + F, err);
+  g.txt = txt;
+  g.img = img;
+  g.L = L;
+  g.gate = mod.rows + 2LL * H;
+  g.map = mod.map;
+  g.gate_stride = 3LL * H;
+  g.k_split = H;
+  // scratch for the K-split of the last wave: h, q, k and vt, all consumed by now
+  g.split_ws = b.h;
+  g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.o) - reinterpret_cast<uint8_t*>(b.h));
+  return gemm_launch_cat(b.o, H, b.a, F, w->wout, H, w->wdown, F, kEpiGated, g, st);
+}
+
 int check_block_args(const dit_dims* d, const float* txt, int L, const float* img, int N, const float* tc,
                      const float* ts, const float* ic, const float* is, const dit_mod* mod, const void* ws,
                      size_t ws_bytes, int variant) {
@@ -279,7 +338,7 @@ const char* dit_status_string(int s) {
 }
 
 size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
-  if (!dims_ok(d) || L < 0 || N < 1 || (variant != 0 && variant != 1)) return 0;
+  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 2) return 0;
   size_t bytes = carve_block_ws(d, L + N, nullptr).bytes;
   if (variant == 1) bytes += int8_scratch_bytes(d);
   return bytes;
@@ -310,6 +369,18 @@ int dit_block_forward(const dit_dims* d, const dit_block_w* w, float* txt, int L
   if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
   return run_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_parallel_block_forward(const dit_dims* d, const dit_block_w* w, float* txt, int L, float* img, int N,
+                               const float* tc, const float* ts, const float* ic, const float* is, const dit_mod* mod,
+                               void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 2);
+  if (rc != DIT_OK) return rc;
+  if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+  if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  if (d->hidden % 256 != 0 || d->ffn % 128 != 0) return DIT_EUNSUPPORTED;  // 256-wide tiles over 3H and 2F
+  return run_parallel_block(d, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dit_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt, int L, float* img, int N,

@@ -17,7 +17,23 @@ constexpr int kNormThreads = 256;
 // the row (x, shift, scale, w) is issued before the reduction, so one pass over global memory
 // serves both the statistics and the output. NC = float4 chunks per thread (H = NC * 4 * 256);
 // NC = 0 is the generic two-pass form for other widths.
-template <int NC>
+// Sum over the CTA (every thread gets the same total, added in the same order).
+__device__ __forceinline__ float block_sum(float v, float* part) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();  // earlier readers of part are done
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
+  return tot;
+}
+
+// LN = false: RMS norm (the row's mean taken as 0, so (x - 0) is x exactly); LN = true: LayerNorm,
+// the mean subtracted first and the variance taken over the deviations (two passes over values held
+// in registers, no E[x^2] - mean^2 cancellation).
+template <int NC, bool LN>
 __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormParams p) {
   const int r = blockIdx.x;
   const float* x = r < p.L ? p.txt + size_t(r) * p.ld_txt : p.img + size_t(r - p.L) * p.ld_img;
@@ -39,6 +55,20 @@ __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormPara
       sc[k] = __ldg(sc4 + i);
       wv[k] = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
     }
+    float mean = 0.f;
+    if constexpr (LN) {
+      float s1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) s1 += (xv[k].x + xv[k].y) + (xv[k].z + xv[k].w);
+      mean = block_sum(s1, part) / float(p.H);
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        xv[k].x -= mean;
+        xv[k].y -= mean;
+        xv[k].z -= mean;
+        xv[k].w -= mean;
+      }
+    }
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
@@ -47,14 +77,7 @@ __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormPara
       ss = fmaf(xv[k].z, xv[k].z, ss);
       ss = fmaf(xv[k].w, xv[k].w, ss);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
-    const float rstd = rsqrtf(tot / float(p.H) + p.eps);
+    const float rstd = rsqrtf(block_sum(ss, part) / float(p.H) + p.eps);
     uint2* out = reinterpret_cast<uint2*>(p.out + size_t(r) * p.H);
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
@@ -65,22 +88,25 @@ __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormPara
       out[threadIdx.x + k * kNormThreads] = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
     }
   } else {
+    float mean = 0.f;
+    if constexpr (LN) {
+      float s1 = 0.f;
+      for (int i = threadIdx.x; i < n4; i += kNormThreads) {
+        const float4 v = x4[i];
+        s1 += (v.x + v.y) + (v.z + v.w);
+      }
+      mean = block_sum(s1, part) / float(p.H);
+    }
     float ss = 0.f;
     for (int i = threadIdx.x; i < n4; i += kNormThreads) {
       const float4 v = x4[i];
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
+      const float a = v.x - mean, b = v.y - mean, c = v.z - mean, d = v.w - mean;
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
+      ss = fmaf(c, c, ss);
+      ss = fmaf(d, d, ss);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
-    const float rstd = rsqrtf(tot / float(p.H) + p.eps);
+    const float rstd = rsqrtf(block_sum(ss, part) / float(p.H) + p.eps);
     uint2* out = reinterpret_cast<uint2*>(p.out + size_t(r) * p.H);
     for (int i = threadIdx.x; i < n4; i += kNormThreads) {
       const float4 v = x4[i];
@@ -88,10 +114,10 @@ __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormPara
       const float4 scv = __ldg(sc4 + i);
       float4 w = make_float4(1.f, 1.f, 1.f, 1.f);
       if (w4) w = __ldg(w4 + i);
-      const float y0 = fmaf(v.x * rstd * w.x, 1.f + scv.x, shv.x);
-      const float y1 = fmaf(v.y * rstd * w.y, 1.f + scv.y, shv.y);
-      const float y2 = fmaf(v.z * rstd * w.z, 1.f + scv.z, shv.z);
-      const float y3 = fmaf(v.w * rstd * w.w, 1.f + scv.w, shv.w);
+      const float y0 = fmaf((v.x - mean) * rstd * w.x, 1.f + scv.x, shv.x);
+      const float y1 = fmaf((v.y - mean) * rstd * w.y, 1.f + scv.y, shv.y);
+      const float y2 = fmaf((v.z - mean) * rstd * w.z, 1.f + scv.z, shv.z);
+      const float y3 = fmaf((v.w - mean) * rstd * w.w, 1.f + scv.w, shv.w);
       out[i] = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
     }
   }
@@ -225,12 +251,22 @@ int grid_for(long long n, int threads) {
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream) {
   if (p.R <= 0) return DIT_OK;
   const int chunks = p.H % (4 * kNormThreads) == 0 ? p.H / (4 * kNormThreads) : 0;
-  switch (chunks) {
-    case 1: modnorm_kernel<1><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    case 2: modnorm_kernel<2><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    case 3: modnorm_kernel<3><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    case 4: modnorm_kernel<4><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    default: modnorm_kernel<0><<<p.R, kNormThreads, 0, stream>>>(p); break;
+  if (p.layernorm) {
+    switch (chunks) {
+      case 1: modnorm_kernel<1, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 2: modnorm_kernel<2, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 3: modnorm_kernel<3, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 4: modnorm_kernel<4, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      default: modnorm_kernel<0, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    }
+  } else {
+    switch (chunks) {
+      case 1: modnorm_kernel<1, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 2: modnorm_kernel<2, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 3: modnorm_kernel<3, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 4: modnorm_kernel<4, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      default: modnorm_kernel<0, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    }
   }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }

@@ -457,7 +457,8 @@ __device__ __forceinline__ void split_finish(const GemmParams& p, const float* p
 template <int BN, int EPI, bool B8>
 __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmS, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   using Cfg = GemmCfg<BN, B8>;
   constexpr int S = Cfg::kStages;
   constexpr int CS = Cfg::kConvStages;
@@ -519,6 +520,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if constexpr (B8) tma_prefetch_desc(&tmS);
+    if (p.k_split > 0) tma_prefetch_desc(&tmA2);
+    if (p.k_split > 0 || p.n_split > 0) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -544,16 +547,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, kErrTimeoutProducer)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, Cfg::kABytes + (B8 ? Cfg::kB8Bytes + Cfg::kSBytes : Cfg::kBBytes));
+          // concatenated operands: the second A/B past the K boundary, the second B past the N boundary
+          const bool k2 = p.k_split > 0 && kb * BK >= p.k_split;
+          const bool n2 = p.n_split > 0 && nb * BN >= p.n_split;
+          const CUtensorMap* ma = k2 ? &tmA2 : &tmA;
+          const CUtensorMap* mbm = (k2 || n2) ? &tmB2 : &tmB;
+          const int kc = k2 ? kb * BK - p.k_split : kb * BK;
+          const int nr = n2 ? nb * BN - p.n_split : nb * BN;
 #pragma unroll
           for (int h = 0; h < Cfg::kMH; ++h)
-            tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), &tmA, fb, kb * BK,
+            tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), ma, fb, kc,
                         mb * Cfg::kTileM + h * BM);
           if constexpr (B8) {
             tma_load_2d(smem_u32(sB + stage * Cfg::kB8Bytes), &tmB, fb, kb * BK, nb * BN);
             // scales of k-blocks (kb & ~3) .. (kb | 3): 8 bf16 per row, 16-byte aligned columns
             tma_load_2d(smem_u32(sSc + stage * Cfg::kSBytes), &tmS, fb, (kb * 2) & ~7, nb * BN);
           } else
-            tma_load_2d(smem_u32(sB + stage * Cfg::kBBytes), &tmB, fb, kb * BK, nb * BN);
+            tma_load_2d(smem_u32(sB + stage * Cfg::kBBytes), mbm, fb, kc, nr);
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1; }
@@ -653,8 +663,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
       for (int h = 0; h < Cfg::kMH; ++h) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + uint32_t((acc * Cfg::kMH + h) * BN + col0);
-        epilogue_tile<Cfg::kEpiCols, EPI, B8>(p, taddr, mb * Cfg::kTileM + h * BM + quad * 32, lane, nb * BN + col0,
-                                          stage);
+        const int row0 = mb * Cfg::kTileM + h * BM + quad * 32, n0 = nb * BN + col0;
+        if constexpr (EPI == kEpiQKVSwiGLU) {
+          if (n0 < p.n_split)
+            epilogue_tile<Cfg::kEpiCols, kEpiQKV, B8>(p, taddr, row0, lane, n0, stage);
+          else
+            epilogue_tile<Cfg::kEpiCols, kEpiSwiGLU, B8>(p, taddr, row0, lane, n0 - p.n_split, stage);
+        } else {
+          epilogue_tile<Cfg::kEpiCols, EPI, B8>(p, taddr, row0, lane, n0, stage);
+        }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));
@@ -689,9 +706,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
 }
 
+struct Maps {
+  CUtensorMap a, b, s, a2, b2;  // s, a2, b2 unused unless int8 / concatenated operands (then copies)
+};
+
 template <int BN, int EPI, bool B8>
-int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ts, const GemmParams& p,
-               cudaStream_t stream) {
+int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
   using Cfg = GemmCfg<BN, B8>;
   static_assert(Cfg::kSmemBytes <= 227 * 1024, "shared memory budget");
   auto kern = gemm_kernel<BN, EPI, B8>;
@@ -699,64 +719,34 @@ int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
   const int tiles = ((p.M + Cfg::kTileM - 1) / Cfg::kTileM) * (p.N / BN);
   const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
   const int grid = items < num_sms() ? items : num_sms();
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, ts, p);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(m.a, m.b, m.s, m.a2, m.b2, p);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
 template <int BN, bool B8>
-int dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ts, const GemmParams& p,
-                 cudaStream_t stream) {
+int dispatch_epi(int epi, const Maps& m, const GemmParams& p, cudaStream_t stream) {
   switch (epi) {
-    case kEpiStoreF32: return launch_one<BN, kEpiStoreF32, B8>(ta, tb, ts, p, stream);
-    case kEpiStoreBF16: return launch_one<BN, kEpiStoreBF16, B8>(ta, tb, ts, p, stream);
-    case kEpiSiluBF16: return launch_one<BN, kEpiSiluBF16, B8>(ta, tb, ts, p, stream);
-    case kEpiGated: return launch_one<BN, kEpiGated, B8>(ta, tb, ts, p, stream);
-    case kEpiSwiGLU: return launch_one<BN, kEpiSwiGLU, B8>(ta, tb, ts, p, stream);
-    case kEpiQKV: return launch_one<BN, kEpiQKV, B8>(ta, tb, ts, p, stream);
+    case kEpiStoreF32: return launch_one<BN, kEpiStoreF32, B8>(m, p, stream);
+    case kEpiStoreBF16: return launch_one<BN, kEpiStoreBF16, B8>(m, p, stream);
+    case kEpiSiluBF16: return launch_one<BN, kEpiSiluBF16, B8>(m, p, stream);
+    case kEpiGated: return launch_one<BN, kEpiGated, B8>(m, p, stream);
+    case kEpiSwiGLU: return launch_one<BN, kEpiSwiGLU, B8>(m, p, stream);
+    case kEpiQKV: return launch_one<BN, kEpiQKV, B8>(m, p, stream);
+    case kEpiQKVSwiGLU:
+      if constexpr (BN == 256 && !B8) return launch_one<BN, kEpiQKVSwiGLU, B8>(m, p, stream);
+      return DIT_EUNSUPPORTED;
     default: return DIT_EINVAL;
   }
 }
 
 }  // namespace
 
-int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmInt8B* b8, int epi,
-                const GemmParams& p, cudaStream_t stream) {
-  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return DIT_EINVAL;
-  if (p.K % BK != 0 || p.N % 64 != 0) return DIT_EUNSUPPORTED;
-  if (reinterpret_cast<uintptr_t>(a) % 16 || (lda * 2) % 16) return DIT_EINVAL;
-  // tile width: 256 where it divides N (fewer A re-reads), else 128, else 64
-  int BN = (p.N % 256 == 0) ? 256 : (p.N % 128 == 0 ? 128 : 64);
-  // QKV epilogue: a tile never straddles q/k/v and holds whole heads
-  if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
-  CUtensorMap ta, tb;
-  if (!make_tmap_2d(&ta, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K, p.M, lda * 2, BK, BM, true)) return DIT_ECUDA;
-  if (b8) {
-    if (reinterpret_cast<uintptr_t>(b8->q) % 16 || reinterpret_cast<uintptr_t>(b8->s) % 16) return DIT_EINVAL;
-    if (BN == 64 || p.K % 256 != 0) return DIT_EUNSUPPORTED;  // scale rows must be 16-byte multiples
-    if (p.M > kInt8MainloopMaxM) {
-      // Many M tiles: the in-mainloop converters would dequantise every weight tile once per M tile
-      // (17 times at 4224 rows) and bound the GEMM; dequantising the weight once, HBM-bound, and
-      // running the bf16 mainloop is faster (measured 1.14 against 1.69 ms per 1024sq block).
-      if (!b8->wbf || reinterpret_cast<uintptr_t>(b8->wbf) % 16) return DIT_EINVAL;
-      const int rc = dequant_int8_launch(b8->q, b8->s, b8->wbf, p.N, p.K, stream);
-      if (rc != DIT_OK) return rc;
-      return gemm_launch(a, lda, b8->wbf, nullptr, epi, p, stream);
-    }
-    CUtensorMap ts;
-    // int8lin tiles are 256 x 128: two M=128 MMAs share each converted B k-block and both accumulator
-    // sets fit in TMEM. (256 x 256 tiles, with one accumulator set and no epilogue overlap, measured
-    // 2.02 ms per 1024sq block against 1.87 ms.)
-    BN = 128;
-    if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
-    if (!make_tmap_2d(&tb, b8->q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.K, p.N, p.K, BK, BN, false)) return DIT_ECUDA;
-    if (!make_tmap_2d(&ts, b8->s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, (long long)(p.K / 32) * 2, 8, BN,
-                      false))
-      return DIT_ECUDA;
-    return dispatch_epi<128, true>(epi, ta, tb, ts, p, stream);
-  }
-  if (reinterpret_cast<uintptr_t>(b) % 16) return DIT_EINVAL;
-  if (!make_tmap_2d(&tb, b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K, p.N, (long long)p.K * 2, BK, BN, true))
-    return DIT_ECUDA;
+namespace {
+
+int pick_bn(int N) { return (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64); }
+
+// bf16 weights: the K-split plan of the gated epilogue, then the launch
+int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, cudaStream_t stream) {
   GemmParams q = p;
   q.split = 1;
   if (epi == kEpiGated && p.split_ws) {
@@ -792,10 +782,91 @@ int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmI
     }
   }
   switch (BN) {
-    case 256: return dispatch_epi<256, false>(epi, ta, tb, tb, q, stream);
-    case 128: return dispatch_epi<128, false>(epi, ta, tb, tb, q, stream);
-    default: return dispatch_epi<64, false>(epi, ta, tb, tb, q, stream);
+    case 256: return dispatch_epi<256, false>(epi, m, q, stream);
+    case 128: return dispatch_epi<128, false>(epi, m, q, stream);
+    default: return dispatch_epi<64, false>(epi, m, q, stream);
   }
+}
+
+bool tmap_bf16(CUtensorMap* m, const uint16_t* ptr, int inner, int outer, long long ld, int box_outer) {
+  return make_tmap_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, ld * 2, BK, box_outer, true);
+}
+
+}  // namespace
+
+int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmInt8B* b8, int epi,
+                const GemmParams& p, cudaStream_t stream) {
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return DIT_EINVAL;
+  if (p.K % BK != 0 || p.N % 64 != 0) return DIT_EUNSUPPORTED;
+  if (p.n_split != 0 || p.k_split != 0 || epi == kEpiQKVSwiGLU) return DIT_EINVAL;  // gemm_launch_cat
+  if (reinterpret_cast<uintptr_t>(a) % 16 || (lda * 2) % 16) return DIT_EINVAL;
+  // tile width: 256 where it divides N (fewer A re-reads), else 128, else 64
+  int BN = pick_bn(p.N);
+  // QKV epilogue: a tile never straddles q/k/v and holds whole heads
+  if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
+  Maps m;
+  if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM)) return DIT_ECUDA;
+  if (b8) {
+    if (reinterpret_cast<uintptr_t>(b8->q) % 16 || reinterpret_cast<uintptr_t>(b8->s) % 16) return DIT_EINVAL;
+    if (BN == 64 || p.K % 256 != 0) return DIT_EUNSUPPORTED;  // scale rows must be 16-byte multiples
+    if (p.M > kInt8MainloopMaxM) {
+      // Many M tiles: the in-mainloop converters would dequantise every weight tile once per M tile
+      // (17 times at 4224 rows) and bound the GEMM; dequantising the weight once, HBM-bound, and
+      // running the bf16 mainloop is faster (measured 1.14 against 1.69 ms per 1024sq block).
+      if (!b8->wbf || reinterpret_cast<uintptr_t>(b8->wbf) % 16) return DIT_EINVAL;
+      const int rc = dequant_int8_launch(b8->q, b8->s, b8->wbf, p.N, p.K, stream);
+      if (rc != DIT_OK) return rc;
+      return gemm_launch(a, lda, b8->wbf, nullptr, epi, p, stream);
+    }
+    // int8lin tiles are 256 x 128: two M=128 MMAs share each converted B k-block and both accumulator
+    // sets fit in TMEM. (256 x 256 tiles, with one accumulator set and no epilogue overlap, measured
+    // 2.02 ms per 1024sq block against 1.87 ms.)
+    BN = 128;
+    if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
+    if (!make_tmap_2d(&m.b, b8->q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.K, p.N, p.K, BK, BN, false)) return DIT_ECUDA;
+    if (!make_tmap_2d(&m.s, b8->s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, (long long)(p.K / 32) * 2, 8,
+                      BN, false))
+      return DIT_ECUDA;
+    m.a2 = m.a;
+    m.b2 = m.b;
+    return dispatch_epi<128, true>(epi, m, p, stream);
+  }
+  if (reinterpret_cast<uintptr_t>(b) % 16) return DIT_EINVAL;
+  if (!tmap_bf16(&m.b, b, p.K, p.N, p.K, BN)) return DIT_ECUDA;
+  m.s = m.b;
+  m.a2 = m.a;
+  m.b2 = m.b;
+  return launch_bf16(m, BN, epi, p, stream);
+}
+
+int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long long lda2, const uint16_t* b,
+                    long long ldb, const uint16_t* b2, long long ldb2, int epi, const GemmParams& p,
+                    cudaStream_t stream) {
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return DIT_EINVAL;
+  if (p.K % BK != 0 || p.N % 64 != 0) return DIT_EUNSUPPORTED;
+  if ((p.n_split > 0) == (p.k_split > 0)) return DIT_EINVAL;  // exactly one kind of concatenation
+  const int BN = pick_bn(p.N);
+  auto al = [](const void* q, long long ld) { return reinterpret_cast<uintptr_t>(q) % 16 == 0 && (ld * 2) % 16 == 0; };
+  Maps m;
+  if (p.n_split > 0) {
+    // B = [b ; b2]: rows [0, n_split) from b, the rest from b2, both [rows, K]
+    if (p.n_split % BN != 0 || p.n_split >= p.N) return DIT_EUNSUPPORTED;
+    if (epi == kEpiQKVSwiGLU && (BN != 256 || BN % p.head_dim != 0 || p.n_split != 3 * p.H)) return DIT_EUNSUPPORTED;
+    if (!al(a, lda) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
+    if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.n_split, ldb, BN) ||
+        !tmap_bf16(&m.b2, b2, p.K, p.N - p.n_split, ldb2, BN))
+      return DIT_ECUDA;
+    m.a2 = m.a;
+  } else {
+    // A = [a | a2], B = [b | b2]: inner columns [0, k_split) from a and b, the rest from a2 and b2
+    if (p.k_split % BK != 0 || p.k_split >= p.K || epi == kEpiQKVSwiGLU) return DIT_EUNSUPPORTED;
+    if (!al(a, lda) || !al(a2, lda2) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
+    if (!tmap_bf16(&m.a, a, p.k_split, p.M, lda, BM) || !tmap_bf16(&m.a2, a2, p.K - p.k_split, p.M, lda2, BM) ||
+        !tmap_bf16(&m.b, b, p.k_split, p.N, ldb, BN) || !tmap_bf16(&m.b2, b2, p.K - p.k_split, p.N, ldb2, BN))
+      return DIT_ECUDA;
+  }
+  m.s = m.b;
+  return launch_bf16(m, BN, epi, p, stream);
 }
 
 }  // namespace dit

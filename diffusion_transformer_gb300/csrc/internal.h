@@ -20,6 +20,7 @@ enum GemmEpilogue : int {
   kEpiGated = 3,        // x[r, n] += gate[map[r]][n] * acc; x rows < L in txt, others in img (fp32, stride N)
   kEpiSwiGLU = 4,       // out bf16 [M, N/2]: a_j = silu(acc_{2j}) * acc_{2j+1}
   kEpiQKV = 5,          // QK-RMSNorm + RoPE on q/k columns -> q, k [heads, R, d]; v -> vt [heads, d, Rp]
+  kEpiQKVSwiGLU = 6,    // columns < n_split as kEpiQKV, the rest as kEpiSwiGLU (parallel block)
 };
 
 struct GemmParams {
@@ -50,6 +51,10 @@ struct GemmParams {
   int split, sk_first;
   float* split_part;   // [tail tiles][split][128][BN] fp32
   int* split_cnt;      // [tail tiles][4] arrivals per 32-row quadrant
+  // concatenated operands (0 = none): output columns >= n_split take B rows from the second B
+  // (row n - n_split); inner indices >= k_split take A and B columns from the second A and B
+  // (column k - k_split)
+  int n_split, k_split;
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row
@@ -66,6 +71,12 @@ inline size_t gemm_int8_scratch_bytes(int N, int K) { return ((size_t(N) * K * 2
 
 // Launch the GEMM. `a` is bf16 [M, K] (row stride lda elements), `b` bf16 [N, K] (stride K) unless
 // `b8` is given. Returns a DIT_* status; checks shapes the kernels support.
+// The same GEMM over concatenated bf16 operands: N-concatenation (p.n_split > 0: B = [b ; b2], b2
+// the rows of output columns >= n_split) or K-concatenation (p.k_split > 0: A = [a | a2],
+// B = [b | b2], a2/b2 the columns from k_split on). Boundaries are multiples of the tile.
+int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long long lda2, const uint16_t* b,
+                    long long ldb, const uint16_t* b2, long long ldb2, int epi, const GemmParams& p,
+                    cudaStream_t stream);
 int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmInt8B* b8, int epi,
                 const GemmParams& p, cudaStream_t stream);
 
@@ -96,6 +107,7 @@ struct ModNormParams {
   const int32_t* map;        // [R] or null (row 0)
   float eps;
   uint16_t* out;             // [R, H] bf16
+  int layernorm;             // 0: RMS norm; 1: LayerNorm (mean subtracted first)
 };
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream);
 

@@ -137,6 +137,22 @@ DIT_API int dit_block_forward_int8(const dit_dims* dims, const dit_block_w8* w, 
                            const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
                            dit_stream_t stream);
 
+/* The parallel (single-stream) block [gizai:dit, Block.parallel]: x + gate * (attention + SwiGLU
+ * MLP), both branches reading one modulated LayerNorm of x:
+ *   h  = (x - mean(x)) * rsqrt(var(x) + eps) * norm1 * (1 + scale) + shift     (var biased, fp32)
+ *   q,k,v = h Wqkv^T with the per-head QK norm and rotation of dit_block_forward
+ *   o  = softmax(q k^T / sqrt(d)) v;   a = silu(h Wup_gate^T) * (h Wup_up^T) (interleaved rows)
+ *   x += gate * (o Wout^T + a Wdown^T)
+ * Weights as dit_block_forward (w->norm2 unused). mod->rows is [M, 3, H] fp32 here: shift, scale,
+ * gate; map as dit_mod. The QKV and gate/up products run as one GEMM over [Wqkv ; Wup] and the
+ * two output products as one GEMM over [o | a] [Wout | Wdown]^T (same arithmetic, fewer launches).
+ * Workspace: dit_workspace_bytes(dims, L, N, 2), 256-byte aligned. Requires H % 256 == 0 and
+ * ffn % 128 == 0 besides the dims rules. Errors as dit_block_forward. */
+DIT_API int dit_parallel_block_forward(const dit_dims* dims, const dit_block_w* w, float* txt, int L, float* img,
+                                       int N, const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                       const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                       dit_stream_t stream);
+
 /* FlowMatch Euler step [host contract, section 6]: x[i] <- x[i] + (sigma_next - sigma) * vel[i],
  * each operation rounded separately in fp32 (no fused multiply-add). n >= 0. */
 DIT_API int dit_euler_step(float* x, const float* vel, int64_t n, float sigma, float sigma_next, dit_stream_t stream);
@@ -182,7 +198,8 @@ DIT_API int dit_denoise(const dit_model* model, float* img_tokens, int N, const 
                 const float* sigmas, int steps, const float* txt_cos, const float* txt_sin,
                 const float* img_cos, const float* img_sin, void* ws, size_t ws_bytes, dit_stream_t stream);
 
-/* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block. Returns 0 for unsupported dims. */
+/* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block, 2 = parallel block. Returns 0 for
+ * unsupported dims. */
 DIT_API size_t dit_workspace_bytes(const dit_dims* dims, int L, int N, int variant);
 DIT_API size_t dit_denoise_workspace_bytes(const dit_model* model, int L, int N, int steps);
 
