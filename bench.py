@@ -4,8 +4,9 @@ Workload (a "step"): one whole block forward - modulated norm, QKV linear with Q
 epilogue, joint attention, out linear with gated residual, second modulated norm, SwiGLU up
 linear, down linear with gated residual - at the 1024^2 shape: hidden 3072, 24 heads x 128,
 ffn 12288, L = 128 text + N = 4096 image rows (R = 4224), bf16 weights, per-row modulation.
-The same run also times the int8lin block (the same shape) and the 32-block, 4-step denoise loop
-(L = 512, N = 4096) and reports them as sub-objects.
+The same run also times the int8lin block (the same shape), the parallel single-stream block (the
+same shape and FLOP count: one modulated LayerNorm feeding attention and the MLP, 4 launches) and
+the 32-block, 4-step denoise loop (L = 512, N = 4096) and reports them as sub-objects.
 
 Metric: block TFLOP/s (algorithmic FLOP = 2R(3H^2 + H^2 + 2HF + FH) + 4R^2 H per block) and
 ms per block. Inputs are larger than L2 (302 MB of weights per block), so no flush is needed.
@@ -431,6 +432,22 @@ def run_ours(args):
         del st8
         st = _block_setup(torch, D, inp)
 
+    # parallel single-stream block, same shape
+    par = None
+    if not args.no_parallel:
+        inpP = DI.parallel_block_inputs(WORKLOAD)
+        stP = _block_setup(torch, D, inpP)
+        callP = lambda: D.dit_parallel_block_forward(stP["dims"], stP["w"], stP["txt"], stP["img"], stP["tc"],
+                                                     stP["ts"], stP["ic"], stP["is_"], stP["mod"], stP["ws"])
+        msP = _time_loop(torch, callP, args.steps, args.warmup, dist) / args.steps
+        D.dit_check()
+        tfP = flops / (msP * 1e-3) / 1e12
+        par = {"workload": "1024sq parallel block: modulated LayerNorm -> [QKV | gate/up] GEMM -> attention -> "
+                           "[o | a][Wout | Wdown] gated GEMM, per-row modulation [R, 3, H]",
+               "ms_per_block": msP, "tflops": tfP, "frac_of_peak": tfP / peaks["bf16_tflops"],
+               "flop_per_block": flops, "launches_per_block": 4}
+        del stP
+
     # end to end through host buffers
     e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
     D.dit_check()
@@ -459,6 +476,7 @@ def run_ours(args):
             "roofline": roof,
             "kernels": kb,
             "int8lin": int8,
+            "parallel_block": par,
             "denoise": den,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -544,6 +562,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4224)
     ap.add_argument("--no-int8", action="store_true")
     ap.add_argument("--no-denoise", action="store_true")
+    ap.add_argument("--no-parallel", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
