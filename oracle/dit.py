@@ -30,7 +30,7 @@ __all__ = [
     "modulated_rmsnorm", "qk_rmsnorm", "rope_apply", "attention", "silu", "swiglu_interleaved",
     "block_forward", "block_forward_rows", "dequant_int8", "euler_step", "shift_sigmas",
     "timestep_sinusoids", "time_embedding", "denoise", "pack_latents", "block_weights_f64",
-    "modulated_layernorm", "parallel_block_forward", "parallel_block_forward_rows",
+    "modulated_layernorm", "parallel_block_forward", "parallel_block_forward_rows", "double_block_forward_rows",
 ]
 
 
@@ -300,6 +300,48 @@ def parallel_block_forward(inp, weights=None, rows=None):
     if rows is not None:
         return y
     return y[:sh.L], y[sh.L:]
+
+
+# ----------------------------------------------------------------------------------------------
+# double-stream block  [klein article, sections 4.3-4.4 (double blocks); gizai:dit, Block.forward]
+# ----------------------------------------------------------------------------------------------
+
+def double_block_forward_rows(x, weights_txt, weights_img, mod, mod_map, cos, sin, heads, head_dim, L,
+                              rows: Optional[np.ndarray] = None, norms_txt=(None, None, None, None),
+                              norms_img=(None, None, None, None), eps=1e-6, qk_eps=1e-6):
+    """The double-stream block over the packed rows x [R, H] (text rows 0..L-1, image rows L..R-1):
+    the sequential block of ``block_forward_rows`` in which each stream has its own four linears
+    and its own norm weights (norm1, norm2, q_norm, k_norm), while the attention is one softmax over
+    the concatenated text and image keys. Modulation rows come through ``mod_map`` as for the
+    sequential block, so each stream's rows pick their own rows of ``mod`` [M, 6, H]."""
+    x = np.asarray(x, dtype=np.float64)
+    R, H = x.shape
+    nh, d = heads, head_dim
+    rows = np.arange(R) if rows is None else np.asarray(rows)
+    m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)]
+    streams = [(np.arange(0, L), weights_txt, norms_txt), (np.arange(L, R), weights_img, norms_img)]
+    q = np.empty((R, nh, d))
+    k = np.empty((R, nh, d))
+    v = np.empty((R, nh, d))
+    for idx, W, nrm in streams:
+        if idx.size == 0:
+            continue
+        h = modulated_rmsnorm(x[idx], nrm[0], m[idx, 0], m[idx, 1], eps)
+        qkv = h @ W[0].T
+        q[idx] = rope_apply(qk_rmsnorm(qkv[:, 0:H].reshape(-1, nh, d), nrm[2], qk_eps), cos[idx], sin[idx])
+        k[idx] = rope_apply(qk_rmsnorm(qkv[:, H:2 * H].reshape(-1, nh, d), nrm[3], qk_eps), cos[idx], sin[idx])
+        v[idx] = qkv[:, 2 * H:3 * H].reshape(-1, nh, d)
+    o = attention(q, k, v, rows)
+    out = np.empty((rows.size, H))
+    for idx, W, nrm in streams:
+        sel = np.isin(rows, idx)
+        if not sel.any():
+            continue
+        r = rows[sel]
+        xr = x[r] + m[r, 2] * (o[sel] @ W[1].T)
+        h2 = modulated_rmsnorm(xr, nrm[1], m[r, 3], m[r, 4], eps)
+        out[sel] = xr + m[r, 5] * (swiglu_interleaved(h2 @ W[2].T) @ W[3].T)
+    return out
 
 
 # ----------------------------------------------------------------------------------------------

@@ -134,3 +134,60 @@ def parallel_block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, 
         gate = mod_rows[r][2]
         out.append([x[r][i] + gate[i] * (att[i] + mlp[i]) for i in range(H)])
     return out
+
+
+def double_block(x, L, Wt, Wi, mod_rows, cos, sin, heads, d, eps, qk_eps, norms_t=None, norms_i=None):
+    """The sequential block with per-stream weights: rows r < L use Wt = (Wq, Wk, Wv, Wo, Wg, Wu, Wd)
+    and norms_t = (norm1, norm2, qn, kn), the others Wi / norms_i; one attention over all rows."""
+    R, H = len(x), len(x[0])
+    one = lambda n: [1.0] * n
+    nt = norms_t or (None, None, None, None)
+    ni = norms_i or (None, None, None, None)
+    pick = lambda r: (Wt, nt) if r < L else (Wi, ni)
+
+    def modnorm(row, w, shift, scale):
+        y = rmsnorm_row(row, eps)
+        w = w or one(H)
+        return [y[i] * w[i] * (1.0 + scale[i]) + shift[i] for i in range(H)]
+
+    Q, K, V = [], [], []
+    for r in range(R):
+        W, nr = pick(r)
+        h = modnorm(x[r], nr[0], mod_rows[r][0], mod_rows[r][1])
+        q, k, v = matvec(W[0], h), matvec(W[1], h), matvec(W[2], h)
+        qn, kn = nr[2] or one(d), nr[3] or one(d)
+        qh, kh, vh = [], [], []
+        for n in range(heads):
+            for (src, wt, dst) in ((q, qn, qh), (k, kn, kh)):
+                seg = rmsnorm_row(src[n * d:(n + 1) * d], qk_eps)
+                seg = [seg[j] * wt[j] for j in range(d)]
+                rot = [0.0] * d
+                for i in range(d // 2):
+                    a, b = seg[2 * i], seg[2 * i + 1]
+                    c, s = cos[r][i], sin[r][i]
+                    rot[2 * i] = a * c - b * s
+                    rot[2 * i + 1] = a * s + b * c
+                dst.append(rot)
+            vh.append(v[n * d:(n + 1) * d])
+        Q.append(qh)
+        K.append(kh)
+        V.append(vh)
+    out = []
+    for r in range(R):
+        W, nr = pick(r)
+        o = []
+        for n in range(heads):
+            scores = [sum(Q[r][n][j] * K[c][n][j] for j in range(d)) / math.sqrt(d) for c in range(R)]
+            m = max(scores)
+            e = [math.exp(s - m) for s in scores]
+            z = sum(e)
+            for j in range(d):
+                o.append(sum(e[c] / z * V[c][n][j] for c in range(R)))
+        att = matvec(W[3], o)
+        xr = [x[r][i] + mod_rows[r][2][i] * att[i] for i in range(H)]
+        h2 = modnorm(xr, nr[1], mod_rows[r][3], mod_rows[r][4])
+        g, u = matvec(W[4], h2), matvec(W[5], h2)
+        a = [g[j] / (1.0 + math.exp(-g[j])) * u[j] for j in range(len(g))]
+        mlp = matvec(W[6], a)
+        out.append([xr[i] + mod_rows[r][5][i] * mlp[i] for i in range(H)])
+    return out
