@@ -15,7 +15,8 @@ from typing import List, Optional, Sequence
 
 __all__ = [
     "DitError", "lib", "library_path", "DitDims", "BlockWeights", "Int8BlockWeights", "Modulation",
-    "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_parallel_block_forward", "dit_euler_step",
+    "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_parallel_block_forward",
+    "dit_double_block_forward", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
     "dit_vt_stride", "dit_attention", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
@@ -66,6 +67,9 @@ _SIGNATURES = {
     "dit_block_forward": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_int, c_void_p, c_int,
                                   c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p, c_size_t,
                                   c_void_p]),
+    "dit_double_block_forward": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), POINTER(dit_block_w), c_void_p,
+                                         c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                         POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
     "dit_parallel_block_forward": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_int, c_void_p, c_int,
                                            c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                            c_size_t, c_void_p]),
@@ -267,6 +271,20 @@ def dit_parallel_block_forward(dims: DitDims, w: BlockWeights, txt, img, txt_cos
                                          _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
                                          _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
         "dit_parallel_block_forward")
+
+
+def dit_double_block_forward(dims: DitDims, w_txt: Optional[BlockWeights], w_img: BlockWeights, txt, img, txt_cos,
+                             txt_sin, img_cos, img_sin, mod: Modulation, ws, stream=None):
+    """The double-stream block: text rows use w_txt, image rows w_img, one joint attention."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_double_block_forward(ctypes.byref(dims.c), None if w_txt is None else ctypes.byref(w_txt.c),
+                                       ctypes.byref(w_img.c), _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"),
+                                       img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32), _ptr(img_cos, f32),
+                                       _ptr(img_sin, f32), ctypes.byref(mod.c), _ptr(ws, None, "ws"),
+                                       ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_double_block_forward")
 
 
 def dit_block_forward_noalloc(dims: DitDims, w: BlockWeights, txt, img, txt_cos, txt_sin, img_cos, img_sin,

@@ -260,6 +260,102 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, float* txt, int 
   return gemm_launch_cat(b.o, H, b.a, F, w->wout, H, w->wdown, F, kEpiGated, g, st);
 }
 
+// The double-stream block: the sequential block in which text rows [0, L) and image rows [L, R)
+// each use their own linears and norm weights; the attention runs once over all R rows. Each
+// stream's norms and GEMMs are launched over its own rows (row_off = its first sequence row), so any
+// L works; the modulation map gives each stream its own modulation rows.
+int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w* wi, float* txt, int L, float* img,
+                     int N, const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod,
+                     void* ws, cudaStream_t st) {
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  const int R = L + N, H = d->hidden, F = d->ffn;
+  const BlockWs b = carve_block_ws(d, R, ws);
+  struct Stream {
+    const dit_block_w* w;
+    int r0, n;
+    bool text;
+  };
+  const Stream S[2] = {{wt, 0, L, true}, {wi, L, N, false}};
+  int rc;
+  // the text stream's rows are txt[0, L) (all below L); the image stream's img[0, N) (L = 0 here)
+  auto norm = [&](const Stream& s, const float* w, long long shift_row) {
+    ModNormParams mp{s.text ? txt : nullptr, s.text ? nullptr : img, s.text ? L : 0, s.n, H, H, H, w,
+                     mod.rows + shift_row * H, mod.rows + (shift_row + 1) * H, 6LL * H,
+                     mod.map ? mod.map + s.r0 : nullptr, d->eps, b.h + size_t(s.r0) * H};
+    return modnorm_launch(mp, st);
+  };
+  auto gated = [&](const Stream& s, int K, long long gate_row) {
+    GemmParams g = base_params(s.n, H, K, err);
+    g.txt = txt;
+    g.img = img;
+    g.L = L;
+    g.gate = mod.rows + gate_row * H;
+    g.map = mod.map;
+    g.gate_stride = 6LL * H;
+    g.row_off = s.r0;
+    return g;
+  };
+
+  // 1. h = modnorm(x; norm1, shift_a, scale_a), per stream
+  for (const Stream& s : S)
+    if (s.n > 0 && (rc = norm(s, s.w->norm1, 0)) != DIT_OK) return rc;
+  // 2. q, k, vt per stream (its own Wqkv and q/k norm weights) into the joint layouts
+  for (const Stream& s : S) {
+    if (s.n == 0) continue;
+    GemmParams g = base_params(s.n, 3 * H, H, err);
+    g.q = b.q;
+    g.k = b.k;
+    g.vt = b.vt;
+    g.H = H;
+    g.heads = d->heads;
+    g.head_dim = d->head_dim;
+    g.Rp = vt_stride(R);
+    g.L = L;
+    g.txt_cos = tc;
+    g.txt_sin = ts;
+    g.img_cos = ic;
+    g.img_sin = is;
+    g.q_norm = s.w->q_norm;
+    g.k_norm = s.w->k_norm;
+    g.qk_eps = d->qk_eps;
+    g.row_off = s.r0;
+    g.R_total = R;
+    if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wqkv, nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
+  }
+  // 3. o = attention over all rows
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+  if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
+  // 4. x += gate_a * (o Wout^T), per stream (K-split scratch: the SwiGLU buffer, not yet written)
+  for (const Stream& s : S) {
+    if (s.n == 0) continue;
+    GemmParams g = gated(s, H, 2);
+    g.split_ws = b.a;
+    g.split_ws_bytes = size_t(R) * F * 2;
+    if ((rc = gemm_launch(b.o + size_t(s.r0) * H, H, s.w->wout, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
+  }
+  // 5. h2 = modnorm(x; norm2, shift_m, scale_m), per stream
+  for (const Stream& s : S)
+    if (s.n > 0 && (rc = norm(s, s.w->norm2, 3)) != DIT_OK) return rc;
+  // 6. a = SwiGLU(h2 Wup^T), per stream
+  for (const Stream& s : S) {
+    if (s.n == 0) continue;
+    GemmParams g = base_params(s.n, 2 * F, H, err);
+    g.out = b.a + size_t(s.r0) * F;
+    g.ldo = F;
+    if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wup, nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
+  }
+  // 7. x += gate_m * (a Wdown^T), per stream (K-split scratch: h, q, k, vt and o, consumed by now)
+  for (const Stream& s : S) {
+    if (s.n == 0) continue;
+    GemmParams g = gated(s, F, 5);
+    g.split_ws = b.h;
+    g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
+    if ((rc = gemm_launch(b.a + size_t(s.r0) * F, F, s.w->wdown, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
+  }
+  return DIT_OK;
+}
+
 int check_block_args(const dit_dims* d, const float* txt, int L, const float* img, int N, const float* tc,
                      const float* ts, const float* ic, const float* is, const dit_mod* mod, const void* ws,
                      size_t ws_bytes, int variant) {
@@ -338,7 +434,7 @@ const char* dit_status_string(int s) {
 }
 
 size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
-  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 2) return 0;
+  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 3) return 0;
   size_t bytes = carve_block_ws(d, L + N, nullptr).bytes;
   if (variant == 1) bytes += int8_scratch_bytes(d);
   return bytes;
@@ -381,6 +477,20 @@ int dit_parallel_block_forward(const dit_dims* d, const dit_block_w* w, float* t
   if (d->hidden % 256 != 0 || d->ffn % 128 != 0) return DIT_EUNSUPPORTED;  // 256-wide tiles over 3H and 2F
   return run_parallel_block(d, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_double_block_forward(const dit_dims* d, const dit_block_w* w_txt, const dit_block_w* w_img, float* txt, int L,
+                             float* img, int N, const float* tc, const float* ts, const float* ic, const float* is,
+                             const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 3);
+  if (rc != DIT_OK) return rc;
+  for (const dit_block_w* w : {w_txt, w_img}) {
+    if (w == w_txt && L == 0) continue;
+    if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+    if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  }
+  return run_double_block(d, w_txt, w_img, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dit_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt, int L, float* img, int N,

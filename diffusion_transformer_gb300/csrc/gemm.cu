@@ -94,7 +94,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
   if constexpr (EPI == kEpiQKV) {
     const int d = p.head_dim;
     const int H = p.H;
-    const int R = p.M;
+    const int R = p.R_total > 0 ? p.R_total : p.M;  // rows of the q, k and vt layouts
+    const int srow = row + p.row_off;                // sequence row of this thread's GEMM row
     const int half = d / 2;
     for (int hh = 0; hh < BN / d; ++hh) {
       const int col0 = n0 + hh * d;
@@ -132,15 +133,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
             col[r >> 1] = lo | (hi << 16);
           }
           (void)st32;
-          uint16_t* dst = p.vt + (size_t(head) * d + c * 32 + j) * p.Rp + row0;
-          if (row0 + 32 <= R) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);  // row0 % 32 == 0 and Rp % 8 == 0: 16-byte aligned
+          uint16_t* dst = p.vt + (size_t(head) * d + c * 32 + j) * p.Rp + row0 + p.row_off;
+          if (row0 + 32 <= p.M && ((row0 + p.row_off) & 7) == 0) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);  // (row0 + row_off) % 8 == 0, Rp % 8 == 0: 16-byte aligned
 #pragma unroll
             for (int q = 0; q < 4; ++q) d4[q] = make_uint4(col[4 * q], col[4 * q + 1], col[4 * q + 2], col[4 * q + 3]);
           } else {
 #pragma unroll
             for (int r = 0; r < 32; ++r)
-              if (row0 + r < R) dst[r] = uint16_t(r & 1 ? col[r >> 1] >> 16 : col[r >> 1] & 0xffffu);
+              if (row0 + r < p.M) dst[r] = uint16_t(r & 1 ? col[r >> 1] >> 16 : col[r >> 1] & 0xffffu);
           }
         }
         continue;
@@ -159,11 +160,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
       }
       const float rstd = rsqrtf(ss / float(d) + p.qk_eps);
       const float* wn = which == 0 ? p.q_norm : p.k_norm;
-      const float4* cs = reinterpret_cast<const float4*>(row < p.L ? p.txt_cos + size_t(row) * half
-                                                                     : p.img_cos + size_t(row - p.L) * half);
-      const float4* sn = reinterpret_cast<const float4*>(row < p.L ? p.txt_sin + size_t(row) * half
-                                                                     : p.img_sin + size_t(row - p.L) * half);
-      uint16_t* dst = (which == 0 ? p.q : p.k) + (size_t(head) * R + row) * d;
+      const float4* cs = reinterpret_cast<const float4*>(srow < p.L ? p.txt_cos + size_t(srow) * half
+                                                                      : p.img_cos + size_t(srow - p.L) * half);
+      const float4* sn = reinterpret_cast<const float4*>(srow < p.L ? p.txt_sin + size_t(srow) * half
+                                                                      : p.img_sin + size_t(srow - p.L) * half);
+      uint16_t* dst = (which == 0 ? p.q : p.k) + (size_t(head) * R + srow) * d;
       // pass 2: normalise, weight, rotate adjacent pairs, store
       for (int c = 0; c < d / 32; ++c) {
         uint32_t v[32];
@@ -198,7 +199,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
   } else if constexpr (EPI == kEpiGated && kRowPerThread) {
     // x[r, n] += gate[map[r], n] * acc, one row per thread: the form for the int8 in-mainloop
     // kernel, whose 320 threads leave 168 registers each (the coalesced form below would spill).
-    const int grow = row_ok ? row : 0;
+    const int grow = (row_ok ? row : 0) + p.row_off;  // sequence row
     float* x = grow < p.L ? p.txt + size_t(grow) * p.N : p.img + size_t(grow - p.L) * p.N;
     const int m = (p.map && row_ok) ? __ldg(p.map + grow) : 0;
     const float* g = p.gate + size_t(m) * p.gate_stride;
@@ -247,7 +248,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
     for (int i = 0; i < 8; ++i) {
       const int r = row0 + (lane >> 3) + 4 * i;
       ok[i] = r < p.M;
-      const int rr = ok[i] ? r : 0;
+      const int rr = (ok[i] ? r : 0) + p.row_off;  // sequence row
       xr[i] = (rr < p.L ? p.txt + size_t(rr) * p.N : p.img + size_t(rr - p.L) * p.N) + n0 + cq * 4;
       gr[i] = p.gate + size_t(p.map ? __ldg(p.map + rr) : 0) * p.gate_stride + n0 + cq * 4;
     }
@@ -425,9 +426,10 @@ __device__ __forceinline__ void split_finish(const GemmParams& p, const float* p
         for (int q = 0; q < S; ++q) v[u][q] = __ldcg(reinterpret_cast<const float4*>(src + q * kSlot));
         xr[u] = nullptr;
         if (r < p.M) {
-          xr[u] = (r < p.L ? p.txt + size_t(r) * p.N : p.img + size_t(r - p.L) * p.N) + n0 + c * 32 + cq * 4;
+          const int sr = r + p.row_off;  // sequence row
+          xr[u] = (sr < p.L ? p.txt + size_t(sr) * p.N : p.img + size_t(sr - p.L) * p.N) + n0 + c * 32 + cq * 4;
           xq[u] = *reinterpret_cast<const float4*>(xr[u]);
-          gq[u] = __ldg(reinterpret_cast<const float4*>(p.gate + size_t(p.map ? __ldg(p.map + r) : 0) * p.gate_stride +
+          gq[u] = __ldg(reinterpret_cast<const float4*>(p.gate + size_t(p.map ? __ldg(p.map + sr) : 0) * p.gate_stride +
                                                         n0 + c * 32 + cq * 4));
         }
       }

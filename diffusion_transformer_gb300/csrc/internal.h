@@ -55,6 +55,9 @@ struct GemmParams {
   // (row n - n_split); inner indices >= k_split take A and B columns from the second A and B
   // (column k - k_split)
   int n_split, k_split;
+  // rows of a sub-range of the sequence (one stream of a double-stream block): GEMM row r is sequence
+  // row r + row_off for the QKV and gated epilogues; q, k and vt hold R_total rows (0: M)
+  int row_off, R_total;
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row

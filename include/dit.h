@@ -153,6 +153,19 @@ DIT_API int dit_parallel_block_forward(const dit_dims* dims, const dit_block_w* 
                                        const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
                                        dit_stream_t stream);
 
+/* The double-stream block [klein article, sections 4.3-4.4: the double blocks' per-stream
+ * projections with the [txt | img] join on the prepared q, k, v]: dit_block_forward in which the
+ * text rows [0, L) use w_txt and the image rows use w_img (all four linears and the four norm
+ * weights), while the attention is one softmax over all L + N rows. mod as dit_block_forward
+ * ([M, 6, H] and map): the map gives each stream its own modulation rows. w_txt may be NULL when
+ * L = 0. Each stream's norms and linears run as their own launches over its rows (13 launches),
+ * so L need not be a multiple of any tile. Workspace: dit_workspace_bytes(dims, L, N, 3).
+ * Errors as dit_block_forward. */
+DIT_API int dit_double_block_forward(const dit_dims* dims, const dit_block_w* w_txt, const dit_block_w* w_img,
+                                     float* txt, int L, float* img, int N, const float* txt_cos,
+                                     const float* txt_sin, const float* img_cos, const float* img_sin,
+                                     const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream);
+
 /* FlowMatch Euler step [host contract, section 6]: x[i] <- x[i] + (sigma_next - sigma) * vel[i],
  * each operation rounded separately in fp32 (no fused multiply-add). n >= 0. */
 DIT_API int dit_euler_step(float* x, const float* vel, int64_t n, float sigma, float sigma_next, dit_stream_t stream);
@@ -198,8 +211,8 @@ DIT_API int dit_denoise(const dit_model* model, float* img_tokens, int N, const 
                 const float* sigmas, int steps, const float* txt_cos, const float* txt_sin,
                 const float* img_cos, const float* img_sin, void* ws, size_t ws_bytes, dit_stream_t stream);
 
-/* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block, 2 = parallel block. Returns 0 for
- * unsupported dims. */
+/* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block, 2 = parallel block, 3 = double-stream
+ * block. Returns 0 for unsupported dims. */
 DIT_API size_t dit_workspace_bytes(const dit_dims* dims, int L, int N, int variant);
 DIT_API size_t dit_denoise_workspace_bytes(const dit_model* model, int L, int N, int steps);
 
