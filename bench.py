@@ -5,7 +5,8 @@ epilogue, joint attention, out linear with gated residual, second modulated norm
 linear, down linear with gated residual - at the 1024^2 shape: hidden 3072, 24 heads x 128,
 ffn 12288, L = 128 text + N = 4096 image rows (R = 4224), bf16 weights, per-row modulation.
 The same run also times the int8lin block (the same shape), the parallel single-stream block (the
-same shape and FLOP count: one modulated LayerNorm feeding attention and the MLP, 4 launches) and
+same shape and FLOP count: one modulated LayerNorm feeding attention and the MLP, 4 launches), the
+double-stream block (the same shape, text and image rows with their own weights, 7 launches) and
 the 32-block, 4-step denoise loop (L = 512, N = 4096) and reports them as sub-objects.
 
 Metric: block TFLOP/s (algorithmic FLOP = 2R(3H^2 + H^2 + 2HF + FH) + 4R^2 H per block) and
@@ -448,6 +449,25 @@ def run_ours(args):
                "flop_per_block": flops, "launches_per_block": 4}
         del stP
 
+    # double-stream block, same shape: text rows with their own weights
+    dbl = None
+    if not args.no_double:
+        inpT = DI.block_inputs(WORKLOAD, seed=sh.seed + 50)
+        wT = D.BlockWeights(_dev_bf16(torch, inpT.wqkv), _dev_bf16(torch, inpT.wout), _dev_bf16(torch, inpT.wup),
+                            _dev_bf16(torch, inpT.wdown))
+        del inpT
+        wsD = torch.empty(D.dit_workspace_bytes(st["dims"], sh.L, sh.N, 3), dtype=torch.uint8, device="cuda")
+        callD = lambda: D.dit_double_block_forward(st["dims"], wT, st["w"], st["txt"], st["img"], st["tc"], st["ts"],
+                                                   st["ic"], st["is_"], st["mod"], wsD)
+        msD = _time_loop(torch, callD, args.steps, args.warmup, dist) / args.steps
+        D.dit_check()
+        tfD = flops / (msD * 1e-3) / 1e12
+        dbl = {"workload": "1024sq double-stream block: the 128 text rows and the 4096 image rows each with their own "
+                           "four linears and norms, one joint attention; per-row modulation",
+               "ms_per_block": msD, "tflops": tfD, "frac_of_peak": tfD / peaks["bf16_tflops"],
+               "flop_per_block": flops, "launches_per_block": 7 if sh.L % 128 == 0 else 13}
+        del wT, wsD
+
     # end to end through host buffers
     e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
     D.dit_check()
@@ -477,6 +497,7 @@ def run_ours(args):
             "kernels": kb,
             "int8lin": int8,
             "parallel_block": par,
+            "double_stream_block": dbl,
             "denoise": den,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -563,6 +584,7 @@ def main():
     ap.add_argument("--no-int8", action="store_true")
     ap.add_argument("--no-denoise", action="store_true")
     ap.add_argument("--no-parallel", action="store_true")
+    ap.add_argument("--no-double", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -297,6 +297,57 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     return g;
   };
 
+  if (L > 0 && L % 128 == 0) {
+    // No 128-row tile mixes the streams: every norm and linear runs once over all rows, the GEMMs
+    // taking the image weights from row L on (m_split) and the norms the image norm weights.
+    auto norm_all = [&](const float* w_t, const float* w_i, long long shift_row) {
+      ModNormParams mp{txt, img, L, R, H, H, H, w_t, mod.rows + shift_row * H, mod.rows + (shift_row + 1) * H,
+                       6LL * H, mod.map, d->eps, b.h};
+      mp.split_w = 1;
+      mp.w_img = w_i;
+      return modnorm_launch(mp, st);
+    };
+    if ((rc = norm_all(wt->norm1, wi->norm1, 0)) != DIT_OK) return rc;
+    GemmParams g = base_params(R, 3 * H, H, err);
+    g.q = b.q;
+    g.k = b.k;
+    g.vt = b.vt;
+    g.H = H;
+    g.heads = d->heads;
+    g.head_dim = d->head_dim;
+    g.Rp = vt_stride(R);
+    g.L = L;
+    g.txt_cos = tc;
+    g.txt_sin = ts;
+    g.img_cos = ic;
+    g.img_sin = is;
+    g.q_norm = wt->q_norm;
+    g.k_norm = wt->k_norm;
+    g.q_norm2 = wi->q_norm;
+    g.k_norm2 = wi->k_norm;
+    g.qk_eps = d->qk_eps;
+    g.m_split = L;
+    if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wqkv, H, wi->wqkv, H, kEpiQKV, g, st)) != DIT_OK) return rc;
+    AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+    if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
+    g = gated(Stream{nullptr, 0, R, false}, H, 2);
+    g.m_split = L;
+    g.split_ws = b.a;
+    g.split_ws_bytes = size_t(R) * F * 2;
+    if ((rc = gemm_launch_cat(b.o, H, nullptr, 0, wt->wout, H, wi->wout, H, kEpiGated, g, st)) != DIT_OK) return rc;
+    if ((rc = norm_all(wt->norm2, wi->norm2, 3)) != DIT_OK) return rc;
+    g = base_params(R, 2 * F, H, err);
+    g.out = b.a;
+    g.ldo = F;
+    g.m_split = L;
+    if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wup, H, wi->wup, H, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
+    g = gated(Stream{nullptr, 0, R, false}, F, 5);
+    g.m_split = L;
+    g.split_ws = b.h;
+    g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
+    return gemm_launch_cat(b.a, F, nullptr, 0, wt->wdown, F, wi->wdown, F, kEpiGated, g, st);
+  }
+
   // 1. h = modnorm(x; norm1, shift_a, scale_a), per stream
   for (const Stream& s : S)
     if (s.n > 0 && (rc = norm(s, s.w->norm1, 0)) != DIT_OK) return rc;

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormPara
   const float4* x4 = reinterpret_cast<const float4*>(x);
   const float4* sh4 = reinterpret_cast<const float4*>(p.shift + size_t(m) * p.mod_stride);
   const float4* sc4 = reinterpret_cast<const float4*>(p.scale + size_t(m) * p.mod_stride);
-  const float4* w4 = reinterpret_cast<const float4*>(p.w);
+  const float4* w4 = reinterpret_cast<const float4*>((p.split_w && r >= p.L) ? p.w_img : p.w);
   const int n4 = p.H >> 2;
   __shared__ float part[kNormThreads / 32];
 

@@ -159,7 +159,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
         }
       }
       const float rstd = rsqrtf(ss / float(d) + p.qk_eps);
-      const float* wn = which == 0 ? p.q_norm : p.k_norm;
+      const bool g2 = p.m_split > 0 && row >= p.m_split;  // second row group: its own head norms
+      const float* wn = which == 0 ? (g2 ? p.q_norm2 : p.q_norm) : (g2 ? p.k_norm2 : p.k_norm);
       const float4* cs = reinterpret_cast<const float4*>(srow < p.L ? p.txt_cos + size_t(srow) * half
                                                                       : p.img_cos + size_t(srow - p.L) * half);
       const float4* sn = reinterpret_cast<const float4*>(srow < p.L ? p.txt_sin + size_t(srow) * half
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     tma_prefetch_desc(&tmB);
     if constexpr (B8) tma_prefetch_desc(&tmS);
     if (p.k_split > 0) tma_prefetch_desc(&tmA2);
-    if (p.k_split > 0 || p.n_split > 0) tma_prefetch_desc(&tmB2);
+    if (p.k_split > 0 || p.n_split > 0 || p.m_split > 0) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -552,8 +553,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
           // concatenated operands: the second A/B past the K boundary, the second B past the N boundary
           const bool k2 = p.k_split > 0 && kb * BK >= p.k_split;
           const bool n2 = p.n_split > 0 && nb * BN >= p.n_split;
+          const bool m2 = p.m_split > 0 && mb * Cfg::kTileM >= p.m_split;
           const CUtensorMap* ma = k2 ? &tmA2 : &tmA;
-          const CUtensorMap* mbm = (k2 || n2) ? &tmB2 : &tmB;
+          const CUtensorMap* mbm = (k2 || n2 || m2) ? &tmB2 : &tmB;
           const int kc = k2 ? kb * BK - p.k_split : kb * BK;
           const int nr = n2 ? nb * BN - p.n_split : nb * BN;
 #pragma unroll
@@ -846,7 +848,7 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
                     cudaStream_t stream) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return DIT_EINVAL;
   if (p.K % BK != 0 || p.N % 64 != 0) return DIT_EUNSUPPORTED;
-  if ((p.n_split > 0) == (p.k_split > 0)) return DIT_EINVAL;  // exactly one kind of concatenation
+  if ((p.n_split > 0) + (p.k_split > 0) + (p.m_split > 0) != 1) return DIT_EINVAL;  // exactly one kind
   const int BN = pick_bn(p.N);
   auto al = [](const void* q, long long ld) { return reinterpret_cast<uintptr_t>(q) % 16 == 0 && (ld * 2) % 16 == 0; };
   Maps m;
@@ -857,6 +859,15 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
     if (!al(a, lda) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
     if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.n_split, ldb, BN) ||
         !tmap_bf16(&m.b2, b2, p.K, p.N - p.n_split, ldb2, BN))
+      return DIT_ECUDA;
+    m.a2 = m.a;
+  } else if (p.m_split > 0) {
+    // rows [0, m_split) with the weights b, rows [m_split, M) with b2 (both [N, K])
+    if (p.m_split % BM != 0 || p.m_split >= p.M || epi == kEpiQKVSwiGLU) return DIT_EUNSUPPORTED;
+    if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
+    if (!al(a, lda) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
+    if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.N, ldb, BN) ||
+        !tmap_bf16(&m.b2, b2, p.K, p.N, ldb2, BN))
       return DIT_ECUDA;
     m.a2 = m.a;
   } else {

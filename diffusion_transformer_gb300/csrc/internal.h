@@ -58,6 +58,10 @@ struct GemmParams {
   // rows of a sub-range of the sequence (one stream of a double-stream block): GEMM row r is sequence
   // row r + row_off for the QKV and gated epilogues; q, k and vt hold R_total rows (0: M)
   int row_off, R_total;
+  // two row groups in one launch (double-stream block, m_split a multiple of 128): rows >= m_split
+  // take B from the second B and, in the QKV epilogue, the head-norm weights q_norm2 / k_norm2
+  int m_split;
+  const float *q_norm2, *k_norm2;
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row
@@ -75,8 +79,9 @@ inline size_t gemm_int8_scratch_bytes(int N, int K) { return ((size_t(N) * K * 2
 // Launch the GEMM. `a` is bf16 [M, K] (row stride lda elements), `b` bf16 [N, K] (stride K) unless
 // `b8` is given. Returns a DIT_* status; checks shapes the kernels support.
 // The same GEMM over concatenated bf16 operands: N-concatenation (p.n_split > 0: B = [b ; b2], b2
-// the rows of output columns >= n_split) or K-concatenation (p.k_split > 0: A = [a | a2],
-// B = [b | b2], a2/b2 the columns from k_split on). Boundaries are multiples of the tile.
+// the rows of output columns >= n_split), K-concatenation (p.k_split > 0: A = [a | a2],
+// B = [b | b2], a2/b2 the columns from k_split on) or two row groups (p.m_split > 0: output rows
+// >= m_split use the weights b2, [N, K] like b). Boundaries are multiples of the tile.
 int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long long lda2, const uint16_t* b,
                     long long ldb, const uint16_t* b2, long long ldb2, int epi, const GemmParams& p,
                     cudaStream_t stream);
@@ -111,6 +116,8 @@ struct ModNormParams {
   float eps;
   uint16_t* out;             // [R, H] bf16
   int layernorm;             // 0: RMS norm; 1: LayerNorm (mean subtracted first)
+  int split_w;               // 1: rows >= L use w_img instead of w (per-stream norm weights)
+  const float* w_img;        // [H] or null
 };
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream);
 

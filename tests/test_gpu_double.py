@@ -99,3 +99,22 @@ def test_double_deterministic():
     a = run_double_gpu(inp, tw)
     b = run_double_gpu(inp, tw)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_double_grouped_path_vs_oracle():
+    # L = 128: no 128-row tile mixes the streams, so each norm and linear is one launch over all rows
+    # (image weights from row 128 on); norm weights per stream
+    sh = DI.BlockShape("dgrp", 256, 4, 64, 768, 128, 12, 12, seed=81)
+    inp, tw = _inputs(sh, M=3, norm_weights=True)
+    t, i = run_double_gpu(inp, tw)
+    ref = oracle_double(inp, tw)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)
+    _check(np.concatenate([t, i]), ref, x_in, "double, one launch per linear (L = 128)")
+
+
+def test_double_grouped_path_with_shared_weights_is_the_sequential_block_bitwise():
+    sh = DI.BlockShape("dgrp_shared", 256, 4, 64, 768, 128, 8, 8, seed=82)
+    inp = DI.block_inputs(sh, norm_weights=True)
+    t, i = run_double_gpu(inp, inp)
+    t_seq, i_seq = run_block_gpu(inp)
+    assert np.array_equal(t, t_seq) and np.array_equal(i, i_seq)
