@@ -108,6 +108,29 @@ GemmParams base_params(int M, int N, int K, int* err) {
   return p;
 }
 
+// QKV epilogue parameters: q, k, vt of the whole sequence (R rows, L text rows) in the block
+// workspace, the rotary tables and the head-norm weights.
+GemmParams qkv_params(const dit_dims* d, int M, int R, int L, const BlockWs& b, const float* tc, const float* ts,
+                      const float* ic, const float* is, const float* qn, const float* kn, int* err) {
+  GemmParams g = base_params(M, 3 * d->hidden, d->hidden, err);
+  g.q = b.q;
+  g.k = b.k;
+  g.vt = b.vt;
+  g.H = d->hidden;
+  g.heads = d->heads;
+  g.head_dim = d->head_dim;
+  g.Rp = vt_stride(R);
+  g.L = L;
+  g.txt_cos = tc;
+  g.txt_sin = ts;
+  g.img_cos = ic;
+  g.img_sin = is;
+  g.q_norm = qn;
+  g.k_norm = kn;
+  g.qk_eps = d->qk_eps;
+  return g;
+}
+
 struct ModRef {
   const float* rows;
   const int32_t* map;
@@ -135,22 +158,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
 
   // 2. q, k, vt = qk-norm + rope epilogue of h Wqkv^T
-  GemmParams g = base_params(R, 3 * H, H, err);
-  g.q = b.q;
-  g.k = b.k;
-  g.vt = b.vt;
-  g.H = H;
-  g.heads = d->heads;
-  g.head_dim = d->head_dim;
-  g.Rp = vt_stride(R);
-  g.L = L;
-  g.txt_cos = tc;
-  g.txt_sin = ts;
-  g.img_cos = ic;
-  g.img_sin = is;
-  g.q_norm = qn;
-  g.k_norm = kn;
-  g.qk_eps = d->qk_eps;
+  GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, qn, kn, err);
   GemmInt8B q8;
   if (w8) q8 = GemmInt8B{w8->q[0], w8->s[0], i8_tiles};
   if ((rc = gemm_launch(b.h, H, w8 ? nullptr : w->wqkv, w8 ? &q8 : nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
@@ -220,22 +228,8 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, float* txt, int 
   if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
 
   // 2. q, k, vt (QK-norm + rope epilogue) and a (SwiGLU epilogue) from h [Wqkv ; Wup]^T
-  GemmParams g = base_params(R, 3 * H + 2 * F, H, err);
-  g.q = b.q;
-  g.k = b.k;
-  g.vt = b.vt;
-  g.H = H;
-  g.heads = d->heads;
-  g.head_dim = d->head_dim;
-  g.Rp = vt_stride(R);
-  g.L = L;
-  g.txt_cos = tc;
-  g.txt_sin = ts;
-  g.img_cos = ic;
-  g.img_sin = is;
-  g.q_norm = w->q_norm;
-  g.k_norm = w->k_norm;
-  g.qk_eps = d->qk_eps;
+  GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, w->q_norm, w->k_norm, err);
+  g.N = 3 * H + 2 * F;
   g.out = b.a;
   g.ldo = F;
   g.n_split = 3 * H;
@@ -308,24 +302,9 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
       return modnorm_launch(mp, st);
     };
     if ((rc = norm_all(wt->norm1, wi->norm1, 0)) != DIT_OK) return rc;
-    GemmParams g = base_params(R, 3 * H, H, err);
-    g.q = b.q;
-    g.k = b.k;
-    g.vt = b.vt;
-    g.H = H;
-    g.heads = d->heads;
-    g.head_dim = d->head_dim;
-    g.Rp = vt_stride(R);
-    g.L = L;
-    g.txt_cos = tc;
-    g.txt_sin = ts;
-    g.img_cos = ic;
-    g.img_sin = is;
-    g.q_norm = wt->q_norm;
-    g.k_norm = wt->k_norm;
+    GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, wt->q_norm, wt->k_norm, err);
     g.q_norm2 = wi->q_norm;
     g.k_norm2 = wi->k_norm;
-    g.qk_eps = d->qk_eps;
     g.m_split = L;
     if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wqkv, H, wi->wqkv, H, kEpiQKV, g, st)) != DIT_OK) return rc;
     AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
@@ -354,22 +333,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   // 2. q, k, vt per stream (its own Wqkv and q/k norm weights) into the joint layouts
   for (const Stream& s : S) {
     if (s.n == 0) continue;
-    GemmParams g = base_params(s.n, 3 * H, H, err);
-    g.q = b.q;
-    g.k = b.k;
-    g.vt = b.vt;
-    g.H = H;
-    g.heads = d->heads;
-    g.head_dim = d->head_dim;
-    g.Rp = vt_stride(R);
-    g.L = L;
-    g.txt_cos = tc;
-    g.txt_sin = ts;
-    g.img_cos = ic;
-    g.img_sin = is;
-    g.q_norm = s.w->q_norm;
-    g.k_norm = s.w->k_norm;
-    g.qk_eps = d->qk_eps;
+    GemmParams g = qkv_params(d, s.n, R, L, b, tc, ts, ic, is, s.w->q_norm, s.w->k_norm, err);
     g.row_off = s.r0;
     g.R_total = R;
     if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wqkv, nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
