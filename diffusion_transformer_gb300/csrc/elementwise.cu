@@ -222,7 +222,7 @@ __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __r
       if (i < chunks) {
         const long long e = 16 * i;
         q16[u] = *reinterpret_cast<const uint4*>(q + e);
-        sc[u] = s[(e / cols) * (cols / 32) + (e % cols) / 32];
+        sc[u] = s[e >> 5];  // row * (cols / 32) + col / 32, since cols % 32 == 0
       }
     }
 #pragma unroll
