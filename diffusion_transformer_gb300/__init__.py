@@ -20,7 +20,7 @@ __all__ = [
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
     "dit_vt_stride", "dit_attention", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
-    "dit_dequant_int8", "dit_linear_int8", "dit_linear_int8_workspace_bytes", "dit_check", "dit_status_string", "dit_version",
+    "dit_dequant_int8", "dit_linear_int8", "dit_linear_int8_workspace_bytes", "dit_check", "dit_selftest_bounded_wait", "dit_status_string", "dit_version",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -100,6 +100,7 @@ _SIGNATURES = {
                                 c_void_p]),
     "dit_linear_int8_workspace_bytes": (c_size_t, [c_int, c_int]),
     "dit_check": (c_int, [c_void_p]),
+    "dit_selftest_bounded_wait": (c_int, [c_int, c_void_p]),
     "dit_status_string": (c_char_p, [c_int]),
     "dit_version": (c_int, []),
 }
@@ -399,6 +400,11 @@ def dit_dequant_int8(q, s, w, stream=None):
     rows, cols = q.shape
     _ok(lib().dit_dequant_int8(_ptr(q, torch.int8, "q"), _ptr(s, _bf16(), "s"), rows, cols, _ptr(w, _bf16(), "w"),
                                _stream(stream)), "dit_dequant_int8")
+
+
+def dit_selftest_bounded_wait(complete: bool, stream=None):
+    """Launch the bounded-wait diagnostic; dit_check() afterwards raises DIT_ETIMEOUT unless complete."""
+    _ok(lib().dit_selftest_bounded_wait(1 if complete else 0, _stream(stream)), "dit_selftest_bounded_wait")
 
 
 def dit_check(stream=None):

@@ -457,6 +457,12 @@ size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
 
 int dit_vt_stride(int R) { return R < 0 ? 0 : vt_stride(R); }
 
+int dit_selftest_bounded_wait(int complete, dit_stream_t stream) {
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  return wait_selftest_launch(complete, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int dit_check(dit_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DIT_ECUDA;
   int* p = err_word();

@@ -239,6 +239,23 @@ __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __r
   }
 }
 
+// Diagnostic of the bounded-wait path every pipeline uses: one warp waits (mbar_wait_warp, the
+// production wait with its 1 s limit) on an mbarrier of its own, which completes only when
+// `complete` is set. Without it the wait gives up, the error word records the site and the kernel
+// returns; nothing is trapped or left running.
+constexpr int kErrTimeoutSelftest = 7;
+
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int complete, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (complete && threadIdx.x == 0) mbar_arrive(smem_u32(&bar));
+  mbar_wait_warp(smem_u32(&bar), 0, err, kErrTimeoutSelftest);
+}
+
 int grid_for(long long n, int threads) {
   long long g = (n + threads - 1) / threads;
   const long long cap = 8LL * num_sms();
@@ -301,6 +318,11 @@ int sinusoid_launch(const float* sigmas, int steps, int dim, uint16_t* out, cuda
 int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t stream) {
   if (n <= 0) return DIT_OK;
   f32_to_bf16_kernel<<<grid_for(n, 256), 256, 0, stream>>>(in, out, n);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int wait_selftest_launch(int complete, int* err, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(complete, err);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 

@@ -120,6 +120,8 @@ struct ModNormParams {
   const float* w_img;        // [H] or null
 };
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream);
+// bounded-wait diagnostic (see dit_selftest_bounded_wait)
+int wait_selftest_launch(int complete, int* err, cudaStream_t stream);
 
 int euler_launch(float* x, const float* vel, long long n, float sigma, float sigma_next, cudaStream_t stream);
 int rope_tables_launch(int L, int gh, int gw, int head_dim, float theta, float* cos, float* sin,

@@ -302,6 +302,15 @@ DIT_API size_t dit_block_noalloc_max_bytes(void);
  * DIT_OK, DIT_ETIMEOUT, or DIT_ECUDA if the stream reported an error. */
 DIT_API int dit_check(dit_stream_t stream);
 
+/* Diagnostic of the failure-detection path (no counterpart on the pages): launches one warp that
+ * waits, with the same bounded mbarrier wait every kernel here uses (1 s of the GPU's global
+ * timer), on a barrier of its own that completes only when `complete` is nonzero. With
+ * complete = 0 the wait gives up after about a second, records its site in the device error word
+ * and the kernel returns, so the next dit_check(stream) returns DIT_ETIMEOUT and the context stays
+ * usable; with complete != 0 dit_check returns DIT_OK. Returns DIT_OK once launched, DIT_ECUDA on a
+ * launch error. */
+DIT_API int dit_selftest_bounded_wait(int complete, dit_stream_t stream);
+
 /* Static description of a status code. */
 DIT_API const char* dit_status_string(int status);
 
