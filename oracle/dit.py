@@ -31,6 +31,7 @@ __all__ = [
     "block_forward", "block_forward_rows", "dequant_int8", "euler_step", "shift_sigmas",
     "timestep_sinusoids", "time_embedding", "denoise", "pack_latents", "block_weights_f64",
     "modulated_layernorm", "parallel_block_forward", "parallel_block_forward_rows", "double_block_forward_rows",
+    "rope_apply_split", "rotate",
 ]
 
 
@@ -147,6 +148,36 @@ def rope_apply(t, cos, sin):
     return out
 
 
+def rope_apply_split(t, cos, sin):
+    """The split-halves partial rotation: with h = cos.shape[1] (3d/8 of a d-wide head), value i and
+    value i + h (i < h) of each head form a pair turned by the row's angle i,
+    (a, b) -> (a cos - b sin, a sin + b cos); values from 2h on (the last quarter) are unchanged.
+    t [R, heads, d], cos/sin [R, h].  [gizai:dit, prepOf ("its first 2 half values turned") and HEAD
+    (a head rotates its first 3/4, head/8 frequencies per axis, twice: split halves)]"""
+    c = np.asarray(cos, dtype=np.float64)[:, None, :]
+    s = np.asarray(sin, dtype=np.float64)[:, None, :]
+    h = c.shape[-1]
+    a = t[..., 0:h]
+    b = t[..., h:2 * h]
+    out = np.array(t, dtype=np.float64, copy=True)
+    out[..., 0:h] = a * c - b * s
+    out[..., h:2 * h] = a * s + b * c
+    return out
+
+
+def rotate(t, cos, sin):
+    """The rotary step of a block, its layout told by the table width: d/2 columns rotate adjacent
+    pairs over the whole head (rope_apply), 3d/8 columns the first 3/4 in split halves
+    (rope_apply_split)."""
+    d = t.shape[-1]
+    w = np.asarray(cos).shape[-1]
+    if w == d // 2:
+        return rope_apply(t, cos, sin)
+    if 8 * w == 3 * d:
+        return rope_apply_split(t, cos, sin)
+    raise ValueError(f"rotary tables of width {w} fit neither layout of a {d}-wide head")
+
+
 def attention(q, k, v, rows: Optional[np.ndarray] = None):
     """Unmasked softmax attention of every query row over every key row, per head, with scale
     1/sqrt(d):  o = softmax(q k^T / sqrt(d)) v  (max-subtracted).  q/k/v [R, heads, d].
@@ -191,7 +222,7 @@ def block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
     1. h  = modnorm(x; norm1, shift_a, scale_a)
     2. [q|k|v] = h Wqkv^T (columns all-Q, all-K, all-V, head-major inside each)
     3. q, k  <- per-head RMS norm times q_norm / k_norm
-    4. rotate q, k pairs by the per-row cos/sin tables
+    4. rotate q, k by the per-row cos/sin tables (adjacent pairs, or split halves: see rotate)
     5. o = softmax(q k^T / sqrt(d)) v over all rows
     6. x += gate_a * (o Wout^T)
     7. h2 = modnorm(x; norm2, shift_m, scale_m)
@@ -213,8 +244,8 @@ def block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
     q = qkv[:, 0:H].reshape(R, nh, d)
     k = qkv[:, H:2 * H].reshape(R, nh, d)
     v = qkv[:, 2 * H:3 * H].reshape(R, nh, d)
-    q = rope_apply(qk_rmsnorm(q, q_norm, qk_eps), cos, sin)
-    k = rope_apply(qk_rmsnorm(k, k_norm, qk_eps), cos, sin)
+    q = rotate(qk_rmsnorm(q, q_norm, qk_eps), cos, sin)
+    k = rotate(qk_rmsnorm(k, k_norm, qk_eps), cos, sin)
     o = attention(q, k, v, rows)
     _, _, ga_r, sm_r, cm_r, gm_r = _mod_rows(mod, mod_map, rows)
     xr = x[rows] + ga_r * (o @ Wout.T)
@@ -279,8 +310,8 @@ def parallel_block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_
     m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)]
     h = modulated_layernorm(x, norm, m[:, 0], m[:, 1], eps)
     qkv = h @ Wqkv.T
-    q = rope_apply(qk_rmsnorm(qkv[:, 0:H].reshape(R, nh, d), q_norm, qk_eps), cos, sin)
-    k = rope_apply(qk_rmsnorm(qkv[:, H:2 * H].reshape(R, nh, d), k_norm, qk_eps), cos, sin)
+    q = rotate(qk_rmsnorm(qkv[:, 0:H].reshape(R, nh, d), q_norm, qk_eps), cos, sin)
+    k = rotate(qk_rmsnorm(qkv[:, H:2 * H].reshape(R, nh, d), k_norm, qk_eps), cos, sin)
     v = qkv[:, 2 * H:3 * H].reshape(R, nh, d)
     o = attention(q, k, v, rows)
     a = swiglu_interleaved(h[rows] @ Wup.T)
@@ -328,8 +359,8 @@ def double_block_forward_rows(x, weights_txt, weights_img, mod, mod_map, cos, si
             continue
         h = modulated_rmsnorm(x[idx], nrm[0], m[idx, 0], m[idx, 1], eps)
         qkv = h @ W[0].T
-        q[idx] = rope_apply(qk_rmsnorm(qkv[:, 0:H].reshape(-1, nh, d), nrm[2], qk_eps), cos[idx], sin[idx])
-        k[idx] = rope_apply(qk_rmsnorm(qkv[:, H:2 * H].reshape(-1, nh, d), nrm[3], qk_eps), cos[idx], sin[idx])
+        q[idx] = rotate(qk_rmsnorm(qkv[:, 0:H].reshape(-1, nh, d), nrm[2], qk_eps), cos[idx], sin[idx])
+        k[idx] = rotate(qk_rmsnorm(qkv[:, H:2 * H].reshape(-1, nh, d), nrm[3], qk_eps), cos[idx], sin[idx])
         v[idx] = qkv[:, 2 * H:3 * H].reshape(-1, nh, d)
     o = attention(q, k, v, rows)
     out = np.empty((rows.size, H))
