@@ -40,7 +40,7 @@ class DitError(RuntimeError):
 # ----------------------------------------------------------------------------------------------
 class dit_dims(ctypes.Structure):
     _fields_ = [("hidden", c_int), ("heads", c_int), ("head_dim", c_int), ("ffn", c_int),
-                ("eps", c_float), ("qk_eps", c_float)]
+                ("eps", c_float), ("qk_eps", c_float), ("rope_split", c_int)]
 
 
 class dit_block_w(ctypes.Structure):
@@ -170,10 +170,11 @@ def _stream(stream):
 
 
 class DitDims:
-    def __init__(self, hidden: int, heads: int, head_dim: int, ffn: int, eps: float = 1e-6, qk_eps: float = 1e-6):
-        self.c = dit_dims(hidden, heads, head_dim, ffn, eps, qk_eps)
+    def __init__(self, hidden: int, heads: int, head_dim: int, ffn: int, eps: float = 1e-6, qk_eps: float = 1e-6,
+                 rope_split: bool = False):
+        self.c = dit_dims(hidden, heads, head_dim, ffn, eps, qk_eps, 1 if rope_split else 0)
         self.hidden, self.heads, self.head_dim, self.ffn = hidden, heads, head_dim, ffn
-        self.eps, self.qk_eps = eps, qk_eps
+        self.eps, self.qk_eps, self.rope_split = eps, qk_eps, bool(rope_split)
 
 
 class BlockWeights:

@@ -54,6 +54,7 @@ bool dims_ok(const dit_dims* d) {
   if (d->heads <= 0 || d->hidden != d->heads * d->head_dim) return false;
   if (d->hidden % 256 != 0 || d->ffn <= 0 || d->ffn % 128 != 0) return false;
   if (!(d->eps >= 0.f) || !(d->qk_eps >= 0.f)) return false;
+  if (d->rope_split != 0 && d->rope_split != 1) return false;
   return true;
 }
 
@@ -128,6 +129,7 @@ GemmParams qkv_params(const dit_dims* d, int M, int R, int L, const BlockWs& b, 
   g.q_norm = qn;
   g.k_norm = kn;
   g.qk_eps = d->qk_eps;
+  g.rope_split = d->rope_split;
   return g;
 }
 
@@ -577,6 +579,7 @@ int dit_qkv_rope(const dit_dims* d, const uint16_t* h, int L, int N, const uint1
   g.q_norm = q_norm;
   g.k_norm = k_norm;
   g.qk_eps = d->qk_eps;
+  g.rope_split = d->rope_split;
   return gemm_launch(h, H, wqkv, nullptr, kEpiQKV, g, reinterpret_cast<cudaStream_t>(stream));
 }
 

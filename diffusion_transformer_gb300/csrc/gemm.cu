@@ -96,7 +96,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
     const int H = p.H;
     const int R = p.R_total > 0 ? p.R_total : p.M;  // rows of the q, k and vt layouts
     const int srow = row + p.row_off;                // sequence row of this thread's GEMM row
-    const int half = d / 2;
+    const int tw = p.rope_split ? 3 * d / 8 : d / 2;  // rotary table columns per row
     for (int hh = 0; hh < BN / d; ++hh) {
       const int col0 = n0 + hh * d;
       const int which = col0 / H;              // 0 = q, 1 = k, 2 = v
@@ -161,11 +161,63 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
       const float rstd = rsqrtf(ss / float(d) + p.qk_eps);
       const bool g2 = p.m_split > 0 && row >= p.m_split;  // second row group: its own head norms
       const float* wn = which == 0 ? (g2 ? p.q_norm2 : p.q_norm) : (g2 ? p.k_norm2 : p.k_norm);
-      const float4* cs = reinterpret_cast<const float4*>(srow < p.L ? p.txt_cos + size_t(srow) * half
-                                                                      : p.img_cos + size_t(srow - p.L) * half);
-      const float4* sn = reinterpret_cast<const float4*>(srow < p.L ? p.txt_sin + size_t(srow) * half
-                                                                      : p.img_sin + size_t(srow - p.L) * half);
+      const float4* cs = reinterpret_cast<const float4*>(srow < p.L ? p.txt_cos + size_t(srow) * tw
+                                                                      : p.img_cos + size_t(srow - p.L) * tw);
+      const float4* sn = reinterpret_cast<const float4*>(srow < p.L ? p.txt_sin + size_t(srow) * tw
+                                                                      : p.img_sin + size_t(srow - p.L) * tw);
       uint16_t* dst = (which == 0 ? p.q : p.k) + (size_t(head) * R + srow) * d;
+      if (p.rope_split) {
+        // pass 2, split halves: values i and i + hr (i < hr = 3d/8) turned by angle i, eight pairs
+        // at a time; the last d/4 values are normalised and weighted only
+        const int hr = 3 * d / 8;
+        for (int i0 = 0; i0 < hr; i0 += 8) {
+          uint32_t va[8], vb[8];
+          tmem_ld8(ta + i0, va);
+          tmem_ld8(ta + i0 + hr, vb);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          const float4 c0 = __ldg(cs + i0 / 4), c1 = __ldg(cs + i0 / 4 + 1);
+          const float4 s0 = __ldg(sn + i0 / 4), s1 = __ldg(sn + i0 / 4 + 1);
+          const float cf[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const float sf[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          uint32_t pa[4], pb[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float a[2], b[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              a[u] = __uint_as_float(va[j + u]) * rstd;
+              b[u] = __uint_as_float(vb[j + u]) * rstd;
+              if (wn) {
+                a[u] *= __ldg(wn + i0 + j + u);
+                b[u] *= __ldg(wn + i0 + hr + j + u);
+              }
+            }
+            pa[j / 2] = pack_bf16x2(a[0] * cf[j] - b[0] * sf[j], a[1] * cf[j + 1] - b[1] * sf[j + 1]);
+            pb[j / 2] = pack_bf16x2(a[0] * sf[j] + b[0] * cf[j], a[1] * sf[j + 1] + b[1] * cf[j + 1]);
+          }
+          *reinterpret_cast<uint4*>(dst + i0) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+          *reinterpret_cast<uint4*>(dst + i0 + hr) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+        }
+        for (int i0 = 2 * hr; i0 < d; i0 += 8) {
+          uint32_t va[8];
+          tmem_ld8(ta + i0, va);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          uint32_t pa[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float a0 = __uint_as_float(va[j]) * rstd, a1 = __uint_as_float(va[j + 1]) * rstd;
+            if (wn) {
+              a0 *= __ldg(wn + i0 + j);
+              a1 *= __ldg(wn + i0 + j + 1);
+            }
+            pa[j / 2] = pack_bf16x2(a0, a1);
+          }
+          *reinterpret_cast<uint4*>(dst + i0) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+        }
+        continue;
+      }
       // pass 2: normalise, weight, rotate adjacent pairs, store
       for (int c = 0; c < d / 32; ++c) {
         uint32_t v[32];

@@ -44,6 +44,7 @@ struct GemmParams {
   const float *txt_cos, *txt_sin, *img_cos, *img_sin;  // [L, d/2], [R-L, d/2]
   const float *q_norm, *k_norm;                         // [d] or null
   float qk_eps;
+  int rope_split;  // 0: adjacent pairs, tables [rows, d/2]; 1: split halves over 3d/4, tables [rows, 3d/8]
   // gated residual, bf16 weights: scratch for the K-split of the last, partial wave of tiles (may be
   // null: no split). Set by gemm_launch: split ways, first split tile, partial slots and counters.
   void* split_ws;

@@ -53,14 +53,19 @@ typedef struct CUstream_st* dit_stream_t; /* same type as cudaStream_t */
 #define DIT_ETIMEOUT (-5)     /* a bounded device wait gave up (reported by dit_check) */
 
 /* Block dimensions. hidden H, heads nh, head_dim d = H / nh, ffn F.
- * Supported: d in {64, 128}; H % 256 == 0; F % 128 == 0. [gizai:dit, Arch] */
+ * Supported: d in {64, 128}; H % 256 == 0; F % 128 == 0. [gizai:dit, Arch]
+ * rope_split selects the rotary layout of q and k:
+ *   0: adjacent pairs (2i, 2i+1) over the whole head, tables [rows, d/2] [host contract, section 4]
+ *   1: split halves over the first 3/4 of the head: values i and i + 3d/8 (i < 3d/8) turned by
+ *      angle i, the last d/4 values unrotated, tables [rows, 3d/8] [gizai:dit, prepOf, HEAD] */
 typedef struct {
   int hidden;
   int heads;
   int head_dim;
   int ffn;
-  float eps;    /* modulated RMSNorm epsilon (1e-6 in every workload) */
-  float qk_eps; /* per-head query/key RMSNorm epsilon */
+  float eps;      /* modulated RMSNorm epsilon (1e-6 in every workload) */
+  float qk_eps;   /* per-head query/key RMSNorm epsilon */
+  int rope_split; /* 0 or 1, see above */
 } dit_dims;
 
 /* bf16 weights of one block. [gizai:dit, Block (indexes QKV, OUT, UP, DOWN, NORM1, NORM2, Q_NORM, K_NORM)]
