@@ -468,6 +468,23 @@ def run_ours(args):
                "flop_per_block": flops, "launches_per_block": 7 if sh.L % 128 == 0 else 13}
         del wT, wsD
 
+    # the sequential block with the split-halves partial rotary layout (tables [R, 3d/8], seeded angles)
+    rsp = None
+    if not args.no_rope_split:
+        dimsS = D.DitDims(sh.hidden, sh.heads, sh.head_dim, sh.ffn, sh.eps, sh.qk_eps, rope_split=True)
+        ang = np.random.default_rng(5).uniform(-20.0, 20.0, size=(sh.R, 3 * sh.head_dim // 8))
+        cS = torch.from_numpy(np.cos(ang).astype(np.float32)).cuda()
+        sS = torch.from_numpy(np.sin(ang).astype(np.float32)).cuda()
+        tS = (cS[:sh.L].contiguous(), sS[:sh.L].contiguous(), cS[sh.L:].contiguous(), sS[sh.L:].contiguous())
+        callS = lambda: D.dit_block_forward(dimsS, st["w"], st["txt"], st["img"], *tS, st["mod"], st["ws"])
+        msS = _time_loop(torch, callS, args.steps, args.warmup, dist) / args.steps
+        D.dit_check()
+        tfS = flops / (msS * 1e-3) / 1e12
+        rsp = {"workload": "1024sq block with the split-halves partial rotary (first 3/4 of each head, tables "
+                           "[R, 3d/8] of seeded angles)", "ms_per_block": msS, "tflops": tfS,
+               "frac_of_peak": tfS / peaks["bf16_tflops"], "flop_per_block": flops, "launches_per_block": 7}
+        del cS, sS, tS
+
     # end to end through host buffers
     e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
     D.dit_check()
@@ -498,6 +515,7 @@ def run_ours(args):
             "int8lin": int8,
             "parallel_block": par,
             "double_stream_block": dbl,
+            "rope_split_block": rsp,
             "denoise": den,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -585,6 +603,7 @@ def main():
     ap.add_argument("--no-denoise", action="store_true")
     ap.add_argument("--no-parallel", action="store_true")
     ap.add_argument("--no-double", action="store_true")
+    ap.add_argument("--no-rope-split", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
