@@ -31,7 +31,7 @@ __all__ = [
     "block_forward", "block_forward_rows", "dequant_int8", "euler_step", "shift_sigmas",
     "timestep_sinusoids", "time_embedding", "denoise", "pack_latents", "block_weights_f64",
     "modulated_layernorm", "parallel_block_forward", "parallel_block_forward_rows", "double_block_forward_rows",
-    "rope_apply_split", "rotate",
+    "rope_apply_split", "rotate", "lora_linear", "lora_merge",
 ]
 
 
@@ -267,6 +267,23 @@ def block_forward(inp, weights=None, rows=None):
     if rows is not None:
         return y
     return y[:sh.L], y[sh.L:]
+
+
+# ----------------------------------------------------------------------------------------------
+# LoRA adapters  [gizai:dit, Block (lora), withLora, loraOf, weightAt]
+# ----------------------------------------------------------------------------------------------
+
+def lora_linear(x, W, A, B):
+    """A linear with its LoRA adapter beside it: x W^T + (x A^T) B^T, A [rank, in], B [out, rank]
+    (the down product, then B's). Float64.  [gizai:dit, loraOf (A product), withLora (B product)]"""
+    x = np.asarray(x, dtype=np.float64)
+    return x @ np.asarray(W, dtype=np.float64).T + (x @ np.asarray(A, dtype=np.float64).T) @ \
+        np.asarray(B, dtype=np.float64).T
+
+
+def lora_merge(W, A, B):
+    """The merged weight W + B A that the adapter stands for.  [gizai:dit, weightAt]"""
+    return np.asarray(W, dtype=np.float64) + np.asarray(B, dtype=np.float64) @ np.asarray(A, dtype=np.float64)
 
 
 # ----------------------------------------------------------------------------------------------
