@@ -16,7 +16,7 @@ from typing import List, Optional, Sequence
 __all__ = [
     "DitError", "lib", "library_path", "DitDims", "BlockWeights", "Int8BlockWeights", "Modulation",
     "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_parallel_block_forward",
-    "dit_double_block_forward", "dit_euler_step",
+    "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
     "dit_vt_stride", "dit_attention", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
@@ -48,6 +48,10 @@ class dit_block_w(ctypes.Structure):
                 ("norm1", c_void_p), ("norm2", c_void_p), ("q_norm", c_void_p), ("k_norm", c_void_p)]
 
 
+class dit_lora(ctypes.Structure):
+    _fields_ = [("A", c_void_p * 4), ("B", c_void_p * 4), ("rank", c_int)]
+
+
 class dit_block_w8(ctypes.Structure):
     _fields_ = [("q", c_void_p * 4), ("s", c_void_p * 4), ("norm1", c_void_p), ("norm2", c_void_p),
                 ("q_norm", c_void_p), ("k_norm", c_void_p)]
@@ -70,6 +74,10 @@ _SIGNATURES = {
     "dit_double_block_forward": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), POINTER(dit_block_w), c_void_p,
                                          c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                                          POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
+    "dit_block_forward_lora": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), POINTER(dit_lora), c_void_p, c_int,
+                                       c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod),
+                                       c_void_p, c_size_t, c_void_p]),
+    "dit_lora_workspace_bytes": (c_size_t, [POINTER(dit_dims), c_int, c_int, c_int]),
     "dit_parallel_block_forward": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_int, c_void_p, c_int,
                                            c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                            c_size_t, c_void_p]),
@@ -212,6 +220,17 @@ class Modulation:
         self.c = dit_mod(_ptr(rows, torch.float32, "mod rows"), _ptr(map, torch.int32, "map"), rows.shape[0])
 
 
+class LoRA:
+    """Adapters of a block's four linears (qkv, out, up, down): lists of bf16 device tensors
+    A[i] [rank, in_i] and B[i] [out_i, rank], or None for a linear without one."""
+
+    def __init__(self, A, B, rank: int):
+        bf = _bf16()
+        self.tensors = (A, B)
+        self.c = dit_lora((c_void_p * 4)(*[_ptr(a, bf, "lora A") for a in A]),
+                          (c_void_p * 4)(*[_ptr(b, bf, "lora B") for b in B]), rank)
+
+
 class DenoiseModel:
     def __init__(self, dims: DitDims, w_in, w_t1, w_t2, w_ada, w_ada_f, w_out, blocks: List[BlockWeights],
                  latent_channels: int = 64):
@@ -260,6 +279,22 @@ def dit_block_forward_int8(dims: DitDims, w: Int8BlockWeights, txt, img, txt_cos
                                      _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
                                      _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
         "dit_block_forward_int8")
+
+
+def dit_block_forward_lora(dims: DitDims, w: BlockWeights, lora: "LoRA", txt, img, txt_cos, txt_sin, img_cos,
+                           img_sin, mod: Modulation, ws, stream=None):
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_block_forward_lora(ctypes.byref(dims.c), ctypes.byref(w.c), ctypes.byref(lora.c),
+                                     _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"), img.shape[0],
+                                     _ptr(txt_cos, f32), _ptr(txt_sin, f32), _ptr(img_cos, f32), _ptr(img_sin, f32),
+                                     ctypes.byref(mod.c), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                     _stream(stream)), "dit_block_forward_lora")
+
+
+def dit_lora_workspace_bytes(dims: DitDims, L: int, N: int, rank: int) -> int:
+    return lib().dit_lora_workspace_bytes(ctypes.byref(dims.c), L, N, rank)
 
 
 def dit_parallel_block_forward(dims: DitDims, w: BlockWeights, txt, img, txt_cos, txt_sin, img_cos, img_sin,

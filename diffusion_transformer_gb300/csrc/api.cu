@@ -140,13 +140,34 @@ struct ModRef {
 };
 
 // One whole block on already-validated arguments. `w8` selects the int8lin path.
+int lora_rank_pad(int rank) { return (rank + 63) / 64 * 64; }
+
 int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, float* txt, int L, float* img, int N,
               const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod, void* ws,
-              cudaStream_t st) {
+              cudaStream_t st, const dit_lora* lora = nullptr) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
   const BlockWs b = carve_block_ws(d, R, ws);
+  // linear i (0 qkv, 1 out, 2 up, 3 down) of input x [R, K]: with a LoRA adapter, down = x A^T into
+  // the scratch after the block workspace ([R, rank padded to 64], the padding computed as zero from
+  // A's missing rows), then [x | down] [W | B]^T through the linear's own epilogue
+  uint16_t* lora_down = lora ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
+  auto linear = [&](int i, const uint16_t* x, int K, const uint16_t* W, const GemmInt8B* w8b, int epi,
+                    GemmParams g) -> int {
+    if (!lora || !lora->A[i]) return gemm_launch(x, K, W, w8b, epi, g, st);
+    const int rp = lora_rank_pad(lora->rank);
+    GemmParams gd = base_params(R, rp, K, err);
+    gd.out = lora_down;
+    gd.ldo = rp;
+    gd.b_rows = lora->rank;
+    int rc = gemm_launch(x, K, lora->A[i], nullptr, kEpiStoreBF16, gd, st);
+    if (rc != DIT_OK) return rc;
+    g.K = K + rp;
+    g.k_split = K;
+    g.b2_inner = lora->rank;
+    return gemm_launch_cat(x, K, lora_down, rp, W, K, lora->B[i], lora->rank, epi, g, st);
+  };
   // int8lin scratch after the block workspace: one dequantised weight at a time
   uint16_t* i8_tiles = w8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
   const float* norm1 = w8 ? w8->norm1 : w->norm1;
@@ -163,7 +184,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, qn, kn, err);
   GemmInt8B q8;
   if (w8) q8 = GemmInt8B{w8->q[0], w8->s[0], i8_tiles};
-  if ((rc = gemm_launch(b.h, H, w8 ? nullptr : w->wqkv, w8 ? &q8 : nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
+  if ((rc = linear(0, b.h, H, w8 ? nullptr : w->wqkv, w8 ? &q8 : nullptr, kEpiQKV, g)) != DIT_OK) return rc;
 
   // 3. o = attention(q, k, v)
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
@@ -181,7 +202,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.split_ws = b.a;
   g.split_ws_bytes = size_t(R) * F * 2;
   if (w8) q8 = GemmInt8B{w8->q[1], w8->s[1], i8_tiles};
-  if ((rc = gemm_launch(b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
+  if ((rc = linear(1, b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, kEpiGated, g)) != DIT_OK) return rc;
 
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
   mp.w = norm2;
@@ -194,7 +215,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.out = b.a;
   g.ldo = F;
   if (w8) q8 = GemmInt8B{w8->q[2], w8->s[2], i8_tiles};
-  if ((rc = gemm_launch(b.h, H, w8 ? nullptr : w->wup, w8 ? &q8 : nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
+  if ((rc = linear(2, b.h, H, w8 ? nullptr : w->wup, w8 ? &q8 : nullptr, kEpiSwiGLU, g)) != DIT_OK) return rc;
 
   // 7. x += gate_m * (a Wdown^T)
   g = base_params(R, H, F, err);
@@ -208,7 +229,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.split_ws = b.h;
   g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
   if (w8) q8 = GemmInt8B{w8->q[3], w8->s[3], i8_tiles};
-  return gemm_launch(b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, kEpiGated, g, st);
+  return linear(3, b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, kEpiGated, g);
 }
 
 // The parallel (single-stream) block [gizai:dit, Block.parallel]: one modulated LayerNorm feeds
@@ -514,6 +535,29 @@ int dit_double_block_forward(const dit_dims* d, const dit_block_w* w_txt, const 
   }
   return run_double_block(d, w_txt, w_img, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dit_lora_workspace_bytes(const dit_dims* d, int L, int N, int rank) {
+  if (!dims_ok(d) || L < 0 || N < 1 || rank < 8 || rank > 1024 || rank % 8 != 0) return 0;
+  return carve_block_ws(d, L + N, nullptr).bytes + (size_t(L + N) * lora_rank_pad(rank) * 2 + 255) / 256 * 256;
+}
+
+int dit_block_forward_lora(const dit_dims* d, const dit_block_w* w, const dit_lora* lora, float* txt, int L, float* img,
+                           int N, const float* tc, const float* ts, const float* ic, const float* is, const dit_mod* mod,
+                           void* ws, size_t ws_bytes, dit_stream_t stream) {
+  if (!lora) return DIT_EINVAL;
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 0);
+  if (rc != DIT_OK) return rc;
+  if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+  if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  if (lora->rank < 8 || lora->rank > 1024 || lora->rank % 8 != 0) return DIT_EUNSUPPORTED;
+  for (int i = 0; i < 4; ++i) {
+    if ((lora->A[i] == nullptr) != (lora->B[i] == nullptr)) return DIT_EINVAL;
+    if (lora->A[i] && (!al16(lora->A[i]) || !al16(lora->B[i]))) return DIT_EINVAL;
+  }
+  if (ws_bytes < dit_lora_workspace_bytes(d, L, N, lora->rank)) return DIT_EWORKSPACE;
+  return run_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                   reinterpret_cast<cudaStream_t>(stream), lora);
 }
 
 int dit_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt, int L, float* img, int N,

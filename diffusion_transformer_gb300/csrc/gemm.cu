@@ -888,7 +888,7 @@ int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmI
     return dispatch_epi<128, true>(epi, m, p, stream);
   }
   if (reinterpret_cast<uintptr_t>(b) % 16) return DIT_EINVAL;
-  if (!tmap_bf16(&m.b, b, p.K, p.N, p.K, BN)) return DIT_ECUDA;
+  if (!tmap_bf16(&m.b, b, p.K, p.b_rows > 0 ? p.b_rows : p.N, p.K, BN)) return DIT_ECUDA;
   m.s = m.b;
   m.a2 = m.a;
   m.b2 = m.b;
@@ -925,9 +925,12 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
   } else {
     // A = [a | a2], B = [b | b2]: inner columns [0, k_split) from a and b, the rest from a2 and b2
     if (p.k_split % BK != 0 || p.k_split >= p.K || epi == kEpiQKVSwiGLU) return DIT_EUNSUPPORTED;
+    if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
     if (!al(a, lda) || !al(a2, lda2) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
-    if (!tmap_bf16(&m.a, a, p.k_split, p.M, lda, BM) || !tmap_bf16(&m.a2, a2, p.K - p.k_split, p.M, lda2, BM) ||
-        !tmap_bf16(&m.b, b, p.k_split, p.N, ldb, BN) || !tmap_bf16(&m.b2, b2, p.K - p.k_split, p.N, ldb2, BN))
+    const int k2 = p.K - p.k_split, b2_inner = p.b2_inner > 0 ? p.b2_inner : k2;
+    if (b2_inner > k2) return DIT_EINVAL;
+    if (!tmap_bf16(&m.a, a, p.k_split, p.M, lda, BM) || !tmap_bf16(&m.a2, a2, k2, p.M, lda2, BM) ||
+        !tmap_bf16(&m.b, b, p.k_split, p.N, ldb, BN) || !tmap_bf16(&m.b2, b2, b2_inner, p.N, ldb2, BN))
       return DIT_ECUDA;
   }
   m.s = m.b;

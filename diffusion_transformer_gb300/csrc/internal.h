@@ -63,6 +63,9 @@ struct GemmParams {
   // take B from the second B and, in the QKV epilogue, the head-norm weights q_norm2 / k_norm2
   int m_split;
   const float *q_norm2, *k_norm2;
+  // TMA extents smaller than the GEMM's (0: the GEMM's): rows of B (columns past them read as zero)
+  // and inner columns of the second B of a K-concatenation (LoRA factors of a rank below the tile)
+  int b_rows, b2_inner;
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row

@@ -110,6 +110,17 @@ typedef struct {
   int M;
 } dit_mod;
 
+/* LoRA adapters of a block's four linears [gizai:dit, Block (lora), loraOf, withLora, weightAt]:
+ * for linear i (0 qkv, 1 out, 2 up, 3 down) with in_i inputs and out_i outputs, A[i] [rank, in_i]
+ * and B[i] [out_i, rank] bf16 row-major; the linear becomes x W^T + (x A^T) B^T, the map of the
+ * merged weight W + B A. A[i] = B[i] = NULL: no adapter on that linear. rank % 8 == 0,
+ * 8 <= rank <= 1024. The caller owns the tensors. */
+typedef struct {
+  const uint16_t* A[4];
+  const uint16_t* B[4];
+  int rank;
+} dit_lora;
+
 /* ---------------------------------------------------------------------------------------------
  * Whole-block forward [gizai:dit, Block.forward]. For packed rows r = 0..L+N-1 (row r < L is
  * txt[r], else img[r - L]) and m = map[r]:
@@ -129,6 +140,16 @@ typedef struct {
 DIT_API int dit_block_forward(const dit_dims* dims, const dit_block_w* w, float* txt, int L, float* img, int N,
                       const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
                       const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* The bf16 block with LoRA adapters beside its linears (dit_lora): each adapted linear runs as
+ * one GEMM for down = x A^T (bf16, [R, rank rounded up to 64], in the workspace) and the linear's
+ * GEMM over [x | down] [W | B]^T with its usual epilogue (QK norm + rotary, gated residual, SwiGLU).
+ * Workspace: dit_lora_workspace_bytes(dims, L, N, rank). Otherwise as dit_block_forward. */
+DIT_API int dit_block_forward_lora(const dit_dims* dims, const dit_block_w* w, const dit_lora* lora, float* txt,
+                                   int L, float* img, int N, const float* txt_cos, const float* txt_sin,
+                                   const float* img_cos, const float* img_sin, const dit_mod* mod, void* ws,
+                                   size_t ws_bytes, dit_stream_t stream);
+DIT_API size_t dit_lora_workspace_bytes(const dit_dims* dims, int L, int N, int rank);
 
 /* The same block with int8lin weights [host contract, section 1]: W = bf16_rne(q * s), then the
  * bf16 MMA. With at most 512 rows the GEMM's converter warps dequantize each weight k-block inside
