@@ -485,6 +485,27 @@ def run_ours(args):
                "frac_of_peak": tfS / peaks["bf16_tflops"], "flop_per_block": flops, "launches_per_block": 7}
         del cS, sS, tS
 
+    # the sequential block with rank-64 LoRA adapters on all four linears
+    lor = None
+    if not args.no_lora:
+        lrank = 64  # LoRA rank (not the process rank)
+        H, F = sh.hidden, sh.ffn
+        gen = torch.Generator(device="cuda").manual_seed(6)
+        mk = lambda r, c: (torch.randn(r, c, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+        shapes = [(3 * H, H), (H, H), (2 * F, H), (H, F)]
+        loraW = D.LoRA([mk(lrank, i) for _, i in shapes], [mk(o, lrank) for o, _ in shapes], lrank)
+        wsL = torch.empty(D.dit_lora_workspace_bytes(st["dims"], sh.L, sh.N, lrank), dtype=torch.uint8, device="cuda")
+        callL = lambda: D.dit_block_forward_lora(st["dims"], st["w"], loraW, st["txt"], st["img"], st["tc"], st["ts"],
+                                                 st["ic"], st["is_"], st["mod"], wsL)
+        msL = _time_loop(torch, callL, args.steps, args.warmup, dist) / args.steps
+        D.dit_check()
+        flL = flops + sum(2.0 * sh.R * lrank * (o + i) for o, i in shapes)
+        tfL = flL / (msL * 1e-3) / 1e12
+        lor = {"workload": "1024sq block with rank-64 LoRA adapters on qkv, out, up and down", "ms_per_block": msL,
+               "tflops": tfL, "frac_of_peak": tfL / peaks["bf16_tflops"], "flop_per_block": flL,
+               "launches_per_block": 11}
+        del loraW, wsL
+
     # end to end through host buffers
     e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
     D.dit_check()
@@ -516,6 +537,7 @@ def run_ours(args):
             "parallel_block": par,
             "double_stream_block": dbl,
             "rope_split_block": rsp,
+            "lora_block": lor,
             "denoise": den,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -604,6 +626,7 @@ def main():
     ap.add_argument("--no-parallel", action="store_true")
     ap.add_argument("--no-double", action="store_true")
     ap.add_argument("--no-rope-split", action="store_true")
+    ap.add_argument("--no-lora", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
