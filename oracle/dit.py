@@ -216,7 +216,7 @@ def _mod_rows(mod, mod_map, rows):
 
 def block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
                        rows: Optional[np.ndarray] = None, norm1=None, norm2=None,
-                       q_norm=None, k_norm=None, eps=1e-6, qk_eps=1e-6):
+                       q_norm=None, k_norm=None, eps=1e-6, qk_eps=1e-6, post_attn=None, post_mlp=None):
     """One AdaLN block over the packed rows x [R, H] (float64 copy returned; x untouched).
 
     1. h  = modnorm(x; norm1, shift_a, scale_a)
@@ -231,6 +231,8 @@ def block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
 
     Steps 1-4 run for every row (keys and values need them); steps 5-9 only for ``rows`` (all by
     default), which lets tests check sampled rows of large sequences.
+    A sandwich block (post_attn / post_mlp, [H] norm weights) norms each branch's output before its
+    gate: x += gate * rmsnorm(y) * post (the block's RMS norm and eps; gizai:dit, POST_ATTN/POST_MLP).
     [gizai:dit, Block.forward, normedInto, weightAt (QKV row order), prepOf, gatedInto, gluRows]"""
     x = np.asarray(x, dtype=np.float64)
     R, H = x.shape
@@ -248,10 +250,11 @@ def block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
     k = rotate(qk_rmsnorm(k, k_norm, qk_eps), cos, sin)
     o = attention(q, k, v, rows)
     _, _, ga_r, sm_r, cm_r, gm_r = _mod_rows(mod, mod_map, rows)
-    xr = x[rows] + ga_r * (o @ Wout.T)
+    post = lambda y, w: y if w is None else modulated_rmsnorm(y, w, 0.0, 0.0, eps)
+    xr = x[rows] + ga_r * post(o @ Wout.T, post_attn)
     h2 = modulated_rmsnorm(xr, norm2, sm_r, cm_r, eps)
     a = swiglu_interleaved(h2 @ Wup.T)
-    return xr + gm_r * (a @ Wdown.T)
+    return xr + gm_r * post(a @ Wdown.T, post_mlp)
 
 
 def block_forward(inp, weights=None, rows=None):

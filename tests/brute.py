@@ -20,7 +20,7 @@ def rmsnorm_row(x, eps):
 
 
 def block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
-          norm1=None, norm2=None, qn=None, kn=None):
+          norm1=None, norm2=None, qn=None, kn=None, post_attn=None, post_mlp=None):
     """x: list of R rows (lists of H floats). mod_rows[r] = 6 lists of H (shift_a, scale_a, gate_a,
     shift_m, scale_m, gate_m) for row r. cos/sin: R lists of d/2. Returns new rows."""
     R, H = len(x), len(x[0])
@@ -67,6 +67,8 @@ def block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_e
             for j in range(d):
                 o.append(sum(e[c] / z * V[c][n][j] for c in range(R)))
         att = matvec(Wo, o)
+        if post_attn is not None:
+            att = [v * w for v, w in zip(rmsnorm_row(att, eps), post_attn)]
         ga = mod_rows[r][2]
         xr = [x[r][i] + ga[i] * att[i] for i in range(H)]
         sm, cm, gm = mod_rows[r][3], mod_rows[r][4], mod_rows[r][5]
@@ -74,6 +76,8 @@ def block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_e
         g, u = matvec(Wg, h2), matvec(Wu, h2)
         a = [g[j] / (1.0 + math.exp(-g[j])) * u[j] for j in range(len(g))]
         mlp = matvec(Wd, a)
+        if post_mlp is not None:
+            mlp = [v * w for v, w in zip(rmsnorm_row(mlp, eps), post_mlp)]
         out.append([xr[i] + gm[i] * mlp[i] for i in range(H)])
     return out
 
