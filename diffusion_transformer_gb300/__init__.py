@@ -16,7 +16,8 @@ from typing import List, Optional, Sequence
 __all__ = [
     "DitError", "lib", "library_path", "DitDims", "BlockWeights", "Int8BlockWeights", "Modulation",
     "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_parallel_block_forward",
-    "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA", "dit_euler_step",
+    "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA",
+    "dit_block_forward_sandwich", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
     "dit_vt_stride", "dit_attention", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
@@ -78,6 +79,9 @@ _SIGNATURES = {
                                        c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod),
                                        c_void_p, c_size_t, c_void_p]),
     "dit_lora_workspace_bytes": (c_size_t, [POINTER(dit_dims), c_int, c_int, c_int]),
+    "dit_block_forward_sandwich": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_void_p, c_void_p,
+                                           c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                           POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
     "dit_parallel_block_forward": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_int, c_void_p, c_int,
                                            c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                            c_size_t, c_void_p]),
@@ -291,6 +295,20 @@ def dit_block_forward_lora(dims: DitDims, w: BlockWeights, lora: "LoRA", txt, im
                                      _ptr(txt_cos, f32), _ptr(txt_sin, f32), _ptr(img_cos, f32), _ptr(img_sin, f32),
                                      ctypes.byref(mod.c), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                      _stream(stream)), "dit_block_forward_lora")
+
+
+def dit_block_forward_sandwich(dims: DitDims, w: BlockWeights, post_attn, post_mlp, txt, img, txt_cos, txt_sin,
+                               img_cos, img_sin, mod: Modulation, ws, stream=None):
+    """The sandwich block: post_attn / post_mlp [H] fp32 norm weights (None: that branch un-normed)."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_block_forward_sandwich(ctypes.byref(dims.c), ctypes.byref(w.c), _ptr(post_attn, f32, "post_attn"),
+                                         _ptr(post_mlp, f32, "post_mlp"), _ptr(txt, f32, "txt"), L,
+                                         _ptr(img, f32, "img"), img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                                         _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
+                                         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_block_forward_sandwich")
 
 
 def dit_lora_workspace_bytes(dims: DitDims, L: int, N: int, rank: int) -> int:

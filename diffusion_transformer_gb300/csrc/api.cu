@@ -144,7 +144,8 @@ int lora_rank_pad(int rank) { return (rank + 63) / 64 * 64; }
 
 int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, float* txt, int L, float* img, int N,
               const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod, void* ws,
-              cudaStream_t st, const dit_lora* lora = nullptr) {
+              cudaStream_t st, const dit_lora* lora = nullptr, const float* post_attn = nullptr,
+              const float* post_mlp = nullptr) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
@@ -167,6 +168,21 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
     g.k_split = K;
     g.b2_inner = lora->rank;
     return gemm_launch_cat(x, K, lora_down, rp, W, K, lora->B[i], lora->rank, epi, g, st);
+  };
+  // a gated linear; with a post-norm weight (sandwich block) its output y goes to the h..vt span as
+  // fp32 (consumed by then, and at least R * H * 4 bytes) and the sandwich kernel adds
+  // gate * rmsnorm(y) * post to x
+  auto gated_linear = [&](int i, const uint16_t* x, int K, const uint16_t* W, const GemmInt8B* w8b, GemmParams g,
+                          const float* post, long long gate_row) -> int {
+    if (!post) return linear(i, x, K, W, w8b, kEpiGated, g);
+    float* y = reinterpret_cast<float*>(b.h);
+    GemmParams gy = base_params(R, H, K, err);
+    gy.out = y;
+    gy.ldo = H;
+    int rc = linear(i, x, K, W, w8b, kEpiStoreF32, gy);
+    if (rc != DIT_OK) return rc;
+    SandwichParams sp{txt, img, L, R, H, y, mod.rows + gate_row * H, 6LL * H, mod.map, post, d->eps};
+    return sandwich_launch(sp, st);
   };
   // int8lin scratch after the block workspace: one dequantised weight at a time
   uint16_t* i8_tiles = w8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
@@ -202,7 +218,8 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.split_ws = b.a;
   g.split_ws_bytes = size_t(R) * F * 2;
   if (w8) q8 = GemmInt8B{w8->q[1], w8->s[1], i8_tiles};
-  if ((rc = linear(1, b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, kEpiGated, g)) != DIT_OK) return rc;
+  if ((rc = gated_linear(1, b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, g, post_attn, 2)) != DIT_OK)
+    return rc;
 
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
   mp.w = norm2;
@@ -229,7 +246,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.split_ws = b.h;
   g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
   if (w8) q8 = GemmInt8B{w8->q[3], w8->s[3], i8_tiles};
-  return linear(3, b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, kEpiGated, g);
+  return gated_linear(3, b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, g, post_mlp, 5);
 }
 
 // The parallel (single-stream) block [gizai:dit, Block.parallel]: one modulated LayerNorm feeds
@@ -558,6 +575,18 @@ int dit_block_forward_lora(const dit_dims* d, const dit_block_w* w, const dit_lo
   if (ws_bytes < dit_lora_workspace_bytes(d, L, N, lora->rank)) return DIT_EWORKSPACE;
   return run_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                    reinterpret_cast<cudaStream_t>(stream), lora);
+}
+
+int dit_block_forward_sandwich(const dit_dims* d, const dit_block_w* w, const float* post_attn, const float* post_mlp,
+                               float* txt, int L, float* img, int N, const float* tc, const float* ts, const float* ic,
+                               const float* is, const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 0);
+  if (rc != DIT_OK) return rc;
+  if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+  if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  if ((post_attn && !al16(post_attn)) || (post_mlp && !al16(post_mlp))) return DIT_EINVAL;
+  return run_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr, post_attn, post_mlp);
 }
 
 int dit_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt, int L, float* img, int N,

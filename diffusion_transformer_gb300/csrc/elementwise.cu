@@ -239,6 +239,60 @@ __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __r
   }
 }
 
+// Sandwich residual (a branch normed before its gate): one CTA per row, H/1024 float4 chunks per
+// thread loaded before the reduction, then x += gate * y * rstd * w.
+template <int NC>
+__global__ void __launch_bounds__(kNormThreads) sandwich_kernel(const SandwichParams p) {
+  const int r = blockIdx.x;
+  float* x = r < p.L ? p.txt + size_t(r) * p.H : p.img + size_t(r - p.L) * p.H;
+  const int m = p.map ? __ldg(p.map + r) : 0;
+  const float4* y4 = reinterpret_cast<const float4*>(p.y + size_t(r) * p.H);
+  const float4* g4 = reinterpret_cast<const float4*>(p.gate + size_t(m) * p.mod_stride);
+  const float4* w4 = reinterpret_cast<const float4*>(p.w);
+  float4* x4 = reinterpret_cast<float4*>(x);
+  __shared__ float part[kNormThreads / 32];
+  const int n4 = p.H >> 2;
+  constexpr int K = NC > 0 ? NC : 1;
+  float4 yv[K];
+  float ss = 0.f;
+  if constexpr (NC > 0) {
+#pragma unroll
+    for (int k = 0; k < NC; ++k) yv[k] = y4[threadIdx.x + k * kNormThreads];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      ss = fmaf(yv[k].x, yv[k].x, ss);
+      ss = fmaf(yv[k].y, yv[k].y, ss);
+      ss = fmaf(yv[k].z, yv[k].z, ss);
+      ss = fmaf(yv[k].w, yv[k].w, ss);
+    }
+  } else {
+    for (int i = threadIdx.x; i < n4; i += kNormThreads) {
+      const float4 v = y4[i];
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+  }
+  const float rstd = rsqrtf(block_sum(ss, part) / float(p.H) + p.eps);
+  auto apply = [&](int i, float4 v) {
+    const float4 g = __ldg(g4 + i);
+    const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
+    float4 xv = x4[i];
+    xv.x = fmaf(g.x, v.x * rstd * w.x, xv.x);
+    xv.y = fmaf(g.y, v.y * rstd * w.y, xv.y);
+    xv.z = fmaf(g.z, v.z * rstd * w.z, xv.z);
+    xv.w = fmaf(g.w, v.w * rstd * w.w, xv.w);
+    x4[i] = xv;
+  };
+  if constexpr (NC > 0) {
+#pragma unroll
+    for (int k = 0; k < NC; ++k) apply(threadIdx.x + k * kNormThreads, yv[k]);
+  } else {
+    for (int i = threadIdx.x; i < n4; i += kNormThreads) apply(i, y4[i]);
+  }
+}
+
 // Diagnostic of the bounded-wait path every pipeline uses: one warp waits (mbar_wait_warp, the
 // production wait with its 1 s limit) on an mbarrier of its own, which completes only when
 // `complete` is set. Without it the wait gives up, the error word records the site and the kernel
@@ -318,6 +372,19 @@ int sinusoid_launch(const float* sigmas, int steps, int dim, uint16_t* out, cuda
 int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t stream) {
   if (n <= 0) return DIT_OK;
   f32_to_bf16_kernel<<<grid_for(n, 256), 256, 0, stream>>>(in, out, n);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int sandwich_launch(const SandwichParams& p, cudaStream_t stream) {
+  if (p.R <= 0) return DIT_OK;
+  const int chunks = p.H % (4 * kNormThreads) == 0 ? p.H / (4 * kNormThreads) : 0;
+  switch (chunks) {
+    case 1: sandwich_kernel<1><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    case 2: sandwich_kernel<2><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    case 3: sandwich_kernel<3><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    case 4: sandwich_kernel<4><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    default: sandwich_kernel<0><<<p.R, kNormThreads, 0, stream>>>(p); break;
+  }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 

@@ -124,6 +124,21 @@ struct ModNormParams {
   const float* w_img;        // [H] or null
 };
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream);
+
+// Sandwich residual: x[r] += gate[map[r]] * y[r] * rsqrt(mean(y[r]^2) + eps) * w, y [R, H] fp32 (the
+// branch's linear output), x rows < L in txt, others in img (row stride H).
+struct SandwichParams {
+  float* txt;
+  float* img;
+  int L, R, H;
+  const float* y;
+  const float* gate;       // row m at gate + m * mod_stride
+  long long mod_stride;
+  const int32_t* map;      // [R] or null
+  const float* w;          // [H] post-norm weight or null (ones)
+  float eps;
+};
+int sandwich_launch(const SandwichParams& p, cudaStream_t stream);
 // bounded-wait diagnostic (see dit_selftest_bounded_wait)
 int wait_selftest_launch(int complete, int* err, cudaStream_t stream);
 

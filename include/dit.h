@@ -151,6 +151,18 @@ DIT_API int dit_block_forward_lora(const dit_dims* dims, const dit_block_w* w, c
                                    size_t ws_bytes, dit_stream_t stream);
 DIT_API size_t dit_lora_workspace_bytes(const dit_dims* dims, int L, int N, int rank);
 
+/* The sandwich block [gizai:dit, POST_ATTN, POST_MLP]: dit_block_forward whose attention and MLP
+ * outputs are normed before their gates: x += gate_a * rmsnorm(o Wout^T) * post_attn and
+ * x += gate_m * rmsnorm(a Wdown^T) * post_mlp, rmsnorm(y) = y * rsqrt(mean(y^2) + eps) (dims.eps).
+ * post_attn / post_mlp: [H] fp32, or NULL for a branch added as it is. Each normed branch runs as
+ * its linear with an fp32 store and a row kernel for the norm and the residual (9 launches with
+ * both). Workspace: dit_workspace_bytes(dims, L, N, 0). Otherwise as dit_block_forward. */
+DIT_API int dit_block_forward_sandwich(const dit_dims* dims, const dit_block_w* w, const float* post_attn,
+                                       const float* post_mlp, float* txt, int L, float* img, int N,
+                                       const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                       const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                       dit_stream_t stream);
+
 /* The same block with int8lin weights [host contract, section 1]: W = bf16_rne(q * s), then the
  * bf16 MMA. With at most 512 rows the GEMM's converter warps dequantize each weight k-block inside
  * the mainloop; with more rows (many M tiles per weight tile) each linear's weight is dequantized
