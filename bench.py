@@ -506,6 +506,22 @@ def run_ours(args):
                "launches_per_block": 11}
         del loraW, wsL
 
+    # the sandwich block: both branches RMS-normed (own weights) before their gates
+    swb = None
+    if not args.no_sandwich:
+        gpost = torch.Generator(device="cuda").manual_seed(7)
+        pa = 1 + 0.2 * torch.randn(sh.hidden, device="cuda", generator=gpost)
+        pm = 1 + 0.2 * torch.randn(sh.hidden, device="cuda", generator=gpost)
+        callW = lambda: D.dit_block_forward_sandwich(st["dims"], st["w"], pa, pm, st["txt"], st["img"], st["tc"],
+                                                     st["ts"], st["ic"], st["is_"], st["mod"], st["ws"])
+        msW = _time_loop(torch, callW, args.steps, args.warmup, dist) / args.steps
+        D.dit_check()
+        tfW = flops / (msW * 1e-3) / 1e12
+        swb = {"workload": "1024sq sandwich block: attention and MLP outputs RMS-normed before their gates",
+               "ms_per_block": msW, "tflops": tfW, "frac_of_peak": tfW / peaks["bf16_tflops"], "flop_per_block": flops,
+               "launches_per_block": 9}
+        del pa, pm
+
     # end to end through host buffers
     e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
     D.dit_check()
@@ -538,6 +554,7 @@ def run_ours(args):
             "double_stream_block": dbl,
             "rope_split_block": rsp,
             "lora_block": lor,
+            "sandwich_block": swb,
             "denoise": den,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -627,6 +644,7 @@ def main():
     ap.add_argument("--no-double", action="store_true")
     ap.add_argument("--no-rope-split", action="store_true")
     ap.add_argument("--no-lora", action="store_true")
+    ap.add_argument("--no-sandwich", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
