@@ -16,6 +16,8 @@
 //   kEpiSwiGLU  a_j = silu(acc_2j) * acc_2j+1      (up linear, interleaved rows)
 //   kEpiQKV     per-head RMS norm * weight, rotary pairs (2i, 2i+1), head-major q/k stores and a
 //               transposed v store for the attention kernel (klein article, section 4.4)
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -31,19 +33,22 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 
-template <int BN, bool B8>
+template <int BN, bool B8, bool PAIR = false>
 struct GemmCfg {
   // int8lin: 256-row CTA tiles (two M=128 MMAs share each converted B k-block), halving the
-  // conversions per FLOP; bf16: 128-row tiles.
+  // conversions per FLOP; bf16: 128-row tiles, or 256 x BN tiles shared by a CTA pair (PAIR: each CTA
+  // brings its 128 rows of A and half of the B tile, the first CTA issues M=256 MMAs over both).
   static constexpr int kMH = B8 ? 2 : 1;             // 128-row halves per CTA tile
-  static constexpr int kTileM = BM * kMH;
-  static constexpr int kStages = B8 ? (BN == 256 ? 3 : 4) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
+  static constexpr int kTileM = PAIR ? 2 * BM : BM * kMH;  // rows of one work tile
+  static constexpr int kStages =
+      B8 ? (BN == 256 ? 3 : 4) : PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
   // TMEM accumulator sets: two (the epilogue drains one while the MMA fills the other) when they fit
   // in the 512 columns, else one.
   static constexpr int kAccBufs = (2 * kMH * BN <= 512) ? 2 : 1;
   static constexpr uint32_t kAHalf = BM * BK * 2;
   static constexpr uint32_t kABytes = kAHalf * kMH;
   static constexpr uint32_t kBBytes = BN * BK * 2;   // bf16 tile the MMA reads
+  static constexpr uint32_t kBLoad = PAIR ? kBBytes / 2 : kBBytes;  // bf16 B bytes this CTA holds per stage
   static constexpr uint32_t kB8Bytes = BN * BK;      // int8 tile TMA writes (B8 only)
   static constexpr uint32_t kSBytes = BN * 16;       // B8: scale tile [BN rows x 8 bf16] (4 k-blocks)
   static constexpr int kConvStages = 2;              // bf16 B tiles produced by the converters
@@ -57,10 +62,10 @@ struct GemmCfg {
   static constexpr int kConvWarp0 = 2 + kEpiWarps;         // first converter warp (B8)
   static constexpr int kThreads = 64 + kEpiThreads + (B8 ? kConvThreads : 0);
   // smem: [A ring][B ring (bf16, or int8 + scales for B8)][B8: converted bf16 ring][barriers][tmem slot]
-  static constexpr uint32_t kRingBytes = kStages * (kABytes + (B8 ? kB8Bytes + kSBytes : kBBytes));
+  static constexpr uint32_t kRingBytes = kStages * (kABytes + (B8 ? kB8Bytes + kSBytes : kBLoad));
   static constexpr uint32_t kConvBytes = B8 ? kConvStages * kBBytes : 0;
   static constexpr uint32_t kEpiBytes = kEpiWarps * 4096;   // epilogue staging, 4 KB per epilogue warp
-  static constexpr uint32_t kBarBytes = 8 * (2 * kStages + 4 + 2 * kConvStages + 2) + 16;
+  static constexpr uint32_t kBarBytes = 8 * (2 * kStages + 4 + 2 * kConvStages + 3) + 16;
   static constexpr uint32_t kSmemBytes = 1024 + kRingBytes + kConvBytes + kEpiBytes + kBarBytes;
 };
 
@@ -509,33 +514,48 @@ __device__ __forceinline__ void split_finish(const GemmParams& p, const float* p
   }
 }
 
-template <int BN, int EPI, bool B8>
-__global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
+// CTA pairs publish in global memory that their barriers are initialised, one word per CTA: it is
+// set to 1 once the CTA's barriers are initialised and back to 0 when the CTA ends, and a CTA touches
+// its peer's shared memory only after reading the peer's word as 1. Launches pick one of
+// kPairSlots word sets in turn (host counter), so launches running at once on different streams
+// use different words.
+constexpr int kPairSlots = 64, kPairMaxCtas = 256;
+__device__ uint32_t g_pair_started[kPairSlots * kPairMaxCtas];
+
+template <int BN, int EPI, bool B8, bool PAIR>
+__global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
-  using Cfg = GemmCfg<BN, B8>;
+  static_assert(!(PAIR && B8), "CTA pairs run the bf16 mainloop only");
+  using Cfg = GemmCfg<BN, B8, PAIR>;
   constexpr int S = Cfg::kStages;
   constexpr int CS = Cfg::kConvStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * Cfg::kABytes;                              // bf16 ring, or int8 ring when B8
-  uint8_t* sSc = sB + S * (B8 ? Cfg::kB8Bytes : Cfg::kBBytes);      // B8: scale-tile ring
+  uint8_t* sSc = sB + S * (B8 ? Cfg::kB8Bytes : Cfg::kBLoad);       // B8: scale-tile ring
   uint8_t* sC = sSc + (B8 ? S * Cfg::kSBytes : 0);                  // B8: converted bf16 ring
   uint8_t* sE = sC + Cfg::kConvBytes;                               // epilogue staging
   uint64_t* bars = reinterpret_cast<uint64_t*>(sE + Cfg::kEpiBytes);
-  uint64_t* full = bars;                 // [S] TMA landed
+  uint64_t* full = bars;                 // [S] TMA landed (PAIR: the first CTA's counts both CTAs' copies)
   uint64_t* empty = bars + S;            // [S] stage free (MMA done; B8: also converter done)
   uint64_t* tfull = bars + 2 * S;        // [2] accumulator ready
-  uint64_t* tempty = bars + 2 * S + 2;   // [2] accumulator drained
+  uint64_t* tempty = bars + 2 * S + 2;   // [2] accumulator drained (PAIR: by both CTAs, first CTA's)
   uint64_t* cfull = bars + 2 * S + 4;    // [CS] converted B tile ready (B8)
   uint64_t* cempty = cfull + CS;         // [CS] converted B tile consumed (B8)
   uint64_t* drain = cempty + CS;         // [1] final MMA completion
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  uint64_t* done = drain + 1;            // [1] PAIR: the peer CTA has finished with this CTA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint32_t* pair_ok = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = lane_id();
+  // PAIR: CTAs 2u and 2u + 1 form cluster u; work unit = the pair, rank 0 issues the MMAs
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  const int unit = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int units = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
   const int num_m = (p.M + Cfg::kTileM - 1) / Cfg::kTileM;
   const int num_n = p.N / BN;
   // Tile order: consecutive tiles share the smaller operand's panel set, so the CTAs running at
@@ -562,13 +582,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), Cfg::kEpiThreads);
+      mbar_init(smem_u32(&tempty[a]), (PAIR ? 2 : 1) * Cfg::kEpiThreads);
     }
     for (int c = 0; c < CS; ++c) {
       mbar_init(smem_u32(&cfull[c]), Cfg::kConvThreads);
       mbar_init(smem_u32(&cempty[c]), 1);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(done), 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -578,7 +599,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     if (p.k_split > 0) tma_prefetch_desc(&tmA2);
     if (p.k_split > 0 || p.n_split > 0 || p.m_split > 0) tma_prefetch_desc(&tmB2);
   }
-  if (warp == 1) {
+  bool up = true;
+  if constexpr (PAIR) {
+    // barriers initialised here -> published; then a bounded wait for the peer's word
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t* words = g_pair_started + (p.pair_epoch % kPairSlots) * kPairMaxCtas;
+      st_release_gpu(&words[blockIdx.x], 1u);
+      const uint64_t t0 = globaltimer_ns();
+      uint32_t ok = 1;
+      while (ld_acquire_gpu(&words[blockIdx.x ^ 1u]) != 1u)
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicCAS(p.err, 0, kErrTimeoutPair);
+          ok = 0;
+          break;
+        }
+      asm volatile("fence.acq_rel.cluster;" ::: "memory");
+      *pair_ok = ok;
+    }
+    __syncthreads();
+    up = *pair_ok != 0;
+    if (warp == 1) {
+      tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+      tmem_relinquish_pair();
+    }
+  } else if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -587,21 +632,27 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (!up) {
+    // the pair never formed: nothing to do
+  } else if (warp == 0) {
     // ------------------------------------------------------------- TMA producer
     if (elect_one()) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      // PAIR: both CTAs' copies complete on the first CTA's barrier, which expects both
+      const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&full[0]), 0) : smem_u32(&full[0]);
+      for (int it = unit; it < items && ok; it += units) {
         const WorkItem w = work_item(p, it, tiles, KB);
         int mb, nb;
         tile_mn(w.tile, mb, nb);
         for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, kErrTimeoutProducer)) { ok = false; break; }
-          const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, Cfg::kABytes + (B8 ? Cfg::kB8Bytes + Cfg::kSBytes : Cfg::kBBytes));
+          const uint32_t fb = full0 + uint32_t(stage) * 8u;
+          if (!PAIR || rank == 0)
+            mbar_arrive_expect_tx(smem_u32(&full[stage]),
+                                  (PAIR ? 2 : 1) * (Cfg::kABytes + (B8 ? Cfg::kB8Bytes + Cfg::kSBytes : Cfg::kBLoad)));
           // concatenated operands: the second A/B past the K boundary, the second B past the N boundary
           const bool k2 = p.k_split > 0 && kb * BK >= p.k_split;
           const bool n2 = p.n_split > 0 && nb * BN >= p.n_split;
@@ -610,38 +661,47 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
           const CUtensorMap* mbm = (k2 || n2 || m2) ? &tmB2 : &tmB;
           const int kc = k2 ? kb * BK - p.k_split : kb * BK;
           const int nr = n2 ? nb * BN - p.n_split : nb * BN;
+          if constexpr (PAIR) {
+            tma_load_2d_pair(smem_u32(sA + stage * Cfg::kABytes), ma, fb, kc, mb * Cfg::kTileM + int(rank) * BM);
+            tma_load_2d_pair(smem_u32(sB + stage * Cfg::kBLoad), mbm, fb, kc, nr + int(rank) * (BN / 2));
+          } else {
 #pragma unroll
-          for (int h = 0; h < Cfg::kMH; ++h)
-            tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), ma, fb, kc,
-                        mb * Cfg::kTileM + h * BM);
-          if constexpr (B8) {
-            tma_load_2d(smem_u32(sB + stage * Cfg::kB8Bytes), &tmB, fb, kb * BK, nb * BN);
-            // scales of k-blocks (kb & ~3) .. (kb | 3): 8 bf16 per row, 16-byte aligned columns
-            tma_load_2d(smem_u32(sSc + stage * Cfg::kSBytes), &tmS, fb, (kb * 2) & ~7, nb * BN);
-          } else
-            tma_load_2d(smem_u32(sB + stage * Cfg::kBBytes), mbm, fb, kc, nr);
+            for (int h = 0; h < Cfg::kMH; ++h)
+              tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), ma, fb, kc,
+                          mb * Cfg::kTileM + h * BM);
+            if constexpr (B8) {
+              tma_load_2d(smem_u32(sB + stage * Cfg::kB8Bytes), &tmB, fb, kb * BK, nb * BN);
+              // scales of k-blocks (kb & ~3) .. (kb | 3): 8 bf16 per row, 16-byte aligned columns
+              tma_load_2d(smem_u32(sSc + stage * Cfg::kSBytes), &tmS, fb, (kb * 2) & ~7, nb * BN);
+            } else
+              tma_load_2d(smem_u32(sB + stage * Cfg::kBBytes), mbm, fb, kc, nr);
+          }
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
-      // every issued copy must have landed before the CTA exits
-      for (int s = 0; s < S; ++s)
-        if (issued_mask & (1u << s))
-          mbar_wait(smem_u32(&full[s]), (last_parity >> s) & 1u, p.err, kErrTimeoutDrain);
+      // every issued copy must have landed before the CTA exits (PAIR: the first CTA's barriers
+      // count the second's copies too, and the second waits for the first before it exits)
+      if (!PAIR || rank == 0)
+        for (int s = 0; s < S; ++s)
+          if (issued_mask & (1u << s))
+            mbar_wait(smem_u32(&full[s]), (last_parity >> s) & 1u, p.err, kErrTimeoutDrain);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (elect_one()) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    if ((!PAIR || rank == 0) && elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16(PAIR ? 2 * BM : BM, BN);
       int stage = 0, cstage = 0;
       uint32_t phase = 0, cphase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      for (int it = unit; it < items && ok; it += units) {
         const WorkItem w = work_item(p, it, tiles, KB);
-        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, kErrTimeoutMma)) break;
+        if (!(PAIR ? mbar_wait_cluster(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, kErrTimeoutMma)
+                   : mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, kErrTimeoutMma)))
+          break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * Cfg::kMH * BN);
         for (int kb = w.k0; kb < w.k1; ++kb) {
@@ -651,7 +711,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
             if (!mbar_wait(smem_u32(&cfull[cstage]), cphase, p.err, kErrTimeoutMma)) { ok = false; break; }
             b_addr = smem_u32(sC + cstage * Cfg::kBBytes);
           } else {
-            b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+            b_addr = smem_u32(sB + stage * Cfg::kBLoad);
           }
           tc_fence_after();
           const uint64_t bdesc = sw128_desc(b_addr);
@@ -659,11 +719,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
           for (int h = 0; h < Cfg::kMH; ++h) {
             const uint64_t adesc = sw128_desc(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes per K=16 step inside the swizzle atom
-              umma_bf16(d + uint32_t(h * BN), adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc,
-                        kb != w.k0 || kk != 0);
+            for (int kk = 0; kk < BK / 16; ++kk) {  // +32 bytes per K=16 step inside the swizzle atom
+              if constexpr (PAIR)
+                umma_bf16_pair(d, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc, kb != w.k0 || kk != 0);
+              else
+                umma_bf16(d + uint32_t(h * BN), adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc,
+                          kb != w.k0 || kk != 0);
+            }
           }
-          umma_commit(smem_u32(&empty[stage]));
+          if constexpr (PAIR) umma_commit_pair_both(smem_u32(&empty[stage]));
+          else umma_commit(smem_u32(&empty[stage]));
           if constexpr (B8) {
             umma_commit(smem_u32(&cempty[cstage]));
             if (++cstage == CS) { cstage = 0; cphase ^= 1; }
@@ -671,11 +736,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&tfull[acc]));
+        if constexpr (PAIR) umma_commit_pair_both(smem_u32(&tfull[acc]));
+        else umma_commit(smem_u32(&tfull[acc]));
         if (++acc == Cfg::kAccBufs) { acc = 0; acc_phase ^= 1; }
       }
       // all MMAs issued by this thread complete before TMEM is released
-      umma_commit(smem_u32(drain));
+      if constexpr (PAIR) umma_commit_pair(smem_u32(drain));
+      else umma_commit(smem_u32(drain));
       mbar_wait(smem_u32(drain), 0, p.err, kErrTimeoutDrain);
     }
   } else if (warp < Cfg::kConvWarp0) {
@@ -683,9 +750,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
     const int quad = warp & 3;                       // TMEM lanes this warp may access
     const int col0 = ((warp - 2) >> 2) * Cfg::kEpiCols;  // its columns of the tile
     uint8_t* stage = sE + (warp - 2) * 4096;
+    // PAIR: this CTA's 128 rows of the pair's tile; the accumulator is released on the first CTA
+    const int rows_of = PAIR ? int(rank) * BM : 0;
+    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : smem_u32(&tempty[0]);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    for (int it = unit; it < items; it += units) {
       const WorkItem w = work_item(p, it, tiles, KB);
       int mb, nb;
       tile_mn(w.tile, mb, nb);
@@ -695,12 +765,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
         if (w.part >= 0) {
           // K-split tile: publish this part, release the accumulator, and let the warp that
           // delivers the quadrant's last part apply the residual update
-          const int ti = w.tile - p.sk_first;
+          const int ti = (w.tile - p.sk_first) * (PAIR ? 2 : 1) + int(rank);  // 128-row slab
           float* parts = p.split_part + size_t(ti) * p.split * BM * BN + size_t(quad) * 32 * BN;
           const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
           split_store<BN>(taddr, parts + size_t(w.part) * BM * BN, lane, stage);
           tc_fence_before();
-          mbar_arrive(smem_u32(&tempty[acc]));
+          if constexpr (PAIR) mbar_arrive_cluster(tempty0 + uint32_t(acc) * 8u);
+          else mbar_arrive(smem_u32(&tempty[acc]));
           if (++acc == Cfg::kAccBufs) { acc = 0; acc_phase ^= 1; }
           __threadfence();
           __syncwarp();
@@ -708,7 +779,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
           if (lane == 0) last = atomicAdd(p.split_cnt + ti * 4 + quad, 1) == p.split - 1;
           if (__shfl_sync(0xffffffffu, last, 0)) {
             __threadfence();
-            const int r0 = mb * BM + quad * 32, n0 = nb * BN;
+            const int r0 = mb * Cfg::kTileM + rows_of + quad * 32, n0 = nb * BN;
             if (p.split == 2) split_finish<BN, 2>(p, parts, r0, n0, lane);
             else split_finish<BN, 3>(p, parts, r0, n0, lane);
           }
@@ -719,7 +790,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
       for (int h = 0; h < Cfg::kMH; ++h) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + uint32_t((acc * Cfg::kMH + h) * BN + col0);
-        const int row0 = mb * Cfg::kTileM + h * BM + quad * 32, n0 = nb * BN + col0;
+        const int row0 = mb * Cfg::kTileM + rows_of + h * BM + quad * 32, n0 = nb * BN + col0;
         if constexpr (EPI == kEpiQKVSwiGLU) {
           if (n0 < p.n_split)
             epilogue_tile<Cfg::kEpiCols, kEpiQKV, B8>(p, taddr, row0, lane, n0, stage);
@@ -730,7 +801,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&tempty[acc]));
+      if constexpr (PAIR) mbar_arrive_cluster(tempty0 + uint32_t(acc) * 8u);
+      else mbar_arrive(smem_u32(&tempty[acc]));
       if (++acc == Cfg::kAccBufs) { acc = 0; acc_phase ^= 1; }
     }
   } else if constexpr (B8) {
@@ -758,38 +830,97 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  if constexpr (PAIR) {
+    // Neither CTA leaves, nor frees its TMEM, while the other may still write its barriers, read its
+    // shared memory or (first CTA's MMAs, drained above) write its TMEM. A peer still ending a
+    // failed wait takes up to a second per role: allow a few.
+    if (up) {
+      if (threadIdx.x == 0) mbar_arrive_cluster(mapa_shared(smem_u32(done), rank ^ 1u));
+      mbar_wait_cluster(smem_u32(done), 0, p.err, kErrTimeoutPair, 4 * kWaitLimitNs, false);
+    }
+    tc_fence_after();
+    if (threadIdx.x == 0) g_pair_started[(p.pair_epoch % kPairSlots) * kPairMaxCtas + blockIdx.x] = 0u;
+    if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  } else {
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
 }
 
 struct Maps {
   CUtensorMap a, b, s, a2, b2;  // s, a2, b2 unused unless int8 / concatenated operands (then copies)
 };
 
-template <int BN, int EPI, bool B8>
-int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
-  using Cfg = GemmCfg<BN, B8>;
-  static_assert(Cfg::kSmemBytes <= 227 * 1024, "shared memory budget");
-  auto kern = gemm_kernel<BN, EPI, B8>;
-  if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
-  const int tiles = ((p.M + Cfg::kTileM - 1) / Cfg::kTileM) * (p.N / BN);
-  const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
-  const int grid = items < num_sms() ? items : num_sms();
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(m.a, m.b, m.s, m.a2, m.b2, p);
-  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+// Work units (CTAs, or CTA pairs) that can be resident at once for a launch of `kern`.
+int resident_units(const void* kern, bool pair, unsigned threads, unsigned smem) {
+  if (!pair) return num_sms();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(num_sms() & ~1));
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return num_sms() / 2;
+  }
+  return n < num_sms() / 2 ? n : num_sms() / 2;
 }
 
-template <int BN, bool B8>
+std::atomic<uint32_t> g_pair_launches{0};
+
+template <int BN, int EPI, bool B8, bool PAIR>
+int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
+  using Cfg = GemmCfg<BN, B8, PAIR>;
+  static_assert(Cfg::kSmemBytes <= 227 * 1024, "shared memory budget");
+  auto kern = gemm_kernel<BN, EPI, B8, PAIR>;
+  if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
+  static int units_max = 0;  // resident units, queried once per kernel
+  if (units_max <= 0) units_max = resident_units(reinterpret_cast<const void*>(kern), PAIR, Cfg::kThreads, Cfg::kSmemBytes);
+  const int tiles = ((p.M + Cfg::kTileM - 1) / Cfg::kTileM) * (p.N / BN);
+  const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
+  const int units = items < units_max ? items : units_max;
+  if constexpr (!PAIR) {
+    kern<<<units, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(m.a, m.b, m.s, m.a2, m.b2, p);
+    return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  } else {
+    if (2 * units > kPairMaxCtas) return DIT_EUNSUPPORTED;
+    GemmParams q = p;
+    q.pair_epoch = g_pair_launches.fetch_add(1, std::memory_order_relaxed);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(2 * units));
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, m.a, m.b, m.s, m.a2, m.b2, q) != cudaSuccess) return DIT_ECUDA;
+    return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  }
+}
+
+template <int BN, bool B8, bool PAIR>
 int dispatch_epi(int epi, const Maps& m, const GemmParams& p, cudaStream_t stream) {
   switch (epi) {
-    case kEpiStoreF32: return launch_one<BN, kEpiStoreF32, B8>(m, p, stream);
-    case kEpiStoreBF16: return launch_one<BN, kEpiStoreBF16, B8>(m, p, stream);
-    case kEpiSiluBF16: return launch_one<BN, kEpiSiluBF16, B8>(m, p, stream);
-    case kEpiGated: return launch_one<BN, kEpiGated, B8>(m, p, stream);
-    case kEpiSwiGLU: return launch_one<BN, kEpiSwiGLU, B8>(m, p, stream);
-    case kEpiQKV: return launch_one<BN, kEpiQKV, B8>(m, p, stream);
+    case kEpiStoreF32: return launch_one<BN, kEpiStoreF32, B8, PAIR>(m, p, stream);
+    case kEpiStoreBF16: return launch_one<BN, kEpiStoreBF16, B8, PAIR>(m, p, stream);
+    case kEpiSiluBF16: return launch_one<BN, kEpiSiluBF16, B8, PAIR>(m, p, stream);
+    case kEpiGated: return launch_one<BN, kEpiGated, B8, PAIR>(m, p, stream);
+    case kEpiSwiGLU: return launch_one<BN, kEpiSwiGLU, B8, PAIR>(m, p, stream);
+    case kEpiQKV: return launch_one<BN, kEpiQKV, B8, PAIR>(m, p, stream);
     case kEpiQKVSwiGLU:
-      if constexpr (BN == 256 && !B8) return launch_one<BN, kEpiQKVSwiGLU, B8>(m, p, stream);
+      if constexpr (BN == 256 && !B8) return launch_one<BN, kEpiQKVSwiGLU, B8, PAIR>(m, p, stream);
       return DIT_EUNSUPPORTED;
     default: return DIT_EINVAL;
   }
@@ -801,8 +932,16 @@ namespace {
 
 int pick_bn(int N) { return (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64); }
 
+// bf16 mainloop on CTA pairs: 256-row tiles, each of the two SMs bringing its 128 rows of A and half
+// of the B tile, so a k-block costs an SM 32 KB of shared-memory fill instead of 48 KB (BN = 256) and
+// one MMA issue covers both. Needs tiles at least 128 wide, more than one 128-row block, and a row
+// group boundary (m_split) on a 256-row tile boundary (both halves of a tile share B).
+bool use_pair(int BN, const GemmParams& p) {
+  return BN >= 128 && p.M > BM && (p.m_split == 0 || p.m_split % (2 * BM) == 0) && num_sms() >= 2;
+}
+
 // bf16 weights: the K-split plan of the gated epilogue, then the launch
-int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, cudaStream_t stream) {
+int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, bool pair, cudaStream_t stream) {
   GemmParams q = p;
   q.split = 1;
   if (epi == kEpiGated && p.split_ws) {
@@ -813,15 +952,16 @@ int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, cudaStream_
     // mainloop hides that (measured at 4224 rows, hidden 3072: K = 12288 222 -> 209 us with s = 3,
     // K = 3072 71 -> 127 us). The partial slots and the arrival counters live in the caller's
     // scratch; the counters start at zero.
-    const int T = ((p.M + BM - 1) / BM) * (p.N / BN), P = num_sms(), KB = p.K / BK;
+    const int TM = pair ? 2 * BM : BM, slabs = pair ? 2 : 1;  // rows of a tile, 128-row slabs in it
+    const int T = ((p.M + TM - 1) / TM) * (p.N / BN), P = pair ? num_sms() / 2 : num_sms(), KB = p.K / BK;
     if (T > P && T % P != 0) {
       const int waves = T / P, tail = T - waves * P;
       double best = waves + 1.0;
       size_t slot_bytes = 0;
       for (int sp : {2, 3}) {
         if (KB % sp != 0 || KB / sp < 32) continue;
-        const size_t sb = (size_t(tail) * sp * BM * BN * 4 + 255) / 256 * 256;
-        if (sb + size_t(tail) * 4 * sizeof(int) > p.split_ws_bytes) continue;
+        const size_t sb = (size_t(tail) * slabs * sp * BM * BN * 4 + 255) / 256 * 256;
+        if (sb + size_t(tail) * slabs * 4 * sizeof(int) > p.split_ws_bytes) continue;
         const double c = waves + double((tail * sp + P - 1) / P) / sp;
         if (c < best - 1e-9) {
           best = c;
@@ -833,14 +973,15 @@ int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, cudaStream_
         q.sk_first = waves * P;
         q.split_part = static_cast<float*>(p.split_ws);
         q.split_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(p.split_ws) + slot_bytes);
-        if (cudaMemsetAsync(q.split_cnt, 0, size_t(tail) * 4 * sizeof(int), stream) != cudaSuccess) return DIT_ECUDA;
+        if (cudaMemsetAsync(q.split_cnt, 0, size_t(tail) * slabs * 4 * sizeof(int), stream) != cudaSuccess)
+          return DIT_ECUDA;
       }
     }
   }
   switch (BN) {
-    case 256: return dispatch_epi<256, false>(epi, m, q, stream);
-    case 128: return dispatch_epi<128, false>(epi, m, q, stream);
-    default: return dispatch_epi<64, false>(epi, m, q, stream);
+    case 256: return pair ? dispatch_epi<256, false, true>(epi, m, q, stream) : dispatch_epi<256, false, false>(epi, m, q, stream);
+    case 128: return pair ? dispatch_epi<128, false, true>(epi, m, q, stream) : dispatch_epi<128, false, false>(epi, m, q, stream);
+    default: return dispatch_epi<64, false, false>(epi, m, q, stream);
   }
 }
 
@@ -885,14 +1026,15 @@ int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmI
       return DIT_ECUDA;
     m.a2 = m.a;
     m.b2 = m.b;
-    return dispatch_epi<128, true>(epi, m, p, stream);
+    return dispatch_epi<128, true, false>(epi, m, p, stream);
   }
   if (reinterpret_cast<uintptr_t>(b) % 16) return DIT_EINVAL;
-  if (!tmap_bf16(&m.b, b, p.K, p.b_rows > 0 ? p.b_rows : p.N, p.K, BN)) return DIT_ECUDA;
+  const bool pair = use_pair(BN, p);
+  if (!tmap_bf16(&m.b, b, p.K, p.b_rows > 0 ? p.b_rows : p.N, p.K, pair ? BN / 2 : BN)) return DIT_ECUDA;
   m.s = m.b;
   m.a2 = m.a;
   m.b2 = m.b;
-  return launch_bf16(m, BN, epi, p, stream);
+  return launch_bf16(m, BN, epi, p, pair, stream);
 }
 
 int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long long lda2, const uint16_t* b,
@@ -903,14 +1045,16 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
   if ((p.n_split > 0) + (p.k_split > 0) + (p.m_split > 0) != 1) return DIT_EINVAL;  // exactly one kind
   const int BN = pick_bn(p.N);
   auto al = [](const void* q, long long ld) { return reinterpret_cast<uintptr_t>(q) % 16 == 0 && (ld * 2) % 16 == 0; };
+  const bool pair = use_pair(BN, p);
+  const int bbox = pair ? BN / 2 : BN;  // B rows one CTA loads per k-block
   Maps m;
   if (p.n_split > 0) {
     // B = [b ; b2]: rows [0, n_split) from b, the rest from b2, both [rows, K]
     if (p.n_split % BN != 0 || p.n_split >= p.N) return DIT_EUNSUPPORTED;
     if (epi == kEpiQKVSwiGLU && (BN != 256 || BN % p.head_dim != 0 || p.n_split != 3 * p.H)) return DIT_EUNSUPPORTED;
     if (!al(a, lda) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
-    if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.n_split, ldb, BN) ||
-        !tmap_bf16(&m.b2, b2, p.K, p.N - p.n_split, ldb2, BN))
+    if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.n_split, ldb, bbox) ||
+        !tmap_bf16(&m.b2, b2, p.K, p.N - p.n_split, ldb2, bbox))
       return DIT_ECUDA;
     m.a2 = m.a;
   } else if (p.m_split > 0) {
@@ -918,8 +1062,8 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
     if (p.m_split % BM != 0 || p.m_split >= p.M || epi == kEpiQKVSwiGLU) return DIT_EUNSUPPORTED;
     if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
     if (!al(a, lda) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
-    if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.N, ldb, BN) ||
-        !tmap_bf16(&m.b2, b2, p.K, p.N, ldb2, BN))
+    if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.N, ldb, bbox) ||
+        !tmap_bf16(&m.b2, b2, p.K, p.N, ldb2, bbox))
       return DIT_ECUDA;
     m.a2 = m.a;
   } else {
@@ -930,11 +1074,11 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
     const int k2 = p.K - p.k_split, b2_inner = p.b2_inner > 0 ? p.b2_inner : k2;
     if (b2_inner > k2) return DIT_EINVAL;
     if (!tmap_bf16(&m.a, a, p.k_split, p.M, lda, BM) || !tmap_bf16(&m.a2, a2, k2, p.M, lda2, BM) ||
-        !tmap_bf16(&m.b, b, p.k_split, p.N, ldb, BN) || !tmap_bf16(&m.b2, b2, b2_inner, p.N, ldb2, BN))
+        !tmap_bf16(&m.b, b, p.k_split, p.N, ldb, bbox) || !tmap_bf16(&m.b2, b2, b2_inner, p.N, ldb2, bbox))
       return DIT_ECUDA;
   }
   m.s = m.b;
-  return launch_bf16(m, BN, epi, p, stream);
+  return launch_bf16(m, BN, epi, p, pair, stream);
 }
 
 }  // namespace dit

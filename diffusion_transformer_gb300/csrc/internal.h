@@ -66,6 +66,8 @@ struct GemmParams {
   // TMA extents smaller than the GEMM's (0: the GEMM's): rows of B (columns past them read as zero)
   // and inner columns of the second B of a K-concatenation (LoRA factors of a rank below the tile)
   int b_rows, b2_inner;
+  // set by the launcher for CTA-pair launches: a launch counter that picks the start-word set
+  uint32_t pair_epoch;
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row

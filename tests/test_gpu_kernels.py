@@ -215,14 +215,15 @@ def test_gated_epilogue(shape, M, which):
     assert np.all(np.abs(got - ref) <= tol), float(np.abs(got - ref).max())
 
 
-@pytest.mark.parametrize("L,gh,gw", [(128, 64, 64), (100, 41, 100)])
-def test_gated_split_last_wave(L, gh, gw):
+@pytest.mark.parametrize("L,gh,gw,splits", [(128, 56, 64, True), (100, 41, 80, True), (128, 64, 64, False)])
+def test_gated_split_last_wave(L, gh, gw, splits):
     which = 1
-    # The MLP linear (K = 12288) at R = 4224 or 4200 rows, hidden 3072: 396 output tiles of
-    # 128 x 256, not a whole number of waves on 152 SMs, so with scratch the last wave's tiles are
-    # split along K (three parts of 4096). The split result
-    # is deterministic, differs from the unsplit kernel only by the order of the fp32 partial sums,
-    # and matches the float64 definition on rows of the split tiles and the ragged last tile.
+    # The MLP linear (K = 12288, hidden 3072) on CTA pairs: 256 x 256 output tiles over 76 pairs. At
+    # R = 3712 (15 row blocks, 180 tiles) or 3380 (14, 168) the last wave holds 28 or 16 tiles, so with
+    # scratch they are split along K (two parts of 6144, three of 4096); at R = 4224 (204 tiles, 52 in
+    # the last wave) no split shortens the critical path and none is taken. The split result is
+    # deterministic, differs from the unsplit kernel only by the order of the fp32 partial sums, and
+    # matches the float64 definition on rows of the split tiles and the ragged last tile.
     sh = DI.BlockShape(f"split_{L}_{gh}x{gw}", 3072, 24, 128, 12288, L, gh, gw, seed=21 + L)
     inp = DI.block_inputs(sh)
     g = np.random.default_rng(6)
@@ -240,7 +241,7 @@ def test_gated_split_last_wave(L, gh, gw):
         outs.append(np.concatenate([txt.cpu().numpy(), img.cpu().numpy()]).astype(np.float64))
     split, split2, whole = outs
     assert np.array_equal(split, split2)
-    assert not np.array_equal(split, whole)  # the split path ran (different summation order)
+    assert np.array_equal(split, whole) != splits  # the split path ran (different summation order) or not
     x = np.concatenate([inp.txt, inp.img]).astype(np.float64)
     gate = inp.mod[inp.mod_map, 2 if which == 0 else 5].astype(np.float64)
     Af, Wf = O.bf16_to_f64(A), O.bf16_to_f64(W)
