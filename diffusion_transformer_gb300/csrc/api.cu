@@ -331,9 +331,10 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     return g;
   };
 
-  if (L > 0 && L % 128 == 0) {
-    // No 128-row tile mixes the streams: every norm and linear runs once over all rows, the GEMMs
-    // taking the image weights from row L on (m_split) and the norms the image norm weights.
+  if (L > 0 && N > 0) {
+    // Every norm and linear runs once over all rows, the GEMMs taking the image weights from row L on
+    // (m_split; when L is not on a row-tile boundary each stream's rows are padded to whole tiles, so
+    // no tile mixes the streams) and the norms the image norm weights.
     auto norm_all = [&](const float* w_t, const float* w_i, long long shift_row) {
       ModNormParams mp{txt, img, L, R, H, H, H, w_t, mod.rows + shift_row * H, mod.rows + (shift_row + 1) * H,
                        6LL * H, mod.map, d->eps, b.h};

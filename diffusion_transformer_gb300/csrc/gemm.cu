@@ -92,10 +92,10 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
 // the warp's column count.
 // ----------------------------------------------------------------------------------------------
 template <int BN, int EPI, bool kRowPerThread>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, int row0, int lane, int n0,
-                                              uint8_t* stage) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t taddr, int row0, int row_end, int lane,
+                                              int n0, uint8_t* stage) {
   const int row = row0 + lane;
-  const bool row_ok = row < p.M;
+  const bool row_ok = row < row_end;
   if constexpr (EPI == kEpiQKV) {
     const int d = p.head_dim;
     const int H = p.H;
@@ -139,14 +139,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
           }
           (void)st32;
           uint16_t* dst = p.vt + (size_t(head) * d + c * 32 + j) * p.Rp + row0 + p.row_off;
-          if (row0 + 32 <= p.M && ((row0 + p.row_off) & 7) == 0) {
+          if (row0 + 32 <= row_end && ((row0 + p.row_off) & 7) == 0) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);  // (row0 + row_off) % 8 == 0, Rp % 8 == 0: 16-byte aligned
 #pragma unroll
             for (int q = 0; q < 4; ++q) d4[q] = make_uint4(col[4 * q], col[4 * q + 1], col[4 * q + 2], col[4 * q + 3]);
           } else {
 #pragma unroll
             for (int r = 0; r < 32; ++r)
-              if (row0 + r < p.M) dst[r] = uint16_t(r & 1 ? col[r >> 1] >> 16 : col[r >> 1] & 0xffffu);
+              if (row0 + r < row_end) dst[r] = uint16_t(r & 1 ? col[r >> 1] >> 16 : col[r >> 1] & 0xffffu);
           }
         }
         continue;
@@ -305,7 +305,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tadd
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = row0 + (lane >> 3) + 4 * i;
-      ok[i] = r < p.M;
+      ok[i] = r < row_end;
       const int rr = (ok[i] ? r : 0) + p.row_off;  // sequence row
       xr[i] = (rr < p.L ? p.txt + size_t(rr) * p.N : p.img + size_t(rr - p.L) * p.N) + n0 + cq * 4;
       gr[i] = p.gate + size_t(p.map ? __ldg(p.map + rr) : 0) * p.gate_stride + n0 + cq * 4;
@@ -467,7 +467,8 @@ __device__ __forceinline__ void split_store(uint32_t taddr, float* slot, int lan
 // in part order (the same sum whichever warp finishes last), then x += gate * acc. Every load of a
 // group of four rows is issued before the first add.
 template <int BN, int S>
-__device__ __forceinline__ void split_finish(const GemmParams& p, const float* parts, int row0, int n0, int lane) {
+__device__ __forceinline__ void split_finish(const GemmParams& p, const float* parts, int row0, int row_end, int n0,
+                                             int lane) {
   const int cq = lane & 7;
   constexpr size_t kSlot = size_t(BM) * BN;
 #pragma unroll 1
@@ -483,7 +484,7 @@ __device__ __forceinline__ void split_finish(const GemmParams& p, const float* p
 #pragma unroll
         for (int q = 0; q < S; ++q) v[u][q] = __ldcg(reinterpret_cast<const float4*>(src + q * kSlot));
         xr[u] = nullptr;
-        if (r < p.M) {
+        if (r < row_end) {
           const int sr = r + p.row_off;  // sequence row
           xr[u] = (sr < p.L ? p.txt + size_t(sr) * p.N : p.img + size_t(sr - p.L) * p.N) + n0 + c * 32 + cq * 4;
           xq[u] = *reinterpret_cast<const float4*>(xr[u]);
@@ -512,6 +513,31 @@ __device__ __forceinline__ void split_finish(const GemmParams& p, const float* p
       }
     }
   }
+}
+
+// Row tiles of a GEMM. With two row groups (m_split > 0) whose boundary is not on a tile boundary,
+// each group is padded to whole tiles (group 0: rows [0, m_split), group 1: rows [m_split, M)), so
+// no tile mixes the groups' weights; otherwise tiles are consecutive 'tile_m'-row blocks.
+__host__ __device__ __forceinline__ bool row_groups_padded(const GemmParams& p, int tile_m) {
+  return p.m_split > 0 && p.m_split % tile_m != 0;
+}
+__host__ __device__ __forceinline__ int row_tiles(const GemmParams& p, int tile_m) {
+  if (row_groups_padded(p, tile_m))
+    return (p.m_split + tile_m - 1) / tile_m + (p.M - p.m_split + tile_m - 1) / tile_m;
+  return (p.M + tile_m - 1) / tile_m;
+}
+// First row, end of the valid rows and group of row tile mb.
+struct TileRows {
+  int base, end;
+  bool g2;
+};
+__device__ __forceinline__ TileRows tile_rows(const GemmParams& p, int tile_m, int mb) {
+  if (row_groups_padded(p, tile_m)) {
+    const int nm0 = (p.m_split + tile_m - 1) / tile_m;
+    if (mb < nm0) return TileRows{mb * tile_m, p.m_split, false};
+    return TileRows{p.m_split + (mb - nm0) * tile_m, p.M, true};
+  }
+  return TileRows{mb * tile_m, p.M, p.m_split > 0 && mb * tile_m >= p.m_split};
 }
 
 // CTA pairs publish in global memory that their barriers are initialised, one word per CTA: it is
@@ -556,7 +582,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
   const uint32_t rank = PAIR ? cluster_ctarank() : 0;
   const int unit = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
   const int units = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
-  const int num_m = (p.M + Cfg::kTileM - 1) / Cfg::kTileM;
+  const int num_m = row_tiles(p, Cfg::kTileM);
   const int num_n = p.N / BN;
   // Tile order: consecutive tiles share the smaller operand's panel set, so the CTAs running at
   // once keep it in L2 and the larger operand streams from DRAM once. m fastest (A resident) when A
@@ -647,6 +673,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
         const WorkItem w = work_item(p, it, tiles, KB);
         int mb, nb;
         tile_mn(w.tile, mb, nb);
+        const TileRows tr = tile_rows(p, Cfg::kTileM, mb);
         for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, kErrTimeoutProducer)) { ok = false; break; }
           const uint32_t fb = full0 + uint32_t(stage) * 8u;
@@ -656,19 +683,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
           // concatenated operands: the second A/B past the K boundary, the second B past the N boundary
           const bool k2 = p.k_split > 0 && kb * BK >= p.k_split;
           const bool n2 = p.n_split > 0 && nb * BN >= p.n_split;
-          const bool m2 = p.m_split > 0 && mb * Cfg::kTileM >= p.m_split;
+          const bool m2 = tr.g2;
           const CUtensorMap* ma = k2 ? &tmA2 : &tmA;
           const CUtensorMap* mbm = (k2 || n2 || m2) ? &tmB2 : &tmB;
           const int kc = k2 ? kb * BK - p.k_split : kb * BK;
           const int nr = n2 ? nb * BN - p.n_split : nb * BN;
           if constexpr (PAIR) {
-            tma_load_2d_pair(smem_u32(sA + stage * Cfg::kABytes), ma, fb, kc, mb * Cfg::kTileM + int(rank) * BM);
+            tma_load_2d_pair(smem_u32(sA + stage * Cfg::kABytes), ma, fb, kc, tr.base + int(rank) * BM);
             tma_load_2d_pair(smem_u32(sB + stage * Cfg::kBLoad), mbm, fb, kc, nr + int(rank) * (BN / 2));
           } else {
 #pragma unroll
             for (int h = 0; h < Cfg::kMH; ++h)
-              tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), ma, fb, kc,
-                          mb * Cfg::kTileM + h * BM);
+              tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), ma, fb, kc, tr.base + h * BM);
             if constexpr (B8) {
               tma_load_2d(smem_u32(sB + stage * Cfg::kB8Bytes), &tmB, fb, kb * BK, nb * BN);
               // scales of k-blocks (kb & ~3) .. (kb | 3): 8 bf16 per row, 16-byte aligned columns
@@ -759,6 +785,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
       const WorkItem w = work_item(p, it, tiles, KB);
       int mb, nb;
       tile_mn(w.tile, mb, nb);
+      const TileRows tr = tile_rows(p, Cfg::kTileM, mb);
       if (!mbar_wait_warp(smem_u32(&tfull[acc]), acc_phase, p.err, kErrTimeoutEpilogue)) break;
       tc_fence_after();
       if constexpr (EPI == kEpiGated && !B8) {
@@ -779,9 +806,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
           if (lane == 0) last = atomicAdd(p.split_cnt + ti * 4 + quad, 1) == p.split - 1;
           if (__shfl_sync(0xffffffffu, last, 0)) {
             __threadfence();
-            const int r0 = mb * Cfg::kTileM + rows_of + quad * 32, n0 = nb * BN;
-            if (p.split == 2) split_finish<BN, 2>(p, parts, r0, n0, lane);
-            else split_finish<BN, 3>(p, parts, r0, n0, lane);
+            const int r0 = tr.base + rows_of + quad * 32, n0 = nb * BN;
+            if (p.split == 2) split_finish<BN, 2>(p, parts, r0, tr.end, n0, lane);
+            else split_finish<BN, 3>(p, parts, r0, tr.end, n0, lane);
           }
           continue;
         }
@@ -790,14 +817,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
       for (int h = 0; h < Cfg::kMH; ++h) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + uint32_t((acc * Cfg::kMH + h) * BN + col0);
-        const int row0 = mb * Cfg::kTileM + rows_of + h * BM + quad * 32, n0 = nb * BN + col0;
+        const int row0 = tr.base + rows_of + h * BM + quad * 32, n0 = nb * BN + col0;
         if constexpr (EPI == kEpiQKVSwiGLU) {
           if (n0 < p.n_split)
-            epilogue_tile<Cfg::kEpiCols, kEpiQKV, B8>(p, taddr, row0, lane, n0, stage);
+            epilogue_tile<Cfg::kEpiCols, kEpiQKV, B8>(p, taddr, row0, tr.end, lane, n0, stage);
           else
-            epilogue_tile<Cfg::kEpiCols, kEpiSwiGLU, B8>(p, taddr, row0, lane, n0 - p.n_split, stage);
+            epilogue_tile<Cfg::kEpiCols, kEpiSwiGLU, B8>(p, taddr, row0, tr.end, lane, n0 - p.n_split, stage);
         } else {
-          epilogue_tile<Cfg::kEpiCols, EPI, B8>(p, taddr, row0, lane, n0, stage);
+          epilogue_tile<Cfg::kEpiCols, EPI, B8>(p, taddr, row0, tr.end, lane, n0, stage);
         }
       }
       tc_fence_before();
@@ -883,7 +910,7 @@ int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
   if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
   static int units_max = 0;  // resident units, queried once per kernel
   if (units_max <= 0) units_max = resident_units(reinterpret_cast<const void*>(kern), PAIR, Cfg::kThreads, Cfg::kSmemBytes);
-  const int tiles = ((p.M + Cfg::kTileM - 1) / Cfg::kTileM) * (p.N / BN);
+  const int tiles = row_tiles(p, Cfg::kTileM) * (p.N / BN);
   const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
   const int units = items < units_max ? items : units_max;
   if constexpr (!PAIR) {
@@ -934,11 +961,8 @@ int pick_bn(int N) { return (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64); }
 
 // bf16 mainloop on CTA pairs: 256-row tiles, each of the two SMs bringing its 128 rows of A and half
 // of the B tile, so a k-block costs an SM 32 KB of shared-memory fill instead of 48 KB (BN = 256) and
-// one MMA issue covers both. Needs tiles at least 128 wide, more than one 128-row block, and a row
-// group boundary (m_split) on a 256-row tile boundary (both halves of a tile share B).
-bool use_pair(int BN, const GemmParams& p) {
-  return BN >= 128 && p.M > BM && (p.m_split == 0 || p.m_split % (2 * BM) == 0) && num_sms() >= 2;
-}
+// one MMA issue covers both. Needs tiles at least 128 wide and more than one 128-row block.
+bool use_pair(int BN, const GemmParams& p) { return BN >= 128 && p.M > BM && num_sms() >= 2; }
 
 // bf16 weights: the K-split plan of the gated epilogue, then the launch
 int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, bool pair, cudaStream_t stream) {
@@ -953,7 +977,7 @@ int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, bool pair, 
     // K = 3072 71 -> 127 us). The partial slots and the arrival counters live in the caller's
     // scratch; the counters start at zero.
     const int TM = pair ? 2 * BM : BM, slabs = pair ? 2 : 1;  // rows of a tile, 128-row slabs in it
-    const int T = ((p.M + TM - 1) / TM) * (p.N / BN), P = pair ? num_sms() / 2 : num_sms(), KB = p.K / BK;
+    const int T = row_tiles(p, TM) * (p.N / BN), P = pair ? num_sms() / 2 : num_sms(), KB = p.K / BK;
     if (T > P && T % P != 0) {
       const int waves = T / P, tail = T - waves * P;
       double best = waves + 1.0;
@@ -1058,8 +1082,9 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
       return DIT_ECUDA;
     m.a2 = m.a;
   } else if (p.m_split > 0) {
-    // rows [0, m_split) with the weights b, rows [m_split, M) with b2 (both [N, K])
-    if (p.m_split % BM != 0 || p.m_split >= p.M || epi == kEpiQKVSwiGLU) return DIT_EUNSUPPORTED;
+    // rows [0, m_split) with the weights b, rows [m_split, M) with b2 (both [N, K]); a boundary inside
+    // a row tile pads each group to whole tiles
+    if (p.m_split >= p.M || epi == kEpiQKVSwiGLU) return DIT_EUNSUPPORTED;
     if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
     if (!al(a, lda) || !al(b, ldb) || !al(b2, ldb2)) return DIT_EINVAL;
     if (!tmap_bf16(&m.a, a, p.K, p.M, lda, BM) || !tmap_bf16(&m.b, b, p.K, p.N, ldb, bbox) ||

@@ -196,9 +196,10 @@ DIT_API int dit_parallel_block_forward(const dit_dims* dims, const dit_block_w* 
  * text rows [0, L) use w_txt and the image rows use w_img (all four linears and the four norm
  * weights), while the attention is one softmax over all L + N rows. mod as dit_block_forward
  * ([M, 6, H] and map): the map gives each stream its own modulation rows. w_txt may be NULL when
- * L = 0. When L is a multiple of 128 no GEMM tile mixes the streams and each norm and linear is
- * one launch over all rows, the image weights taken from row L on (7 launches); otherwise each
- * stream's norms and linears run over its own rows (13 launches), so any L works.
+ * L = 0. With both streams present each norm and linear is one launch over all rows, the image
+ * weights taken from row L on, each stream's rows padded to whole GEMM tiles when L is not on a tile
+ * boundary, so no tile mixes the streams (7 launches); with one stream empty its norms and linears
+ * run over the other's rows only. Any L works.
  * Workspace: dit_workspace_bytes(dims, L, N, 3).
  * Errors as dit_block_forward. */
 DIT_API int dit_double_block_forward(const dit_dims* dims, const dit_block_w* w_txt, const dit_block_w* w_img,

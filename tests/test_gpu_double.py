@@ -55,9 +55,10 @@ def test_double_tiny_all_rows(M, nw):
     _check(np.concatenate([t, i]), ref, x_in, f"double tiny M={M} norm_weights={nw}")
 
 
-@pytest.mark.parametrize("L,gh,gw", [(13, 9, 10), (1, 5, 7), (8, 16, 20)])
+@pytest.mark.parametrize("L,gh,gw", [(13, 9, 10), (1, 5, 7), (8, 16, 20), (100, 16, 20), (200, 16, 20)])
 def test_double_head64_unaligned_text_rows(L, gh, gw):
-    # L = 13 and 1: the image stream's rows start at an offset that is not a multiple of 8
+    # L = 13, 1 and 100: the image stream's rows start at an offset that is not a multiple of 8; with
+    # 420 and 520 rows the GEMMs run on CTA pairs (256-row tiles), each stream padded to whole tiles
     sh = DI.BlockShape(f"dd64_{L}_{gh}x{gw}", 256, 4, 64, 768, L, gh, gw, seed=L + gh + 60)
     inp, tw = _inputs(sh, M=2, norm_weights=True)
     t, i = run_double_gpu(inp, tw)
@@ -102,8 +103,8 @@ def test_double_deterministic():
 
 
 def test_double_grouped_path_vs_oracle():
-    # L = 128: no 128-row tile mixes the streams, so each norm and linear is one launch over all rows
-    # (image weights from row 128 on); norm weights per stream
+    # L = 128: each norm and linear is one launch over all rows (image weights from row 128 on; on CTA
+    # pairs the text rows fill half of a padded 256-row tile); norm weights per stream
     sh = DI.BlockShape("dgrp", 256, 4, 64, 768, 128, 12, 12, seed=81)
     inp, tw = _inputs(sh, M=3, norm_weights=True)
     t, i = run_double_gpu(inp, tw)
