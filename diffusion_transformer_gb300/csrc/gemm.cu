@@ -38,20 +38,20 @@ struct GemmCfg {
   // int8lin: 256-row CTA tiles (two M=128 MMAs share each converted B k-block), halving the
   // conversions per FLOP; bf16: 128-row tiles, or 256 x BN tiles shared by a CTA pair (PAIR: each CTA
   // brings its 128 rows of A and half of the B tile, the first CTA issues M=256 MMAs over both).
-  static constexpr int kMH = B8 ? 2 : 1;             // 128-row halves per CTA tile
+  static constexpr int kMH = (B8 && !PAIR) ? 2 : 1;  // 128-row halves per CTA tile
   static constexpr int kTileM = PAIR ? 2 * BM : BM * kMH;  // rows of one work tile
-  static constexpr int kStages =
-      B8 ? (BN == 256 ? 3 : 4) : PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
+  static constexpr int kStages = B8 ? (PAIR ? 5 : (BN == 256 ? 3 : 4))
+                                    : PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
   // TMEM accumulator sets: two (the epilogue drains one while the MMA fills the other) when they fit
   // in the 512 columns, else one.
   static constexpr int kAccBufs = (2 * kMH * BN <= 512) ? 2 : 1;
   static constexpr uint32_t kAHalf = BM * BK * 2;
   static constexpr uint32_t kABytes = kAHalf * kMH;
-  static constexpr uint32_t kBBytes = BN * BK * 2;   // bf16 tile the MMA reads
-  static constexpr uint32_t kBLoad = PAIR ? kBBytes / 2 : kBBytes;  // bf16 B bytes this CTA holds per stage
-  static constexpr uint32_t kB8Bytes = BN * BK;      // int8 tile TMA writes (B8 only)
-  static constexpr uint32_t kSBytes = BN * 16;       // B8: scale tile [BN rows x 8 bf16] (4 k-blocks)
-  static constexpr int kConvStages = 2;              // bf16 B tiles produced by the converters
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of B this CTA brings (PAIR: its half)
+  static constexpr uint32_t kBLoad = kBRows * BK * 2;  // bf16 B bytes this CTA holds per stage (B8: converted)
+  static constexpr uint32_t kB8Bytes = kBRows * BK;  // int8 tile TMA writes (B8 only)
+  static constexpr uint32_t kSBytes = kBRows * 16;   // B8: scale tile [rows x 8 bf16] (4 k-blocks)
+  static constexpr int kConvStages = PAIR ? 4 : 2;   // bf16 B tiles produced by the converters
   static constexpr int kConvThreads = 128;           // B8: converter warps 6..9, one per SM sub-partition
   static constexpr uint32_t kTmemCols = (kAccBufs * kMH * BN < 32) ? 32 : kAccBufs * kMH * BN;
   // epilogue warps: one per TMEM lane quadrant (two per quadrant, each taking half of the columns,
@@ -63,7 +63,7 @@ struct GemmCfg {
   static constexpr int kThreads = 64 + kEpiThreads + (B8 ? kConvThreads : 0);
   // smem: [A ring][B ring (bf16, or int8 + scales for B8)][B8: converted bf16 ring][barriers][tmem slot]
   static constexpr uint32_t kRingBytes = kStages * (kABytes + (B8 ? kB8Bytes + kSBytes : kBLoad));
-  static constexpr uint32_t kConvBytes = B8 ? kConvStages * kBBytes : 0;
+  static constexpr uint32_t kConvBytes = B8 ? kConvStages * kBLoad : 0;
   static constexpr uint32_t kEpiBytes = kEpiWarps * 4096;   // epilogue staging, 4 KB per epilogue warp
   static constexpr uint32_t kBarBytes = 8 * (2 * kStages + 4 + 2 * kConvStages + 3) + 16;
   static constexpr uint32_t kSmemBytes = 1024 + kRingBytes + kConvBytes + kEpiBytes + kBarBytes;
@@ -553,7 +553,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
-  static_assert(!(PAIR && B8), "CTA pairs run the bf16 mainloop only");
   using Cfg = GemmCfg<BN, B8, PAIR>;
   constexpr int S = Cfg::kStages;
   constexpr int CS = Cfg::kConvStages;
@@ -604,14 +603,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), B8 ? 1 + Cfg::kConvThreads : 1);  // B8: MMA commit + converters
+      mbar_init(smem_u32(&empty[s]), B8 ? 1 + Cfg::kConvThreads / 32 : 1);  // B8: MMA commit + converter warps
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
       mbar_init(smem_u32(&tempty[a]), (PAIR ? 2 : 1) * Cfg::kEpiThreads);
     }
     for (int c = 0; c < CS; ++c) {
-      mbar_init(smem_u32(&cfull[c]), Cfg::kConvThreads);
+      mbar_init(smem_u32(&cfull[c]), (PAIR ? 2 : 1) * Cfg::kConvThreads / 32);  // converter warps (PAIR: both CTAs')
       mbar_init(smem_u32(&cempty[c]), 1);
     }
     mbar_init(smem_u32(drain), 1);
@@ -667,8 +666,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;
       bool ok = true;
-      // PAIR: both CTAs' copies complete on the first CTA's barrier, which expects both
-      const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&full[0]), 0) : smem_u32(&full[0]);
+      // PAIR (bf16): both CTAs' copies complete on the first CTA's barrier, which expects both.
+      // PAIR (int8): each CTA's copies complete on its own barrier, which its converters wait on.
+      constexpr bool kLocalFull = !PAIR || B8;
+      constexpr uint32_t kOwnBytes = Cfg::kABytes + (B8 ? Cfg::kB8Bytes + Cfg::kSBytes : Cfg::kBLoad);
+      const uint32_t full0 = kLocalFull ? smem_u32(&full[0]) : mapa_shared(smem_u32(&full[0]), 0);
       for (int it = unit; it < items && ok; it += units) {
         const WorkItem w = work_item(p, it, tiles, KB);
         int mb, nb;
@@ -677,9 +679,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
         for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, kErrTimeoutProducer)) { ok = false; break; }
           const uint32_t fb = full0 + uint32_t(stage) * 8u;
-          if (!PAIR || rank == 0)
-            mbar_arrive_expect_tx(smem_u32(&full[stage]),
-                                  (PAIR ? 2 : 1) * (Cfg::kABytes + (B8 ? Cfg::kB8Bytes + Cfg::kSBytes : Cfg::kBLoad)));
+          if (kLocalFull || rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), (kLocalFull ? 1 : 2) * kOwnBytes);
           // concatenated operands: the second A/B past the K boundary, the second B past the N boundary
           const bool k2 = p.k_split > 0 && kb * BK >= p.k_split;
           const bool n2 = p.n_split > 0 && nb * BN >= p.n_split;
@@ -688,28 +688,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
           const CUtensorMap* mbm = (k2 || n2 || m2) ? &tmB2 : &tmB;
           const int kc = k2 ? kb * BK - p.k_split : kb * BK;
           const int nr = n2 ? nb * BN - p.n_split : nb * BN;
-          if constexpr (PAIR) {
+          if constexpr (B8) {
+            // int8 B rows of this CTA (PAIR: its half of the tile) with their scales
+            const int brow = nb * BN + int(rank) * Cfg::kBRows;
+#pragma unroll
+            for (int h = 0; h < Cfg::kMH; ++h)
+              tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), ma, fb, kc,
+                          tr.base + int(rank) * BM + h * BM);
+            tma_load_2d(smem_u32(sB + stage * Cfg::kB8Bytes), &tmB, fb, kb * BK, brow);
+            // scales of k-blocks (kb & ~3) .. (kb | 3): 8 bf16 per row, 16-byte aligned columns
+            tma_load_2d(smem_u32(sSc + stage * Cfg::kSBytes), &tmS, fb, (kb * 2) & ~7, brow);
+          } else if constexpr (PAIR) {
             tma_load_2d_pair(smem_u32(sA + stage * Cfg::kABytes), ma, fb, kc, tr.base + int(rank) * BM);
             tma_load_2d_pair(smem_u32(sB + stage * Cfg::kBLoad), mbm, fb, kc, nr + int(rank) * (BN / 2));
           } else {
-#pragma unroll
-            for (int h = 0; h < Cfg::kMH; ++h)
-              tma_load_2d(smem_u32(sA + stage * Cfg::kABytes + h * Cfg::kAHalf), ma, fb, kc, tr.base + h * BM);
-            if constexpr (B8) {
-              tma_load_2d(smem_u32(sB + stage * Cfg::kB8Bytes), &tmB, fb, kb * BK, nb * BN);
-              // scales of k-blocks (kb & ~3) .. (kb | 3): 8 bf16 per row, 16-byte aligned columns
-              tma_load_2d(smem_u32(sSc + stage * Cfg::kSBytes), &tmS, fb, (kb * 2) & ~7, nb * BN);
-            } else
-              tma_load_2d(smem_u32(sB + stage * Cfg::kBBytes), mbm, fb, kc, nr);
+            tma_load_2d(smem_u32(sA + stage * Cfg::kABytes), ma, fb, kc, tr.base);
+            tma_load_2d(smem_u32(sB + stage * Cfg::kBLoad), mbm, fb, kc, nr);
           }
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
-      // every issued copy must have landed before the CTA exits (PAIR: the first CTA's barriers
+      // every issued copy must have landed before the CTA exits (PAIR bf16: the first CTA's barriers
       // count the second's copies too, and the second waits for the first before it exits)
-      if (!PAIR || rank == 0)
+      if (kLocalFull || rank == 0)
         for (int s = 0; s < S; ++s)
           if (issued_mask & (1u << s))
             mbar_wait(smem_u32(&full[s]), (last_parity >> s) & 1u, p.err, kErrTimeoutDrain);
@@ -734,8 +737,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
           if (!mbar_wait(smem_u32(&full[stage]), phase, p.err, kErrTimeoutMma)) { ok = false; break; }
           uint32_t b_addr;
           if constexpr (B8) {
-            if (!mbar_wait(smem_u32(&cfull[cstage]), cphase, p.err, kErrTimeoutMma)) { ok = false; break; }
-            b_addr = smem_u32(sC + cstage * Cfg::kBBytes);
+            // PAIR: the count covers both CTAs' converters, each of which waited for its own CTA's
+            // copies of this stage (A included) before converting
+            if (!(PAIR ? mbar_wait_cluster(smem_u32(&cfull[cstage]), cphase, p.err, kErrTimeoutMma)
+                       : mbar_wait(smem_u32(&cfull[cstage]), cphase, p.err, kErrTimeoutMma))) {
+              ok = false;
+              break;
+            }
+            b_addr = smem_u32(sC + cstage * Cfg::kBLoad);
           } else {
             b_addr = smem_u32(sB + stage * Cfg::kBLoad);
           }
@@ -756,7 +765,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
           if constexpr (PAIR) umma_commit_pair_both(smem_u32(&empty[stage]));
           else umma_commit(smem_u32(&empty[stage]));
           if constexpr (B8) {
-            umma_commit(smem_u32(&cempty[cstage]));
+            if constexpr (PAIR) umma_commit_pair_both(smem_u32(&cempty[cstage]));
+            else umma_commit(smem_u32(&cempty[cstage]));
             if (++cstage == CS) { cstage = 0; cphase ^= 1; }
           }
           if (++stage == S) { stage = 0; phase ^= 1; }
@@ -838,17 +848,25 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
     int stage = 0, cstage = 0;
     uint32_t phase = 0, cphase = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+    // PAIR: the converted tile is read by the first CTA's MMAs, whose barrier counts both CTAs
+    const uint32_t cfull0 = PAIR ? mapa_shared(smem_u32(&cfull[0]), 0) : smem_u32(&cfull[0]);
+    for (int it = unit; it < items && ok; it += units) {
       const WorkItem w = work_item(p, it, tiles, KB);
       for (int kb = w.k0; kb < w.k1; ++kb) {
-        if (!mbar_wait(smem_u32(&full[stage]), phase, p.err, kErrTimeoutConverter)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&cempty[cstage]), cphase ^ 1, p.err, kErrTimeoutConverter)) { ok = false; break; }
-        convert_kblock<BN, Cfg::kConvThreads>(sB + stage * Cfg::kB8Bytes,
-                                              reinterpret_cast<const uint16_t*>(sSc + stage * Cfg::kSBytes),
-                                              (kb * 2) & 7, sC + cstage * Cfg::kBBytes, ct);
+        // warp-uniform verdicts: the warp meets again at the __syncwarp below
+        if (!mbar_wait_warp(smem_u32(&full[stage]), phase, p.err, kErrTimeoutConverter)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&cempty[cstage]), cphase ^ 1, p.err, kErrTimeoutConverter)) { ok = false; break; }
+        convert_kblock<Cfg::kBRows, Cfg::kConvThreads>(sB + stage * Cfg::kB8Bytes,
+                                                       reinterpret_cast<const uint16_t*>(sSc + stage * Cfg::kSBytes),
+                                                       (kb * 2) & 7, sC + cstage * Cfg::kBLoad, ct);
+        // every lane's writes to the async proxy, then one arrival per warp
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&cfull[cstage]));
-        mbar_arrive(smem_u32(&empty[stage]));  // this thread is done reading the int8 stage
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) mbar_arrive_cluster(cfull0 + uint32_t(cstage) * 8u);
+          else mbar_arrive(smem_u32(&cfull[cstage]));
+          mbar_arrive(smem_u32(&empty[stage]));  // this warp is done reading the int8 stage
+        }
         if (++cstage == CS) { cstage = 0; cphase ^= 1; }
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
@@ -1032,12 +1050,26 @@ int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmI
     if (BN == 64 || p.K % 256 != 0) return DIT_EUNSUPPORTED;  // scale rows must be 16-byte multiples
     if (p.M > kInt8MainloopMaxM) {
       // Many M tiles: the in-mainloop converters would dequantise every weight tile once per M tile
-      // (17 times at 4224 rows) and bound the GEMM; dequantising the weight once, HBM-bound, and
-      // running the bf16 mainloop is faster (measured 1.14 against 1.69 ms per 1024sq block).
+      // (17 times at 4224 rows) and bound the GEMM at about 800 TFLOP/s, single CTAs or pairs alike;
+      // dequantising the weight once, HBM-bound, and running the bf16 mainloop is faster (measured
+      // 1.06-1.08 against 1.69 ms per 1024sq block).
       if (!b8->wbf || reinterpret_cast<uintptr_t>(b8->wbf) % 16) return DIT_EINVAL;
       const int rc = dequant_int8_launch(b8->q, b8->s, b8->wbf, p.N, p.K, stream);
       if (rc != DIT_OK) return rc;
       return gemm_launch(a, lda, b8->wbf, nullptr, epi, p, stream);
+    }
+    if (use_pair(BN, p)) {
+      // CTA pairs: 256 x BN tiles, each CTA converting its half of every int8 k-block of B (BN/2
+      // rows) into the bf16 tile the pair's MMAs read: the conversions per FLOP of the 256 x 128
+      // single-CTA tile, with a third less shared-memory traffic per SM
+      if (epi == kEpiQKV && (BN % p.head_dim != 0 || p.H % BN != 0)) return DIT_EUNSUPPORTED;
+      if (!make_tmap_2d(&m.b, b8->q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.K, p.N, p.K, BK, BN / 2, false) ||
+          !make_tmap_2d(&m.s, b8->s, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, (long long)(p.K / 32) * 2, 8,
+                        BN / 2, false))
+        return DIT_ECUDA;
+      m.a2 = m.a;
+      m.b2 = m.b;
+      return BN == 256 ? dispatch_epi<256, true, true>(epi, m, p, stream) : dispatch_epi<128, true, true>(epi, m, p, stream);
     }
     // int8lin tiles are 256 x 128: two M=128 MMAs share each converted B k-block and both accumulator
     // sets fit in TMEM. (256 x 256 tiles, with one accumulator set and no epilogue overlap, measured
