@@ -125,8 +125,12 @@ def test_dequant_bit_exact():
 # ---------------------------------------------------------------------------------- plain GEMM
 
 @pytest.mark.parametrize("M,N,K", [(72, 256, 256), (128, 128, 64), (200, 64, 128), (1088, 768, 3072),
-                                   (4, 3072, 256), (333, 512, 1024), (4224, 256, 3072)])
+                                   (4, 3072, 256), (333, 512, 1024), (4224, 256, 3072), (129, 256, 64),
+                                   (256, 384, 192), (2048, 2560, 256)])
 def test_linear_f32(M, N, K):
+    # rows > 128 and N a multiple of 128 run on CTA pairs (256-row tiles): 129 rows leave one valid
+    # row in the second CTA's half; 256 x 384 is one 256 x 128 tile per 128 columns; 2048 x 2560 has
+    # 80 tiles for 76 pairs, so some pairs take a second tile (both accumulator sets in use)
     g = np.random.default_rng(M + N + K)
     A = _bf16_rand(g, (M, K), 1.0)
     W = _bf16_rand(g, (N, K), 0.02)
