@@ -202,8 +202,8 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   if (w8) q8 = GemmInt8B{w8->q[0], w8->s[0], i8_tiles};
   if ((rc = linear(0, b.h, H, w8 ? nullptr : w->wqkv, w8 ? &q8 : nullptr, kEpiQKV, g)) != DIT_OK) return rc;
 
-  // 3. o = attention(q, k, v)
-  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+  // 3. o = attention(q, k, v); q and k rows QK-normed with qn, kn
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, qn, kn, nullptr, nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
 
   // 4. x += gate_a * (o Wout^T)
@@ -275,8 +275,9 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, float* txt, int 
   g.n_split = 3 * H;
   if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, w->wqkv, H, w->wup, H, kEpiQKVSwiGLU, g, st)) != DIT_OK) return rc;
 
-  // 3. o = attention(q, k, v)
-  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+  // 3. o = attention(q, k, v); q and k rows QK-normed
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, w->q_norm, w->k_norm, nullptr,
+                nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
 
   // 4. x += gate * ([o | a] [Wout | Wdown]^T)
@@ -348,7 +349,8 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.k_norm2 = wi->k_norm;
     g.m_split = L;
     if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wqkv, H, wi->wqkv, H, kEpiQKV, g, st)) != DIT_OK) return rc;
-    AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+    AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 2, wt->q_norm, wt->k_norm,
+                  wi->q_norm, wi->k_norm};
     if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, H, 2);
     g.m_split = L;
@@ -379,8 +381,11 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.R_total = R;
     if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wqkv, nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
   }
-  // 3. o = attention over all rows
-  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err};
+  // 3. o = attention over all rows (q and k QK-normed with the weights of the streams that have rows)
+  const Stream* s0 = S[0].n > 0 ? &S[0] : &S[1];
+  const Stream* s1 = (S[0].n > 0 && S[1].n > 0) ? &S[1] : nullptr;
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, s1 ? 2 : 1, s0->w->q_norm,
+                s0->w->k_norm, s1 ? s1->w->q_norm : nullptr, s1 ? s1->w->k_norm : nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
   // 4. x += gate_a * (o Wout^T), per stream (K-split scratch: the SwiGLU buffer, not yet written)
   for (const Stream& s : S) {
@@ -665,6 +670,17 @@ int dit_attention(const dit_dims* d, int R, const uint16_t* q, const uint16_t* k
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), q, k, vt, o, err};
+  return attention_launch(ap, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_attention_qknorm(const dit_dims* d, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
+                         const float* q_norm, const float* k_norm, uint16_t* o, dit_stream_t stream) {
+  if (!d || R < 1 || !q || !k || !vt || !o) return DIT_EINVAL;
+  if (!dims_ok(d)) return DIT_EUNSUPPORTED;
+  if (!al16(q) || !al16(k) || !al16(vt) || !al16(o)) return DIT_EINVAL;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), q, k, vt, o, err, 1, q_norm, k_norm, nullptr, nullptr};
   return attention_launch(ap, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -102,6 +102,11 @@ struct AttnParams {
   const uint16_t *q, *k, *vt;  // [heads, R, d], [heads, R, d], [heads, d, Rp]
   uint16_t* o;                 // [R, heads * d]
   int* err;
+  // qk_normed > 0: every q and k row was RMS-normalised per head and scaled by one of qk_normed (1 or
+  // 2: the two streams of a double-stream block) sets of weights ([d] each, null = ones), as the QKV
+  // epilogue does. The softmax may then subtract a fixed maximum (see attention.cu).
+  int qk_normed;
+  const float *qn0, *kn0, *qn1, *kn1;
 };
 int attention_launch(const AttnParams& p, cudaStream_t stream);
 

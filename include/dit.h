@@ -281,6 +281,15 @@ DIT_API int dit_vt_stride(int R);
 DIT_API int dit_attention(const dit_dims* dims, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
                   uint16_t* o, dit_stream_t stream);
 
+/* The same attention for q and k rows as dit_qkv_rope writes them: RMS-normalised per head and
+ * scaled by q_norm / k_norm ([d] fp32 each, NULL = ones; the caller vouches for this, the kernel
+ * does not check it). Every scaled score then lies within a bound B = d max|q_norm| max|k_norm| /
+ * sqrt(d) (log2 units); when B < 60 the softmax subtracts B instead of a running row maximum, which
+ * lets it split each row over two warps (the result differs from dit_attention by rounding only);
+ * otherwise it is dit_attention. */
+DIT_API int dit_attention_qknorm(const dit_dims* dims, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
+                                 const float* q_norm, const float* k_norm, uint16_t* o, dit_stream_t stream);
+
 /* Linear with gated residual [gizai:dit, gatedInto]: x[r] += gate[map[r]] * (a[r] W^T) for the
  * attention (which = 0, W = wout [H, H], a [R, H]) or the MLP (which = 1, W = wdown [H, F],
  * a [R, F]) gate of the modulation rows. x rows < L in txt, others in img.

@@ -313,6 +313,50 @@ def test_attention_vs_oracle(R, nh, d, qscale):
     assert np.all(np.abs(got - ref) <= 2 ** -8 * vmax + 2 ** -8 * np.abs(ref)), max_abs(got, ref)
 
 
+def _qknormed(g, nh, R, d, w):
+    """bf16 rows RMS-normalised per head and scaled by w ([d] or None), as the QKV epilogue writes them."""
+    x = g.standard_normal((nh, R, d))
+    x = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + 1e-6)
+    if w is not None:
+        x = x * w
+    return DI.bf16_bits_from_f32(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("R,nh,d", [(72, 4, 64), (200, 2, 128), (1088, 2, 128), (4224, 2, 128)])
+@pytest.mark.parametrize("wkind", ["ones", "near_one", "large"])
+def test_attention_qknorm_vs_oracle(R, nh, d, wkind):
+    # q and k as the QK-norm epilogue leaves them: with weights near one the scaled scores stay
+    # within the fixed bound B = d max|w_q| max|w_k| / sqrt(d) < 60 (log2 units) and the softmax
+    # subtracts B; weights of 4 put B above 60 and the kernel keeps the running maximum
+    g = np.random.default_rng(R * 3 + nh + len(wkind))
+    wq = wk = None
+    if wkind == "near_one":
+        wq = (1 + 0.02 * g.standard_normal(d)).astype(np.float32)
+        wk = (1 + 0.02 * g.standard_normal(d)).astype(np.float32)
+    elif wkind == "large":
+        wq = np.full(d, 4.0, np.float32)
+        wk = np.full(d, 1.5, np.float32)
+    q, k = _qknormed(g, nh, R, d, wq), _qknormed(g, nh, R, d, wk)
+    v = _bf16_rand(g, (nh, R, d), 1.0)
+    Rp = D.dit_vt_stride(R)
+    vt = np.zeros((nh, d, Rp), np.uint16)
+    vt[:, :, :R] = v.transpose(0, 2, 1)
+    dims = D.DitDims(nh * d, nh, d, 256)
+    o = torch.empty(R, nh * d, dtype=torch.bfloat16, device="cuda")
+    o_gen = torch.empty_like(o)
+    tw = lambda w: None if w is None else dev(w)
+    D.dit_attention_qknorm(dims, R, dev_bf16(q), dev_bf16(k), dev_bf16(vt), tw(wq), tw(wk), o)
+    D.dit_attention(dims, R, dev_bf16(q), dev_bf16(k), dev_bf16(vt), o_gen)
+    D.dit_check()
+    f = lambda a: O.bf16_to_f64(a).transpose(1, 0, 2)
+    ref = O.attention(f(q), f(k), f(v))
+    vmax = np.abs(O.bf16_to_f64(v)).max()
+    for got in (bf16_f64(o), bf16_f64(o_gen)):
+        assert np.all(np.abs(got - ref) <= 2 ** -8 * vmax + 2 ** -8 * np.abs(ref)), max_abs(got, ref)
+    if wkind == "large":  # B > 60: the same kernel path as dit_attention, bit for bit
+        assert torch.equal(o, o_gen)
+
+
 def test_attention_zero_query_gives_mean_value():
     R, nh, d = 300, 2, 128
     q, k, v = _attn_case(R, nh, d, 1)
