@@ -47,7 +47,6 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct AttnCfg {
-  static constexpr int kThreads = 320;                  // producer, MMA, 2 x 4 softmax warps
   static constexpr uint32_t kAtom = 128 * 128;          // one [128 rows x 64 bf16] swizzled atom
   static constexpr uint32_t kQBytes = 128 * D * 2;      // one query tile, D/64 atoms
   static constexpr uint32_t kKBytes = 128 * D * 2;      // per stage, D/64 atoms
@@ -64,9 +63,18 @@ struct AttnCfg {
 // decided per launch from the norm weights (both paths compiled, so kept apart from the other two,
 // whose register allocation it would otherwise share).
 enum AttnMode : int { kAttnRunning = 0, kAttnFixed = 1, kAttnAuto = 2 };
+// Key parts per softmax row under the fixed maximum: four (sixteen softmax warps, four per SM
+// sub-partition, 32 keys each) in the fixed kernel at d = 128, whose path needs about 100 registers;
+// two where the running path (168 registers) shares the kernel, or at d = 64 (d / 4 output columns
+// would be narrower than one TMEM load).
+template <int D, int MODE>
+struct AttnSplit {
+  static constexpr int kParts = (MODE == kAttnFixed && D == 128) ? 4 : 2;
+  static constexpr int kThreads = 64 + 128 * kParts;
+};
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnParams p, float scale_log2) {
   using Cfg = AttnCfg<D>;
@@ -125,7 +133,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(smem_u32(&k_empty[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
       mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&p_full[s]), fixed ? 256 : 128);  // softmax threads per tile
+      mbar_init(smem_u32(&p_full[s]), fixed ? 128 * AttnSplit<D, MODE>::kParts : 128);  // softmax threads per tile
       mbar_init(smem_u32(&o_done[s]), 1);
     }
     mbar_init(smem_u32(drain), 1);
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit(smem_u32(&s_full[t]));
       };
       // O_t += P_t V_j; P_t in TMEM: keys 16 kk .. 16 kk + 15 at column 128 t + 8 kk (running max), or
-      // at 128 t + 64 (kk / 4) + 8 (kk % 4) (fixed maximum: each key half inside its own S columns)
+      // inside their part's own S columns (fixed maximum: part p of KP keys at 128 t + KP p)
       auto issue_pv = [&](int t, int j) {
         const int s = j & 1;
         const uint32_t dO = tmem_base + 256u + uint32_t(t * D);
@@ -204,7 +212,8 @@ __global__ void __launch_bounds__(320, 1)
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t b = kk >> 2, off = uint32_t(2 * (kk & 3));
           const uint64_t bd = sw128_desc(smem_u32(sV + s * Cfg::kVBytes + b * Cfg::kVAtom)) + off;
-          const uint32_t pcol = fixed ? uint32_t(t * 128 + (kk >> 2) * 64 + (kk & 3) * 8) : uint32_t(t * 128 + kk * 8);
+          constexpr int KP = 128 / AttnSplit<D, MODE>::kParts;  // keys per part (fixed maximum)
+          const uint32_t pcol = fixed ? uint32_t(t * 128 + (kk * 16 / KP) * KP + (kk * 16 % KP) / 2) : uint32_t(t * 128 + kk * 8);
           umma_bf16_ts(dO, tmem_base + pcol, bd, idesc_o, (j | kk) != 0);
         }
       };
@@ -244,9 +253,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait(smem_u32(drain), 0, p.err, kErrTimeoutDrain);
     }
   } else if (fixed) {
-    // ------------------------------------------------------------------ softmax warps 2..9, fixed max
-    // warp (quad, half): rows quad * 32 + lane of each tile, keys [64 half, 64 half + 64)
-    const int half = (warp - 2) >> 2;
+    // ------------------------------------------------------------------ softmax warps, fixed max
+    // warp (quad, part): rows quad * 32 + lane of each tile, keys [KP part, KP part + KP)
+    constexpr int KS = AttnSplit<D, MODE>::kParts, KP = 128 / KS;
+    const int part = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = uint32_t(quad * 32) << 16;
@@ -255,20 +265,20 @@ __global__ void __launch_bounds__(320, 1)
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     const uint64_t negm2 = f2_pack(-m_fixed, -m_fixed);
     for (int j = 0; j < nkv && ok; ++j) {
-      const int valid = R - j * 128 - half * 64;  // keys of this half that exist (the same for the CTA)
-      const bool full = valid >= 64;
+      const int valid = R - j * 128 - part * KP;  // keys of this part that exist (the same for the CTA)
+      const bool full = valid >= KP;
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {
         if (!mbar_wait_warp(smem_u32(&s_full[t]), j & 1, p.err, kErrTimeoutSoftmax)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tS = tmem_base + lane_off + uint32_t(t * 128 + half * 64);
-        uint32_t r[64];
+        const uint32_t tS = tmem_base + lane_off + uint32_t(t * 128 + part * KP);
+        uint32_t r[KP];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) tmem_ld32(tS + uint32_t(c * 32), *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+        for (int c = 0; c < KP / 32; ++c) tmem_ld32(tS + uint32_t(c * 32), *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
         tmem_ld_wait();
         uint64_t sum2[4] = {0, 0, 0, 0};  // eight fp32 partial sums (four packed pairs)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < KP / 32; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -294,32 +304,35 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     // Both tiles' last P V done: every MMA has completed, so the Q tiles' shared memory is free and
-    // holds the two halves' row sums.
+    // holds the parts' row sums.
     bool done = ok;
     for (int t = 0; t < 2; ++t)
       done = done && mbar_wait_warp(smem_u32(&o_done[t]), 0, p.err, kErrTimeoutSoftmax);
-    float* lsum = reinterpret_cast<float*>(sQ);  // [tile][half][128 rows]
+    float* lsum = reinterpret_cast<float*>(sQ);  // [tile][part][128 rows]
     if (done) {
-      lsum[(0 * 2 + half) * 128 + row] = l[0];
-      lsum[(1 * 2 + half) * 128 + row] = l[1];
+      lsum[(0 * KS + part) * 128 + row] = l[0];
+      lsum[(1 * KS + part) * 128 + row] = l[1];
     }
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight softmax warps
+    asm volatile("bar.sync 1, %0;" ::"n"(128 * KS) : "memory");  // the softmax warps
     if (done) {
       tc_fence_after();
       const int H = p.heads * D;
+      constexpr int DC = D / KS;  // output columns of this warp
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {
-        // this warp's rows, output columns [half d/2, half d/2 + d/2)
-        const uint32_t tO = tmem_base + lane_off + 256u + uint32_t(t * D + half * (D / 2));
+        const uint32_t tO = tmem_base + lane_off + 256u + uint32_t(t * D + part * DC);
         const int grow = (2 * qp + t) * 128 + row;
-        const float inv_l = 1.0f / (lsum[(t * 2 + 0) * 128 + row] + lsum[(t * 2 + 1) * 128 + row]);
+        float lt = 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int q = 0; q < KS; ++q) lt += lsum[(t * KS + q) * 128 + row];
+        const float inv_l = 1.0f / lt;
+#pragma unroll
+        for (int c = 0; c < DC / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tO + uint32_t(c * 32), r);
           tmem_ld_wait();
           if (grow < R) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + size_t(grow) * H + head * D + half * (D / 2) + c * 32);
+            uint4* dst = reinterpret_cast<uint4*>(p.o + size_t(grow) * H + head * D + part * DC + c * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               dst[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv_l, __uint_as_float(r[8 * q + 1]) * inv_l),
@@ -462,7 +475,10 @@ int launch_d(const AttnParams& p, cudaStream_t stream) {
   if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
   const float scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
   dim3 grid((p.R + 255) / 256, p.heads);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p, scale_log2);
+  const int threads = p.qk_normed <= 0 ? AttnSplit<D, kAttnRunning>::kThreads
+                      : unit             ? AttnSplit<D, kAttnFixed>::kThreads
+                                         : AttnSplit<D, kAttnAuto>::kThreads;
+  kern<<<grid, threads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p, scale_log2);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
