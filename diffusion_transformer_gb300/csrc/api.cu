@@ -90,13 +90,38 @@ BlockWs carve_block_ws(const dit_dims* d, int R, void* base) {
   return w;
 }
 
-// int8lin scratch of a block: the dequantised weight of its largest linear
-size_t int8_scratch_bytes(const dit_dims* d) {
+// int8lin scratch of a block: two slots, each the dequantised weight of its largest linear (the
+// weights are dequantised one linear ahead of their use, alternating slots)
+size_t int8_slot_bytes(const dit_dims* d) {
   const int H = d->hidden, F = d->ffn;
   const int shapes[4][2] = {{3 * H, H}, {H, H}, {2 * F, H}, {H, F}};
   size_t tl = 0;
   for (auto& s : shapes) tl = std::max(tl, gemm_int8_scratch_bytes(s[0], s[1]));
   return tl;
+}
+size_t int8_scratch_bytes(const dit_dims* d) { return 2 * int8_slot_bytes(d); }
+
+// Per device: a second stream and events for the int8lin block's weight dequantisation, which runs
+// beside the block's kernels (fork from and join to the caller's stream through events). The mutex
+// keeps one block's enqueue sequence whole when several host threads share the device.
+struct SideStream {
+  std::mutex mu;
+  bool tried = false, ok = false;
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[8] = {};
+};
+SideStream g_side[kMaxDevices];
+SideStream* side_stream() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  SideStream& ss = g_side[dev];
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!ss.tried) {
+    ss.tried = true;
+    ss.ok = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) == cudaSuccess;
+    for (auto& e : ss.ev) ss.ok = ss.ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+  }
+  return ss.ok ? &ss : nullptr;
 }
 
 GemmParams base_params(int M, int N, int K, int* err) {
@@ -184,8 +209,56 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
     SandwichParams sp{txt, img, L, R, H, y, mod.rows + gate_row * H, 6LL * H, mod.map, post, d->eps};
     return sandwich_launch(sp, st);
   };
-  // int8lin scratch after the block workspace: one dequantised weight at a time
+  // int8lin scratch after the block workspace: two slots of dequantised weights
   uint16_t* i8_tiles = w8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
+  // Rows above kInt8MainloopMaxM: each linear's weight is dequantised once (HBM-bound) on a side
+  // stream one linear ahead, into alternating slots, while the main stream runs the previous
+  // kernels; each GEMM then runs the bf16 mainloop on its slot. ev: 0 fork, 1-4 weight i ready,
+  // 5-6 slot 0 / 1 free again. (Fewer rows: the GEMMs dequantise inside their mainloop.)
+  SideStream* side = nullptr;
+  std::unique_lock<std::mutex> side_lock;
+  uint16_t* slot[2] = {nullptr, nullptr};
+  if (w8 && R > kInt8MainloopMaxM) {
+    side = side_stream();
+    if (!side) return DIT_ECUDA;
+    side_lock = std::unique_lock<std::mutex>(side->mu);
+    slot[0] = i8_tiles;
+    slot[1] = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(i8_tiles) + int8_slot_bytes(d));
+  }
+  const int wshape[4][2] = {{3 * H, H}, {H, H}, {2 * F, H}, {H, F}};
+  // weight i into slot i % 2 on the side stream, after `after` (an event index, or -1)
+  auto dequant_ahead = [&](int i, int after) -> int {
+    if (after >= 0 && cudaStreamWaitEvent(side->s, side->ev[after], 0) != cudaSuccess) return DIT_ECUDA;
+    int r = dequant_int8_launch(w8->q[i], w8->s[i], slot[i % 2], wshape[i][0], wshape[i][1], side->s);
+    if (r != DIT_OK) return r;
+    return cudaEventRecord(side->ev[1 + i], side->s) == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  };
+  // the int8lin GEMM of linear i: on the prefetched slot, or with the in-mainloop dequantisation
+  auto gemm8 = [&](int i, const uint16_t* x, int K, int epi, const GemmParams& g) -> int {
+    if (!side) {
+      GemmInt8B q8{w8->q[i], w8->s[i], i8_tiles};
+      return gemm_launch(x, K, nullptr, &q8, epi, g, st);
+    }
+    if (cudaStreamWaitEvent(st, side->ev[1 + i], 0) != cudaSuccess) return DIT_ECUDA;
+    int r = gemm_launch(x, K, slot[i % 2], nullptr, epi, g, st);
+    if (r != DIT_OK) return r;
+    return cudaEventRecord(side->ev[5 + i % 2], st) == cudaSuccess ? DIT_OK : DIT_ECUDA;  // slot free
+  };
+  // On every exit the caller's stream also waits for the side stream's last work (after a normal
+  // finish that is already the case; after an error it keeps the scratch's users in order).
+  struct Join {
+    SideStream* side;
+    cudaStream_t st;
+    ~Join() {
+      if (side && cudaEventRecord(side->ev[7], side->s) == cudaSuccess) cudaStreamWaitEvent(st, side->ev[7], 0);
+    }
+  } join{side, st};
+  if (side) {
+    if (cudaEventRecord(side->ev[0], st) != cudaSuccess) return DIT_ECUDA;  // fork
+    int r = dequant_ahead(0, 0);
+    if (r == DIT_OK) r = dequant_ahead(1, -1);
+    if (r != DIT_OK) return r;
+  }
   const float* norm1 = w8 ? w8->norm1 : w->norm1;
   const float* norm2 = w8 ? w8->norm2 : w->norm2;
   const float* qn = w8 ? w8->q_norm : w->q_norm;
@@ -198,9 +271,8 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
 
   // 2. q, k, vt = qk-norm + rope epilogue of h Wqkv^T
   GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, qn, kn, err);
-  GemmInt8B q8;
-  if (w8) q8 = GemmInt8B{w8->q[0], w8->s[0], i8_tiles};
-  if ((rc = linear(0, b.h, H, w8 ? nullptr : w->wqkv, w8 ? &q8 : nullptr, kEpiQKV, g)) != DIT_OK) return rc;
+  if ((rc = w8 ? gemm8(0, b.h, H, kEpiQKV, g) : linear(0, b.h, H, w->wqkv, nullptr, kEpiQKV, g)) != DIT_OK) return rc;
+  if (side && (rc = dequant_ahead(2, 5)) != DIT_OK) return rc;  // up into slot 0 once the QKV GEMM is done
 
   // 3. o = attention(q, k, v); q and k rows QK-normed with qn, kn
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, qn, kn, nullptr, nullptr};
@@ -217,9 +289,9 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   // scratch for the K-split of the last wave: the SwiGLU buffer, not yet written
   g.split_ws = b.a;
   g.split_ws_bytes = size_t(R) * F * 2;
-  if (w8) q8 = GemmInt8B{w8->q[1], w8->s[1], i8_tiles};
-  if ((rc = gated_linear(1, b.o, H, w8 ? nullptr : w->wout, w8 ? &q8 : nullptr, g, post_attn, 2)) != DIT_OK)
+  if ((rc = w8 ? gemm8(1, b.o, H, kEpiGated, g) : gated_linear(1, b.o, H, w->wout, nullptr, g, post_attn, 2)) != DIT_OK)
     return rc;
+  if (side && (rc = dequant_ahead(3, 6)) != DIT_OK) return rc;  // down into slot 1 once the out GEMM is done
 
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
   mp.w = norm2;
@@ -231,8 +303,8 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g = base_params(R, 2 * F, H, err);
   g.out = b.a;
   g.ldo = F;
-  if (w8) q8 = GemmInt8B{w8->q[2], w8->s[2], i8_tiles};
-  if ((rc = linear(2, b.h, H, w8 ? nullptr : w->wup, w8 ? &q8 : nullptr, kEpiSwiGLU, g)) != DIT_OK) return rc;
+  if ((rc = w8 ? gemm8(2, b.h, H, kEpiSwiGLU, g) : linear(2, b.h, H, w->wup, nullptr, kEpiSwiGLU, g)) != DIT_OK)
+    return rc;
 
   // 7. x += gate_m * (a Wdown^T)
   g = base_params(R, H, F, err);
@@ -245,8 +317,8 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   // scratch for the K-split of the last wave: h, q, k, vt and o, all consumed by now
   g.split_ws = b.h;
   g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
-  if (w8) q8 = GemmInt8B{w8->q[3], w8->s[3], i8_tiles};
-  return gated_linear(3, b.a, F, w8 ? nullptr : w->wdown, w8 ? &q8 : nullptr, g, post_mlp, 5);
+  // (int8lin: the down GEMM waits for its weight, the side stream's last work: the join)
+  return w8 ? gemm8(3, b.a, F, kEpiGated, g) : gated_linear(3, b.a, F, w->wdown, nullptr, g, post_mlp, 5);
 }
 
 // The parallel (single-stream) block [gizai:dit, Block.parallel]: one modulated LayerNorm feeds

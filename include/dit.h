@@ -167,9 +167,12 @@ DIT_API int dit_block_forward_sandwich(const dit_dims* dims, const dit_block_w* 
  * bf16 MMA. With at most 512 rows the GEMM's converter warps dequantize each weight k-block inside
  * the mainloop; with more rows (many M tiles per weight tile) each linear's weight is dequantized
  * once into the workspace by an HBM-bound kernel with the same arithmetic and the bf16 mainloop
- * runs on it (bitwise the same result). Requires in % 256 == 0 for every linear.
- * Workspace: dit_workspace_bytes(dims, L, N, 1) (the bf16 block workspace plus the dequantized
- * weight of the largest linear). */
+ * runs on it (bitwise the same result). Those dequantizations run on a library-owned second stream
+ * (created once per device), each one linear ahead into alternating workspace slots, forked from
+ * and joined back to `stream` through events, so they overlap the previous linear's kernels; all
+ * work stays ordered with respect to `stream`. Requires in % 256 == 0 for every linear.
+ * Workspace: dit_workspace_bytes(dims, L, N, 1) (the bf16 block workspace plus two slots, each the
+ * dequantized weight of the largest linear). */
 DIT_API int dit_block_forward_int8(const dit_dims* dims, const dit_block_w8* w, float* txt, int L, float* img, int N,
                            const float* txt_cos, const float* txt_sin, const float* img_cos,
                            const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
