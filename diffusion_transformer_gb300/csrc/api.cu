@@ -521,9 +521,10 @@ EncodeTiledFn encode_tiled_fn() {
 bool smem_attr_once(const void* kernel, unsigned bytes) {
   const int dev = current_device();
   if (dev < 0) return false;
-  static const void* done[kMaxDevices][32];
+  constexpr int kKernels = 128;  // more than the library's kernel instantiations
+  static const void* done[kMaxDevices][kKernels];
   std::lock_guard<std::mutex> lk(g_mu);
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < kKernels; ++i) {
     if (done[dev][i] == kernel) return true;
     if (!done[dev][i]) {
       if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) != cudaSuccess)

@@ -926,8 +926,12 @@ int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
   static_assert(Cfg::kSmemBytes <= 227 * 1024, "shared memory budget");
   auto kern = gemm_kernel<BN, EPI, B8, PAIR>;
   if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
-  static int units_max = 0;  // resident units, queried once per kernel
-  if (units_max <= 0) units_max = resident_units(reinterpret_cast<const void*>(kern), PAIR, Cfg::kThreads, Cfg::kSmemBytes);
+  static int units_cached[64];  // resident units, queried once per kernel and device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DIT_ECUDA;
+  if (units_cached[dev] <= 0)
+    units_cached[dev] = resident_units(reinterpret_cast<const void*>(kern), PAIR, Cfg::kThreads, Cfg::kSmemBytes);
+  const int units_max = units_cached[dev];
   const int tiles = row_tiles(p, Cfg::kTileM) * (p.N / BN);
   const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
   const int units = items < units_max ? items : units_max;
