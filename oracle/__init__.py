@@ -8,8 +8,9 @@ no code with the CUDA path: its only common dependency is the seeded input gener
 
 Everything is plain NumPy in float64, except where the pages fix a precision: the Euler update is
 float32 (the RGBA-Image-2.1 host contract, section 6, "all arrays are fp32") and the int8lin
-dequantised weight is rounded to bfloat16 (same contract, section 1). Weights enter as the exact
-values of their bfloat16 bit patterns; no intermediate activation is rounded.
+dequantised weight is rounded to bfloat16 (same contract, section 1), and the W8A8 quantisers take
+their code decisions in float32 with the activation at its bfloat16 value (``w8a8``). Weights enter
+as the exact values of their bfloat16 bit patterns; no other intermediate activation is rounded.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in ``tests/test_oracle_*.py``
 against closed forms, invariants, brute force on tiny inputs or values the pages print. No function
@@ -17,3 +18,4 @@ is "parity unpinned".
 """
 
 from .dit import *  # noqa: F401,F403
+from .w8a8 import *  # noqa: F401,F403

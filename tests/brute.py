@@ -20,9 +20,16 @@ def rmsnorm_row(x, eps):
 
 
 def block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
-          norm1=None, norm2=None, qn=None, kn=None, post_attn=None, post_mlp=None):
+          norm1=None, norm2=None, qn=None, kn=None, post_attn=None, post_mlp=None, linear=None):
     """x: list of R rows (lists of H floats). mod_rows[r] = 6 lists of H (shift_a, scale_a, gate_a,
-    shift_m, scale_m, gate_m) for row r. cos/sin: R lists of d/2. Returns new rows."""
+    shift_m, scale_m, gate_m) for row r. cos/sin: R lists of d/2. Returns new rows.
+    linear(W, row) replaces the plain W row products when given (one call per weight matrix)."""
+    return _block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
+                  norm1, norm2, qn, kn, post_attn, post_mlp, linear or matvec)
+
+
+def _block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
+           norm1, norm2, qn, kn, post_attn, post_mlp, matvec):
     R, H = len(x), len(x[0])
     one = lambda n: [1.0] * n
     n1 = norm1 or one(H)
