@@ -6,8 +6,10 @@ linear, down linear with gated residual - at the 1024^2 shape: hidden 3072, 24 h
 ffn 12288, L = 128 text + N = 4096 image rows (R = 4224), bf16 weights, per-row modulation.
 The same run also times the int8lin block (the same shape), the parallel single-stream block (the
 same shape and FLOP count: one modulated LayerNorm feeding attention and the MLP, 4 launches), the
-double-stream block (the same shape, text and image rows with their own weights, 7 launches) and
-the 32-block, 4-step denoise loop (L = 512, N = 4096) and reports them as sub-objects.
+double-stream block (the same shape, text and image rows with their own weights, 7 launches), the
+block with split-halves rotary, with rank-64 LoRA adapters, with sandwich post-norms and with W8A8
+linears (per-token int8 activations, per-channel int8 weights), and the 32-block, 4-step denoise
+loop (L = 512, N = 4096), and reports them as sub-objects.
 
 Metric: block TFLOP/s (algorithmic FLOP = 2R(3H^2 + H^2 + 2HF + FH) + 4R^2 H per block) and
 ms per block. Inputs are larger than L2 (302 MB of weights per block), so no flush is needed.
@@ -523,6 +525,28 @@ def run_ours(args):
                "launches_per_block": 9}
         del pa, pm
 
+    # the W8A8 block (opt-in lossy tier): the block's bf16 weights quantised per output channel
+    # on the device, no SmoothQuant divisors; activations quantised per token on every call
+    w8a = None
+    if not args.no_w8a8:
+        wq, wsc = [], []
+        for W in st["w"].tensors[:4]:
+            wq.append(torch.empty(W.shape, dtype=torch.int8, device="cuda"))
+            wsc.append(torch.empty(W.shape[0], dtype=torch.float32, device="cuda"))
+            D.dit_w8a8_quantize_weight(W, None, wq[-1], wsc[-1])
+        wA = D.W8A8BlockWeights(wq, wsc)
+        wsA = torch.empty(D.dit_workspace_bytes(st["dims"], sh.L, sh.N, 4), dtype=torch.uint8, device="cuda")
+        callA = lambda: D.dit_block_forward_w8a8(st["dims"], wA, st["txt"], st["img"], st["tc"], st["ts"], st["ic"],
+                                                 st["is_"], st["mod"], wsA)
+        msA = _time_loop(torch, callA, args.steps, args.warmup, dist) / args.steps
+        D.dit_check()
+        tfA = flops / (msA * 1e-3) / 1e12
+        w8a = {"workload": "1024sq W8A8 block: per-token int8 activation codes x per-channel int8 weight codes, "
+                           "exact on the bf16 tensor cores, scales applied to the integer accumulator",
+               "ms_per_block": msA, "tflops": tfA, "frac_of_peak": tfA / peaks["bf16_tflops"], "flop_per_block": flops,
+               "launches_per_block": 11}
+        del wA, wsA, wq, wsc
+
     # end to end through host buffers
     e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
     D.dit_check()
@@ -556,6 +580,7 @@ def run_ours(args):
             "rope_split_block": rsp,
             "lora_block": lor,
             "sandwich_block": swb,
+            "w8a8_block": w8a,
             "denoise": den,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -646,6 +671,7 @@ def main():
     ap.add_argument("--no-rope-split", action="store_true")
     ap.add_argument("--no-lora", action="store_true")
     ap.add_argument("--no-sandwich", action="store_true")
+    ap.add_argument("--no-w8a8", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

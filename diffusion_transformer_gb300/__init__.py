@@ -16,6 +16,8 @@ from typing import List, Optional, Sequence
 __all__ = [
     "DitError", "lib", "library_path", "DitDims", "BlockWeights", "Int8BlockWeights", "Modulation",
     "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_parallel_block_forward",
+    "W8A8BlockWeights", "dit_block_forward_w8a8", "dit_w8a8_quantize_weight", "dit_w8a8_quantize_rows",
+    "dit_linear_w8a8", "dit_linear_w8a8_workspace_bytes",
     "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA",
     "dit_block_forward_sandwich", "dit_euler_step",
     "dit_rope_tables",
@@ -58,6 +60,11 @@ class dit_block_w8(ctypes.Structure):
                 ("q_norm", c_void_p), ("k_norm", c_void_p)]
 
 
+class dit_block_w8a8(ctypes.Structure):
+    _fields_ = [("q", c_void_p * 4), ("scale", c_void_p * 4), ("smooth", c_void_p * 4), ("norm1", c_void_p),
+                ("norm2", c_void_p), ("q_norm", c_void_p), ("k_norm", c_void_p)]
+
+
 class dit_mod(ctypes.Structure):
     _fields_ = [("rows", c_void_p), ("map", c_void_p), ("M", c_int)]
 
@@ -88,6 +95,14 @@ _SIGNATURES = {
     "dit_block_forward_int8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8), c_void_p, c_int, c_void_p, c_int,
                                        c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                        c_size_t, c_void_p]),
+    "dit_block_forward_w8a8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8a8), c_void_p, c_int, c_void_p, c_int,
+                                       c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
+                                       c_size_t, c_void_p]),
+    "dit_w8a8_quantize_weight": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dit_w8a8_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "dit_linear_w8a8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                c_size_t, c_void_p]),
+    "dit_linear_w8a8_workspace_bytes": (c_size_t, [c_int, c_int, c_int]),
     "dit_block_forward_noalloc": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_int, c_void_p, c_int,
                                           c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p]),
     "dit_block_noalloc_max_bytes": (c_size_t, []),
@@ -215,6 +230,23 @@ class Int8BlockWeights:
         sp = (c_void_p * 4)(*[_ptr(t, _bf16(), "s") for t in s])
         self.c = dit_block_w8(qp, sp, _ptr(norm1, f32, "norm1"), _ptr(norm2, f32, "norm2"),
                               _ptr(q_norm, f32, "q_norm"), _ptr(k_norm, f32, "k_norm"))
+
+
+class W8A8BlockWeights:
+    """Device tensors of one W8A8 block: q [4] int8 [out, in], scale [4] fp32 [out], smooth [4] fp32
+    [in] or None (SmoothQuant divisors folded into q), and the norm weights."""
+
+    def __init__(self, q: Sequence, scale: Sequence, smooth: Optional[Sequence] = None, norm1=None, norm2=None,
+                 q_norm=None, k_norm=None):
+        import torch
+        f32 = torch.float32
+        smooth = list(smooth) if smooth is not None else [None] * 4
+        self.tensors = (tuple(q), tuple(scale), tuple(smooth), norm1, norm2, q_norm, k_norm)
+        self.c = dit_block_w8a8((c_void_p * 4)(*[_ptr(t, torch.int8, "q") for t in q]),
+                                (c_void_p * 4)(*[_ptr(t, f32, "scale") for t in scale]),
+                                (c_void_p * 4)(*[_ptr(t, f32, "smooth") for t in smooth]),
+                                _ptr(norm1, f32, "norm1"), _ptr(norm2, f32, "norm2"), _ptr(q_norm, f32, "q_norm"),
+                                _ptr(k_norm, f32, "k_norm"))
 
 
 class Modulation:
@@ -450,6 +482,48 @@ def dit_linear(a, w, out, stream=None):
 
 def dit_linear_int8_workspace_bytes(N: int, K: int) -> int:
     return lib().dit_linear_int8_workspace_bytes(N, K)
+
+
+def dit_block_forward_w8a8(dims: DitDims, w: W8A8BlockWeights, txt, img, txt_cos, txt_sin, img_cos, img_sin,
+                           mod: Modulation, ws, stream=None):
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_block_forward_w8a8(ctypes.byref(dims.c), ctypes.byref(w.c), _ptr(txt, f32, "txt"), L,
+                                     _ptr(img, f32, "img"), img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                                     _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
+                                     _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_block_forward_w8a8")
+
+
+def dit_w8a8_quantize_weight(w, smooth, q, scale, stream=None):
+    import torch
+    N, K = w.shape
+    _ok(lib().dit_w8a8_quantize_weight(_ptr(w, _bf16(), "w"), N, K, _ptr(smooth, torch.float32, "smooth"),
+                                       _ptr(q, torch.int8, "q"), _ptr(scale, torch.float32, "scale"), _stream(stream)),
+        "dit_w8a8_quantize_weight")
+
+
+def dit_w8a8_quantize_rows(x, smooth, scale, stream=None):
+    """Per-token codes of x (bf16 [R, K]) written over x; scale [R] fp32."""
+    import torch
+    R, K = x.shape
+    _ok(lib().dit_w8a8_quantize_rows(_ptr(x, _bf16(), "x"), R, K, _ptr(smooth, torch.float32, "smooth"),
+                                     _ptr(scale, torch.float32, "scale"), _stream(stream)), "dit_w8a8_quantize_rows")
+
+
+def dit_linear_w8a8_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib().dit_linear_w8a8_workspace_bytes(M, N, K)
+
+
+def dit_linear_w8a8(a, q, scale, smooth, out, ws, stream=None):
+    import torch
+    M, K = a.shape
+    N = q.shape[0]
+    _ok(lib().dit_linear_w8a8(_ptr(a, _bf16(), "a"), M, K, _ptr(q, torch.int8, "q"), _ptr(scale, torch.float32, "scale"),
+                              _ptr(smooth, torch.float32, "smooth"), N, _ptr(out, torch.float32, "out"),
+                              _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_linear_w8a8")
 
 
 def dit_linear_int8(a, wq, wscale, out, ws, stream=None):

@@ -124,6 +124,67 @@ SideStream* side_stream() {
   return ss.ok ? &ss : nullptr;
 }
 
+// The weights of a block's four linears prepared (dequantised, or widened from int8 codes) on the
+// side stream one linear ahead of their use, into two alternating workspace slots: linear i goes to
+// slot i % 2; linears 0 and 1 start at the fork, 2 once linear 0's GEMM has released slot 0, 3 once
+// linear 1's GEMM has released slot 1. Events: 0 fork, 1-4 weight i ready, 5-6 slot 0 / 1 free,
+// 7 the join that every exit makes (the caller's stream then waits for all side work).
+class WeightPrefetch {
+ public:
+  // prep(i, dst, stream) launches the preparation of linear i's weight into dst
+  using Prep = int (*)(const void* ctx, int i, uint16_t* dst, cudaStream_t stream);
+  WeightPrefetch(cudaStream_t st, uint16_t* slot0, size_t slot_bytes, Prep prep, const void* ctx)
+      : st_(st), prep_(prep), ctx_(ctx) {
+    slot_[0] = slot0;
+    slot_[1] = slot0 ? reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(slot0) + slot_bytes) : nullptr;
+  }
+  ~WeightPrefetch() {
+    if (side_ && cudaEventRecord(side_->ev[7], side_->s) == cudaSuccess) cudaStreamWaitEvent(st_, side_->ev[7], 0);
+  }
+  // fork and start linears 0 and 1
+  int start() {
+    side_ = side_stream();
+    if (!side_) return DIT_ECUDA;
+    lock_ = std::unique_lock<std::mutex>(side_->mu);
+    if (cudaEventRecord(side_->ev[0], st_) != cudaSuccess) return DIT_ECUDA;
+    int r = ahead(0, 0);
+    return r == DIT_OK ? ahead(1, -1) : r;
+  }
+  // the weight of linear i, ready for a launch on the caller's stream
+  int use(int i, const uint16_t** w) {
+    if (cudaStreamWaitEvent(st_, side_->ev[1 + i], 0) != cudaSuccess) return DIT_ECUDA;
+    *w = slot_[i % 2];
+    return DIT_OK;
+  }
+  // after linear i's GEMM: its slot is free, and linear i + 2 (if any) may be prepared into it
+  int done(int i) {
+    if (cudaEventRecord(side_->ev[5 + i % 2], st_) != cudaSuccess) return DIT_ECUDA;
+    return i + 2 < 4 ? ahead(i + 2, 5 + i % 2) : DIT_OK;
+  }
+
+ private:
+  int ahead(int i, int after) {
+    if (after >= 0 && cudaStreamWaitEvent(side_->s, side_->ev[after], 0) != cudaSuccess) return DIT_ECUDA;
+    int r = prep_(ctx_, i, slot_[i % 2], side_->s);
+    if (r != DIT_OK) return r;
+    return cudaEventRecord(side_->ev[1 + i], side_->s) == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  }
+  cudaStream_t st_;
+  Prep prep_;
+  const void* ctx_;
+  uint16_t* slot_[2];
+  SideStream* side_ = nullptr;
+  std::unique_lock<std::mutex> lock_;
+};
+
+// [out, in] of linear i (0 qkv, 1 out, 2 up, 3 down)
+void linear_shape(const dit_dims* d, int i, int* n, int* k) {
+  const int H = d->hidden, F = d->ffn;
+  const int shp[4][2] = {{3 * H, H}, {H, H}, {2 * F, H}, {H, F}};
+  *n = shp[i][0];
+  *k = shp[i][1];
+}
+
 GemmParams base_params(int M, int N, int K, int* err) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -211,59 +272,38 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   };
   // int8lin scratch after the block workspace: two slots of dequantised weights
   uint16_t* i8_tiles = w8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
-  // Rows above kInt8MainloopMaxM: each linear's weight is dequantised once (HBM-bound) on a side
-  // stream one linear ahead, into alternating slots, while the main stream runs the previous
-  // kernels; each GEMM then runs the bf16 mainloop on its slot. ev: 0 fork, 1-4 weight i ready,
-  // 5-6 slot 0 / 1 free again. (Fewer rows: the GEMMs dequantise inside their mainloop.)
-  SideStream* side = nullptr;
-  std::unique_lock<std::mutex> side_lock;
-  uint16_t* slot[2] = {nullptr, nullptr};
-  if (w8 && R > kInt8MainloopMaxM) {
-    side = side_stream();
-    if (!side) return DIT_ECUDA;
-    side_lock = std::unique_lock<std::mutex>(side->mu);
-    slot[0] = i8_tiles;
-    slot[1] = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(i8_tiles) + int8_slot_bytes(d));
-  }
-  const int wshape[4][2] = {{3 * H, H}, {H, H}, {2 * F, H}, {H, F}};
-  // weight i into slot i % 2 on the side stream, after `after` (an event index, or -1)
-  auto dequant_ahead = [&](int i, int after) -> int {
-    if (after >= 0 && cudaStreamWaitEvent(side->s, side->ev[after], 0) != cudaSuccess) return DIT_ECUDA;
-    int r = dequant_int8_launch(w8->q[i], w8->s[i], slot[i % 2], wshape[i][0], wshape[i][1], side->s);
-    if (r != DIT_OK) return r;
-    return cudaEventRecord(side->ev[1 + i], side->s) == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  // Rows above kInt8MainloopMaxM: each linear's weight is dequantised once (HBM-bound) on the side
+  // stream one linear ahead, while the main stream runs the previous kernels; each GEMM then runs
+  // the bf16 mainloop on its slot. (Fewer rows: the GEMMs dequantise inside their mainloop.)
+  struct DequantCtx {
+    const dit_dims* d;
+    const dit_block_w8* w8;
+  } dctx{d, w8};
+  auto dequant = [](const void* c, int i, uint16_t* dst, cudaStream_t s2) -> int {
+    const DequantCtx* x = static_cast<const DequantCtx*>(c);
+    int n, k;
+    linear_shape(x->d, i, &n, &k);
+    return dequant_int8_launch(x->w8->q[i], x->w8->s[i], dst, n, k, s2);
   };
+  const bool prefetch = w8 && R > kInt8MainloopMaxM;
+  WeightPrefetch pf(st, i8_tiles, w8 ? int8_slot_bytes(d) : 0, dequant, &dctx);
+  int rc;
+  if (prefetch && (rc = pf.start()) != DIT_OK) return rc;
   // the int8lin GEMM of linear i: on the prefetched slot, or with the in-mainloop dequantisation
   auto gemm8 = [&](int i, const uint16_t* x, int K, int epi, const GemmParams& g) -> int {
-    if (!side) {
+    if (!prefetch) {
       GemmInt8B q8{w8->q[i], w8->s[i], i8_tiles};
       return gemm_launch(x, K, nullptr, &q8, epi, g, st);
     }
-    if (cudaStreamWaitEvent(st, side->ev[1 + i], 0) != cudaSuccess) return DIT_ECUDA;
-    int r = gemm_launch(x, K, slot[i % 2], nullptr, epi, g, st);
-    if (r != DIT_OK) return r;
-    return cudaEventRecord(side->ev[5 + i % 2], st) == cudaSuccess ? DIT_OK : DIT_ECUDA;  // slot free
+    const uint16_t* wb;
+    int r = pf.use(i, &wb);
+    if (r == DIT_OK) r = gemm_launch(x, K, wb, nullptr, epi, g, st);
+    return r == DIT_OK ? pf.done(i) : r;
   };
-  // On every exit the caller's stream also waits for the side stream's last work (after a normal
-  // finish that is already the case; after an error it keeps the scratch's users in order).
-  struct Join {
-    SideStream* side;
-    cudaStream_t st;
-    ~Join() {
-      if (side && cudaEventRecord(side->ev[7], side->s) == cudaSuccess) cudaStreamWaitEvent(st, side->ev[7], 0);
-    }
-  } join{side, st};
-  if (side) {
-    if (cudaEventRecord(side->ev[0], st) != cudaSuccess) return DIT_ECUDA;  // fork
-    int r = dequant_ahead(0, 0);
-    if (r == DIT_OK) r = dequant_ahead(1, -1);
-    if (r != DIT_OK) return r;
-  }
   const float* norm1 = w8 ? w8->norm1 : w->norm1;
   const float* norm2 = w8 ? w8->norm2 : w->norm2;
   const float* qn = w8 ? w8->q_norm : w->q_norm;
   const float* kn = w8 ? w8->k_norm : w->k_norm;
-  int rc;
 
   // 1. h = modnorm(x; norm1, shift_a, scale_a)
   ModNormParams mp{txt, img, L, R, H, H, H, norm1, mod.rows, mod.rows + H, 6LL * H, mod.map, d->eps, b.h};
@@ -272,7 +312,6 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   // 2. q, k, vt = qk-norm + rope epilogue of h Wqkv^T
   GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, qn, kn, err);
   if ((rc = w8 ? gemm8(0, b.h, H, kEpiQKV, g) : linear(0, b.h, H, w->wqkv, nullptr, kEpiQKV, g)) != DIT_OK) return rc;
-  if (side && (rc = dequant_ahead(2, 5)) != DIT_OK) return rc;  // up into slot 0 once the QKV GEMM is done
 
   // 3. o = attention(q, k, v); q and k rows QK-normed with qn, kn
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, qn, kn, nullptr, nullptr};
@@ -291,7 +330,6 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.split_ws_bytes = size_t(R) * F * 2;
   if ((rc = w8 ? gemm8(1, b.o, H, kEpiGated, g) : gated_linear(1, b.o, H, w->wout, nullptr, g, post_attn, 2)) != DIT_OK)
     return rc;
-  if (side && (rc = dequant_ahead(3, 6)) != DIT_OK) return rc;  // down into slot 1 once the out GEMM is done
 
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
   mp.w = norm2;
@@ -319,6 +357,92 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
   // (int8lin: the down GEMM waits for its weight, the side stream's last work: the join)
   return w8 ? gemm8(3, b.a, F, kEpiGated, g) : gated_linear(3, b.a, F, w->wdown, nullptr, g, post_mlp, 5);
+}
+
+// W8A8 scratch after the block workspace: two slots of bf16-widened weight codes (as for int8lin),
+// then the per-token scales [R] of the activation being quantised
+size_t w8a8_extra_bytes(const dit_dims* d, int R) {
+  return int8_scratch_bytes(d) + round_up(size_t(R) * sizeof(float), 256);
+}
+
+// The block with W8A8 linears [klein, section 5 and its D4/D5 entries]: each linear's activation
+// (h, o, h2, a) is quantised per token in place (bf16 integer codes over the bf16 values; SmoothQuant
+// divisor first when given) with its scales in the workspace; the weight's int8 codes are widened to
+// bf16 on the side stream one linear ahead; the GEMM's integer-valued accumulator (exact while every
+// partial sum stays below 2^24) is multiplied by the row's and the column's scales before the
+// linear's usual epilogue.
+int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L, float* img, int N,
+                   const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod, void* ws,
+                   cudaStream_t st) {
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  const int R = L + N, H = d->hidden, F = d->ffn;
+  const BlockWs b = carve_block_ws(d, R, ws);
+  uint16_t* slots = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes);
+  float* sa = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + b.bytes + int8_scratch_bytes(d));
+  struct CodesCtx {
+    const dit_dims* d;
+    const dit_block_w8a8* w;
+  } cctx{d, w};
+  auto widen = [](const void* c, int i, uint16_t* dst, cudaStream_t s2) -> int {
+    const CodesCtx* x = static_cast<const CodesCtx*>(c);
+    int n, k;
+    linear_shape(x->d, i, &n, &k);
+    return codes_bf16_launch(x->w->q[i], dst, (long long)n * k, s2);
+  };
+  WeightPrefetch pf(st, slots, int8_slot_bytes(d), widen, &cctx);
+  int rc;
+  if ((rc = pf.start()) != DIT_OK) return rc;
+  // linear i on activation codes x [R, K] (quantised in place first)
+  auto linear = [&](int i, uint16_t* x, int K, int epi, GemmParams g) -> int {
+    int r = quant_rows_launch(x, R, K, w->smooth[i], sa, st);
+    if (r != DIT_OK) return r;
+    const uint16_t* wc;
+    if ((r = pf.use(i, &wc)) != DIT_OK) return r;
+    g.a_scale = sa;
+    g.w_scale = w->scale[i];
+    if ((r = gemm_launch(x, K, wc, nullptr, epi, g, st)) != DIT_OK) return r;
+    return pf.done(i);
+  };
+  auto gated = [&](int K, long long gate_row, void* split_ws, size_t split_bytes) {
+    GemmParams g = base_params(R, H, K, err);
+    g.txt = txt;
+    g.img = img;
+    g.L = L;
+    g.gate = mod.rows + gate_row * H;
+    g.map = mod.map;
+    g.gate_stride = 6LL * H;
+    g.split_ws = split_ws;
+    g.split_ws_bytes = split_bytes;
+    return g;
+  };
+
+  // 1. h = modnorm(x; norm1, shift_a, scale_a)
+  ModNormParams mp{txt, img, L, R, H, H, H, w->norm1, mod.rows, mod.rows + H, 6LL * H, mod.map, d->eps, b.h};
+  if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+  // 2. q, k, vt from the W8A8 QKV linear with the QK-norm + rotary epilogue
+  if ((rc = linear(0, b.h, H, kEpiQKV, qkv_params(d, R, R, L, b, tc, ts, ic, is, w->q_norm, w->k_norm, err))) !=
+      DIT_OK)
+    return rc;
+  // 3. o = attention(q, k, v)
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, w->q_norm, w->k_norm, nullptr,
+                nullptr};
+  if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
+  // 4. x += gate_a * W8A8(o, Wout)
+  if ((rc = linear(1, b.o, H, kEpiGated, gated(H, 2, b.a, size_t(R) * F * 2))) != DIT_OK) return rc;
+  // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
+  mp.w = w->norm2;
+  mp.shift = mod.rows + 3LL * H;
+  mp.scale = mod.rows + 4LL * H;
+  if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+  // 6. a = SwiGLU(W8A8(h2, Wup))
+  GemmParams g = base_params(R, 2 * F, H, err);
+  g.out = b.a;
+  g.ldo = F;
+  if ((rc = linear(2, b.h, H, kEpiSwiGLU, g)) != DIT_OK) return rc;
+  // 7. x += gate_m * W8A8(a, Wdown)
+  return linear(3, b.a, F, kEpiGated,
+                gated(F, 5, b.h, size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h))));
 }
 
 // The parallel (single-stream) block [gizai:dit, Block.parallel]: one modulated LayerNorm feeds
@@ -568,9 +692,10 @@ const char* dit_status_string(int s) {
 }
 
 size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
-  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 3) return 0;
+  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 4) return 0;
   size_t bytes = carve_block_ws(d, L + N, nullptr).bytes;
   if (variant == 1) bytes += int8_scratch_bytes(d);
+  if (variant == 4) bytes += w8a8_extra_bytes(d, L + N);
   return bytes;
 }
 
@@ -666,6 +791,61 @@ int dit_block_forward_sandwich(const dit_dims* d, const dit_block_w* w, const fl
   if ((post_attn && !al16(post_attn)) || (post_mlp && !al16(post_mlp))) return DIT_EINVAL;
   return run_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                    reinterpret_cast<cudaStream_t>(stream), nullptr, post_attn, post_mlp);
+}
+
+int dit_block_forward_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L, float* img, int N,
+                           const float* tc, const float* ts, const float* ic, const float* is, const dit_mod* mod,
+                           void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 4);
+  if (rc != DIT_OK) return rc;
+  if (!w) return DIT_EINVAL;
+  for (int i = 0; i < 4; ++i)
+    if (!w->q[i] || !w->scale[i] || !al16(w->q[i]) || !al16(w->scale[i])) return DIT_EINVAL;
+  return run_block_w8a8(d, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_w8a8_quantize_weight(const uint16_t* w, int N, int K, const float* smooth, int8_t* q, float* scale,
+                             dit_stream_t stream) {
+  if (!w || !q || !scale || N < 1 || K < 1) return DIT_EINVAL;
+  return quant_weight_launch(w, N, K, smooth, q, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_w8a8_quantize_rows(uint16_t* x, int R, int K, const float* smooth, float* scale, dit_stream_t stream) {
+  if (!x || !scale || R < 1 || K < 1) return DIT_EINVAL;
+  if (K % 8 != 0) return DIT_EUNSUPPORTED;
+  if (!al16(x)) return DIT_EINVAL;
+  return quant_rows_launch(x, R, K, smooth, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dit_linear_w8a8_workspace_bytes(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 1) return 0;
+  return round_up(size_t(M) * K * 2, 256) + round_up(size_t(N) * K * 2, 256) + round_up(size_t(M) * 4, 256);
+}
+
+int dit_linear_w8a8(const uint16_t* a, int M, int K, const int8_t* q, const float* scale, const float* smooth, int N,
+                    float* out, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  if (!a || !q || !scale || !out || M < 1 || N < 1 || K < 1) return DIT_EINVAL;
+  if (K % 64 != 0 || N % 64 != 0) return DIT_EUNSUPPORTED;
+  if (!al16(a) || !al16(q) || !al16(out) || !ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DIT_EINVAL;
+  if (ws_bytes < dit_linear_w8a8_workspace_bytes(M, N, K)) return DIT_EWORKSPACE;
+  int* err = err_word();
+  if (!err) return DIT_ECUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  uint16_t* ac = reinterpret_cast<uint16_t*>(p);
+  uint16_t* wc = reinterpret_cast<uint16_t*>(p + round_up(size_t(M) * K * 2, 256));
+  float* sa = reinterpret_cast<float*>(p + round_up(size_t(M) * K * 2, 256) + round_up(size_t(N) * K * 2, 256));
+  if (cudaMemcpyAsync(ac, a, size_t(M) * K * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return DIT_ECUDA;
+  int rc = quant_rows_launch(ac, M, K, smooth, sa, st);
+  if (rc == DIT_OK) rc = codes_bf16_launch(q, wc, (long long)N * K, st);
+  if (rc != DIT_OK) return rc;
+  GemmParams g = base_params(M, N, K, err);
+  g.out = out;
+  g.ldo = N;
+  g.a_scale = sa;
+  g.w_scale = scale;
+  return gemm_launch(ac, K, wc, nullptr, kEpiStoreF32, g, st);
 }
 
 int dit_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt, int L, float* img, int N,

@@ -393,6 +393,128 @@ int wait_selftest_launch(int complete, int* err, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
+// ----------------------------------------------------------------------------------------------
+// W8A8 quantisers (klein article, section 5 and its D4/D5 entries): symmetric absmax / 127 codes,
+// per token for activations (x / smooth first) and per output channel for weights (w * smooth,
+// the SmoothQuant fold, first). Every decision in float32 with IEEE division (__fdiv_rn) and
+// round-half-to-even (rintf), the codes clipped to [-127, 127]; a row of zeros has scale 0, codes 0.
+// ----------------------------------------------------------------------------------------------
+__device__ __forceinline__ float block_max(float v, float* part) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) m = fmaxf(m, part[i]);
+  return m;
+}
+
+__device__ __forceinline__ float w8a8_code(float v, float scale) {
+  if (scale == 0.f) return 0.f;
+  return fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(v, scale))));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// One CTA per row of x [rows, K] bf16 (K a multiple of 8): codes written over x as bf16 (exact small
+// integers: the bf16 MMA then multiplies them exactly), the row's scale to scale[row]. Two passes
+// over the row (it is re-read from L2 after the maximum).
+__global__ void __launch_bounds__(kNormThreads) quant_rows_kernel(uint16_t* x, int K, const float* smooth,
+                                                                  float* scale) {
+  __shared__ float part[kNormThreads / 32];
+  uint4* row = reinterpret_cast<uint4*>(x + size_t(blockIdx.x) * K);
+  const int n8 = K / 8;
+  float m = 0.f;
+  for (int i = threadIdx.x; i < n8; i += kNormThreads) {
+    const uint4 u = row[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+      if (smooth) {
+        a = __fdiv_rn(a, __ldg(smooth + 8 * i + 2 * j));
+        b = __fdiv_rn(b, __ldg(smooth + 8 * i + 2 * j + 1));
+      }
+      m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
+    }
+  }
+  const float sc = __fdiv_rn(block_max(m, part), 127.f);
+  for (int i = threadIdx.x; i < n8; i += kNormThreads) {
+    const uint4 u = row[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+      if (smooth) {
+        a = __fdiv_rn(a, __ldg(smooth + 8 * i + 2 * j));
+        b = __fdiv_rn(b, __ldg(smooth + 8 * i + 2 * j + 1));
+      }
+      o[j] = pack_bf16x2(w8a8_code(a, sc), w8a8_code(b, sc));  // integers up to 127: exact in bf16
+    }
+    row[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) scale[blockIdx.x] = sc;
+}
+
+// One CTA per output channel of w [N, K] bf16: codes int8 [N, K], scale[n] (smooth folded first).
+__global__ void __launch_bounds__(kNormThreads) quant_weight_kernel(const uint16_t* w, int K, const float* smooth,
+                                                                    int8_t* q, float* scale) {
+  __shared__ float part[kNormThreads / 32];
+  const uint16_t* row = w + size_t(blockIdx.x) * K;
+  auto val = [&](int k) {
+    const float v = __uint_as_float(uint32_t(row[k]) << 16);
+    return smooth ? __fmul_rn(v, __ldg(smooth + k)) : v;
+  };
+  float m = 0.f;
+  for (int k = threadIdx.x; k < K; k += kNormThreads) m = fmaxf(m, fabsf(val(k)));
+  const float sc = __fdiv_rn(block_max(m, part), 127.f);
+  for (int k = threadIdx.x; k < K; k += kNormThreads) q[size_t(blockIdx.x) * K + k] = int8_t(w8a8_code(val(k), sc));
+  if (threadIdx.x == 0) scale[blockIdx.x] = sc;
+}
+
+// int8 codes -> the same integers in bf16, 16 per thread step.
+__global__ void codes_bf16_kernel(const int8_t* q, uint16_t* w, long long n16) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
+    const uint4 u = reinterpret_cast<const uint4*>(q)[i];
+    const uint32_t b[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int8_t* c = reinterpret_cast<const int8_t*>(&b[j]);
+      o[2 * j] = pack_bf16x2(float(c[0]), float(c[1]));
+      o[2 * j + 1] = pack_bf16x2(float(c[2]), float(c[3]));
+    }
+    uint4* dst = reinterpret_cast<uint4*>(w) + 2 * i;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+int quant_rows_launch(uint16_t* x, int rows, int K, const float* smooth, float* scale, cudaStream_t stream) {
+  if (rows <= 0) return DIT_OK;
+  if (K % 8 != 0) return DIT_EUNSUPPORTED;
+  quant_rows_kernel<<<rows, kNormThreads, 0, stream>>>(x, K, smooth, scale);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int quant_weight_launch(const uint16_t* w, int N, int K, const float* smooth, int8_t* q, float* scale,
+                        cudaStream_t stream) {
+  if (N <= 0 || K <= 0) return DIT_OK;
+  quant_weight_kernel<<<N, kNormThreads, 0, stream>>>(w, K, smooth, q, scale);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
+int codes_bf16_launch(const int8_t* q, uint16_t* w, long long n, cudaStream_t stream) {
+  if (n <= 0) return DIT_OK;
+  if (n % 16 != 0) return DIT_EUNSUPPORTED;
+  codes_bf16_kernel<<<grid_for(n / 16, 256), 256, 0, stream>>>(q, w, n / 16);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
 int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long long rows, long long cols,
                         cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return DIT_OK;

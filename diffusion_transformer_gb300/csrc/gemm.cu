@@ -798,6 +798,27 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
       const TileRows tr = tile_rows(p, Cfg::kTileM, mb);
       if (!mbar_wait_warp(smem_u32(&tfull[acc]), acc_phase, p.err, kErrTimeoutEpilogue)) break;
       tc_fence_after();
+      if constexpr (!B8) {
+        if (p.a_scale) {
+          // W8A8: the accumulator holds exact integer dot products of codes; scale it in place by
+          // the row's and the column's scales, then run the epilogue on it as usual
+          static_assert(Cfg::kEpiCols == BN, "one epilogue warp per TMEM lane quadrant");
+          const int row = tr.base + rows_of + quad * 32 + lane;
+          const float sa = row < tr.end ? __ldg(p.a_scale + row) : 0.f;
+          const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c * 32, v);
+            tmem_ld_wait();
+            const float* sw = p.w_scale + nb * BN + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sa * __ldg(sw + j));
+            tmem_st32(taddr + c * 32, v);
+          }
+          tmem_st_wait();
+        }
+      }
       if constexpr (EPI == kEpiGated && !B8) {
         if (w.part >= 0) {
           // K-split tile: publish this part, release the accumulator, and let the warp that

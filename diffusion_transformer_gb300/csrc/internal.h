@@ -68,6 +68,9 @@ struct GemmParams {
   int b_rows, b2_inner;
   // set by the launcher for CTA-pair launches: a launch counter that picks the start-word set
   uint32_t pair_epoch;
+  // W8A8 (both non-null): the accumulator is multiplied by a_scale[GEMM row] * w_scale[column]
+  // before the epilogue (per-token and per-output-channel scales of integer codes)
+  const float *a_scale, *w_scale;
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row
@@ -156,6 +159,12 @@ int sinusoid_launch(const float* sigmas, int steps, int dim, uint16_t* out, cuda
 int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t stream);
 int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long long rows, long long cols,
                         cudaStream_t stream);
+// W8A8: per-token codes of x [rows, K] bf16 written over x (as bf16 integers) with scale[rows];
+// per-output-channel codes of a bf16 weight [N, K] (int8) with scale[N]; int8 codes to bf16 (n % 16 == 0)
+int quant_rows_launch(uint16_t* x, int rows, int K, const float* smooth, float* scale, cudaStream_t stream);
+int quant_weight_launch(const uint16_t* w, int N, int K, const float* smooth, int8_t* q, float* scale,
+                        cudaStream_t stream);
+int codes_bf16_launch(const int8_t* q, uint16_t* w, long long n, cudaStream_t stream);
 
 int num_sms();
 

@@ -101,6 +101,22 @@ typedef struct {
   const float* k_norm;
 } dit_block_w8;
 
+/* W8A8 weights of one block [klein, section 5 (int8 detail) and its D4/D5 entries]: each linear
+ * (0 qkv, 1 out, 2 up, 3 down) as symmetric int8 codes q [out, in] with one fp32 scale per output
+ * channel, scale [out] (absmax / 127, as dit_w8a8_quantize_weight makes them), and an optional
+ * SmoothQuant divisor smooth [in] (NULL: none) that was folded into the weight before its
+ * quantisation and divides the activation before its per-token quantisation. Row orders and norm
+ * weights as in dit_block_w. */
+typedef struct {
+  const int8_t* q[4];
+  const float* scale[4];
+  const float* smooth[4];
+  const float* norm1;
+  const float* norm2;
+  const float* q_norm;
+  const float* k_norm;
+} dit_block_w8a8;
+
 /* Modulation rows [gizai:dit, Modulation and Sequence.map]: rows [M, 6, H] fp32 holding, for each
  * modulation row, shift_a, scale_a, gate_a (attention) then shift_m, scale_m, gate_m (MLP).
  * map [L + N] int32 gives each packed row's modulation row (0 <= map[r] < M); NULL means row 0. */
@@ -177,6 +193,39 @@ DIT_API int dit_block_forward_int8(const dit_dims* dims, const dit_block_w8* w, 
                            const float* txt_cos, const float* txt_sin, const float* img_cos,
                            const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
                            dit_stream_t stream);
+
+/* The block with W8A8 linears (an opt-in lossy tier on the pages [klein, section 5]): before each
+ * linear its activation (h, o, h2, a) is quantised per token, codes = clip(rint(v / s_r), -127, 127)
+ * with s_r = max |v / smooth| / 127 over the row (float32, IEEE division, ties to even; a zero row has
+ * scale 0), and the linear is the integer dot product of the codes times s_r times the weight's
+ * per-channel scale, then the linear's usual epilogue. The codes are multiplied exactly on the bf16
+ * tensor cores (integers up to 127 are bf16 values, their products fp32 values); the fp32
+ * accumulation is exact while every partial sum stays below 2^24 in magnitude. The int8 weight codes
+ * are widened to bf16 on a library-owned second stream one linear ahead (as in
+ * dit_block_forward_int8). Workspace: dit_workspace_bytes(dims, L, N, 4). Errors as
+ * dit_block_forward. */
+DIT_API int dit_block_forward_w8a8(const dit_dims* dims, const dit_block_w8a8* w, float* txt, int L, float* img,
+                                   int N, const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                   const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                   dit_stream_t stream);
+
+/* W8A8 weight quantisation [klein, D4 quantize_weight, D5 quantize_weight_smooth]: w bf16 [N, K]
+ * (rows = output channels), smooth [K] fp32 or NULL: w' = fp32(w * smooth) (the fold), scale[n] =
+ * max_k |w'[n, k]| / 127, q = clip(rint(w' / scale), -127, 127) int8 [N, K] (float32 decisions as in
+ * dit_block_forward_w8a8). */
+DIT_API int dit_w8a8_quantize_weight(const uint16_t* w, int N, int K, const float* smooth, int8_t* q, float* scale,
+                                     dit_stream_t stream);
+
+/* Per-token quantisation in place [klein, D4 quantize_rows]: x bf16 [R, K] (K % 8 == 0, 16-byte
+ * aligned) is replaced by its codes (as bf16 integers), scale [R] fp32 receives the row scales. */
+DIT_API int dit_w8a8_quantize_rows(uint16_t* x, int R, int K, const float* smooth, float* scale, dit_stream_t stream);
+
+/* One W8A8 linear, fp32 out [M, N] = codes(a) codes(W)^T * s_a[row] * scale[col] (a bf16 [M, K] is not
+ * modified; its codes go to the workspace). K and N multiples of 64.
+ * Workspace: dit_linear_w8a8_workspace_bytes(M, N, K), 256-byte aligned. */
+DIT_API int dit_linear_w8a8(const uint16_t* a, int M, int K, const int8_t* q, const float* scale, const float* smooth,
+                            int N, float* out, void* ws, size_t ws_bytes, dit_stream_t stream);
+DIT_API size_t dit_linear_w8a8_workspace_bytes(int M, int N, int K);
 
 /* The parallel (single-stream) block [gizai:dit, Block.parallel]: x + gate * (attention + SwiGLU
  * MLP), both branches reading one modulated LayerNorm of x:
@@ -256,7 +305,7 @@ DIT_API int dit_denoise(const dit_model* model, float* img_tokens, int N, const 
                 const float* img_cos, const float* img_sin, void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block, 2 = parallel block, 3 = double-stream
- * block. Returns 0 for unsupported dims. */
+ * block, 4 = W8A8 block. Returns 0 for unsupported dims. */
 DIT_API size_t dit_workspace_bytes(const dit_dims* dims, int L, int N, int variant);
 DIT_API size_t dit_denoise_workspace_bytes(const dit_model* model, int L, int N, int steps);
 
