@@ -24,11 +24,12 @@
 // score lies in [-B, B], B = d max|w_q| max|w_k| scale (log2 units, with a margin for the bf16
 // rounding). For B below 60 the softmax subtracts m = B throughout: the weights exp2(s - B) lie in
 // [2^-120, 1], normal in fp32 and bf16, the same relative rounding as with a running max, and no row
-// max is needed. Then no thread needs a whole row, and all eight softmax warps work on each query
-// tile in turn, warp (quadrant, half) taking 32 rows and 64 of the 128 keys: two warps per SM
-// sub-partition share every softmax, so its latency halves and the next S no longer waits on it.
-// P of key half h goes to columns [64 h, 64 h + 32) of the tile's S region (inside what that warp
-// has consumed), and the P V MMA reads it from there.
+// max is needed. Then no thread needs a whole row, and all the softmax warps work on each query
+// tile in turn, warp (quadrant, part) taking 32 rows and 128 / parts of the keys (two parts and
+// eight warps, or four parts and sixteen warps in the fixed kernel at d = 128): several warps per SM
+// sub-partition share every softmax, so its latency drops and the next S no longer waits on it.
+// P of key part p goes to the first half of that part's own S columns (inside what that warp has
+// consumed), and the P V MMA reads it from there.
 // V arrives transposed ([d, keys]) from the QKV epilogue so the P V MMA takes a K-major B operand.
 #include <cuda.h>
 #include <cuda_bf16.h>

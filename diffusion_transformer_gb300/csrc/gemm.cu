@@ -7,8 +7,13 @@
 // warp 1 issues tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators; warps 2-5 drain
 // the other accumulator through the epilogue, so a tile's epilogue overlaps the next tile's
 // mainloop. For int8lin weights (B8 = true) warps 6-9 convert each int8 k-block of B with its bf16
-// block-32 scales (both brought in by TMA) into the bf16 swizzled tile the MMA reads: w = bf16_rne(q * s) (the host
-// contract's int8lin scheme, section 1) - the dequantisation sits inside the mainloop.
+// block-32 scales (both brought in by TMA) into the bf16 swizzled tile the MMA reads:
+// w = bf16_rne(q * s) (the host contract's int8lin scheme, section 1), inside the mainloop.
+// PAIR = true: two CTAs of a cluster on two SMs share one 256 x BN tile (each brings its 128 rows
+// of A and BN/2 rows of B; the first issues cta_group::2 MMAs over both), so a k-block costs each SM
+// a third less shared-memory fill; every cross-CTA wait is a bounded mbarrier wait (see below).
+// W8A8 (a_scale / w_scale set): the accumulator, an exact integer dot product of codes, is scaled
+// in TMEM by the row's and the column's scales before the epilogue.
 //
 // Epilogues (the gizai:dit reference's linearInto / gatedInto / gluRows / prepOf):
 //   kEpiStoreF32 / kEpiStoreBF16 / kEpiSiluBF16   plain stores
@@ -16,6 +21,7 @@
 //   kEpiSwiGLU  a_j = silu(acc_2j) * acc_2j+1      (up linear, interleaved rows)
 //   kEpiQKV     per-head RMS norm * weight, rotary pairs (2i, 2i+1), head-major q/k stores and a
 //               transposed v store for the attention kernel (klein article, section 4.4)
+//   kEpiQKVSwiGLU  kEpiQKV on the columns below n_split, kEpiSwiGLU above (the parallel block)
 #include <atomic>
 
 #include <cuda.h>
