@@ -4,12 +4,13 @@ Workload (a "step"): one whole block forward - modulated norm, QKV linear with Q
 epilogue, joint attention, out linear with gated residual, second modulated norm, SwiGLU up
 linear, down linear with gated residual - at the 1024^2 shape: hidden 3072, 24 heads x 128,
 ffn 12288, L = 128 text + N = 4096 image rows (R = 4224), bf16 weights, per-row modulation.
-The same run also times the int8lin block (the same shape), the parallel single-stream block (the
-same shape and FLOP count: one modulated LayerNorm feeding attention and the MLP, 4 launches), the
-double-stream block (the same shape, text and image rows with their own weights, 7 launches), the
-block with split-halves rotary, with rank-64 LoRA adapters, with sandwich post-norms and with W8A8
-linears (per-token int8 activations, per-channel int8 weights), and the 32-block, 4-step denoise
-loop (L = 512, N = 4096), and reports them as sub-objects.
+The same run also times the int8lin block (the same shape; also in its parallel and double-stream
+forms), the parallel single-stream block (the same shape and FLOP count: one modulated LayerNorm
+feeding attention and the MLP, 4 launches), the double-stream block (the same shape, text and image
+rows with their own weights, 7 launches), the block with split-halves rotary, with rank-64 LoRA
+adapters, with sandwich post-norms and with W8A8 linears (per-token int8 activations, per-channel
+int8 weights), and the 32-block, 4-step denoise loop (L = 512, N = 4096), and reports them as
+sub-objects.
 
 Metric: block TFLOP/s (algorithmic FLOP = 2R(3H^2 + H^2 + 2HF + FH) + 4R^2 H per block) and
 ms per block. Inputs are larger than L2 (302 MB of weights per block), so no flush is needed.
@@ -438,7 +439,9 @@ def run_ours(args):
     if not args.no_int8:
         del st
         inp8 = DI.int8_block_inputs("1024sq_int8")
+        sh8 = inp8.shape
         st8 = _block_setup(torch, D, inp8, int8=True)
+        del inp8
         ms8 = _time_blocks(torch, st8, lambda t, i: _block_call(D, st8, True, t, i), args.steps, args.warmup,
                            dist) / args.steps
         D.dit_check()
@@ -458,6 +461,38 @@ def run_ours(args):
                 "frac_of_peak": tf8 / peaks["bf16_tflops"], "dequant": deq,
                 "path": "rows > 512: each linear's weight dequantised once per call (HBM-bound kernel), then "
                         "the bf16 tcgen05 mainloop; rows <= 512: dequantised inside the GEMM mainloop"}
+        # the int8lin parallel block (the same int8 weights, its own [M, 3, H] modulation rows) and the
+        # int8lin double-stream block (text rows with their own int8 weights)
+        if not args.no_parallel:
+            inpP8 = DI.int8_parallel_block_inputs("1024sq_int8")
+            modP8 = D.Modulation(_dev(torch, inpP8.mod), _dev(torch, inpP8.mod_map))
+            del inpP8
+            wsP8 = torch.empty(D.dit_workspace_bytes(st8["dims"], sh.L, sh.N, 5), dtype=torch.uint8, device="cuda")
+            callP8 = lambda t, i: D.dit_parallel_block_forward_int8(st8["dims"], st8["w"], t, i, st8["tc"], st8["ts"],
+                                                                    st8["ic"], st8["is_"], modP8, wsP8)
+            msP8 = _time_blocks(torch, st8, callP8, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            tfP8 = flops / (msP8 * 1e-3) / 1e12
+            int8["parallel_block"] = {"ms_per_block": msP8, "tflops": tfP8, "frac_of_peak": tfP8 / peaks["bf16_tflops"],
+                                      "path": "[Wqkv ; Wup] and [Wout | Wdown] dequantised once per call on a second "
+                                              "stream, then the bf16 parallel block's 4 launches"}
+            del modP8, wsP8
+        if not args.no_double:
+            inpT8 = DI.int8_block_inputs("1024sq_int8", seed=sh8.seed + 50)
+            wT8 = D.Int8BlockWeights([_dev(torch, q) for q in inpT8.q8], [_dev_bf16(torch, s) for s in inpT8.s8])
+            del inpT8
+            wsD8 = torch.empty(D.dit_workspace_bytes(st8["dims"], sh.L, sh.N, 6), dtype=torch.uint8, device="cuda")
+            callD8 = lambda t, i: D.dit_double_block_forward_int8(st8["dims"], wT8, st8["w"], t, i, st8["tc"],
+                                                                  st8["ts"], st8["ic"], st8["is_"], st8["mod"], wsD8)
+            msD8 = _time_blocks(torch, st8, callD8, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            tfD8 = flops / (msD8 * 1e-3) / 1e12
+            int8["double_stream_block"] = {"ms_per_block": msD8, "tflops": tfD8,
+                                           "frac_of_peak": tfD8 / peaks["bf16_tflops"],
+                                           "path": "each linear's text and image weights dequantised once per call "
+                                                   "on a second stream, one linear ahead, then the bf16 double-stream "
+                                                   "block's 7 launches"}
+            del wT8, wsD8
         del st8
         st = _block_setup(torch, D, inp)
 

@@ -16,6 +16,7 @@ from typing import List, Optional, Sequence
 __all__ = [
     "DitError", "lib", "library_path", "DitDims", "BlockWeights", "Int8BlockWeights", "Modulation",
     "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_parallel_block_forward",
+    "dit_parallel_block_forward_int8", "dit_double_block_forward_int8",
     "W8A8BlockWeights", "dit_block_forward_w8a8", "dit_w8a8_quantize_weight", "dit_w8a8_quantize_rows",
     "dit_linear_w8a8", "dit_linear_w8a8_workspace_bytes",
     "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA",
@@ -95,6 +96,12 @@ _SIGNATURES = {
     "dit_block_forward_int8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8), c_void_p, c_int, c_void_p, c_int,
                                        c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                        c_size_t, c_void_p]),
+    "dit_parallel_block_forward_int8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8), c_void_p, c_int, c_void_p,
+                                                c_int, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod),
+                                                c_void_p, c_size_t, c_void_p]),
+    "dit_double_block_forward_int8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8), POINTER(dit_block_w8),
+                                              c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
+                                              c_void_p, POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
     "dit_block_forward_w8a8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8a8), c_void_p, c_int, c_void_p, c_int,
                                        c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                        c_size_t, c_void_p]),
@@ -374,6 +381,34 @@ def dit_double_block_forward(dims: DitDims, w_txt: Optional[BlockWeights], w_img
                                        _ptr(img_sin, f32), ctypes.byref(mod.c), _ptr(ws, None, "ws"),
                                        ws.numel() * ws.element_size(), _stream(stream)),
         "dit_double_block_forward")
+
+
+def dit_parallel_block_forward_int8(dims: DitDims, w: Int8BlockWeights, txt, img, txt_cos, txt_sin, img_cos,
+                                    img_sin, mod: Modulation, ws, stream=None):
+    """The parallel block with int8lin weights; mod rows are [M, 3, H] (shift, scale, gate)."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_parallel_block_forward_int8(ctypes.byref(dims.c), ctypes.byref(w.c), _ptr(txt, f32, "txt"), L,
+                                              _ptr(img, f32, "img"), img.shape[0], _ptr(txt_cos, f32),
+                                              _ptr(txt_sin, f32), _ptr(img_cos, f32), _ptr(img_sin, f32),
+                                              ctypes.byref(mod.c), _ptr(ws, None, "ws"),
+                                              ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_parallel_block_forward_int8")
+
+
+def dit_double_block_forward_int8(dims: DitDims, w_txt: Optional[Int8BlockWeights], w_img: Int8BlockWeights, txt,
+                                  img, txt_cos, txt_sin, img_cos, img_sin, mod: Modulation, ws, stream=None):
+    """The double-stream block with int8lin weights: text rows use w_txt, image rows w_img."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_double_block_forward_int8(ctypes.byref(dims.c), None if w_txt is None else ctypes.byref(w_txt.c),
+                                            ctypes.byref(w_img.c), _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"),
+                                            img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                                            _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
+                                            _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_double_block_forward_int8")
 
 
 def dit_block_forward_noalloc(dims: DitDims, w: BlockWeights, txt, img, txt_cos, txt_sin, img_cos, img_sin,

@@ -100,6 +100,15 @@ size_t int8_slot_bytes(const dit_dims* d) {
   return tl;
 }
 size_t int8_scratch_bytes(const dit_dims* d) { return 2 * int8_slot_bytes(d); }
+// int8lin parallel block: slot 0 = [Wqkv ; Wup] [3H + 2F, H], slot 1 = Wout [H, H] then Wdown [H, F]
+size_t int8_parallel_slot0_bytes(const dit_dims* d) {
+  return gemm_int8_scratch_bytes(3 * d->hidden + 2 * d->ffn, d->hidden);
+}
+size_t int8_parallel_scratch_bytes(const dit_dims* d) {
+  return int8_parallel_slot0_bytes(d) + gemm_int8_scratch_bytes(d->hidden, d->hidden + d->ffn);
+}
+// int8lin double-stream block: two slots, each one linear's text weight followed by its image weight
+size_t int8_double_scratch_bytes(const dit_dims* d) { return 4 * int8_slot_bytes(d); }
 
 // Per device: a second stream and events for the int8lin block's weight dequantisation, which runs
 // beside the block's kernels (fork from and join to the caller's stream through events). The mutex
@@ -124,17 +133,17 @@ SideStream* side_stream() {
   return ss.ok ? &ss : nullptr;
 }
 
-// The weights of a block's four linears prepared (dequantised, or widened from int8 codes) on the
-// side stream one linear ahead of their use, into two alternating workspace slots: linear i goes to
-// slot i % 2; linears 0 and 1 start at the fork, 2 once linear 0's GEMM has released slot 0, 3 once
-// linear 1's GEMM has released slot 1. Events: 0 fork, 1-4 weight i ready, 5-6 slot 0 / 1 free,
-// 7 the join that every exit makes (the caller's stream then waits for all side work).
+// The weights of a block's n <= 4 GEMMs prepared (dequantised, or widened from int8 codes) on the
+// side stream one GEMM ahead of their use, into two alternating workspace slots: weight i goes to
+// slot i % 2; weights 0 and 1 start at the fork, 2 once GEMM 0 has released slot 0, 3 once GEMM 1
+// has released slot 1. Events: 0 fork, 1-4 weight i ready, 5-6 slot 0 / 1 free, 7 the join that
+// every exit makes (the caller's stream then waits for all side work).
 class WeightPrefetch {
  public:
   // prep(i, dst, stream) launches the preparation of linear i's weight into dst
   using Prep = int (*)(const void* ctx, int i, uint16_t* dst, cudaStream_t stream);
-  WeightPrefetch(cudaStream_t st, uint16_t* slot0, size_t slot_bytes, Prep prep, const void* ctx)
-      : st_(st), prep_(prep), ctx_(ctx) {
+  WeightPrefetch(cudaStream_t st, uint16_t* slot0, size_t slot_bytes, Prep prep, const void* ctx, int n = 4)
+      : st_(st), prep_(prep), ctx_(ctx), n_(n) {
     slot_[0] = slot0;
     slot_[1] = slot0 ? reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(slot0) + slot_bytes) : nullptr;
   }
@@ -148,7 +157,7 @@ class WeightPrefetch {
     lock_ = std::unique_lock<std::mutex>(side_->mu);
     if (cudaEventRecord(side_->ev[0], st_) != cudaSuccess) return DIT_ECUDA;
     int r = ahead(0, 0);
-    return r == DIT_OK ? ahead(1, -1) : r;
+    return r == DIT_OK && n_ > 1 ? ahead(1, -1) : r;
   }
   // the weight of linear i, ready for a launch on the caller's stream
   int use(int i, const uint16_t** w) {
@@ -156,10 +165,11 @@ class WeightPrefetch {
     *w = slot_[i % 2];
     return DIT_OK;
   }
-  // after linear i's GEMM: its slot is free, and linear i + 2 (if any) may be prepared into it
+  // after GEMM i: its slot is free, and weight i + 2 (if any) may be prepared into it
   int done(int i) {
+    if (i + 2 >= n_) return DIT_OK;
     if (cudaEventRecord(side_->ev[5 + i % 2], st_) != cudaSuccess) return DIT_ECUDA;
-    return i + 2 < 4 ? ahead(i + 2, 5 + i % 2) : DIT_OK;
+    return ahead(i + 2, 5 + i % 2);
   }
 
  private:
@@ -172,6 +182,7 @@ class WeightPrefetch {
   cudaStream_t st_;
   Prep prep_;
   const void* ctx_;
+  int n_;
   uint16_t* slot_[2];
   SideStream* side_ = nullptr;
   std::unique_lock<std::mutex> lock_;
@@ -448,32 +459,65 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
 // The parallel (single-stream) block [gizai:dit, Block.parallel]: one modulated LayerNorm feeds
 // both branches; mod rows [M, 3, H] = shift, scale, gate. Four launches: the norm, one GEMM over
 // [Wqkv ; Wup] with the QKV epilogue on its first 3H columns and SwiGLU on the rest, the attention,
-// and one GEMM over [o | a] [Wout | Wdown]^T with the gated residual.
-int run_parallel_block(const dit_dims* d, const dit_block_w* w, float* txt, int L, float* img, int N,
-                       const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod,
+// and one GEMM over [o | a] [Wout | Wdown]^T with the gated residual. `w8` selects the int8lin
+// weights: on the side stream, [Wqkv ; Wup] is dequantised into one scratch slot (overlapping the
+// norm) and Wout, Wdown into a second (overlapping the first GEMM and the attention), whatever the
+// row count; the GEMMs are then the bf16 ones on the slots.
+int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, float* txt, int L, float* img,
+                       int N, const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod,
                        void* ws, cudaStream_t st) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
   const BlockWs b = carve_block_ws(d, R, ws);
+  struct DequantCtx {
+    const dit_dims* d;
+    const dit_block_w8* w8;
+  } dctx{d, w8};
+  // weight 0: Wqkv then Wup (rows 3H on); weight 1: Wout then Wdown (at H * H)
+  auto dequant = [](const void* c, int i, uint16_t* dst, cudaStream_t s2) -> int {
+    const DequantCtx* x = static_cast<const DequantCtx*>(c);
+    const int H_ = x->d->hidden;
+    const int first = i == 0 ? 0 : 1, second = i == 0 ? 2 : 3;
+    int n, k;
+    linear_shape(x->d, first, &n, &k);
+    int r = dequant_int8_launch(x->w8->q[first], x->w8->s[first], dst, n, k, s2);
+    if (r != DIT_OK) return r;
+    uint16_t* dst2 = dst + (i == 0 ? size_t(3) * H_ * H_ : size_t(H_) * H_);
+    linear_shape(x->d, second, &n, &k);
+    return dequant_int8_launch(x->w8->q[second], x->w8->s[second], dst2, n, k, s2);
+  };
+  uint16_t* slots = w8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
+  WeightPrefetch pf(st, slots, w8 ? int8_parallel_slot0_bytes(d) : 0, dequant, &dctx, 2);
   int rc;
+  if (w8 && (rc = pf.start()) != DIT_OK) return rc;
+  const float* norm = w8 ? w8->norm1 : w->norm1;
+  const float* qn = w8 ? w8->q_norm : w->q_norm;
+  const float* kn = w8 ? w8->k_norm : w->k_norm;
+  const uint16_t *wqkv = w8 ? nullptr : w->wqkv, *wup = w8 ? nullptr : w->wup;
+  const uint16_t *wout = w8 ? nullptr : w->wout, *wdown = w8 ? nullptr : w->wdown;
 
   // 1. h = LayerNorm(x) * norm * (1 + scale) + shift
-  ModNormParams mp{txt, img, L, R, H, H, H, w->norm1, mod.rows, mod.rows + H, 3LL * H, mod.map, d->eps, b.h};
+  ModNormParams mp{txt, img, L, R, H, H, H, norm, mod.rows, mod.rows + H, 3LL * H, mod.map, d->eps, b.h};
   mp.layernorm = 1;
   if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
 
   // 2. q, k, vt (QK-norm + rope epilogue) and a (SwiGLU epilogue) from h [Wqkv ; Wup]^T
-  GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, w->q_norm, w->k_norm, err);
+  GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, qn, kn, err);
   g.N = 3 * H + 2 * F;
   g.out = b.a;
   g.ldo = F;
   g.n_split = 3 * H;
-  if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, w->wqkv, H, w->wup, H, kEpiQKVSwiGLU, g, st)) != DIT_OK) return rc;
+  if (w8) {
+    const uint16_t* s0;
+    if ((rc = pf.use(0, &s0)) != DIT_OK) return rc;
+    wqkv = s0;
+    wup = s0 + size_t(3) * H * H;
+  }
+  if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wqkv, H, wup, H, kEpiQKVSwiGLU, g, st)) != DIT_OK) return rc;
 
   // 3. o = attention(q, k, v); q and k rows QK-normed
-  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, w->q_norm, w->k_norm, nullptr,
-                nullptr};
+  AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, qn, kn, nullptr, nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
 
   // 4. x += gate * ([o | a] [Wout | Wdown]^T)
@@ -488,20 +532,74 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, float* txt, int 
   // scratch for the K-split of the last wave: h, q, k and vt, all consumed by now
   g.split_ws = b.h;
   g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.o) - reinterpret_cast<uint8_t*>(b.h));
-  return gemm_launch_cat(b.o, H, b.a, F, w->wout, H, w->wdown, F, kEpiGated, g, st);
+  if (w8) {
+    const uint16_t* s1;
+    if ((rc = pf.use(1, &s1)) != DIT_OK) return rc;
+    wout = s1;
+    wdown = s1 + size_t(H) * H;
+  }
+  return gemm_launch_cat(b.o, H, b.a, F, wout, H, wdown, F, kEpiGated, g, st);
 }
 
 // The double-stream block: the sequential block in which text rows [0, L) and image rows [L, R)
 // each use their own linears and norm weights; the attention runs once over all R rows. Each
 // stream's norms and GEMMs are launched over its own rows (row_off = its first sequence row), so any
-// L works; the modulation map gives each stream its own modulation rows.
-int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w* wi, float* txt, int L, float* img,
-                     int N, const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod,
-                     void* ws, cudaStream_t st) {
+// L works; the modulation map gives each stream its own modulation rows. `w8t`, `w8i` select the
+// int8lin weights: linear i's text and image weights are dequantised on the side stream into one
+// scratch slot (text first, none when L = 0), one linear ahead of their GEMM, whatever the row count.
+int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w* wi, const dit_block_w8* w8t,
+                     const dit_block_w8* w8i, float* txt, int L, float* img, int N, const float* tc, const float* ts,
+                     const float* ic, const float* is, const ModRef& mod, void* ws, cudaStream_t st) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
   const BlockWs b = carve_block_ws(d, R, ws);
+  // int8lin: the weights each GEMM reads live in the prefetch slots; tw8 / iw8 point at them, linear
+  // by linear, once the side stream has written them
+  struct DequantCtx {
+    const dit_dims* d;
+    const dit_block_w8* t;
+    const dit_block_w8* i;
+    int L;
+  } dctx{d, w8t, w8i, L};
+  auto dequant = [](const void* c, int i, uint16_t* dst, cudaStream_t s2) -> int {
+    const DequantCtx* x = static_cast<const DequantCtx*>(c);
+    int n, k;
+    linear_shape(x->d, i, &n, &k);
+    if (x->L > 0) {
+      int r = dequant_int8_launch(x->t->q[i], x->t->s[i], dst, n, k, s2);
+      if (r != DIT_OK) return r;
+      dst += size_t(n) * k;
+    }
+    return dequant_int8_launch(x->i->q[i], x->i->s[i], dst, n, k, s2);
+  };
+  const bool q8 = w8i != nullptr;
+  uint16_t* slots = q8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
+  WeightPrefetch pf(st, slots, q8 ? 2 * int8_slot_bytes(d) : 0, dequant, &dctx);
+  dit_block_w tw8{}, iw8{};
+  if (q8) {
+    if (L > 0) tw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, w8t->norm1, w8t->norm2, w8t->q_norm, w8t->k_norm};
+    iw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, w8i->norm1, w8i->norm2, w8i->q_norm, w8i->k_norm};
+    wt = &tw8;
+    wi = &iw8;
+    const int r = pf.start();
+    if (r != DIT_OK) return r;
+  }
+  // before linear i's GEMMs: its weights ready on the caller's stream; after them: the slot released
+  auto before = [&](int i) -> int {
+    if (!q8) return DIT_OK;
+    const uint16_t* slot;
+    const int r = pf.use(i, &slot);
+    int n, k;
+    linear_shape(d, i, &n, &k);
+    const uint16_t* img_w = L > 0 ? slot + size_t(n) * k : slot;
+    const uint16_t** ft[4] = {&tw8.wqkv, &tw8.wout, &tw8.wup, &tw8.wdown};
+    const uint16_t** fi[4] = {&iw8.wqkv, &iw8.wout, &iw8.wup, &iw8.wdown};
+    *ft[i] = L > 0 ? slot : nullptr;
+    *fi[i] = img_w;
+    return r;
+  };
+  auto after = [&](int i) -> int { return q8 ? pf.done(i) : DIT_OK; };
   struct Stream {
     const dit_block_w* w;
     int r0, n;
@@ -544,7 +642,9 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.q_norm2 = wi->q_norm;
     g.k_norm2 = wi->k_norm;
     g.m_split = L;
+    if ((rc = before(0)) != DIT_OK) return rc;
     if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wqkv, H, wi->wqkv, H, kEpiQKV, g, st)) != DIT_OK) return rc;
+    if ((rc = after(0)) != DIT_OK) return rc;
     AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 2, wt->q_norm, wt->k_norm,
                   wi->q_norm, wi->k_norm};
     if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
@@ -552,17 +652,22 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.m_split = L;
     g.split_ws = b.a;
     g.split_ws_bytes = size_t(R) * F * 2;
+    if ((rc = before(1)) != DIT_OK) return rc;
     if ((rc = gemm_launch_cat(b.o, H, nullptr, 0, wt->wout, H, wi->wout, H, kEpiGated, g, st)) != DIT_OK) return rc;
+    if ((rc = after(1)) != DIT_OK) return rc;
     if ((rc = norm_all(wt->norm2, wi->norm2, 3)) != DIT_OK) return rc;
     g = base_params(R, 2 * F, H, err);
     g.out = b.a;
     g.ldo = F;
     g.m_split = L;
+    if ((rc = before(2)) != DIT_OK) return rc;
     if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wup, H, wi->wup, H, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
+    if ((rc = after(2)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, F, 5);
     g.m_split = L;
     g.split_ws = b.h;
     g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
+    if ((rc = before(3)) != DIT_OK) return rc;
     return gemm_launch_cat(b.a, F, nullptr, 0, wt->wdown, F, wi->wdown, F, kEpiGated, g, st);
   }
 
@@ -570,6 +675,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   for (const Stream& s : S)
     if (s.n > 0 && (rc = norm(s, s.w->norm1, 0)) != DIT_OK) return rc;
   // 2. q, k, vt per stream (its own Wqkv and q/k norm weights) into the joint layouts
+  if ((rc = before(0)) != DIT_OK) return rc;
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = qkv_params(d, s.n, R, L, b, tc, ts, ic, is, s.w->q_norm, s.w->k_norm, err);
@@ -577,6 +683,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.R_total = R;
     if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wqkv, nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
   }
+  if ((rc = after(0)) != DIT_OK) return rc;
   // 3. o = attention over all rows (q and k QK-normed with the weights of the streams that have rows)
   const Stream* s0 = S[0].n > 0 ? &S[0] : &S[1];
   const Stream* s1 = (S[0].n > 0 && S[1].n > 0) ? &S[1] : nullptr;
@@ -584,6 +691,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
                 s0->w->k_norm, s1 ? s1->w->q_norm : nullptr, s1 ? s1->w->k_norm : nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
   // 4. x += gate_a * (o Wout^T), per stream (K-split scratch: the SwiGLU buffer, not yet written)
+  if ((rc = before(1)) != DIT_OK) return rc;
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, H, 2);
@@ -591,10 +699,12 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.split_ws_bytes = size_t(R) * F * 2;
     if ((rc = gemm_launch(b.o + size_t(s.r0) * H, H, s.w->wout, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
   }
+  if ((rc = after(1)) != DIT_OK) return rc;
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m), per stream
   for (const Stream& s : S)
     if (s.n > 0 && (rc = norm(s, s.w->norm2, 3)) != DIT_OK) return rc;
   // 6. a = SwiGLU(h2 Wup^T), per stream
+  if ((rc = before(2)) != DIT_OK) return rc;
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = base_params(s.n, 2 * F, H, err);
@@ -602,7 +712,9 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.ldo = F;
     if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wup, nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
   }
+  if ((rc = after(2)) != DIT_OK) return rc;
   // 7. x += gate_m * (a Wdown^T), per stream (K-split scratch: h, q, k, vt and o, consumed by now)
+  if ((rc = before(3)) != DIT_OK) return rc;
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, F, 5);
@@ -692,10 +804,12 @@ const char* dit_status_string(int s) {
 }
 
 size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
-  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 4) return 0;
+  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 6) return 0;
   size_t bytes = carve_block_ws(d, L + N, nullptr).bytes;
   if (variant == 1) bytes += int8_scratch_bytes(d);
   if (variant == 4) bytes += w8a8_extra_bytes(d, L + N);
+  if (variant == 5) bytes += int8_parallel_scratch_bytes(d);
+  if (variant == 6) bytes += int8_double_scratch_bytes(d);
   return bytes;
 }
 
@@ -740,7 +854,7 @@ int dit_parallel_block_forward(const dit_dims* d, const dit_block_w* w, float* t
   if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
   if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
   if (d->hidden % 256 != 0 || d->ffn % 128 != 0) return DIT_EUNSUPPORTED;  // 256-wide tiles over 3H and 2F
-  return run_parallel_block(d, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+  return run_parallel_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -754,8 +868,38 @@ int dit_double_block_forward(const dit_dims* d, const dit_block_w* w_txt, const 
     if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
     if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
   }
-  return run_double_block(d, w_txt, w_img, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
-                          reinterpret_cast<cudaStream_t>(stream));
+  return run_double_block(d, w_txt, w_img, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
+                          ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_parallel_block_forward_int8(const dit_dims* d, const dit_block_w8* w, float* txt, int L, float* img, int N,
+                                    const float* tc, const float* ts, const float* ic, const float* is,
+                                    const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 5);
+  if (rc != DIT_OK) return rc;
+  if (!w) return DIT_EINVAL;
+  if (d->hidden % 256 != 0 || d->ffn % 256 != 0) return DIT_EUNSUPPORTED;
+  for (int i = 0; i < 4; ++i)
+    if (!w->q[i] || !w->s[i] || !al16(w->q[i]) || !al16(w->s[i])) return DIT_EINVAL;
+  return run_parallel_block(d, nullptr, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_double_block_forward_int8(const dit_dims* d, const dit_block_w8* w_txt, const dit_block_w8* w_img, float* txt,
+                                  int L, float* img, int N, const float* tc, const float* ts, const float* ic,
+                                  const float* is, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                  dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 6);
+  if (rc != DIT_OK) return rc;
+  if (d->hidden % 256 != 0 || d->ffn % 256 != 0) return DIT_EUNSUPPORTED;
+  for (const dit_block_w8* w : {w_txt, w_img}) {
+    if (w == w_txt && L == 0) continue;
+    if (!w) return DIT_EINVAL;
+    for (int i = 0; i < 4; ++i)
+      if (!w->q[i] || !w->s[i] || !al16(w->q[i]) || !al16(w->s[i])) return DIT_EINVAL;
+  }
+  return run_double_block(d, nullptr, nullptr, L > 0 ? w_txt : nullptr, w_img, txt, L, img, N, tc, ts, ic, is,
+                          ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t dit_lora_workspace_bytes(const dit_dims* d, int L, int N, int rank) {

@@ -192,6 +192,17 @@ def int8_block_inputs(shape: BlockShape | str = "1024sq_int8", M: Optional[int] 
     return out
 
 
+def int8_parallel_block_inputs(shape: BlockShape | str = "1024sq_int8", M: Optional[int] = None,
+                               seed: Optional[int] = None) -> BlockInputs:
+    """int8lin weights and rows of ``int8_block_inputs`` with the parallel block's own modulation
+    rows [M, 3, H] (shift, scale, gate), N(0, 0.1), drawn as in ``parallel_block_inputs``."""
+    out = int8_block_inputs(shape, M=M, seed=seed)
+    s = out.shape.seed if seed is None else seed
+    Mr = out.mod.shape[0]
+    out.mod = _rng(s, 4).standard_normal((Mr, 3, out.shape.hidden), dtype=np.float32) * np.float32(0.1)
+    return out
+
+
 @dataclass
 class DenoiseInputs:
     shape: BlockShape

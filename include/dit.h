@@ -259,6 +259,29 @@ DIT_API int dit_double_block_forward(const dit_dims* dims, const dit_block_w* w_
                                      const float* txt_sin, const float* img_cos, const float* img_sin,
                                      const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream);
 
+/* The int8lin forms of the parallel and the double-stream blocks [host contract, section 1 (the
+ * int8 weight format); gizai:dit, Block.parallel; klein article, sections 4.3-4.4]: the blocks above
+ * with every linear given as int8 values and bf16 block-32 scales (dit_block_w8), W = bf16_rne(q s).
+ * Each weight is dequantised once per call, whatever the row count, on a library-owned second stream
+ * that forks from and joins `stream` (as dit_block_forward_int8 does above 512 rows): for the
+ * parallel block [Wqkv ; Wup] into one scratch slot while the norm runs, then Wout and Wdown into a
+ * second while the first GEMM runs; for the double-stream block each linear's text and image
+ * weights into one of two alternating slots, one linear ahead of its GEMM. The GEMMs are those of
+ * the bf16 blocks on the dequantised weights, so each output equals the bf16 block's on
+ * dit_dequant_int8 of the same weights bit for bit. Norm weights from the dit_block_w8 structs;
+ * w_txt may be NULL when L = 0. Requires H % 256 == 0 and ffn % 256 == 0 besides the dims rules.
+ * Workspace: dit_workspace_bytes(dims, L, N, 5) (parallel) and (dims, L, N, 6) (double-stream).
+ * Errors as dit_block_forward. */
+DIT_API int dit_parallel_block_forward_int8(const dit_dims* dims, const dit_block_w8* w, float* txt, int L,
+                                            float* img, int N, const float* txt_cos, const float* txt_sin,
+                                            const float* img_cos, const float* img_sin, const dit_mod* mod,
+                                            void* ws, size_t ws_bytes, dit_stream_t stream);
+DIT_API int dit_double_block_forward_int8(const dit_dims* dims, const dit_block_w8* w_txt,
+                                          const dit_block_w8* w_img, float* txt, int L, float* img, int N,
+                                          const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                          const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                          dit_stream_t stream);
+
 /* FlowMatch Euler step [host contract, section 6]: x[i] <- x[i] + (sigma_next - sigma) * vel[i],
  * each operation rounded separately in fp32 (no fused multiply-add). n >= 0. */
 DIT_API int dit_euler_step(float* x, const float* vel, int64_t n, float sigma, float sigma_next, dit_stream_t stream);
@@ -305,7 +328,8 @@ DIT_API int dit_denoise(const dit_model* model, float* img_tokens, int N, const 
                 const float* img_cos, const float* img_sin, void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block, 2 = parallel block, 3 = double-stream
- * block, 4 = W8A8 block. Returns 0 for unsupported dims. */
+ * block, 4 = W8A8 block, 5 = int8lin parallel block, 6 = int8lin double-stream block. Returns 0 for
+ * unsupported dims. */
 DIT_API size_t dit_workspace_bytes(const dit_dims* dims, int L, int N, int variant);
 DIT_API size_t dit_denoise_workspace_bytes(const dit_model* model, int L, int N, int steps);
 
