@@ -19,7 +19,7 @@ __all__ = [
     "dit_parallel_block_forward_int8", "dit_double_block_forward_int8",
     "W8A8BlockWeights", "dit_block_forward_w8a8", "dit_w8a8_quantize_weight", "dit_w8a8_quantize_rows",
     "dit_linear_w8a8", "dit_linear_w8a8_workspace_bytes",
-    "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA",
+    "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA", "dit_lora_merge",
     "dit_block_forward_sandwich", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
@@ -105,6 +105,7 @@ _SIGNATURES = {
     "dit_block_forward_w8a8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8a8), c_void_p, c_int, c_void_p, c_int,
                                        c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                        c_size_t, c_void_p]),
+    "dit_lora_merge": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
     "dit_w8a8_quantize_weight": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dit_w8a8_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "dit_linear_w8a8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
@@ -381,6 +382,17 @@ def dit_double_block_forward(dims: DitDims, w_txt: Optional[BlockWeights], w_img
                                        _ptr(img_sin, f32), ctypes.byref(mod.c), _ptr(ws, None, "ws"),
                                        ws.numel() * ws.element_size(), _stream(stream)),
         "dit_double_block_forward")
+
+
+def dit_lora_merge(W, A, B, merged, stream=None):
+    """merged = bf16(W + B A): W [out, in], A [rank, in], B [out, rank], merged [out, in] (may be W)."""
+    bf = _bf16()
+    n_out, n_in = W.shape
+    rank = A.shape[0]
+    if tuple(A.shape) != (rank, n_in) or tuple(B.shape) != (n_out, rank) or tuple(merged.shape) != (n_out, n_in):
+        raise ValueError("dit_lora_merge: W [out, in], A [rank, in], B [out, rank], merged [out, in]")
+    _ok(lib().dit_lora_merge(_ptr(W, bf, "W"), n_out, n_in, _ptr(A, bf, "A"), _ptr(B, bf, "B"), rank,
+                             _ptr(merged, bf, "merged"), _stream(stream)), "dit_lora_merge")
 
 
 def dit_parallel_block_forward_int8(dims: DitDims, w: Int8BlockWeights, txt, img, txt_cos, txt_sin, img_cos,

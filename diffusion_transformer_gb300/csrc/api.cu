@@ -902,6 +902,13 @@ int dit_double_block_forward_int8(const dit_dims* d, const dit_block_w8* w_txt, 
                           ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int dit_lora_merge(const uint16_t* W, int n_out, int n_in, const uint16_t* A, const uint16_t* B, int rank,
+                   uint16_t* merged, dit_stream_t stream) {
+  if (!W || !A || !B || !merged || n_out < 1 || n_in < 1 || rank < 1) return DIT_EINVAL;
+  if ((n_out + 63) / 64 > 65535) return DIT_EUNSUPPORTED;
+  return lora_merge_launch(W, A, B, merged, n_out, n_in, rank, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t dit_lora_workspace_bytes(const dit_dims* d, int L, int N, int rank) {
   if (!dims_ok(d) || L < 0 || N < 1 || rank < 8 || rank > 1024 || rank % 8 != 0) return 0;
   return carve_block_ws(d, L + N, nullptr).bytes + (size_t(L + N) * lora_rank_pad(rank) * 2 + 255) / 256 * 256;

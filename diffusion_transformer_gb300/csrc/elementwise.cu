@@ -515,6 +515,72 @@ int codes_bf16_launch(const int8_t* q, uint16_t* w, long long n, cudaStream_t st
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
+// LoRA merge [gizai:dit, weightAt: a BF16 block's linear with its adapter's update B A added]:
+// merged[o, i] = bf16_rne(W[o, i] + sum_r B[o, r] A[r, i]). One CTA per 64 x 64 output tile, 256
+// threads with 4 x 4 outputs each; 32 ranks of B's rows and A's columns staged in shared memory (as
+// fp32, zero past the edges) per step. Each product of two bf16 values is exact in fp32, so the sum
+// over r is one fp32 FMA chain in rank order; W (exact in fp32) is added last, then one
+// round-to-nearest-even to bf16. merged may be W itself (each element is read before it is written,
+// by the thread that writes it).
+constexpr int kMergeTile = 64, kMergeRanks = 32;
+__global__ void __launch_bounds__(256) lora_merge_kernel(const uint16_t* W, const uint16_t* __restrict__ A,
+                                                         const uint16_t* __restrict__ B, uint16_t* merged, int n_out,
+                                                         int n_in, int rank) {
+  __shared__ float sB[kMergeTile][kMergeRanks + 1];
+  __shared__ float sA[kMergeRanks][kMergeTile];
+  const int o0 = blockIdx.y * kMergeTile, i0 = blockIdx.x * kMergeTile;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int r0 = 0; r0 < rank; r0 += kMergeRanks) {
+    for (int e = threadIdx.x; e < kMergeTile * kMergeRanks; e += 256) {
+      const int rr = e % kMergeRanks, oo = e / kMergeRanks, o = o0 + oo, r = r0 + rr;
+      sB[oo][rr] = (o < n_out && r < rank) ? __uint_as_float(uint32_t(B[size_t(o) * rank + r]) << 16) : 0.f;
+    }
+    for (int e = threadIdx.x; e < kMergeRanks * kMergeTile; e += 256) {
+      const int ii = e % kMergeTile, rr = e / kMergeTile, i = i0 + ii, r = r0 + rr;
+      sA[rr][ii] = (i < n_in && r < rank) ? __uint_as_float(uint32_t(A[size_t(r) * n_in + i]) << 16) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int rr = 0; rr < kMergeRanks; ++rr) {
+      float b[4], a[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        b[k] = sB[ty + 16 * k][rr];
+        a[k] = sA[rr][tx + 16 * k];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int l = 0; l < 4; ++l) acc[k][l] = __fmaf_rn(b[k], a[l], acc[k][l]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int o = o0 + ty + 16 * k;
+    if (o >= n_out) continue;
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const int i = i0 + tx + 16 * l;
+      if (i >= n_in) continue;
+      const size_t at = size_t(o) * n_in + i;
+      const float v = __fadd_rn(__uint_as_float(uint32_t(W[at]) << 16), acc[k][l]);
+      __nv_bfloat16 h = __float2bfloat16_rn(v);
+      merged[at] = *reinterpret_cast<uint16_t*>(&h);
+    }
+  }
+}
+
+int lora_merge_launch(const uint16_t* W, const uint16_t* A, const uint16_t* B, uint16_t* merged, int n_out, int n_in,
+                      int rank, cudaStream_t stream) {
+  if (n_out <= 0 || n_in <= 0) return DIT_OK;
+  const dim3 grid((n_in + kMergeTile - 1) / kMergeTile, (n_out + kMergeTile - 1) / kMergeTile);
+  if (grid.y > 65535u) return DIT_EUNSUPPORTED;
+  lora_merge_kernel<<<grid, 256, 0, stream>>>(W, A, B, merged, n_out, n_in, rank);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+}
+
 int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long long rows, long long cols,
                         cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return DIT_OK;

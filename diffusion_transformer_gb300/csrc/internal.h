@@ -157,6 +157,8 @@ int rope_tables_launch(int L, int gh, int gw, int head_dim, float theta, float* 
                        cudaStream_t stream);
 int sinusoid_launch(const float* sigmas, int steps, int dim, uint16_t* out, cudaStream_t stream);
 int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t stream);
+int lora_merge_launch(const uint16_t* W, const uint16_t* A, const uint16_t* B, uint16_t* merged, int n_out, int n_in,
+                      int rank, cudaStream_t stream);
 int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long long rows, long long cols,
                         cudaStream_t stream);
 // W8A8: per-token codes of x [rows, K] bf16 written over x (as bf16 integers) with scale[rows];

@@ -157,6 +157,18 @@ DIT_API int dit_block_forward(const dit_dims* dims, const dit_block_w* w, float*
                       const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
                       const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream);
 
+/* LoRA merge [gizai:dit, weightAt and loadBlock: a BF16 block's linear is loaded with its adapter's
+ * update added, W + B A]: merged[o, i] = bf16_rne(W[o, i] + sum_r B[o, r] A[r, i]) for W [n_out, n_in],
+ * A [rank, n_in], B [n_out, rank], all bf16 row-major (device). The sum over r is an fp32 FMA chain
+ * in rank order (each product of two bf16 values is exact in fp32), W is added in fp32, then one
+ * rounding to bf16, so a result differs from the rounding of the exact value only where that value
+ * lies within the fp32 sum's rounding error of a bf16 rounding boundary. merged may be W itself (in
+ * place) but must not otherwise overlap the inputs. The merged weights then serve any block form
+ * (sequential, parallel, double-stream) with no adapter work per call. Errors: DIT_EINVAL for null
+ * pointers or sizes < 1. */
+DIT_API int dit_lora_merge(const uint16_t* W, int n_out, int n_in, const uint16_t* A, const uint16_t* B, int rank,
+                           uint16_t* merged, dit_stream_t stream);
+
 /* The bf16 block with LoRA adapters beside its linears (dit_lora): each adapted linear runs as
  * one GEMM for down = x A^T (bf16, [R, rank rounded up to 64], in the workspace) and the linear's
  * GEMM over [x | down] [W | B]^T with its usual epilogue (QK norm + rotary, gated residual, SwiGLU).
