@@ -72,3 +72,40 @@ def test_invalid_arguments_rejected_before_any_cuda_call(libdit):
     assert L.dit_euler_step(None, None, 5, ctypes.c_float(1.0), ctypes.c_float(0.5), None) == -1
     assert L.dit_rope_tables(4, 2, 2, 96, ctypes.c_float(1e4), ctypes.c_void_p(16), ctypes.c_void_p(16), None) == -2
     assert L.dit_dequant_int8(ctypes.c_void_p(16), ctypes.c_void_p(16), 4, 33, ctypes.c_void_p(16), None) == -2
+
+
+def _ru(n, a=256):
+    return (n + a - 1) // a * a
+
+
+@pytest.mark.parametrize("H,nh,hd,F,L,N", [(3072, 24, 128, 12288, 128, 4096), (256, 4, 64, 768, 8, 64),
+                                           (3072, 24, 128, 12288, 0, 1), (512, 8, 64, 1536, 13, 90)])
+def test_workspace_variants_host_only(libdit, H, nh, hd, F, L, N):
+    # block workspace: h, q, k, vt (rows padded to 8), o, a, each 256-byte aligned; variants add
+    # the int8lin slots (two of the largest dequantised linear), the W8A8 slots and per-row scales,
+    # the parallel block's [Wqkv ; Wup] and [Wout | Wdown] slots, the double-stream block's two
+    # text + image slots
+    d = D.DitDims(H, nh, hd, F)
+    R = L + N
+    block = (_ru(R * H * 2) + 2 * _ru(nh * R * hd * 2) + _ru(nh * hd * _ru(R, 8) * 2) + _ru(R * H * 2) +
+             _ru(R * F * 2))
+    slot = _ru(max(3 * H * H, H * H, 2 * F * H, H * F) * 2)
+    expect = {0: block, 1: block + 2 * slot, 2: block, 3: block, 4: block + 2 * slot + _ru(R * 4),
+              5: block + _ru((3 * H + 2 * F) * H * 2) + _ru(H * (H + F) * 2), 6: block + 4 * slot}
+    for variant, want in expect.items():
+        assert D.dit_workspace_bytes(d, L, N, variant) == want, variant
+    assert D.dit_workspace_bytes(d, L, N, 7) == 0 and D.dit_workspace_bytes(d, L, N, -1) == 0
+
+
+def test_new_entries_reject_invalid_arguments_before_any_cuda_call(libdit):
+    import ctypes
+    L = libdit
+    p = ctypes.c_void_p(256)
+    # LoRA merge: null pointers, empty sizes
+    assert L.dit_lora_merge(None, 4, 4, p, p, 8, p, None) == -1
+    assert L.dit_lora_merge(p, 0, 4, p, p, 8, p, None) == -1
+    assert L.dit_lora_merge(p, 4, 4, p, p, 0, p, None) == -1
+    # int8lin parallel / double-stream blocks: null dims or weights
+    args = (None, 0, None, 1, None, None, None, None, None, None, 0, None)
+    assert L.dit_parallel_block_forward_int8(None, None, *args) == -1
+    assert L.dit_double_block_forward_int8(None, None, None, *args) == -1
