@@ -72,6 +72,20 @@ def test_block_sampled_rows(shape):
     _check(got[rows], ref, x_in, f"{shape} sampled rows")
 
 
+def test_block_2048sq_ragged_sampled_rows():
+    # the largest case: a 2048^2-shaped image (128 x 128 grid, N = 16384) with L = 100 text rows, so
+    # R = 16484 is ragged against the 128-row query and key tiles; per-row modulation (1.2 GB of
+    # modulation rows); every index above 2^24 elements goes through 64-bit offsets
+    sh = DI.BlockShape("2048sq_L100", 3072, 24, 128, 12288, 100, 128, 128, seed=5)
+    inp = DI.block_inputs(sh)
+    t, i = run_block_gpu(inp)
+    got = np.concatenate([t, i])
+    rows = _sample_rows(sh, n=32, seed=5)
+    ref = O.block_forward(inp, rows=rows)
+    x_in = np.concatenate([inp.txt, inp.img]).astype(np.float64)[rows]
+    _check(got[rows], ref, x_in, "2048sq (L = 100) sampled rows")
+
+
 def test_block_deterministic():
     inp = DI.block_inputs("512sq")
     a = run_block_gpu(inp)
