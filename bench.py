@@ -528,7 +528,7 @@ def run_ours(args):
         dbl = {"workload": "1024sq double-stream block: the 128 text rows and the 4096 image rows each with their own "
                            "four linears and norms, one joint attention; per-row modulation",
                "ms_per_block": msD, "tflops": tfD, "frac_of_peak": tfD / peaks["bf16_tflops"],
-               "flop_per_block": flops, "launches_per_block": 7 if sh.L % 128 == 0 else 13}
+               "flop_per_block": flops, "launches_per_block": 7}
         del wT, wsD
 
     # the sequential block with the split-halves partial rotary layout (tables [R, 3d/8], seeded angles)
