@@ -334,7 +334,8 @@ typedef struct {
  * x <- x + (sigmas[i+1] - sigmas[i]) vel in fp32. x (img_tokens [N, C] fp32, device) holds the
  * packed noise on entry and the result on return. txt_feats [L, H] fp32. Rotary tables as in
  * dit_block_forward. The step-invariant work (time embeddings and every block's modulation for all
- * steps) is computed once up front. Workspace: dit_denoise_workspace_bytes(). */
+ * steps) is computed once up front. Any L >= 0 and N >= 1 (the host contract's graphs take
+ * L = 8..512, N = 64..4096). Workspace: dit_denoise_workspace_bytes(). */
 DIT_API int dit_denoise(const dit_model* model, float* img_tokens, int N, const float* txt_feats, int L,
                 const float* sigmas, int steps, const float* txt_cos, const float* txt_sin,
                 const float* img_cos, const float* img_sin, void* ws, size_t ws_bytes, dit_stream_t stream);
