@@ -122,6 +122,23 @@ def test_dequant_bit_exact():
     assert np.array_equal(bf16_bits(w), O.dequant_int8(q, s))
 
 
+def test_dequant_bit_exact_every_code_and_finite_scale():
+    # every pair (code in [-127, 127], finite bf16 scale bit pattern: zeros, subnormals, normals, the
+    # largest exponents, both signs): one row per scale pattern, that scale on all of the row's
+    # 8 blocks of 32, the row's 256 codes every code value once plus a 0
+    sb = np.arange(0x10000, dtype=np.uint32)
+    sb = sb[((sb >> 7) & 0xFF) != 0xFF].astype(np.uint16)  # drop infinities and NaNs
+    codes = np.concatenate([np.arange(-127, 128), [0]]).astype(np.int8)
+    q = np.tile(codes, (sb.size, 1))
+    s = np.repeat(sb[:, None], 8, axis=1)
+    w = torch.empty(sb.size, 256, dtype=torch.bfloat16, device="cuda")
+    D.dit_dequant_int8(dev(q), dev_bf16(s), w)
+    D.dit_check()
+    got, ref = bf16_bits(w), O.dequant_int8(q, s)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, [(hex(int(sb[r])), int(q[r, c]), hex(int(got[r, c])), hex(int(ref[r, c]))) for r, c in bad[:8]]
+
+
 # ---------------------------------------------------------------------------------- plain GEMM
 
 @pytest.mark.parametrize("M,N,K", [(72, 256, 256), (128, 128, 64), (200, 64, 128), (1088, 768, 3072),
