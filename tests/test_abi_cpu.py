@@ -109,3 +109,31 @@ def test_new_entries_reject_invalid_arguments_before_any_cuda_call(libdit):
     args = (None, 0, None, 1, None, None, None, None, None, None, 0, None)
     assert L.dit_parallel_block_forward_int8(None, None, *args) == -1
     assert L.dit_double_block_forward_int8(None, None, None, *args) == -1
+
+
+def test_header_is_plain_c_and_links(libdit, tmp_path):
+    # a C11 client (no C++) includes the header, takes every declared entry point's address, links
+    # against libdit.so and calls the host-only queries
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    names = _declared()
+    src = tmp_path / "client.c"
+    src.write_text(
+        '#include "dit.h"\n#include <stdio.h>\n'
+        "typedef void (*fn_t)(void);\n"
+        "static const fn_t fns[] = {\n" + ",\n".join(f"  (fn_t){n}" for n in names) + "\n};\n"
+        "int main(void) {\n"
+        "  dit_dims d = {3072, 24, 128, 12288, 1e-6f, 1e-6f, 0};\n"
+        '  printf("%d %zu %zu %s\\n", dit_version(), sizeof(fns) / sizeof(fns[0]),\n'
+        "         dit_workspace_bytes(&d, 128, 4096, 0), dit_status_string(DIT_EWORKSPACE));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(D.library_path)
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", libdir, "-ldit", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert int(out[0]) == D.dit_version() and int(out[1]) == len(names)
+    assert int(out[2]) == D.dit_workspace_bytes(D.DitDims(3072, 24, 128, 12288), 128, 4096, 0)
+    assert " ".join(out[3:]) == D.dit_status_string(-3)
