@@ -137,3 +137,13 @@ def test_header_is_plain_c_and_links(libdit, tmp_path):
     assert int(out[0]) == D.dit_version() and int(out[1]) == len(names)
     assert int(out[2]) == D.dit_workspace_bytes(D.DitDims(3072, 24, 128, 12288), 128, 4096, 0)
     assert " ".join(out[3:]) == D.dit_status_string(-3)
+
+
+def test_missing_library_fails_loudly():
+    # no fallback: with the library absent every call raises instead of computing anything elsewhere
+    import sys
+    code = ("import diffusion_transformer_gb300 as D\n"
+            "D.library_path = '/nonexistent/libdit.so'\nD._lib = None\n"
+            "try:\n    D.dit_version()\nexcept RuntimeError as e:\n    print('raised', e)\n")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT).stdout
+    assert out.startswith("raised") and "not built" in out
