@@ -372,10 +372,12 @@ DIT_API int dit_attention(const dit_dims* dims, int R, const uint16_t* q, const 
 
 /* The same attention for q and k rows as dit_qkv_rope writes them: RMS-normalised per head and
  * scaled by q_norm / k_norm ([d] fp32 each, NULL = ones; the caller vouches for this, the kernel
- * does not check it). Every scaled score then lies within a bound B = d max|q_norm| max|k_norm| /
- * sqrt(d) (log2 units); when B < 60 the softmax subtracts B instead of a running row maximum, which
- * lets it split each row over two warps (the result differs from dit_attention by rounding only);
- * otherwise it is dit_attention. */
+ * does not check it). Every scaled score then lies within a bound
+ * B = (1 + 2^-6)^2 d max|q_norm| max|k_norm| log2(e) / sqrt(d) (log2 units; the margin covers the
+ * bf16 rounding of q and k; 16.8 at d = 128 with unit weights); when B < 60 the softmax subtracts B
+ * instead of a running row maximum, which lets it split each row over several warps (two, or four
+ * at d = 128; the result differs from dit_attention by rounding only); otherwise it is
+ * dit_attention. */
 DIT_API int dit_attention_qknorm(const dit_dims* dims, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
                                  const float* q_norm, const float* k_norm, uint16_t* o, dit_stream_t stream);
 
