@@ -48,7 +48,7 @@ WORKLOAD = "1024sq"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a kernel, from one ncu
 # capture of this workload, with the SHA-256 of the CUDA sources that kernel is built from. The
 # figure is reported only while those sources are unchanged (otherwise the counters no longer
-# describe the kernel and `traffic` is null). Captures: profiles/ncu_gemm_up_swiglu_1024sq.md.
+# describe the kernel and `traffic` is null).
 KERNEL_SOURCES = {
     "gemm": ["gemm.cu", "ptx.cuh", "tmap.h", "internal.h"],
     "attention": ["attention.cu", "ptx.cuh", "tmap.h", "internal.h"],
@@ -59,6 +59,13 @@ KERNEL_FAMILY = {"modnorm": "modnorm", "attention": "attention", "gemm_qkv_rope"
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, sha256 of its sources at capture)
     "gemm_up_swiglu": (262_337_536, "4977a7e4ec5b964a457eb7b7daadcc5765003d96a0d3e6b82fa21eb987a86698"),
+}
+# sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of a kernel from the same kind of
+# capture, with the same source check: a counter-based view of tensor utilisation beside the
+# event-timed fraction of the measured peak (which a cuBLAS burst figure taken at a lower clock
+# can flatter).
+NCU_TENSOR_ACTIVE = {
+    "gemm_up_swiglu": (0.910, "4977a7e4ec5b964a457eb7b7daadcc5765003d96a0d3e6b82fa21eb987a86698"),
 }
 
 
@@ -84,8 +91,8 @@ def _sources_hash(family):
     return h.hexdigest()
 
 
-def _traffic(kernel):
-    t = NCU_TRAFFIC.get(kernel)
+def _traffic(kernel, table=None):
+    t = (NCU_TRAFFIC if table is None else table).get(kernel)
     if t and t[1] == _sources_hash(KERNEL_FAMILY[kernel]):
         return t[0]
     return None
@@ -421,6 +428,7 @@ def run_ours(args):
         ach = dk["flop_per_launch"] / (dk["ms_per_launch"] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": ach / peaks["bf16_tflops"], "traffic": _traffic(dom),
+                "ncu_tensor_active": _traffic(dom, NCU_TENSOR_ACTIVE),
                 "peak_source": f"bf16_tflops burst, {peaks['source']}"}
     else:
         ach = dk["bytes_per_launch"] / (dk["ms_per_launch"] * 1e-3) / 1e9
@@ -633,6 +641,9 @@ def run_ours(args):
                        "inputs": "a fresh copy of the seeded rows per call",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "frac_of_peak": value / world / peaks["bf16_tflops"],
+            "int8lin_ms_per_block": int8["ms_per_block"] if int8 else None,
+            "int8lin_tflops": int8["tflops"] if int8 else None,
+            "int8lin_frac": int8["frac_of_peak"] if int8 else None,
             "roofline": roof,
             "kernels": kb,
             "int8lin": int8,
@@ -651,6 +662,15 @@ def run_ours(args):
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "peaks": peaks,
+            # the two halves of the metric once more at the end of the line (short, so a record that
+            # keeps only the line's tail still holds them)
+            "headline": {"bf16_ms_per_block": ms_step, "bf16_tflops": value / world,
+                         "bf16_frac": value / world / peaks["bf16_tflops"],
+                         "int8lin_ms_per_block": int8["ms_per_block"] if int8 else None,
+                         "int8lin_tflops": int8["tflops"] if int8 else None,
+                         "int8lin_frac": int8["frac_of_peak"] if int8 else None,
+                         "dominant_kernel": roof["kernel"], "dominant_frac": roof["frac"],
+                         "dominant_ncu_tensor_active": roof.get("ncu_tensor_active")},
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -741,6 +741,19 @@ int check_block_args(const dit_dims* d, const float* txt, int L, const float* im
 
 }  // namespace
 
+int check_block_call_without_workspace(const dit_dims* d, const dit_block_w* w, const float* txt, int L,
+                                       const float* img, int N, const float* tc, const float* ts, const float* ic,
+                                       const float* is, const dit_mod* mod) {
+  if (!d || !mod) return DIT_EINVAL;
+  if (!dims_ok(d)) return DIT_EUNSUPPORTED;
+  if (L < 0 || N < 1 || (L > 0 && (!txt || !tc || !ts)) || !img || !ic || !is) return DIT_EINVAL;
+  if (!mod->rows || mod->M < 1) return DIT_EINVAL;
+  if (!al16(txt) || !al16(img) || !al16(mod->rows)) return DIT_EINVAL;
+  if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+  if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  return DIT_OK;
+}
+
 EncodeTiledFn encode_tiled_fn() {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_encode_tried) {

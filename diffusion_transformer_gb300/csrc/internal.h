@@ -170,6 +170,12 @@ int codes_bf16_launch(const int8_t* q, uint16_t* w, long long n, cudaStream_t st
 
 int num_sms();
 
+// Every check dit_block_forward makes before launching, except those on the workspace: DIT_OK, or the
+// status it would return. Touches no CUDA state.
+int check_block_call_without_workspace(const dit_dims* d, const dit_block_w* w, const float* txt, int L,
+                                       const float* img, int N, const float* tc, const float* ts, const float* ic,
+                                       const float* is, const dit_mod* mod);
+
 // Raise a kernel's dynamic shared-memory limit on the current device (once per kernel and device).
 bool smem_attr_once(const void* kernel, unsigned bytes);
 

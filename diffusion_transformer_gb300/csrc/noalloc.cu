@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "../../include/dit.h"
+#include "internal.h"
 
 namespace {
 
@@ -57,13 +58,14 @@ size_t dit_block_noalloc_max_bytes(void) { return kStaticScratchBytes; }
 int dit_block_forward_noalloc(const dit_dims* dims, const dit_block_w* w, float* txt, int L, float* img, int N,
                               const float* txt_cos, const float* txt_sin, const float* img_cos, const float* img_sin,
                               const dit_mod* mod, dit_stream_t stream) {
-  if (!dims) return DIT_EINVAL;
+  // every argument check comes before the first CUDA call, as in the other entry points
+  int rc = dit::check_block_call_without_workspace(dims, w, txt, L, img, N, txt_cos, txt_sin, img_cos, img_sin, mod);
+  if (rc != DIT_OK) return rc;
   const size_t need = dit_workspace_bytes(dims, L, N, 0);
+  if (need == 0) return DIT_EINVAL;
   if (need > kStaticScratchBytes) return DIT_EWORKSPACE;  // the shape needs more than the static array
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
-  if (rc != DIT_OK) return rc;
-  // need == 0 (unsupported dims or sizes): the block forward's own validation reports the error
+  if ((rc = scratch_address(&scratch)) != DIT_OK) return rc;
   return dit_block_forward(dims, w, txt, L, img, N, txt_cos, txt_sin, img_cos, img_sin, mod, scratch,
                            kStaticScratchBytes, stream);
 }

@@ -25,6 +25,11 @@
  *   - Calls that share a workspace must not overlap on the device.
  *   - Device-side waits are bounded: a stuck pipeline sets the device error word, the kernel frees
  *     what it holds and returns. dit_check() reports it as DIT_ETIMEOUT.
+ *   - Per-device state is created on the first call that needs it and kept until the process
+ *     exits: the device addresses of the library's static device arrays (the error word, the
+ *     no-allocation scratch), the int8lin side stream and its events, kernel attributes. It is keyed
+ *     by device ordinal, so it does not survive cudaDeviceReset(): after a reset the cached
+ *     addresses and handles are stale, and the library must not be called again in that process.
  */
 #ifndef DIT_H_
 #define DIT_H_

@@ -11,11 +11,19 @@ Sources, cited by page title and section:
   points), section 4.3 (attention: softmax with 1/sqrt(d) applied in fp32), section 4.4 (qk prep:
   QK-RMSNorm as mean of squares + eps -> rsqrt).
 
-Readings where the pages are silent (each is listed with its basis in the design notes):
-modulation uses (1 + scale); RMSNorm is x * (mean(x^2) + eps)^-1/2 with eps = 1e-6; RoPE rotates
-adjacent pairs (2i, 2i+1) of the whole head; d = 64 heads use axis widths (8, 28, 28); the block is
-sequential (attention residual lands before the second norm); the final norm of the denoise loop is
-a modulated RMSNorm without an affine weight; no linear has a bias.
+Readings where the pages are silent, each with its basis:
+* modulation uses (1 + scale): the pages name shift, scale and gate only [gizai:dit, Modulation];
+  (1 + scale) is the AdaLN convention and keeps the norm's gain near 1 for small scales;
+* RMSNorm is x * (mean(x^2) + eps)^-1/2 with eps = 1e-6 for both norms and the QK norm [klein,
+  section 4.4: "mean of squares + eps -> rsqrt"];
+* RoPE rotates adjacent pairs (2i, 2i+1) of the whole head [host contract, section 4: complex
+  pairs built with torch.polar]; d = 64 heads scale the d = 128 axis widths (16, 56, 56) by d / 128,
+  giving (8, 28, 28), since the pages give only d = 128;
+* the block is sequential, the attention residual landing before the second norm [gizai:dit,
+  Block.forward, as opposed to Block.parallel];
+* the final norm of the denoise loop is a modulated RMSNorm without an affine weight, and no linear
+  has a bias [gizai:dit, Block: a block's linear biases are optional, and a block built from
+  weights alone has none; the pages show no head or tail weights].
 """
 
 from __future__ import annotations

@@ -10,7 +10,7 @@ divides the activation by a per-input-channel divisor before its quantisation an
 divisor into the weight (diag(s) W in float32) before the weight's quantisation; the divisor comes
 from calibration statistics through a smoothing formula with exponent alpha.
 
-Readings where the pages are silent (each is listed in the design notes):
+Readings where the pages are silent (the pages give the scheme, not these details):
 * the scale is absmax / 127 in float32; a code is clip(rint(v / scale), -127, 127) with the float32
   division and round-half-to-even (the rounding of jnp.round); a row or channel of zeros has scale
   0 and codes 0;

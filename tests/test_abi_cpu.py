@@ -109,6 +109,26 @@ def test_new_entries_reject_invalid_arguments_before_any_cuda_call(libdit):
     args = (None, 0, None, 1, None, None, None, None, None, None, 0, None)
     assert L.dit_parallel_block_forward_int8(None, None, *args) == -1
     assert L.dit_double_block_forward_int8(None, None, None, *args) == -1
+    # no-allocation block: every argument is checked before the scratch address is looked up (that
+    # lookup is the call's first CUDA call), so on this GPU-less host the errors are the argument
+    # errors, never DIT_ECUDA
+    na = (None, 0, None, 1, None, None, None, None, None, None)
+    assert L.dit_block_forward_noalloc(None, None, *na) == -1
+    dims = D.dit_dims(3072, 24, 128, 12288, 1e-6, 1e-6, 0)
+    assert L.dit_block_forward_noalloc(ctypes.byref(dims), None, *na) == -1                # no weights, no rows
+    bad = D.dit_dims(3072, 24, 96, 12288, 1e-6, 1e-6, 0)
+    mod = D.dit_mod(256, None, 1)
+    assert L.dit_block_forward_noalloc(ctypes.byref(bad), None, None, 0, p, 1, None, None, p, p,
+                                       ctypes.byref(mod), None) == -2                     # head_dim 96
+    w = D.dit_block_w(256, 256, 256, 256, None, None, None, None)
+    assert L.dit_block_forward_noalloc(ctypes.byref(dims), ctypes.byref(w), None, 0, p, 0, None, None, p, p,
+                                       ctypes.byref(mod), None) == -1                     # N = 0
+    wmis = D.dit_block_w(256, 258, 256, 256, None, None, None, None)
+    assert L.dit_block_forward_noalloc(ctypes.byref(dims), ctypes.byref(wmis), None, 0, p, 8, None, None, p, p,
+                                       ctypes.byref(mod), None) == -1                     # misaligned weight
+    # the 1024sq shape exceeds the static array: rejected with DIT_EWORKSPACE, still before CUDA
+    assert L.dit_block_forward_noalloc(ctypes.byref(dims), ctypes.byref(w), p, 128, p, 4096, p, p, p, p,
+                                       ctypes.byref(mod), None) == -3
 
 
 def test_header_is_plain_c_and_links(libdit, tmp_path):

@@ -1,7 +1,7 @@
 """Whole-block parity of the CUDA path (dit_block_forward / dit_block_forward_int8 through the C ABI)
 against the float64 oracle on the same seeded inputs.
 
-Gates (written here, derived in the design notes):
+Gates (derived here from the arithmetic of the GPU path):
 * the stated bar: max |out_gpu - out_ref| <= 2e-2 * RMS(out_ref);
 * a stricter gate on the block's own contribution delta = out - in (the residual input dominates
   RMS(out), so the first gate alone would let a wrong branch through):
