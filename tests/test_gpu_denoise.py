@@ -77,3 +77,18 @@ def test_denoise_full_size_identity_blocks():
     got = _run(inp, model)
     ref = O.denoise(inp, blocks=0).astype(np.float64)
     _check(got, ref, inp.latents.astype(np.float64), "full-size denoise, identity blocks")
+
+
+def test_denoise_full_size_real_blocks():
+    # The denoise workload's own sequence (L = 512 text rows + N = 4096 image rows, seed 4) through
+    # the whole loop, all four Euler steps over sigmas [1, .75, .5, .25, 0], with two real blocks of
+    # the 1024sq architecture: non-zero modulation weights, so every block's modulation comes from
+    # the hoisted adaLN rows of its own (step, block), the blocks chain through the residual rows,
+    # and the final norm and patch-out run on real residuals. The oracle runs the same loop with the
+    # same two blocks (about 13 TFLOP in float64).
+    inp = DI.denoise_inputs("denoise", blocks=2)
+    assert (inp.shape.L, inp.shape.N, len(inp.steps_sigmas)) == (512, 4096, 5)
+    assert np.count_nonzero(inp.w_ada) > 0
+    got = _run(inp, _model_dev(inp))
+    ref = O.denoise(inp).astype(np.float64)
+    _check(got, ref, inp.latents.astype(np.float64), "full-size denoise, 2 real blocks")

@@ -386,3 +386,44 @@ def test_attention_zero_query_gives_mean_value():
     mean_v = O.bf16_to_f64(v).mean(axis=1).reshape(1, nh * d)
     got = bf16_f64(o)
     assert np.all(np.abs(got - mean_v) <= 2 ** -8 * np.abs(O.bf16_to_f64(v)).max())
+
+
+@pytest.mark.parametrize("w,path", [(1.8559, "fixed"), (1.9188, "running")])
+def test_attention_qknorm_near_the_fixed_maximum_cutoff(w, path):
+    # Norm weights that put the bound B = (1 + 2^-6)^2 d w^2 log2(e) / sqrt(d) just below (58) and
+    # just above (62) the cutoff of 60 at which the kernel leaves the fixed maximum for the running
+    # one. Some key rows equal a query row (score near +B) and some its negation (score near -B), so
+    # under the fixed maximum the weights exp2(s - B) reach down to about 2^-116 and their products
+    # with small values near the bottom of the fp32 range; both paths must still match the oracle.
+    R, nh, d = 1088, 2, 128
+    B = (1 + 2 ** -6) ** 2 * d * w * w / np.log(2.0) / np.sqrt(d)
+    assert (B < 60) == (path == "fixed") and abs(B - (58 if path == "fixed" else 62)) < 0.1
+    g = np.random.default_rng(int(w * 1e4))
+    wv = np.full(d, w, np.float32)
+    q, k = _qknormed(g, nh, R, d, wv), _qknormed(g, nh, R, d, wv)
+    idx = g.choice(R, 96, replace=False)
+    k[:, idx[:48]] = q[:, idx[:48]]                     # aligned: s close to +B
+    k[:, idx[48:]] = q[:, idx[48:]] ^ np.uint16(0x8000)  # anti-aligned: s close to -B
+    v = _bf16_rand(g, (nh, R, d), 1.0)
+    v[:, idx[48:64]] = DI.bf16_bits_from_f32((O.bf16_to_f64(v[:, idx[48:64]]) * 2.0 ** -10).astype(np.float32))
+    Rp = D.dit_vt_stride(R)
+    vt = np.zeros((nh, d, Rp), np.uint16)
+    vt[:, :, :R] = v.transpose(0, 2, 1)
+    dims = D.DitDims(nh * d, nh, d, 256)
+    o = torch.empty(R, nh * d, dtype=torch.bfloat16, device="cuda")
+    o_gen = torch.empty_like(o)
+    D.dit_attention_qknorm(dims, R, dev_bf16(q), dev_bf16(k), dev_bf16(vt), dev(wv), dev(wv), o)
+    D.dit_attention(dims, R, dev_bf16(q), dev_bf16(k), dev_bf16(vt), o_gen)
+    D.dit_check()
+    f = lambda a: O.bf16_to_f64(a).transpose(1, 0, 2)
+    qf, kf = f(q), f(k)
+    s = np.einsum("rhd,chd->hrc", qf, kf) / np.sqrt(d) / np.log(2.0)
+    assert s.max() > 0.95 * B and s.min() < -0.95 * B  # the scores span nearly [-B, B]
+    ref = O.attention(qf, kf, f(v))
+    vmax = np.abs(O.bf16_to_f64(v)).max()
+    for got in (bf16_f64(o), bf16_f64(o_gen)):
+        assert np.all(np.abs(got - ref) <= 2 ** -8 * vmax + 2 ** -8 * np.abs(ref)), max_abs(got, ref)
+    if path == "running":  # B > 60: the same kernel path as dit_attention, bit for bit
+        assert torch.equal(o, o_gen)
+    else:                  # B < 60: the fixed path, which rounds differently from the running one
+        assert not torch.equal(o, o_gen)
