@@ -261,8 +261,8 @@ def _kernel_breakdown(torch, D, st, inp, steps):
     vt = torch.zeros(nh, d, D.dit_vt_stride(R), dtype=torch.bfloat16, device="cuda")
     o = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
     a = torch.empty(R, F, dtype=torch.bfloat16, device="cuda")
-    # scratch for the K-split of the gated GEMMs' last wave, as the block gives them
-    split_ws = torch.empty(((R + 127) // 128 * 128) * H * 12 + 4096, dtype=torch.uint8, device="cuda")
+    # the block runs every linear on whole tiles (no stream-K scratch), and so do these calls
+    split_ws = None
     w = st["w"].tensors
     M = inp.mod.shape[0]
     norm_bytes = R * H * 4 + R * H * 2 + 2 * M * H * 4
@@ -270,14 +270,14 @@ def _kernel_breakdown(torch, D, st, inp, steps):
     kernels = [
         ("modnorm", lambda: D.dit_modnorm(dims, st["txt"], st["img"], None, st["mod"], 0, h), 0.0, norm_bytes),
         ("gemm_qkv_rope", lambda: D.dit_qkv_rope(dims, h, sh.L, sh.N, w[0], None, None, st["tc"], st["ts"], st["ic"],
-                                                 st["is_"], q, k, vt), 2.0 * R * 3 * H * H,
+                                                 st["is_"], q, k, vt, ws=split_ws), 2.0 * R * 3 * H * H,
          R * H * 2 + 3 * H * H * 2 + 3 * R * H * 2),
         # q and k from the QK-norm epilogue above (unit norm weights), as in the block
         ("attention", lambda: D.dit_attention_qknorm(dims, R, q, k, vt, None, None, o), 4.0 * R * R * H, 4 * R * H * 2),
         ("gemm_out_gated", lambda: D.dit_linear_gated(dims, o, sh.L, sh.N, w[1], st["mod"], 0, st["txt"], st["img"],
                                                   split_ws),
          2.0 * R * H * H, gated_bytes(H)),
-        ("gemm_up_swiglu", lambda: D.dit_linear_swiglu(dims, h, w[2], a), 2.0 * R * 2 * F * H,
+        ("gemm_up_swiglu", lambda: D.dit_linear_swiglu(dims, h, w[2], a, ws=split_ws), 2.0 * R * 2 * F * H,
          R * H * 2 + 2 * F * H * 2 + R * F * 2),
         ("gemm_down_gated", lambda: D.dit_linear_gated(dims, a, sh.L, sh.N, w[3], st["mod"], 1, st["txt"], st["img"],
                                                    split_ws),

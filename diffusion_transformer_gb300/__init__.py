@@ -23,7 +23,7 @@ __all__ = [
     "dit_block_forward_sandwich", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
-    "dit_vt_stride", "dit_attention", "dit_attention_qknorm", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
+    "dit_vt_stride", "dit_stream_k_workspace_bytes", "dit_attention", "dit_attention_qknorm", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
     "dit_dequant_int8", "dit_linear_int8", "dit_linear_int8_workspace_bytes", "dit_check", "dit_selftest_bounded_wait", "dit_status_string", "dit_version",
 ]
 
@@ -123,14 +123,17 @@ _SIGNATURES = {
     "dit_modnorm": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_int, c_void_p, POINTER(dit_mod), c_int,
                             c_void_p, c_void_p]),
     "dit_qkv_rope": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
-                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                             c_void_p]),
+    "dit_stream_k_workspace_bytes": (c_size_t, []),
     "dit_vt_stride": (c_int, [c_int]),
     "dit_attention": (c_int, [POINTER(dit_dims), c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dit_attention_qknorm": (c_int, [POINTER(dit_dims), c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p]),
     "dit_linear_gated": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_int, c_void_p, POINTER(dit_mod), c_int,
                                  c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
-    "dit_linear_swiglu": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
+    "dit_linear_swiglu": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_size_t,
+                                  c_void_p]),
     "dit_linear": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p]),
     "dit_dequant_int8": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "dit_linear_int8": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t,
@@ -474,14 +477,22 @@ def dit_modnorm(dims: DitDims, txt, img, w, mod: Modulation, which: int, h, stre
         "dit_modnorm")
 
 
+def dit_stream_k_workspace_bytes() -> int:
+    return lib().dit_stream_k_workspace_bytes()
+
+
+def _ws_bytes(ws):
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
 def dit_qkv_rope(dims: DitDims, h, L: int, N: int, wqkv, q_norm, k_norm, txt_cos, txt_sin, img_cos, img_sin,
-                 q, k, vt, stream=None):
+                 q, k, vt, ws=None, stream=None):
     import torch
     f32, bf = torch.float32, _bf16()
     _ok(lib().dit_qkv_rope(ctypes.byref(dims.c), _ptr(h, bf, "h"), L, N, _ptr(wqkv, bf, "wqkv"),
                            _ptr(q_norm, f32), _ptr(k_norm, f32), _ptr(txt_cos, f32), _ptr(txt_sin, f32),
                            _ptr(img_cos, f32), _ptr(img_sin, f32), _ptr(q, bf, "q"), _ptr(k, bf, "k"),
-                           _ptr(vt, bf, "vt"), _stream(stream)), "dit_qkv_rope")
+                           _ptr(vt, bf, "vt"), _ptr(ws), _ws_bytes(ws), _stream(stream)), "dit_qkv_rope")
 
 
 def dit_attention(dims: DitDims, R: int, q, k, vt, o, stream=None):
@@ -511,10 +522,10 @@ def dit_linear_gated(dims: DitDims, a, L: int, N: int, w, mod: Modulation, which
         "dit_linear_gated")
 
 
-def dit_linear_swiglu(dims: DitDims, h2, wup, a, stream=None):
+def dit_linear_swiglu(dims: DitDims, h2, wup, a, ws=None, stream=None):
     bf = _bf16()
     _ok(lib().dit_linear_swiglu(ctypes.byref(dims.c), _ptr(h2, bf, "h2"), h2.shape[0], _ptr(wup, bf, "wup"),
-                                _ptr(a, bf, "a"), _stream(stream)), "dit_linear_swiglu")
+                                _ptr(a, bf, "a"), _ptr(ws), _ws_bytes(ws), _stream(stream)), "dit_linear_swiglu")
 
 
 def dit_linear(a, w, out, stream=None):

@@ -336,9 +336,6 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.gate = mod.rows + 2LL * H;
   g.map = mod.map;
   g.gate_stride = 6LL * H;
-  // scratch for the K-split of the last wave: the SwiGLU buffer, not yet written
-  g.split_ws = b.a;
-  g.split_ws_bytes = size_t(R) * F * 2;
   if ((rc = w8 ? gemm8(1, b.o, H, kEpiGated, g) : gated_linear(1, b.o, H, w->wout, nullptr, g, post_attn, 2)) != DIT_OK)
     return rc;
 
@@ -363,9 +360,6 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   g.gate = mod.rows + 5LL * H;
   g.map = mod.map;
   g.gate_stride = 6LL * H;
-  // scratch for the K-split of the last wave: h, q, k, vt and o, all consumed by now
-  g.split_ws = b.h;
-  g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
   // (int8lin: the down GEMM waits for its weight, the side stream's last work: the join)
   return w8 ? gemm8(3, b.a, F, kEpiGated, g) : gated_linear(3, b.a, F, w->wdown, nullptr, g, post_mlp, 5);
 }
@@ -415,7 +409,7 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
     if ((r = gemm_launch(x, K, wc, nullptr, epi, g, st)) != DIT_OK) return r;
     return pf.done(i);
   };
-  auto gated = [&](int K, long long gate_row, void* split_ws, size_t split_bytes) {
+  auto gated = [&](int K, long long gate_row) {
     GemmParams g = base_params(R, H, K, err);
     g.txt = txt;
     g.img = img;
@@ -423,8 +417,6 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
     g.gate = mod.rows + gate_row * H;
     g.map = mod.map;
     g.gate_stride = 6LL * H;
-    g.split_ws = split_ws;
-    g.split_ws_bytes = split_bytes;
     return g;
   };
 
@@ -440,7 +432,7 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
                 nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
   // 4. x += gate_a * W8A8(o, Wout)
-  if ((rc = linear(1, b.o, H, kEpiGated, gated(H, 2, b.a, size_t(R) * F * 2))) != DIT_OK) return rc;
+  if ((rc = linear(1, b.o, H, kEpiGated, gated(H, 2))) != DIT_OK) return rc;
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m)
   mp.w = w->norm2;
   mp.shift = mod.rows + 3LL * H;
@@ -452,8 +444,7 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
   g.ldo = F;
   if ((rc = linear(2, b.h, H, kEpiSwiGLU, g)) != DIT_OK) return rc;
   // 7. x += gate_m * W8A8(a, Wdown)
-  return linear(3, b.a, F, kEpiGated,
-                gated(F, 5, b.h, size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h))));
+  return linear(3, b.a, F, kEpiGated, gated(F, 5));
 }
 
 // The parallel (single-stream) block [gizai:dit, Block.parallel]: one modulated LayerNorm feeds
@@ -529,9 +520,6 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
   g.map = mod.map;
   g.gate_stride = 3LL * H;
   g.k_split = H;
-  // scratch for the K-split of the last wave: h, q, k and vt, all consumed by now
-  g.split_ws = b.h;
-  g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.o) - reinterpret_cast<uint8_t*>(b.h));
   if (w8) {
     const uint16_t* s1;
     if ((rc = pf.use(1, &s1)) != DIT_OK) return rc;
@@ -650,8 +638,6 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, H, 2);
     g.m_split = L;
-    g.split_ws = b.a;
-    g.split_ws_bytes = size_t(R) * F * 2;
     if ((rc = before(1)) != DIT_OK) return rc;
     if ((rc = gemm_launch_cat(b.o, H, nullptr, 0, wt->wout, H, wi->wout, H, kEpiGated, g, st)) != DIT_OK) return rc;
     if ((rc = after(1)) != DIT_OK) return rc;
@@ -665,8 +651,6 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if ((rc = after(2)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, F, 5);
     g.m_split = L;
-    g.split_ws = b.h;
-    g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
     if ((rc = before(3)) != DIT_OK) return rc;
     return gemm_launch_cat(b.a, F, nullptr, 0, wt->wdown, F, wi->wdown, F, kEpiGated, g, st);
   }
@@ -690,13 +674,11 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, s1 ? 2 : 1, s0->w->q_norm,
                 s0->w->k_norm, s1 ? s1->w->q_norm : nullptr, s1 ? s1->w->k_norm : nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
-  // 4. x += gate_a * (o Wout^T), per stream (K-split scratch: the SwiGLU buffer, not yet written)
+  // 4. x += gate_a * (o Wout^T), per stream
   if ((rc = before(1)) != DIT_OK) return rc;
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, H, 2);
-    g.split_ws = b.a;
-    g.split_ws_bytes = size_t(R) * F * 2;
     if ((rc = gemm_launch(b.o + size_t(s.r0) * H, H, s.w->wout, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
   }
   if ((rc = after(1)) != DIT_OK) return rc;
@@ -713,13 +695,11 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wup, nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
   }
   if ((rc = after(2)) != DIT_OK) return rc;
-  // 7. x += gate_m * (a Wdown^T), per stream (K-split scratch: h, q, k, vt and o, consumed by now)
+  // 7. x += gate_m * (a Wdown^T), per stream
   if ((rc = before(3)) != DIT_OK) return rc;
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, F, 5);
-    g.split_ws = b.h;
-    g.split_ws_bytes = size_t(reinterpret_cast<uint8_t*>(b.a) - reinterpret_cast<uint8_t*>(b.h));
     if ((rc = gemm_launch(b.a + size_t(s.r0) * F, F, s.w->wdown, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
   }
   return DIT_OK;
@@ -841,6 +821,8 @@ int dit_check(dit_stream_t stream) {
   int v = 0;
   if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DIT_ECUDA;
   if (v != 0) {
+    // an aborted launch may leave stream-K arrivals counted: clear them with the error word
+    gemm_clear_stream_k_counters();
     const int z = 0;
     cudaMemcpy(p, &z, sizeof(int), cudaMemcpyHostToDevice);
     return DIT_ETIMEOUT;
@@ -1049,13 +1031,19 @@ int dit_modnorm(const dit_dims* d, const float* txt, int L, const float* img, in
   return modnorm_launch(mp, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t dit_stream_k_workspace_bytes(void) {
+  // two fp32 partial slots of a 128 x 256 tile slab per SM (CTA pairs: two slabs per pair unit)
+  return size_t(num_sms()) * 2 * 128 * 256 * sizeof(float);
+}
+
 int dit_qkv_rope(const dit_dims* d, const uint16_t* h, int L, int N, const uint16_t* wqkv, const float* q_norm,
                  const float* k_norm, const float* tc, const float* ts, const float* ic, const float* is, uint16_t* q,
-                 uint16_t* k, uint16_t* vt, dit_stream_t stream) {
+                 uint16_t* k, uint16_t* vt, void* ws, size_t ws_bytes, dit_stream_t stream) {
   if (!d || !h || !wqkv || !q || !k || !vt || L < 0 || N < 1 || !ic || !is || (L > 0 && (!tc || !ts)))
     return DIT_EINVAL;
   if (!dims_ok(d)) return DIT_EUNSUPPORTED;
   if (!al16(h) || !al16(wqkv) || !al16(q) || !al16(k) || !al16(vt)) return DIT_EINVAL;
+  if (ws && reinterpret_cast<uintptr_t>(ws) % 256 != 0) return DIT_EINVAL;
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden;
@@ -1076,6 +1064,8 @@ int dit_qkv_rope(const dit_dims* d, const uint16_t* h, int L, int N, const uint1
   g.k_norm = k_norm;
   g.qk_eps = d->qk_eps;
   g.rope_split = d->rope_split;
+  g.split_ws = ws_bytes ? ws : nullptr;
+  g.split_ws_bytes = ws ? ws_bytes : 0;
   return gemm_launch(h, H, wqkv, nullptr, kEpiQKV, g, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1124,16 +1114,19 @@ int dit_linear_gated(const dit_dims* d, const uint16_t* a, int L, int N, const u
   return gemm_launch(a, K, w, nullptr, kEpiGated, g, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int dit_linear_swiglu(const dit_dims* d, const uint16_t* h2, int R, const uint16_t* wup, uint16_t* a,
-                      dit_stream_t stream) {
+int dit_linear_swiglu(const dit_dims* d, const uint16_t* h2, int R, const uint16_t* wup, uint16_t* a, void* ws,
+                      size_t ws_bytes, dit_stream_t stream) {
   if (!d || !h2 || !wup || !a || R < 1) return DIT_EINVAL;
   if (!dims_ok(d)) return DIT_EUNSUPPORTED;
   if (!al16(h2) || !al16(wup) || !al16(a)) return DIT_EINVAL;
+  if (ws && reinterpret_cast<uintptr_t>(ws) % 256 != 0) return DIT_EINVAL;
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   GemmParams g = base_params(R, 2 * d->ffn, d->hidden, err);
   g.out = a;
   g.ldo = d->ffn;
+  g.split_ws = ws_bytes ? ws : nullptr;
+  g.split_ws_bytes = ws ? ws_bytes : 0;
   return gemm_launch(h2, d->hidden, wup, nullptr, kEpiSwiGLU, g, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -23,6 +23,7 @@
 //               transposed v store for the attention kernel (klein article, section 4.4)
 //   kEpiQKVSwiGLU  kEpiQKV on the columns below n_split, kEpiSwiGLU above (the parallel block)
 #include <atomic>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,6 +39,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+constexpr int kSkMaxParts = 3;  // stream-K segments per tile at most (the plan guarantees it)
 
 template <int BN, bool B8, bool PAIR = false>
 struct GemmCfg {
@@ -428,27 +430,63 @@ __device__ __forceinline__ void convert_kblock(const uint8_t* src8, const uint16
 }
 
 // ----------------------------------------------------------------------------------------------
-// Work items of the persistent loop. With p.split > 1, the tiles from p.sk_first on (as many as
-// the last, partial wave would hold) are each cut into p.split equal K-ranges, and these parts come
-// first: they spread that wave's work over all SMs, and each split tile is finished while whole
-// tiles still run, so the kernel ends on ordinary tiles. Then come the whole tiles 0 .. sk_first-1.
+// Work items of the persistent loop. Without stream-K (p.sk_tiles == 0) unit u takes tiles u,
+// u + units, ... whole. With stream-K the last p.sk_tiles tiles (in tile order) form a region whose
+// k-blocks, sk_tiles * KB of them in tile-major order, are cut into p.sk_units equal ranges; unit u
+// first works through its range, tile segment by tile segment, then takes (tiles - sk_tiles) /
+// sk_units whole tiles (an exact quotient by construction). Every unit thus does the same number of
+// k-blocks to within one, whatever the tile count, and the partial tiles come first, so the work of
+// finishing them overlaps whole tiles' mainloops. A range covers at most two partial segments (the
+// one it starts in and the one it ends in), each with a slot of its own.
 // ----------------------------------------------------------------------------------------------
 struct WorkItem {
-  int tile, k0, k1, part;  // part < 0: the whole tile
+  int tile, k0, k1;
+  int part;      // < 0: the whole tile; else this segment's index among the tile's segments
+  int nparts;    // segments of the tile
+  int u_first;   // unit of the tile's first segment (segment i is unit u_first + i's)
+  int trel;      // tile index within the stream-K region
 };
-__device__ __forceinline__ WorkItem work_item(const GemmParams& p, int it, int tiles, int KB) {
-  if (p.split <= 1) return WorkItem{it, 0, KB, -1};
-  const int n_parts = (tiles - p.sk_first) * p.split;
-  if (it >= n_parts) return WorkItem{it - n_parts, 0, KB, -1};
-  const int part = it % p.split, kl = KB / p.split;
-  return WorkItem{p.sk_first + it / p.split, part * kl, (part + 1) * kl, part};
+
+__host__ __device__ __forceinline__ int sk_begin(const GemmParams& p, int u, int KB) {
+  return int((long long)u * p.sk_tiles * KB / p.sk_units);  // first k-block of unit u's range
+}
+// The unit whose range holds region k-block a: the largest u with sk_begin(u) <= a.
+__host__ __device__ __forceinline__ int sk_unit_of(const GemmParams& p, int a, int KB) {
+  const long long S = (long long)p.sk_tiles * KB;
+  return int(((long long)(a + 1) * p.sk_units + S - 1) / S) - 1;
+}
+__host__ __device__ __forceinline__ int sk_segments(const GemmParams& p, int u, int KB) {
+  const int a0 = sk_begin(p, u, KB), a1 = sk_begin(p, u + 1, KB);
+  return a1 > a0 ? (a1 - 1) / KB - a0 / KB + 1 : 0;
+}
+__host__ __device__ __forceinline__ int unit_items(const GemmParams& p, int u, int units, int tiles, int KB) {
+  if (p.sk_tiles <= 0) return u < tiles ? (tiles - u + units - 1) / units : 0;
+  return sk_segments(p, u, KB) + (tiles - p.sk_tiles) / units;
+}
+__host__ __device__ __forceinline__ WorkItem unit_item(const GemmParams& p, int u, int i, int units, int tiles,
+                                                       int KB) {
+  if (p.sk_tiles <= 0) return WorkItem{u + i * units, 0, KB, -1, 1, 0, 0};
+  const int nseg = sk_segments(p, u, KB);
+  if (i >= nseg) return WorkItem{u + (i - nseg) * units, 0, KB, -1, 1, 0, 0};
+  const int a0 = sk_begin(p, u, KB), a1 = sk_begin(p, u + 1, KB);
+  const int trel = a0 / KB + i;
+  const int k0 = i == 0 ? a0 - trel * KB : 0;
+  const int k1 = i == nseg - 1 ? a1 - trel * KB : KB;
+  const int tile = tiles - p.sk_tiles + trel;
+  if (k0 == 0 && k1 == KB) return WorkItem{tile, 0, KB, -1, 1, 0, trel};
+  const int uf = sk_unit_of(p, trel * KB, KB), ul = sk_unit_of(p, trel * KB + KB - 1, KB);
+  return WorkItem{tile, k0, k1, u - uf, ul - uf + 1, uf, trel};
+}
+// Partial slot of unit v's segment on region tile trel: 2v for the tile its range starts in, 2v + 1
+// for the tile it ends in.
+__host__ __device__ __forceinline__ int sk_slot(const GemmParams& p, int v, int trel, int KB) {
+  return 2 * v + (sk_begin(p, v, KB) < trel * KB ? 1 : 0);
 }
 
-// Gated residual of a K-split tile, part 1: the warp's 32 rows of its partial accumulator go to
-// their slot (fp32, row stride BN) through the shared transpose, as whole 128-byte lines.
+// A warp's 32 rows x BN fp32 partial accumulator to its slot, in the thread-per-row layout
+// [32-column chunk][float4 of the chunk][lane]: every store instruction writes 512 contiguous bytes.
 template <int BN>
-__device__ __forceinline__ void split_store(uint32_t taddr, float* slot, int lane, uint8_t* stage) {
-  const int cq = lane & 7;
+__device__ __forceinline__ void sk_store(uint32_t taddr, float* dst, int lane) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t v[32];
@@ -456,69 +494,68 @@ __device__ __forceinline__ void split_store(uint32_t taddr, float* slot, int lan
     tmem_ld_wait();
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      *reinterpret_cast<uint4*>(stage + lane * 128 + ((q ^ (lane & 7)) << 4)) =
-          make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rl = (lane >> 3) + 4 * i;
-      const float4 a = *reinterpret_cast<const float4*>(stage + rl * 128 + ((cq ^ (rl & 7)) << 4));
-      __stcg(reinterpret_cast<float4*>(slot + rl * BN + c * 32 + cq * 4), a);
-    }
-    __syncwarp();
+      __stcg(reinterpret_cast<float4*>(dst) + (c * 8 + q) * 32 + lane,
+             make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                         __uint_as_float(v[4 * q + 3])));
   }
 }
 
-// Part 2, run by the warp that delivered a quadrant's last partial: acc = ((p0 + p1) + p2) ...
-// in part order (the same sum whichever warp finishes last), then x += gate * acc. Every load of a
-// group of four rows is issued before the first add.
-template <int BN, int S>
-__device__ __forceinline__ void split_finish(const GemmParams& p, const float* parts, int row0, int row_end, int n0,
-                                             int lane) {
-  const int cq = lane & 7;
-  constexpr size_t kSlot = size_t(BM) * BN;
+// The warp that delivered a tile quadrant's last segment: the sum of all segments' partials, in
+// segment order (((p0 + p1) + p2) ..., the same whichever unit finishes), written over its own
+// accumulator in TMEM; W8A8 accumulators (exact integer sums) are scaled by the row's and the
+// column's scales after the sum, as a whole tile's are. The epilogue then runs on it unchanged.
+// `part(i)` is segment i's slot (this warp's rows). The loads of parts 0 and 1 of a chunk are issued
+// together (one L2 round trip for the usual two-part tile), a third part's after them.
+template <int BN, typename PartFn>
+__device__ __forceinline__ void sk_sum(const GemmParams& p, uint32_t taddr, PartFn part, int nparts, int lane, int row,
+                                       int row_end, int n0) {
+  static_assert(kSkMaxParts == 3, "parts 0 and 1 together, then part 2");
+  const float sa = (p.a_scale && row < row_end) ? __ldg(p.a_scale + row) : 0.f;
+  const float4* s0 = reinterpret_cast<const float4*>(part(0)) + lane;
+  const float4* s1 = reinterpret_cast<const float4*>(part(1)) + lane;
+  const float4* s2 = reinterpret_cast<const float4*>(part(nparts > 2 ? 2 : 1)) + lane;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
+    float4 a[8], b[8];  // chunk c of a part: 8 float4 at part + c * 256 + q * 32
 #pragma unroll
-    for (int ih = 0; ih < 2; ++ih) {
-      float4 v[4][S], xq[4], gq[4];
-      float* xr[4];
+    for (int q = 0; q < 8; ++q) {
+      a[q] = __ldcg(s0 + c * 256 + q * 32);
+      b[q] = __ldcg(s1 + c * 256 + q * 32);
+    }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int rl = (lane >> 3) + 4 * (4 * ih + u), r = row0 + rl;
-        const float* src = parts + rl * BN + c * 32 + cq * 4;
+    for (int q = 0; q < 8; ++q) {
+      a[q].x += b[q].x;
+      a[q].y += b[q].y;
+      a[q].z += b[q].z;
+      a[q].w += b[q].w;
+    }
+    if (nparts > 2) {
 #pragma unroll
-        for (int q = 0; q < S; ++q) v[u][q] = __ldcg(reinterpret_cast<const float4*>(src + q * kSlot));
-        xr[u] = nullptr;
-        if (r < row_end) {
-          const int sr = r + p.row_off;  // sequence row
-          xr[u] = (sr < p.L ? p.txt + size_t(sr) * p.N : p.img + size_t(sr - p.L) * p.N) + n0 + c * 32 + cq * 4;
-          xq[u] = *reinterpret_cast<const float4*>(xr[u]);
-          gq[u] = __ldg(reinterpret_cast<const float4*>(p.gate + size_t(p.map ? __ldg(p.map + sr) : 0) * p.gate_stride +
-                                                        n0 + c * 32 + cq * 4));
-        }
-      }
+      for (int q = 0; q < 8; ++q) b[q] = __ldcg(s2 + c * 256 + q * 32);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float4 a = v[u][0];
-#pragma unroll
-        for (int q = 1; q < S; ++q) {
-          a.x += v[u][q].x;
-          a.y += v[u][q].y;
-          a.z += v[u][q].z;
-          a.w += v[u][q].w;
-        }
-        if (xr[u]) {
-          float4 o;
-          o.x = fmaf(gq[u].x, a.x, xq[u].x);
-          o.y = fmaf(gq[u].y, a.y, xq[u].y);
-          o.z = fmaf(gq[u].z, a.z, xq[u].z);
-          o.w = fmaf(gq[u].w, a.w, xq[u].w);
-          *reinterpret_cast<float4*>(xr[u]) = o;
-        }
+      for (int q = 0; q < 8; ++q) {
+        a[q].x += b[q].x;
+        a[q].y += b[q].y;
+        a[q].z += b[q].z;
+        a[q].w += b[q].w;
       }
     }
+    uint32_t v[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[4 * q] = __float_as_uint(a[q].x);
+      v[4 * q + 1] = __float_as_uint(a[q].y);
+      v[4 * q + 2] = __float_as_uint(a[q].z);
+      v[4 * q + 3] = __float_as_uint(a[q].w);
+    }
+    if (p.a_scale) {
+      const float* sw = p.w_scale + n0 + c * 32;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sa * __ldg(sw + j));
+    }
+    tmem_st32(taddr + c * 32, v);
   }
+  tmem_st_wait();
 }
 
 // Row tiles of a GEMM. With two row groups (m_split > 0) whose boundary is not on a tile boundary,
@@ -553,6 +590,13 @@ __device__ __forceinline__ TileRows tile_rows(const GemmParams& p, int tile_m, i
 // use different words.
 constexpr int kPairSlots = 64, kPairMaxCtas = 256;
 __device__ uint32_t g_pair_started[kPairSlots * kPairMaxCtas];
+
+// Stream-K arrival counters, one set per launch slot (launches take the kSkSlots sets in turn, so
+// launches running at once on different streams count on different sets). The warp that brings a
+// counter to its tile's segment count sets it back to zero, so every launch that finishes leaves
+// its set at zero; an aborted launch may not, and dit_check() clears them all when it reports one.
+constexpr int kSkSlots = 64, kSkMaxCounters = 2048;
+__device__ uint32_t g_sk_cnt[kSkSlots * kSkMaxCounters];
 
 template <int BN, int EPI, bool B8, bool PAIR>
 __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
@@ -604,7 +648,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
   };
   const int tiles = num_m * num_n;
   const int KB = p.K / BK;
-  const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
+  const int items = unit_items(p, unit, units, tiles, KB);  // this unit's work items
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -677,8 +721,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
       constexpr bool kLocalFull = !PAIR || B8;
       constexpr uint32_t kOwnBytes = Cfg::kABytes + (B8 ? Cfg::kB8Bytes + Cfg::kSBytes : Cfg::kBLoad);
       const uint32_t full0 = kLocalFull ? smem_u32(&full[0]) : mapa_shared(smem_u32(&full[0]), 0);
-      for (int it = unit; it < items && ok; it += units) {
-        const WorkItem w = work_item(p, it, tiles, KB);
+      for (int it = 0; it < items && ok; ++it) {
+        const WorkItem w = unit_item(p, unit, it, units, tiles, KB);
         int mb, nb;
         tile_mn(w.tile, mb, nb);
         const TileRows tr = tile_rows(p, Cfg::kTileM, mb);
@@ -732,8 +776,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int it = unit; it < items && ok; it += units) {
-        const WorkItem w = work_item(p, it, tiles, KB);
+      for (int it = 0; it < items && ok; ++it) {
+        const WorkItem w = unit_item(p, unit, it, units, tiles, KB);
         if (!(PAIR ? mbar_wait_cluster(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, kErrTimeoutMma)
                    : mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, p.err, kErrTimeoutMma)))
           break;
@@ -797,21 +841,50 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
     const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : smem_u32(&tempty[0]);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int it = unit; it < items; it += units) {
-      const WorkItem w = work_item(p, it, tiles, KB);
+    for (int it = 0; it < items; ++it) {
+      const WorkItem w = unit_item(p, unit, it, units, tiles, KB);
       int mb, nb;
       tile_mn(w.tile, mb, nb);
       const TileRows tr = tile_rows(p, Cfg::kTileM, mb);
       if (!mbar_wait_warp(smem_u32(&tfull[acc]), acc_phase, p.err, kErrTimeoutEpilogue)) break;
       tc_fence_after();
       if constexpr (!B8) {
-        if (p.a_scale) {
+        static_assert(B8 || Cfg::kEpiCols == BN, "one epilogue warp per TMEM lane quadrant");
+        const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
+        const int row = tr.base + rows_of + quad * 32 + lane;
+        bool scaled = false;
+        if (w.part >= 0) {
+          // stream-K segment: publish this warp's partial, count it, and if it was the quadrant's
+          // last segment sum them all into this accumulator and go on to the epilogue; otherwise
+          // release the accumulator
+          constexpr int kSlabs = PAIR ? 2 : 1;
+          const size_t slab = size_t(BM) * BN, warp_off = size_t(quad) * 32 * BN;
+          float* mine = p.sk_part + (size_t(sk_slot(p, unit, w.trel, KB)) * kSlabs + rank) * slab + warp_off;
+          sk_store<BN>(taddr, mine, lane);
+          __threadfence();
+          __syncwarp();
+          uint32_t* cnt = p.sk_cnt + (w.trel * kSlabs + int(rank)) * 4 + quad;
+          int last = 0;
+          if (lane == 0) last = atomicAdd(cnt, 1u) == uint32_t(w.nparts - 1);
+          if (!__shfl_sync(0xffffffffu, last, 0)) {
+            tc_fence_before();
+            if constexpr (PAIR) mbar_arrive_cluster(tempty0 + uint32_t(acc) * 8u);
+            else mbar_arrive(smem_u32(&tempty[acc]));
+            if (++acc == Cfg::kAccBufs) { acc = 0; acc_phase ^= 1; }
+            continue;
+          }
+          __threadfence();
+          auto part = [&](int i) -> const float* {
+            return p.sk_part + (size_t(sk_slot(p, w.u_first + i, w.trel, KB)) * kSlabs + rank) * slab + warp_off;
+          };
+          sk_sum<BN>(p, taddr, part, w.nparts, lane, row, tr.end, nb * BN);
+          if (lane == 0) atomicExch(cnt, 0u);  // zero again for the next launch
+          scaled = true;
+        }
+        if (p.a_scale && !scaled) {
           // W8A8: the accumulator holds exact integer dot products of codes; scale it in place by
           // the row's and the column's scales, then run the epilogue on it as usual
-          static_assert(Cfg::kEpiCols == BN, "one epilogue warp per TMEM lane quadrant");
-          const int row = tr.base + rows_of + quad * 32 + lane;
           const float sa = row < tr.end ? __ldg(p.a_scale + row) : 0.f;
-          const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t v[32];
@@ -823,31 +896,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
             tmem_st32(taddr + c * 32, v);
           }
           tmem_st_wait();
-        }
-      }
-      if constexpr (EPI == kEpiGated && !B8) {
-        if (w.part >= 0) {
-          // K-split tile: publish this part, release the accumulator, and let the warp that
-          // delivers the quadrant's last part apply the residual update
-          const int ti = (w.tile - p.sk_first) * (PAIR ? 2 : 1) + int(rank);  // 128-row slab
-          float* parts = p.split_part + size_t(ti) * p.split * BM * BN + size_t(quad) * 32 * BN;
-          const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
-          split_store<BN>(taddr, parts + size_t(w.part) * BM * BN, lane, stage);
-          tc_fence_before();
-          if constexpr (PAIR) mbar_arrive_cluster(tempty0 + uint32_t(acc) * 8u);
-          else mbar_arrive(smem_u32(&tempty[acc]));
-          if (++acc == Cfg::kAccBufs) { acc = 0; acc_phase ^= 1; }
-          __threadfence();
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) last = atomicAdd(p.split_cnt + ti * 4 + quad, 1) == p.split - 1;
-          if (__shfl_sync(0xffffffffu, last, 0)) {
-            __threadfence();
-            const int r0 = tr.base + rows_of + quad * 32, n0 = nb * BN;
-            if (p.split == 2) split_finish<BN, 2>(p, parts, r0, tr.end, n0, lane);
-            else split_finish<BN, 3>(p, parts, r0, tr.end, n0, lane);
-          }
-          continue;
         }
       }
 #pragma unroll 1
@@ -877,8 +925,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
     bool ok = true;
     // PAIR: the converted tile is read by the first CTA's MMAs, whose barrier counts both CTAs
     const uint32_t cfull0 = PAIR ? mapa_shared(smem_u32(&cfull[0]), 0) : smem_u32(&cfull[0]);
-    for (int it = unit; it < items && ok; it += units) {
-      const WorkItem w = work_item(p, it, tiles, KB);
+    for (int it = 0; it < items && ok; ++it) {
+      const WorkItem w = unit_item(p, unit, it, units, tiles, KB);
       for (int kb = w.k0; kb < w.k1; ++kb) {
         // warp-uniform verdicts: the warp meets again at the __syncwarp below
         if (!mbar_wait_warp(smem_u32(&full[stage]), phase, p.err, kErrTimeoutConverter)) { ok = false; break; }
@@ -946,6 +994,55 @@ int resident_units(const void* kern, bool pair, unsigned threads, unsigned smem)
 }
 
 std::atomic<uint32_t> g_pair_launches{0};
+std::atomic<uint32_t> g_sk_launches{0};
+
+// Device address of g_sk_cnt on the current device (looked up once per device).
+uint32_t* sk_counters() {
+  static uint32_t* addr[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sk_cnt) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return addr[dev];
+}
+
+// Stream-K plan of a bf16 launch over `units` work units of `slabs` 128-row slabs and tiles of BN
+// columns: sets q.sk_* when it pays, else leaves q.sk_tiles = 0. With W whole waves and rem < units
+// tiles over, the region is the last rem tiles (or rem + units when rem is below half the units, so
+// that each unit's share stays at least half a tile and a tile meets at most three units); the
+// critical path drops from W + 1 to W + rem / units tile-times, taken when that saves at least a
+// tenth of a tile. Needs two partial slots per unit in the caller's scratch and at least eight
+// k-blocks per tile.
+void plan_stream_k(GemmParams& q, int tiles, int units, int slabs, int BN) {
+  q.sk_tiles = 0;
+  const int KB = q.K / BK;
+  if (!q.split_ws || units < 2 || KB < 8) return;
+  const int W = tiles / units, rem = tiles % units;
+  if (rem == 0 || 10 * rem > 9 * units) return;
+  int sk = rem;
+  if (2 * sk < units) {
+    if (W == 0) return;
+    sk += units;
+  }
+  if (sk * slabs * 4 > kSkMaxCounters) return;
+  if (size_t(2) * units * slabs * BM * BN * sizeof(float) > q.split_ws_bytes) return;
+  GemmParams t = q;
+  t.sk_tiles = sk;
+  t.sk_units = units;
+  for (int r = 0; r < sk; ++r)
+    if (sk_unit_of(t, r * KB + KB - 1, KB) - sk_unit_of(t, r * KB, KB) + 1 > kSkMaxParts) return;
+  uint32_t* cnt = sk_counters();
+  if (!cnt) return;
+  q.sk_tiles = sk;
+  q.sk_units = units;
+  q.sk_part = static_cast<float*>(q.split_ws);
+  q.sk_cnt = cnt + size_t(g_sk_launches.fetch_add(1, std::memory_order_relaxed) % kSkSlots) * kSkMaxCounters;
+}
 
 template <int BN, int EPI, bool B8, bool PAIR>
 int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
@@ -960,14 +1057,15 @@ int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
     units_cached[dev] = resident_units(reinterpret_cast<const void*>(kern), PAIR, Cfg::kThreads, Cfg::kSmemBytes);
   const int units_max = units_cached[dev];
   const int tiles = row_tiles(p, Cfg::kTileM) * (p.N / BN);
-  const int items = p.split > 1 ? p.sk_first + (tiles - p.sk_first) * p.split : tiles;
-  const int units = items < units_max ? items : units_max;
+  GemmParams q = p;
+  if constexpr (!B8) plan_stream_k(q, tiles, units_max, PAIR ? 2 : 1, BN);
+  else q.sk_tiles = 0;
+  const int units = q.sk_tiles > 0 ? units_max : (tiles < units_max ? tiles : units_max);
   if constexpr (!PAIR) {
-    kern<<<units, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(m.a, m.b, m.s, m.a2, m.b2, p);
+    kern<<<units, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(m.a, m.b, m.s, m.a2, m.b2, q);
     return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
   } else {
     if (2 * units > kPairMaxCtas) return DIT_EUNSUPPORTED;
-    GemmParams q = p;
     q.pair_epoch = g_pair_launches.fetch_add(1, std::memory_order_relaxed);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(2 * units));
@@ -1013,44 +1111,8 @@ int pick_bn(int N) { return (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64); }
 // one MMA issue covers both. Needs tiles at least 128 wide and more than one 128-row block.
 bool use_pair(int BN, const GemmParams& p) { return BN >= 128 && p.M > BM && num_sms() >= 2; }
 
-// bf16 weights: the K-split plan of the gated epilogue, then the launch
-int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& p, bool pair, cudaStream_t stream) {
-  GemmParams q = p;
-  q.split = 1;
-  if (epi == kEpiGated && p.split_ws) {
-    // The last wave holds tail < SMs tiles: cut each into s = 2 or 3 K-ranges (s divides K/64)
-    // when that shortens the critical path, counted in tile-times: waves + ceil(tail s / SMs) / s
-    // (e.g. 396 tiles on 152 SMs: 3 tile-times whole, 2.67 with s = 3). Each part keeps at least 32
-    // k-blocks: finishing a split tile reads s partials besides x and the gate, and only a long
-    // mainloop hides that (measured at 4224 rows, hidden 3072: K = 12288 222 -> 209 us with s = 3,
-    // K = 3072 71 -> 127 us). The partial slots and the arrival counters live in the caller's
-    // scratch; the counters start at zero.
-    const int TM = pair ? 2 * BM : BM, slabs = pair ? 2 : 1;  // rows of a tile, 128-row slabs in it
-    const int T = row_tiles(p, TM) * (p.N / BN), P = pair ? num_sms() / 2 : num_sms(), KB = p.K / BK;
-    if (T > P && T % P != 0) {
-      const int waves = T / P, tail = T - waves * P;
-      double best = waves + 1.0;
-      size_t slot_bytes = 0;
-      for (int sp : {2, 3}) {
-        if (KB % sp != 0 || KB / sp < 32) continue;
-        const size_t sb = (size_t(tail) * slabs * sp * BM * BN * 4 + 255) / 256 * 256;
-        if (sb + size_t(tail) * slabs * 4 * sizeof(int) > p.split_ws_bytes) continue;
-        const double c = waves + double((tail * sp + P - 1) / P) / sp;
-        if (c < best - 1e-9) {
-          best = c;
-          q.split = sp;
-          slot_bytes = sb;
-        }
-      }
-      if (q.split > 1) {
-        q.sk_first = waves * P;
-        q.split_part = static_cast<float*>(p.split_ws);
-        q.split_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(p.split_ws) + slot_bytes);
-        if (cudaMemsetAsync(q.split_cnt, 0, size_t(tail) * slabs * 4 * sizeof(int), stream) != cudaSuccess)
-          return DIT_ECUDA;
-      }
-    }
-  }
+// bf16 weights: the launch (stream-K is planned per kernel in launch_one, which knows its units)
+int launch_bf16(const Maps& m, int BN, int epi, const GemmParams& q, bool pair, cudaStream_t stream) {
   switch (BN) {
     case 256: return pair ? dispatch_epi<256, false, true>(epi, m, q, stream) : dispatch_epi<256, false, false>(epi, m, q, stream);
     case 128: return pair ? dispatch_epi<128, false, true>(epi, m, q, stream) : dispatch_epi<128, false, false>(epi, m, q, stream);
@@ -1122,6 +1184,12 @@ int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmI
   m.a2 = m.a;
   m.b2 = m.b;
   return launch_bf16(m, BN, epi, p, pair, stream);
+}
+
+int gemm_clear_stream_k_counters() {
+  uint32_t* cnt = sk_counters();
+  if (!cnt) return DIT_ECUDA;
+  return cudaMemset(cnt, 0, sizeof(uint32_t) * kSkSlots * kSkMaxCounters) == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
 int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long long lda2, const uint16_t* b,

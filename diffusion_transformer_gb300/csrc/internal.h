@@ -45,13 +45,16 @@ struct GemmParams {
   const float *q_norm, *k_norm;                         // [d] or null
   float qk_eps;
   int rope_split;  // 0: adjacent pairs, tables [rows, d/2]; 1: split halves over 3d/4, tables [rows, 3d/8]
-  // gated residual, bf16 weights: scratch for the K-split of the last, partial wave of tiles (may be
-  // null: no split). Set by gemm_launch: split ways, first split tile, partial slots and counters.
+  // bf16 weights: caller scratch for stream-K (may be null: every tile whole). When the tiles are
+  // not a whole number of waves, gemm_launch divides the k-blocks of the last sk_tiles tiles evenly
+  // over the sk_units work units (CTAs or CTA pairs); a unit's share of a tile is a segment whose
+  // fp32 partial accumulator goes to one of its two slots, and the unit that delivers a tile's
+  // last segment sums the segments in order and runs the epilogue. Set by gemm_launch.
   void* split_ws;
   size_t split_ws_bytes;
-  int split, sk_first;
-  float* split_part;   // [tail tiles][split][128][BN] fp32
-  int* split_cnt;      // [tail tiles][4] arrivals per 32-row quadrant
+  int sk_tiles, sk_units;
+  float* sk_part;      // partial slots [2 * sk_units][slabs][128][BN] fp32 (slabs: 2 on CTA pairs)
+  uint32_t* sk_cnt;    // arrivals per (stream-K tile, slab, 32-row quadrant); zero between launches
   // concatenated operands (0 = none): output columns >= n_split take B rows from the second B
   // (row n - n_split); inner indices >= k_split take A and B columns from the second A and B
   // (column k - k_split)
@@ -96,6 +99,9 @@ int gemm_launch_cat(const uint16_t* a, long long lda, const uint16_t* a2, long l
                     cudaStream_t stream);
 int gemm_launch(const uint16_t* a, long long lda, const uint16_t* b, const GemmInt8B* b8, int epi,
                 const GemmParams& p, cudaStream_t stream);
+// Zero the stream-K arrival counters of the current device (after an aborted launch, which may
+// leave some counted; dit_check does this when it finds the error word set). Synchronous.
+int gemm_clear_stream_k_counters();
 
 // ------------------------------------------------------------------------------------------
 // attention

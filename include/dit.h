@@ -360,14 +360,28 @@ DIT_API size_t dit_denoise_workspace_bytes(const dit_model* model, int L, int N,
 DIT_API int dit_modnorm(const dit_dims* dims, const float* txt, int L, const float* img, int N, const float* w,
                 const dit_mod* mod, int which, uint16_t* h, dit_stream_t stream);
 
+/* Stream-K scratch (no counterpart on the pages: a scheduling device of this library). The linears
+ * below that take `ws` / `ws_bytes` run stream-K when their output tiles do not fill a whole number
+ * of waves over the SMs and the scratch holds dit_stream_k_workspace_bytes(): the k-blocks of the
+ * last tiles are divided evenly over all work units, each unit's share of a tile goes to the
+ * scratch as an fp32 partial sum, and the unit that delivers a tile's last share adds the shares
+ * in a fixed order and runs the epilogue (the result does not depend on timing; it differs from
+ * the whole-tile result by the order of fp32 additions only). ws may be NULL (every tile whole);
+ * when given it must be 256-byte aligned and not overlap the call's other buffers. The block calls
+ * run their linears on whole tiles: on a GB300 at its power limit the partial sums cost energy and
+ * bought no time (the GEMMs run at clocks the power limit sets, so an idle tail wave is not lost
+ * time the way it is at a fixed clock). */
+DIT_API size_t dit_stream_k_workspace_bytes(void);
+
 /* QKV linear with its fused epilogue [gizai:dit, prepOf; klein, section 4.4]: qkv = h Wqkv^T;
  * q and k heads RMS-normed (times q_norm / k_norm, NULL = ones) then rotated by the tables;
  * stored bf16 as q, k [heads, R, d] (R = L + N) and v transposed as vt [heads, d, Rp] with
- * Rp = dit_vt_stride(R) (columns >= R unused). h [R, H] bf16. */
+ * Rp = dit_vt_stride(R) (columns >= R unused). h [R, H] bf16. ws / ws_bytes: optional stream-K
+ * scratch (see dit_stream_k_workspace_bytes). */
 DIT_API int dit_qkv_rope(const dit_dims* dims, const uint16_t* h, int L, int N, const uint16_t* wqkv,
                  const float* q_norm, const float* k_norm, const float* txt_cos, const float* txt_sin,
                  const float* img_cos, const float* img_sin, uint16_t* q, uint16_t* k, uint16_t* vt,
-                 dit_stream_t stream);
+                 void* ws, size_t ws_bytes, dit_stream_t stream);
 DIT_API int dit_vt_stride(int R);
 
 /* Joint attention [klein, section 4.3]: o[r, n*d + j] = sum_c softmax_c(q_n[r] . k_n[c] / sqrt(d))
@@ -389,19 +403,16 @@ DIT_API int dit_attention_qknorm(const dit_dims* dims, int R, const uint16_t* q,
 /* Linear with gated residual [gizai:dit, gatedInto]: x[r] += gate[map[r]] * (a[r] W^T) for the
  * attention (which = 0, W = wout [H, H], a [R, H]) or the MLP (which = 1, W = wdown [H, F],
  * a [R, F]) gate of the modulation rows. x rows < L in txt, others in img.
- * ws / ws_bytes: optional device scratch (NULL / 0 allowed; 256-byte aligned). When the output
- * tiles do not fill a whole number of waves over the SMs, the tiles of the last wave are split
- * along K into partial sums that fit in the scratch and added in a fixed order (the result does
- * not depend on timing); ((R + 127) / 128 * 128) * H * 12 + 4096 bytes always suffice. Without
- * scratch every tile is computed whole. */
+ * ws / ws_bytes: optional stream-K scratch (see dit_stream_k_workspace_bytes). */
 DIT_API int dit_linear_gated(const dit_dims* dims, const uint16_t* a, int L, int N, const uint16_t* w,
                      const dit_mod* mod, int which, float* txt, float* img, void* ws, size_t ws_bytes,
                      dit_stream_t stream);
 
 /* Up linear with SwiGLU epilogue [gizai:dit, gluRows]: u = h2 Wup^T [R, 2F];
- * a[r, j] = bf16(silu(u[r, 2j]) * u[r, 2j+1]) [R, F]. */
+ * a[r, j] = bf16(silu(u[r, 2j]) * u[r, 2j+1]) [R, F]. ws / ws_bytes: optional stream-K scratch
+ * (see dit_stream_k_workspace_bytes). */
 DIT_API int dit_linear_swiglu(const dit_dims* dims, const uint16_t* h2, int R, const uint16_t* wup, uint16_t* a,
-                      dit_stream_t stream);
+                      void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* Plain linear: out = a W^T with a [M, K] bf16, W [N, K] bf16; out fp32 (out_bf16 = 0) or bf16
  * (out_bf16 = 1), [M, N]. Supports K % 64 == 0 and N % 64 == 0. */

@@ -236,46 +236,6 @@ def test_gated_epilogue(shape, M, which):
     assert np.all(np.abs(got - ref) <= tol), float(np.abs(got - ref).max())
 
 
-@pytest.mark.parametrize("L,gh,gw,splits", [(128, 56, 64, True), (100, 41, 80, True), (128, 64, 64, False)])
-def test_gated_split_last_wave(L, gh, gw, splits):
-    which = 1
-    # The MLP linear (K = 12288, hidden 3072) on CTA pairs: 256 x 256 output tiles over 76 pairs. At
-    # R = 3712 (15 row blocks, 180 tiles) or 3380 (14, 168) the last wave holds 28 or 16 tiles, so with
-    # scratch they are split along K (two parts of 6144, three of 4096); at R = 4224 (204 tiles, 52 in
-    # the last wave) no split shortens the critical path and none is taken. The split result is
-    # deterministic, differs from the unsplit kernel only by the order of the fp32 partial sums, and
-    # matches the float64 definition on rows of the split tiles and the ragged last tile.
-    sh = DI.BlockShape(f"split_{L}_{gh}x{gw}", 3072, 24, 128, 12288, L, gh, gw, seed=21 + L)
-    inp = DI.block_inputs(sh)
-    g = np.random.default_rng(6)
-    K = sh.hidden if which == 0 else sh.ffn
-    A = _bf16_rand(g, (sh.R, K), 1.0)
-    W = inp.wout if which == 0 else inp.wdown
-    dims, a, w = dims_of(sh), dev_bf16(A), dev_bf16(W)
-    mod = D.Modulation(dev(inp.mod), dev(inp.mod_map))
-    ws = workspace(((sh.R + 127) // 128 * 128) * sh.hidden * 12 + 4096)
-    outs = []
-    for scratch in (ws, ws, None):
-        txt, img = dev(inp.txt), dev(inp.img)
-        D.dit_linear_gated(dims, a, sh.L, sh.N, w, mod, which, txt, img, ws=scratch)
-        D.dit_check()
-        outs.append(np.concatenate([txt.cpu().numpy(), img.cpu().numpy()]).astype(np.float64))
-    split, split2, whole = outs
-    assert np.array_equal(split, split2)
-    assert np.array_equal(split, whole) != splits  # the split path ran (different summation order) or not
-    x = np.concatenate([inp.txt, inp.img]).astype(np.float64)
-    gate = inp.mod[inp.mod_map, 2 if which == 0 else 5].astype(np.float64)
-    Af, Wf = O.bf16_to_f64(A), O.bf16_to_f64(W)
-    # |split - whole| <= the fp32 rounding of a K-long sum of products (both orders), times the gate
-    bound_rows = g.choice(sh.R, 64, replace=False)
-    bnd = _gemm_bound(Af[bound_rows], Wf)
-    assert np.all(np.abs(split - whole)[bound_rows] <= 2 * GEMM_RTOL * np.abs(gate[bound_rows]) * bnd + 1e-30)
-    rows = np.unique(np.concatenate([np.arange(3200, 3200 + 8), np.arange(sh.R - 40, sh.R), bound_rows]))
-    ref = x[rows] + gate[rows] * (Af[rows] @ Wf.T)
-    tol = GEMM_RTOL * np.abs(gate[rows]) * _gemm_bound(Af[rows], Wf) + 2 ** -23 * np.abs(ref) + 1e-30
-    assert np.all(np.abs(split[rows] - ref) <= tol), float(np.abs(split[rows] - ref).max())
-
-
 @pytest.mark.parametrize("shape,nw", [("tiny", False), ("tiny", True), ("512sq", True)])
 def test_qkv_rope_epilogue(shape, nw):
     inp = DI.block_inputs(shape, norm_weights=nw)
