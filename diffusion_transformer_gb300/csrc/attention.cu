@@ -103,10 +103,11 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
   const int R = p.R;
   const int nkv = (R + 127) / 128;
 
-  // fixed-maximum mode (the same verdict in every warp: an exact max over the same values)
+  // fixed-maximum mode (the same verdict in every warp: an exact max over the same values); the
+  // norm weights are read after pdl_wait, before the barriers' set-up when they decide its counts
   float m_fixed = 0.f;
   bool fixed = MODE == kAttnFixed;
-  if (MODE != kAttnRunning) {
+  auto fixed_bound = [&]() {
     float mq = 0.f, mk = 0.f;
     for (int i = lane; i < D; i += 32) {
       mq = fmaxf(mq, p.qn0 ? fabsf(p.qn0[i]) : 1.f);
@@ -124,6 +125,10 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
     // margin 2^-6 per factor: bf16 rounding of q and k, fp32 normalisation
     m_fixed = 1.015625f * mq * 1.015625f * mk * float(D) * scale_log2;
     if (MODE == kAttnAuto) fixed = m_fixed < 60.f;
+  };
+  if constexpr (MODE == kAttnAuto) {
+    pdl_wait();
+    fixed_bound();
   }
 
   if (threadIdx.x == 0) {
@@ -153,6 +158,10 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above may overlap the previous kernel in the stream; its results only from here
+  pdl_wait();
+  pdl_trigger();
+  if constexpr (MODE == kAttnFixed) fixed_bound();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -479,7 +488,8 @@ int launch_d(const AttnParams& p, cudaStream_t stream) {
   const int threads = p.qk_normed <= 0 ? AttnSplit<D, kAttnRunning>::kThreads
                       : unit             ? AttnSplit<D, kAttnFixed>::kThreads
                                          : AttnSplit<D, kAttnAuto>::kThreads;
-  kern<<<grid, threads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p, scale_log2);
+  if (launch_pdl(kern, grid, dim3(threads), Cfg::kSmemBytes, stream, 1, tq, tk, tv, p, scale_log2) != cudaSuccess)
+    return DIT_ECUDA;
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 

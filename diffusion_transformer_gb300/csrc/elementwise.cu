@@ -35,6 +35,8 @@ __device__ __forceinline__ float block_sum(float v, float* part) {
 // in registers, no E[x^2] - mean^2 cancellation).
 template <int NC, bool LN>
 __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const float* x = r < p.L ? p.txt + size_t(r) * p.ld_txt : p.img + size_t(r - p.L) * p.ld_img;
   const int m = p.map ? __ldg(p.map + r) : 0;
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(kNormThreads) modnorm_kernel(const ModNormPara
 // FlowMatch Euler step (host contract, section 6): x + (sigma_next - sigma) * vel, each operation
 // rounded separately in fp32.
 __global__ void euler_kernel(float* __restrict__ x, const float* __restrict__ vel, long long n, float s0, float s1) {
+  pdl_wait();
+  pdl_trigger();
   const float dt = __fsub_rn(s1, s0);
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -133,6 +137,8 @@ __global__ void euler_kernel(float* __restrict__ x, const float* __restrict__ ve
 }
 
 __global__ void euler_kernel_v4(float4* __restrict__ x, const float4* __restrict__ vel, long long n4, float s0, float s1) {
+  pdl_wait();
+  pdl_trigger();
   const float dt = __fsub_rn(s1, s0);
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -150,6 +156,8 @@ __global__ void euler_kernel_v4(float4* __restrict__ x, const float4* __restrict
 // (L, y - (h - h/2), x - (w - w/2)); axis widths (16, 56, 56) scaled by d / 128; column k of axis a
 // holds pos_a * theta^(-2k / width_a), evaluated in fp64 and rounded once to fp32.
 __global__ void rope_kernel(int L, int gh, int gw, int d, double theta, float* cos_out, float* sin_out, long long total) {
+  pdl_wait();
+  pdl_trigger();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= total) return;
   const int half = d / 2;
@@ -184,6 +192,8 @@ struct SigmaList {
 // Timestep sinusoids (gizai:dit reference, sinusoids): row i = [cos | sin] of 1000 * t_i times
 // 10000^(-k / (dim/2)), fp64 angles, stored bf16 as the time MLP's input.
 __global__ void sinusoid_kernel(SigmaList sig, int steps, int dim, uint16_t* out) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   const int half = dim / 2;
   for (int k = threadIdx.x; k < half; k += blockDim.x) {
@@ -197,6 +207,8 @@ __global__ void sinusoid_kernel(SigmaList sig, int steps, int dim, uint16_t* out
 }
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ in, uint16_t* __restrict__ out, long long n) {
+  pdl_wait();
+  pdl_trigger();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     __nv_bfloat16 b = __float2bfloat16_rn(in[i]);
@@ -209,6 +221,8 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, uint16_t* __res
 // thread keeps four chunks' loads in flight per iteration.
 __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ s, uint16_t* __restrict__ w,
                                long long rows, long long cols) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kU = 4;
   const long long chunks = rows * cols / 16;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
@@ -243,6 +257,8 @@ __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __r
 // thread loaded before the reduction, then x += gate * y * rstd * w.
 template <int NC>
 __global__ void __launch_bounds__(kNormThreads) sandwich_kernel(const SandwichParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   float* x = r < p.L ? p.txt + size_t(r) * p.H : p.img + size_t(r - p.L) * p.H;
   const int m = p.map ? __ldg(p.map + r) : 0;
@@ -322,34 +338,37 @@ int grid_for(long long n, int threads) {
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream) {
   if (p.R <= 0) return DIT_OK;
   const int chunks = p.H % (4 * kNormThreads) == 0 ? p.H / (4 * kNormThreads) : 0;
+  cudaError_t rc;
   if (p.layernorm) {
     switch (chunks) {
-      case 1: modnorm_kernel<1, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      case 2: modnorm_kernel<2, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      case 3: modnorm_kernel<3, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      case 4: modnorm_kernel<4, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      default: modnorm_kernel<0, true><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 1: rc = launch_pdl(modnorm_kernel<1, true>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      case 2: rc = launch_pdl(modnorm_kernel<2, true>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      case 3: rc = launch_pdl(modnorm_kernel<3, true>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      case 4: rc = launch_pdl(modnorm_kernel<4, true>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      default: rc = launch_pdl(modnorm_kernel<0, true>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
     }
   } else {
     switch (chunks) {
-      case 1: modnorm_kernel<1, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      case 2: modnorm_kernel<2, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      case 3: modnorm_kernel<3, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      case 4: modnorm_kernel<4, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
-      default: modnorm_kernel<0, false><<<p.R, kNormThreads, 0, stream>>>(p); break;
+      case 1: rc = launch_pdl(modnorm_kernel<1, false>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      case 2: rc = launch_pdl(modnorm_kernel<2, false>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      case 3: rc = launch_pdl(modnorm_kernel<3, false>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      case 4: rc = launch_pdl(modnorm_kernel<4, false>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+      default: rc = launch_pdl(modnorm_kernel<0, false>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
     }
   }
-  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
 int euler_launch(float* x, const float* vel, long long n, float sigma, float sigma_next, cudaStream_t stream) {
   if (n <= 0) return DIT_OK;
   if (n % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(vel) % 16 == 0) {
-    euler_kernel_v4<<<grid_for(n / 4, 256), 256, 0, stream>>>(reinterpret_cast<float4*>(x),
-                                                              reinterpret_cast<const float4*>(vel), n / 4, sigma,
-                                                              sigma_next);
+    if (launch_pdl(euler_kernel_v4, dim3(grid_for(n / 4, 256)), dim3(256), 0, stream, 1, reinterpret_cast<float4*>(x),
+                   reinterpret_cast<const float4*>(vel), n / 4, sigma, sigma_next) != cudaSuccess)
+      return DIT_ECUDA;
   } else {
-    euler_kernel<<<grid_for(n, 256), 256, 0, stream>>>(x, vel, n, sigma, sigma_next);
+    if (launch_pdl(euler_kernel, dim3(grid_for(n, 256)), dim3(256), 0, stream, 1, x, vel, n, sigma, sigma_next) !=
+        cudaSuccess)
+      return DIT_ECUDA;
   }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
@@ -365,27 +384,30 @@ int sinusoid_launch(const float* sigmas, int steps, int dim, uint16_t* out, cuda
   if (steps <= 0 || steps > 64) return DIT_EUNSUPPORTED;
   SigmaList sl{};
   for (int i = 0; i < steps; ++i) sl.s[i] = sigmas[i];
-  sinusoid_kernel<<<steps, 128, 0, stream>>>(sl, steps, dim, out);
+  if (launch_pdl(sinusoid_kernel, dim3(steps), dim3(128), 0, stream, 1, sl, steps, dim, out) != cudaSuccess)
+    return DIT_ECUDA;
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
 int f32_to_bf16_launch(const float* in, uint16_t* out, long long n, cudaStream_t stream) {
   if (n <= 0) return DIT_OK;
-  f32_to_bf16_kernel<<<grid_for(n, 256), 256, 0, stream>>>(in, out, n);
+  if (launch_pdl(f32_to_bf16_kernel, dim3(grid_for(n, 256)), dim3(256), 0, stream, 1, in, out, n) != cudaSuccess)
+    return DIT_ECUDA;
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
 int sandwich_launch(const SandwichParams& p, cudaStream_t stream) {
   if (p.R <= 0) return DIT_OK;
   const int chunks = p.H % (4 * kNormThreads) == 0 ? p.H / (4 * kNormThreads) : 0;
+  cudaError_t rc;
   switch (chunks) {
-    case 1: sandwich_kernel<1><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    case 2: sandwich_kernel<2><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    case 3: sandwich_kernel<3><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    case 4: sandwich_kernel<4><<<p.R, kNormThreads, 0, stream>>>(p); break;
-    default: sandwich_kernel<0><<<p.R, kNormThreads, 0, stream>>>(p); break;
+    case 1: rc = launch_pdl(sandwich_kernel<1>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+    case 2: rc = launch_pdl(sandwich_kernel<2>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+    case 3: rc = launch_pdl(sandwich_kernel<3>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+    case 4: rc = launch_pdl(sandwich_kernel<4>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
+    default: rc = launch_pdl(sandwich_kernel<0>, dim3(p.R), dim3(kNormThreads), 0, stream, 1, p); break;
   }
-  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
 int wait_selftest_launch(int complete, int* err, cudaStream_t stream) {
@@ -424,6 +446,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u 
 // over the row (it is re-read from L2 after the maximum).
 __global__ void __launch_bounds__(kNormThreads) quant_rows_kernel(uint16_t* x, int K, const float* smooth,
                                                                   float* scale) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float part[kNormThreads / 32];
   uint4* row = reinterpret_cast<uint4*>(x + size_t(blockIdx.x) * K);
   const int n8 = K / 8;
@@ -463,6 +487,8 @@ __global__ void __launch_bounds__(kNormThreads) quant_rows_kernel(uint16_t* x, i
 // One CTA per output channel of w [N, K] bf16: codes int8 [N, K], scale[n] (smooth folded first).
 __global__ void __launch_bounds__(kNormThreads) quant_weight_kernel(const uint16_t* w, int K, const float* smooth,
                                                                     int8_t* q, float* scale) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float part[kNormThreads / 32];
   const uint16_t* row = w + size_t(blockIdx.x) * K;
   auto val = [&](int k) {
@@ -478,6 +504,8 @@ __global__ void __launch_bounds__(kNormThreads) quant_weight_kernel(const uint16
 
 // int8 codes -> the same integers in bf16, 16 per thread step.
 __global__ void codes_bf16_kernel(const int8_t* q, uint16_t* w, long long n16) {
+  pdl_wait();
+  pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
     const uint4 u = reinterpret_cast<const uint4*>(q)[i];
     const uint32_t b[4] = {u.x, u.y, u.z, u.w};
@@ -497,7 +525,8 @@ __global__ void codes_bf16_kernel(const int8_t* q, uint16_t* w, long long n16) {
 int quant_rows_launch(uint16_t* x, int rows, int K, const float* smooth, float* scale, cudaStream_t stream) {
   if (rows <= 0) return DIT_OK;
   if (K % 8 != 0) return DIT_EUNSUPPORTED;
-  quant_rows_kernel<<<rows, kNormThreads, 0, stream>>>(x, K, smooth, scale);
+  if (launch_pdl(quant_rows_kernel, dim3(rows), dim3(kNormThreads), 0, stream, 1, x, K, smooth, scale) != cudaSuccess)
+    return DIT_ECUDA;
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
@@ -526,6 +555,8 @@ constexpr int kMergeTile = 64, kMergeRanks = 32;
 __global__ void __launch_bounds__(256) lora_merge_kernel(const uint16_t* W, const uint16_t* __restrict__ A,
                                                          const uint16_t* __restrict__ B, uint16_t* merged, int n_out,
                                                          int n_in, int rank) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sB[kMergeTile][kMergeRanks + 1];
   __shared__ float sA[kMergeRanks][kMergeTile];
   const int o0 = blockIdx.y * kMergeTile, i0 = blockIdx.x * kMergeTile;

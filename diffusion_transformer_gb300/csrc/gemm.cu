@@ -706,6 +706,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above (barriers, tensor memory, descriptor prefetch, the pair hand-shake on words of
+  // this launch's own set) may overlap the previous kernel in the stream; its results only from here.
+  pdl_wait();
+  pdl_trigger();
 
   if (!up) {
     // the pair never formed: nothing to do
@@ -1061,27 +1065,15 @@ int launch_one(const Maps& m, const GemmParams& p, cudaStream_t stream) {
   if constexpr (!B8) plan_stream_k(q, tiles, units_max, PAIR ? 2 : 1, BN);
   else q.sk_tiles = 0;
   const int units = q.sk_tiles > 0 ? units_max : (tiles < units_max ? tiles : units_max);
-  if constexpr (!PAIR) {
-    kern<<<units, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(m.a, m.b, m.s, m.a2, m.b2, q);
-    return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
-  } else {
+  if constexpr (PAIR) {
     if (2 * units > kPairMaxCtas) return DIT_EUNSUPPORTED;
     q.pair_epoch = g_pair_launches.fetch_add(1, std::memory_order_relaxed);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(2 * units));
-    cfg.blockDim = dim3(Cfg::kThreads);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, m.a, m.b, m.s, m.a2, m.b2, q) != cudaSuccess) return DIT_ECUDA;
-    return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
   }
+  const int ctas = PAIR ? 2 * units : units;
+  if (launch_pdl(kern, dim3(unsigned(ctas)), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, PAIR ? 2 : 1, m.a, m.b, m.s,
+                 m.a2, m.b2, q) != cudaSuccess)
+    return DIT_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }
 
 template <int BN, bool B8, bool PAIR>

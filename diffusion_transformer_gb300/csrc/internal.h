@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "../../include/dit.h"
 
 namespace dit {
@@ -175,6 +177,34 @@ int quant_weight_launch(const uint16_t* w, int N, int K, const float* smooth, in
 int codes_bf16_launch(const int8_t* q, uint16_t* w, long long n, cudaStream_t stream);
 
 int num_sms();
+
+// Launch `kern` on `stream` with programmatic dependent launch allowed (and a cluster of
+// `cluster_x` CTAs when above 1). Only kernels that call pdl_wait() (ptx.cuh) before their first
+// global memory access are launched this way.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = unsigned(cluster_x);
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = unsigned(n);
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Every check dit_block_forward makes before launching, except those on the workspace: DIT_OK, or the
 // status it would return. Touches no CUDA state.

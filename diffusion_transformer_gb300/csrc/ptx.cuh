@@ -37,6 +37,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
+// Programmatic dependent launch. A kernel launched with launch_pdl may start while the previous
+// kernel in its stream is still running (once every CTA of that kernel has called pdl_trigger or
+// exited). pdl_wait() returns once the previous kernel has completed and its memory operations are
+// visible (at once for a kernel launched without the attribute), so every such kernel calls it
+// before its first access to global memory that another kernel may write or read; what comes
+// before it (barrier initialisation, tensor-memory allocation, descriptor prefetch) overlaps the
+// previous kernel's tail. pdl_trigger() lets the next kernel be scheduled early; it grants no
+// access to this kernel's results (the next kernel's pdl_wait still waits for completion).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile(
