@@ -58,14 +58,14 @@ KERNEL_FAMILY = {"modnorm": "modnorm", "attention": "attention", "gemm_qkv_rope"
                  "gemm_up_swiglu": "gemm", "gemm_down_gated": "gemm"}
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, sha256 of its sources at capture)
-    "gemm_up_swiglu": (262_337_536, "4977a7e4ec5b964a457eb7b7daadcc5765003d96a0d3e6b82fa21eb987a86698"),
+    "gemm_up_swiglu": (262_223_616, "375329b57de148389ee93d93a34d6be285f31a30762d0918f2aff58c19036234"),
 }
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of a kernel from the same kind of
 # capture, with the same source check: a counter-based view of tensor utilisation beside the
 # event-timed fraction of the measured peak (which a cuBLAS burst figure taken at a lower clock
 # can flatter).
 NCU_TENSOR_ACTIVE = {
-    "gemm_up_swiglu": (0.910, "4977a7e4ec5b964a457eb7b7daadcc5765003d96a0d3e6b82fa21eb987a86698"),
+    "gemm_up_swiglu": (0.9051, "375329b57de148389ee93d93a34d6be285f31a30762d0918f2aff58c19036234"),
 }
 
 
