@@ -29,11 +29,12 @@ from typing import Optional
 
 import numpy as np
 
-from .dit import (attention, bf16_rne_bits, bf16_to_f64, modulated_rmsnorm, qk_rmsnorm, rotate,
-                  swiglu_interleaved, _mod_rows)
+from .dit import (attention, bf16_rne_bits, bf16_to_f64, modulated_layernorm, modulated_rmsnorm, qk_rmsnorm,
+                  rotate, swiglu_interleaved, _mod_rows)
 
 __all__ = ["quantize_codes", "quantize_rows", "quantize_weight", "smooth_scales", "w8a8_linear",
-           "w8a8_linear_f", "block_forward_w8a8_rows"]
+           "w8a8_linear_f", "block_forward_w8a8_rows", "parallel_block_forward_w8a8_rows",
+           "double_block_forward_w8a8_rows"]
 
 
 def quantize_codes(v32: np.ndarray, scale32: np.ndarray) -> np.ndarray:
@@ -128,3 +129,75 @@ def block_forward_w8a8_rows(x, qweights, mod, mod_map, cos, sin, heads, head_dim
     h2 = modulated_rmsnorm(xr, norm2, sm_r, cm_r, eps)
     a = swiglu_interleaved(lin(2, h2))
     return xr + gm_r * lin(3, a)
+
+
+def parallel_block_forward_w8a8_rows(x, linear1, linear2, mod, mod_map, cos, sin, heads, head_dim,
+                                     rows: Optional[np.ndarray] = None, norm=None, q_norm=None, k_norm=None,
+                                     eps=1e-6, qk_eps=1e-6, smooth1=None, smooth2=None):
+    """The parallel block (see oracle.dit.parallel_block_forward_rows) with its two linears in W8A8
+    form, as the klein article quantises a single block: linear1 = [Wqkv ; Wup] ([3H + 2F, H], rows
+    Q|K|V then gate/up interleaved) over the normed rows h, and linear2 = [Wout | Wdown] ([H, H + F])
+    over the joined row [o | a] of the attention output and the SwiGLU output, each an (int8 codes,
+    float32 per-output-channel scales) pair quantised over its whole row (smooth1 [H] and smooth2
+    [H + F] the SmoothQuant divisors used for it, or None). Each activation (h, then [o | a]) enters
+    at its bfloat16 value and is quantised per token over its whole row.
+    [klein, section 5 (int8 detail: single linear1 and linear2) and its D4 / D5 entries]"""
+    x = np.asarray(x, dtype=np.float64)
+    R, H = x.shape
+    nh, d = heads, head_dim
+    rows = np.arange(R) if rows is None else np.asarray(rows)
+    m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)]
+    h = modulated_layernorm(x, norm, m[:, 0], m[:, 1], eps)
+    u = w8a8_linear_f(h, linear1[0], linear1[1], smooth1)
+    q = rotate(qk_rmsnorm(u[:, 0:H].reshape(R, nh, d), q_norm, qk_eps), cos, sin)
+    k = rotate(qk_rmsnorm(u[:, H:2 * H].reshape(R, nh, d), k_norm, qk_eps), cos, sin)
+    v = u[:, 2 * H:3 * H].reshape(R, nh, d)
+    o = attention(q, k, v, rows)
+    a = swiglu_interleaved(u[rows, 3 * H:])
+    y = w8a8_linear_f(np.concatenate([o, a], axis=1), linear2[0], linear2[1], smooth2)
+    return x[rows] + m[rows, 2] * y
+
+
+def double_block_forward_w8a8_rows(x, qweights_txt, qweights_img, mod, mod_map, cos, sin, heads, head_dim, L,
+                                   rows: Optional[np.ndarray] = None, norms_txt=(None, None, None, None),
+                                   norms_img=(None, None, None, None), eps=1e-6, qk_eps=1e-6, smooth_txt=None,
+                                   smooth_img=None):
+    """The double-stream block (see oracle.dit.double_block_forward_rows) with each stream's four
+    linears in W8A8 form: qweights_* are four (codes, scales) pairs (qkv, out, up, down) quantised
+    with that stream's SmoothQuant divisors smooth_* (four [in] arrays or None), as the klein article
+    quantises a double block's image and text qkv, proj, mlp.0 and mlp.2 linears. Each activation
+    enters at its bfloat16 value and is quantised per token with its own stream's divisors.
+    [klein, section 5 (int8 detail) and its D4 / D5 entries; klein, sections 4.3-4.4 (double blocks)]"""
+    x = np.asarray(x, dtype=np.float64)
+    R, H = x.shape
+    nh, d = heads, head_dim
+    rows = np.arange(R) if rows is None else np.asarray(rows)
+    m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)]
+    streams = [(np.arange(0, L), qweights_txt, norms_txt, smooth_txt),
+               (np.arange(L, R), qweights_img, norms_img, smooth_img)]
+    q = np.empty((R, nh, d))
+    k = np.empty((R, nh, d))
+    v = np.empty((R, nh, d))
+    for idx, qw, nrm, sm in streams:
+        if len(idx) == 0:
+            continue
+        sm = sm if sm is not None else (None, None, None, None)
+        h = modulated_rmsnorm(x[idx], nrm[0], m[idx, 0], m[idx, 1], eps)
+        u = w8a8_linear_f(h, qw[0][0], qw[0][1], sm[0])
+        n = len(idx)
+        q[idx] = rotate(qk_rmsnorm(u[:, 0:H].reshape(n, nh, d), nrm[2], qk_eps), cos[idx], sin[idx])
+        k[idx] = rotate(qk_rmsnorm(u[:, H:2 * H].reshape(n, nh, d), nrm[3], qk_eps), cos[idx], sin[idx])
+        v[idx] = u[:, 2 * H:3 * H].reshape(n, nh, d)
+    o = attention(q, k, v, rows)
+    out = np.empty((len(rows), H))
+    for idx, qw, nrm, sm in streams:
+        sel = np.nonzero(np.isin(rows, idx))[0]
+        if len(sel) == 0:
+            continue
+        sm = sm if sm is not None else (None, None, None, None)
+        r = rows[sel]
+        xr = x[r] + m[r, 2] * w8a8_linear_f(o[sel], qw[1][0], qw[1][1], sm[1])
+        h2 = modulated_rmsnorm(xr, nrm[1], m[r, 3], m[r, 4], eps)
+        a = swiglu_interleaved(w8a8_linear_f(h2, qw[2][0], qw[2][1], sm[2]))
+        out[sel] = xr + m[r, 5] * w8a8_linear_f(a, qw[3][0], qw[3][1], sm[3])
+    return out

@@ -97,9 +97,13 @@ def layernorm_row(x, eps):
 
 
 def parallel_block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
-                   norm=None, qn=None, kn=None):
+                   norm=None, qn=None, kn=None, linear=None, linear2=None):
     """The parallel block: x + gate * (attention + SwiGLU MLP), both branches reading one modulated
-    LayerNorm. mod_rows[r] = 3 lists of H (shift, scale, gate) for row r. Returns new rows."""
+    LayerNorm. mod_rows[r] = 3 lists of H (shift, scale, gate) for row r. Returns new rows.
+    linear(W, row) replaces the products of Wq, Wk, Wv, Wg and Wu when given; linear2(o, a) replaces
+    the sum of the two output products Wo o + Wd a (one linear over the joined input [o | a])."""
+    matvec_ = linear or matvec
+    joint = linear2 or (lambda o, a: [u + v for u, v in zip(matvec(Wo, o), matvec(Wd, a))])
     R, H = len(x), len(x[0])
     one = lambda n: [1.0] * n
     w = norm or one(H)
@@ -111,7 +115,7 @@ def parallel_block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, 
         y = layernorm_row(x[r], eps)
         h = [y[i] * w[i] * (1.0 + scale[i]) + shift[i] for i in range(H)]
         hs.append(h)
-        q, k, v = matvec(Wq, h), matvec(Wk, h), matvec(Wv, h)
+        q, k, v = matvec_(Wq, h), matvec_(Wk, h), matvec_(Wv, h)
         qh, kh, vh = [], [], []
         for n in range(heads):
             for (src, wt, dst) in ((q, qn, qh), (k, kn, kh)):
@@ -138,18 +142,20 @@ def parallel_block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, 
             z = sum(e)
             for j in range(d):
                 o.append(sum(e[c] / z * V[c][n][j] for c in range(R)))
-        att = matvec(Wo, o)
-        g, u = matvec(Wg, hs[r]), matvec(Wu, hs[r])
+        g, u = matvec_(Wg, hs[r]), matvec_(Wu, hs[r])
         a = [g[j] / (1.0 + math.exp(-g[j])) * u[j] for j in range(len(g))]
-        mlp = matvec(Wd, a)
+        both = joint(o, a)
         gate = mod_rows[r][2]
-        out.append([x[r][i] + gate[i] * (att[i] + mlp[i]) for i in range(H)])
+        out.append([x[r][i] + gate[i] * both[i] for i in range(H)])
     return out
 
 
-def double_block(x, L, Wt, Wi, mod_rows, cos, sin, heads, d, eps, qk_eps, norms_t=None, norms_i=None):
+def double_block(x, L, Wt, Wi, mod_rows, cos, sin, heads, d, eps, qk_eps, norms_t=None, norms_i=None,
+                 linear=None):
     """The sequential block with per-stream weights: rows r < L use Wt = (Wq, Wk, Wv, Wo, Wg, Wu, Wd)
-    and norms_t = (norm1, norm2, qn, kn), the others Wi / norms_i; one attention over all rows."""
+    and norms_t = (norm1, norm2, qn, kn), the others Wi / norms_i; one attention over all rows.
+    linear(W, row) replaces the plain W row products when given (one call per weight matrix)."""
+    matvec = linear or globals()["matvec"]
     R, H = len(x), len(x[0])
     one = lambda n: [1.0] * n
     nt = norms_t or (None, None, None, None)

@@ -171,3 +171,137 @@ def test_w8a8_block_matches_scalar_brute_force(seed, use_smooth):
                               eps=eps, qk_eps=qk_eps)
     rel = np.abs(y - yf).max() / np.sqrt(np.mean(yf ** 2))
     assert 1e-5 < rel < 0.1, rel
+
+
+# ------------------------------------------------------------ parallel and double-stream W8A8 blocks
+
+def _quantised_linear(qrows, sm):
+    """linear(W, row) of a quantised weight (rows of (codes, scale)): per-token codes of the row."""
+    def lin(_W, row):
+        codes, sc = _quant_row(row, sm)
+        return [sum(a * b for a, b in zip(codes, qc)) * sc * sw for qc, sw in qrows]
+    return lin
+
+
+@pytest.mark.parametrize("seed,use_smooth", [(0, False), (1, True)])
+def test_parallel_w8a8_block_matches_scalar_brute_force(seed, use_smooth):
+    # linear1 = [Wqkv ; Wup] over h; linear2 = [Wout | Wdown] over the joined row [o | a], one code
+    # row and one scale per output channel over all H + F inputs [klein, section 5: single linear1
+    # and linear2]
+    from tests.test_oracle_parallel import _case
+    c = _case(seed + 30)
+    eps, qk_eps = 0.5, 1e-2
+    H, F = c["x"].shape[1], c["Wg"].shape[0]
+    g = np.random.default_rng(seed + 50)
+    sm1 = g.uniform(0.5, 2.0, size=H).astype(np.float32) if use_smooth else None
+    sm2 = g.uniform(0.5, 2.0, size=H + F).astype(np.float32) if use_smooth else None
+    lin1 = {k: _quant_matrix(c[k].astype(np.float32).tolist(), None if sm1 is None else sm1.tolist())
+            for k in ("Wq", "Wk", "Wv", "Wg", "Wu")}
+    W2 = np.concatenate([c["Wo"], c["Wd"]], axis=1).astype(np.float32)
+    lin2 = _quant_matrix(W2.tolist(), None if sm2 is None else sm2.tolist())
+    mats = {k: c[k].tolist() for k in lin1}
+
+    def linear(W, row):
+        for k in mats:
+            if W is mats[k]:
+                return _quantised_linear(lin1[k], None if sm1 is None else sm1.tolist())(W, row)
+        raise AssertionError("unknown weight")
+
+    def linear2(o, a):
+        return _quantised_linear(lin2, None if sm2 is None else sm2.tolist())(None, list(o) + list(a))
+
+    mod_rows = [[list(c["mod"][c["mod_map"][r], i]) for i in range(3)] for r in range(len(c["x"]))]
+    yb = np.array(brute.parallel_block([list(r) for r in c["x"]], mats["Wq"], mats["Wk"], mats["Wv"],
+                                       c["Wo"].tolist(), mats["Wg"], mats["Wu"], c["Wd"].tolist(), mod_rows,
+                                       c["cos"].tolist(), c["sin"].tolist(), c["heads"], c["d"], eps, qk_eps,
+                                       linear=linear, linear2=linear2))
+    Wqkv, _, Wup, _ = _fused(c)
+    q1 = O.quantize_weight(np.concatenate([Wqkv, Wup], axis=0).astype(np.float32), sm1)
+    q2 = O.quantize_weight(W2, sm2)
+    y = O.parallel_block_forward_w8a8_rows(c["x"], q1, q2, c["mod"], c["mod_map"], c["cos"], c["sin"], c["heads"],
+                                           c["d"], eps=eps, qk_eps=qk_eps, smooth1=sm1, smooth2=sm2)
+    np.testing.assert_allclose(y, yb, rtol=1e-9, atol=1e-9)
+    # a perturbation of the float parallel block, not the float block
+    yf = O.parallel_block_forward_rows(c["x"], _fused(c), c["mod"], c["mod_map"], c["cos"], c["sin"], c["heads"],
+                                       c["d"], eps=eps, qk_eps=qk_eps)
+    rel = np.abs(y - yf).max() / np.sqrt(np.mean(yf ** 2))
+    assert 1e-5 < rel < 0.1, rel
+
+
+def test_parallel_w8a8_linear2_is_one_joint_quantisation():
+    # quantising [o | a] and [Wout | Wdown] as one row each is not the sum of two separately
+    # quantised linears (different per-token and per-channel scales): the planted mistake is caught
+    from tests.test_oracle_parallel import _case
+    c = _case(7)
+    H, F = c["x"].shape[1], c["Wg"].shape[0]
+    Wqkv, _, Wup, _ = _fused(c)
+    q1 = O.quantize_weight(np.concatenate([Wqkv, Wup], axis=0).astype(np.float32))
+    W2 = np.concatenate([c["Wo"], c["Wd"]], axis=1).astype(np.float32)
+    y = O.parallel_block_forward_w8a8_rows(c["x"], q1, O.quantize_weight(W2), c["mod"], c["mod_map"], c["cos"],
+                                           c["sin"], c["heads"], c["d"])
+    # the mistaken form: linear2 as two W8A8 linears added
+    qo, qd = O.quantize_weight(c["Wo"].astype(np.float32)), O.quantize_weight(c["Wd"].astype(np.float32))
+    x = c["x"]
+    m = c["mod"][c["mod_map"]]
+    h = O.modulated_layernorm(x, None, m[:, 0], m[:, 1], 1e-6)
+    u = O.w8a8_linear_f(h, *q1)
+    nh, d = c["heads"], c["d"]
+    R = x.shape[0]
+    q = O.rotate(O.qk_rmsnorm(u[:, :H].reshape(R, nh, d), None, 1e-6), c["cos"], c["sin"])
+    k = O.rotate(O.qk_rmsnorm(u[:, H:2 * H].reshape(R, nh, d), None, 1e-6), c["cos"], c["sin"])
+    o = O.attention(q, k, u[:, 2 * H:3 * H].reshape(R, nh, d))
+    a = O.swiglu_interleaved(u[:, 3 * H:])
+    wrong = x + m[:, 2] * (O.w8a8_linear_f(o, *qo) + O.w8a8_linear_f(a, *qd))
+    assert np.abs(wrong - y).max() > 1e-4 * np.abs(y).max()
+
+
+@pytest.mark.parametrize("seed,L,use_smooth", [(0, 2, False), (1, 3, True), (2, 0, True)])
+def test_double_w8a8_block_matches_scalar_brute_force(seed, L, use_smooth):
+    # each stream's four linears quantised with its own divisors [klein, section 5: double img / txt
+    # qkv, proj, mlp.0, mlp.2]
+    from tests.test_oracle_double import _stream
+    c = _tiny_case(seed + 60, L=L)
+    eps, qk_eps = 1e-3, 1e-2
+    H, F = c["x"].shape[1], c["Wg"].shape[0]
+    g = np.random.default_rng(seed + 70)
+    Wt, Wi = _stream(g, H, F), _stream(g, H, F)
+    ins = (H, H, H, F)
+    sm_t = [g.uniform(0.5, 2.0, size=n).astype(np.float32) for n in ins] if use_smooth else None
+    sm_i = [g.uniform(0.5, 2.0, size=n).astype(np.float32) for n in ins] if use_smooth else None
+    sm_of = {"Wq": 0, "Wk": 0, "Wv": 0, "Wo": 1, "Wg": 2, "Wu": 2, "Wd": 3}
+    order = ("Wq", "Wk", "Wv", "Wo", "Wg", "Wu", "Wd")
+    brute_t = [Wt[k].astype(np.float32).tolist() for k in order]
+    brute_i = [Wi[k].astype(np.float32).tolist() for k in order]
+    table = []
+    for W, sm, mats in ((Wt, sm_t, brute_t), (Wi, sm_i, brute_i)):
+        for k, mat in zip(order, mats):
+            s = None if sm is None else sm[sm_of[k]].tolist()
+            table.append((mat, _quantised_linear(_quant_matrix(W[k].astype(np.float32).tolist(), s), s)))
+
+    def linear(W, row):
+        for mat, lin in table:
+            if W is mat:
+                return lin(W, row)
+        raise AssertionError("unknown weight")
+
+    mod_rows = [[list(c["mod"][c["mod_map"][r], i]) for i in range(6)] for r in range(len(c["x"]))]
+    yb = np.array(brute.double_block([list(r) for r in c["x"]], L, brute_t, brute_i, mod_rows, c["cos"].tolist(),
+                                     c["sin"].tolist(), c["heads"], c["d"], eps, qk_eps, linear=linear))
+    qt = [O.quantize_weight(W.astype(np.float32), None if sm_t is None else sm_t[i]) for i, W in enumerate(_fused(Wt))]
+    qi = [O.quantize_weight(W.astype(np.float32), None if sm_i is None else sm_i[i]) for i, W in enumerate(_fused(Wi))]
+    y = O.double_block_forward_w8a8_rows(c["x"], qt, qi, c["mod"], c["mod_map"], c["cos"], c["sin"], c["heads"],
+                                         c["d"], L, eps=eps, qk_eps=qk_eps, smooth_txt=sm_t, smooth_img=sm_i)
+    np.testing.assert_allclose(y, yb, rtol=1e-9, atol=1e-9)
+
+
+def test_double_w8a8_with_shared_weights_is_the_sequential_w8a8_block():
+    c = _tiny_case(9, L=3, gh=3, gw=3)
+    g = np.random.default_rng(11)
+    H, F = c["x"].shape[1], c["Wg"].shape[0]
+    sm = [g.uniform(0.5, 2.0, size=n).astype(np.float32) for n in (H, H, H, F)]
+    qws = [O.quantize_weight(W.astype(np.float32), sm[i]) for i, W in enumerate(_fused(c))]
+    seq = O.block_forward_w8a8_rows(c["x"], qws, c["mod"], c["mod_map"], c["cos"], c["sin"], c["heads"], c["d"],
+                                    smooth=sm)
+    dbl = O.double_block_forward_w8a8_rows(c["x"], qws, qws, c["mod"], c["mod_map"], c["cos"], c["sin"], c["heads"],
+                                           c["d"], 3, smooth_txt=sm, smooth_img=sm)
+    np.testing.assert_array_equal(dbl, seq)
