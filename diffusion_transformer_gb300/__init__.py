@@ -18,6 +18,7 @@ __all__ = [
     "DenoiseModel", "dit_block_forward", "dit_block_forward_int8", "dit_parallel_block_forward",
     "dit_parallel_block_forward_int8", "dit_double_block_forward_int8",
     "W8A8BlockWeights", "dit_block_forward_w8a8", "dit_w8a8_quantize_weight", "dit_w8a8_quantize_rows",
+    "ParallelW8A8Weights", "dit_parallel_block_forward_w8a8", "dit_double_block_forward_w8a8",
     "dit_linear_w8a8", "dit_linear_w8a8_workspace_bytes",
     "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA", "dit_lora_merge",
     "dit_block_forward_sandwich", "dit_euler_step",
@@ -66,6 +67,11 @@ class dit_block_w8a8(ctypes.Structure):
                 ("norm2", c_void_p), ("q_norm", c_void_p), ("k_norm", c_void_p)]
 
 
+class dit_parallel_w8a8(ctypes.Structure):
+    _fields_ = [("q1", c_void_p), ("scale1", c_void_p), ("smooth1", c_void_p), ("q2", c_void_p), ("scale2", c_void_p),
+                ("smooth2", c_void_p), ("norm1", c_void_p), ("q_norm", c_void_p), ("k_norm", c_void_p)]
+
+
 class dit_mod(ctypes.Structure):
     _fields_ = [("rows", c_void_p), ("map", c_void_p), ("M", c_int)]
 
@@ -105,6 +111,12 @@ _SIGNATURES = {
     "dit_block_forward_w8a8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8a8), c_void_p, c_int, c_void_p, c_int,
                                        c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod), c_void_p,
                                        c_size_t, c_void_p]),
+    "dit_parallel_block_forward_w8a8": (c_int, [POINTER(dit_dims), POINTER(dit_parallel_w8a8), c_void_p, c_int,
+                                                c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
+    "dit_double_block_forward_w8a8": (c_int, [POINTER(dit_dims), POINTER(dit_block_w8a8), POINTER(dit_block_w8a8),
+                                              c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
+                                              c_void_p, POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
     "dit_lora_merge": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
     "dit_w8a8_quantize_weight": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dit_w8a8_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
@@ -258,6 +270,20 @@ class W8A8BlockWeights:
                                 (c_void_p * 4)(*[_ptr(t, f32, "smooth") for t in smooth]),
                                 _ptr(norm1, f32, "norm1"), _ptr(norm2, f32, "norm2"), _ptr(q_norm, f32, "q_norm"),
                                 _ptr(k_norm, f32, "k_norm"))
+
+
+class ParallelW8A8Weights:
+    """Device tensors of one W8A8 parallel block: linear1 = [Wqkv ; Wup] codes q1 int8 [3H + 2F, H] with
+    scale1 fp32 [3H + 2F], linear2 = [Wout | Wdown] codes q2 int8 [H, H + F] with scale2 fp32 [H], the
+    SmoothQuant divisors smooth1 [H] and smooth2 [H + F] (or None), and the norm weights."""
+
+    def __init__(self, q1, scale1, q2, scale2, smooth1=None, smooth2=None, norm1=None, q_norm=None, k_norm=None):
+        import torch
+        f32 = torch.float32
+        self.tensors = (q1, scale1, q2, scale2, smooth1, smooth2, norm1, q_norm, k_norm)
+        self.c = dit_parallel_w8a8(_ptr(q1, torch.int8, "q1"), _ptr(scale1, f32, "scale1"), _ptr(smooth1, f32, "smooth1"),
+                                   _ptr(q2, torch.int8, "q2"), _ptr(scale2, f32, "scale2"), _ptr(smooth2, f32, "smooth2"),
+                                   _ptr(norm1, f32, "norm1"), _ptr(q_norm, f32, "q_norm"), _ptr(k_norm, f32, "k_norm"))
 
 
 class Modulation:
@@ -552,6 +578,34 @@ def dit_block_forward_w8a8(dims: DitDims, w: W8A8BlockWeights, txt, img, txt_cos
                                      _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
                                      _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
         "dit_block_forward_w8a8")
+
+
+def dit_parallel_block_forward_w8a8(dims: DitDims, w: ParallelW8A8Weights, txt, img, txt_cos, txt_sin, img_cos,
+                                    img_sin, mod: Modulation, ws, stream=None):
+    """The parallel block with W8A8 linear1 / linear2; mod rows are [M, 3, H] (shift, scale, gate)."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_parallel_block_forward_w8a8(ctypes.byref(dims.c), ctypes.byref(w.c), _ptr(txt, f32, "txt"), L,
+                                              _ptr(img, f32, "img"), img.shape[0], _ptr(txt_cos, f32),
+                                              _ptr(txt_sin, f32), _ptr(img_cos, f32), _ptr(img_sin, f32),
+                                              ctypes.byref(mod.c), _ptr(ws, None, "ws"),
+                                              ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_parallel_block_forward_w8a8")
+
+
+def dit_double_block_forward_w8a8(dims: DitDims, w_txt: Optional[W8A8BlockWeights], w_img: W8A8BlockWeights, txt,
+                                  img, txt_cos, txt_sin, img_cos, img_sin, mod: Modulation, ws, stream=None):
+    """The double-stream block with W8A8 linears: text rows use w_txt, image rows w_img."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_double_block_forward_w8a8(ctypes.byref(dims.c), None if w_txt is None else ctypes.byref(w_txt.c),
+                                            ctypes.byref(w_img.c), _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"),
+                                            img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                                            _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
+                                            _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_double_block_forward_w8a8")
 
 
 def dit_w8a8_quantize_weight(w, smooth, q, scale, stream=None):

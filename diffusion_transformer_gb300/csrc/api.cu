@@ -454,9 +454,9 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
 // weights: on the side stream, [Wqkv ; Wup] is dequantised into one scratch slot (overlapping the
 // norm) and Wout, Wdown into a second (overlapping the first GEMM and the attention), whatever the
 // row count; the GEMMs are then the bf16 ones on the slots.
-int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, float* txt, int L, float* img,
-                       int N, const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod,
-                       void* ws, cudaStream_t st) {
+int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, const dit_parallel_w8a8* wq,
+                       float* txt, int L, float* img, int N, const float* tc, const float* ts, const float* ic,
+                       const float* is, const ModRef& mod, void* ws, cudaStream_t st) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
@@ -464,11 +464,17 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
   struct DequantCtx {
     const dit_dims* d;
     const dit_block_w8* w8;
-  } dctx{d, w8};
-  // weight 0: Wqkv then Wup (rows 3H on); weight 1: Wout then Wdown (at H * H)
+    const dit_parallel_w8a8* wq;
+  } dctx{d, w8, wq};
+  // weight 0: Wqkv then Wup (rows 3H on); weight 1: Wout then Wdown (at H * H). W8A8: the codes of
+  // linear1 [3H + 2F, H] and of linear2 [H, H + F] widened to bf16
   auto dequant = [](const void* c, int i, uint16_t* dst, cudaStream_t s2) -> int {
     const DequantCtx* x = static_cast<const DequantCtx*>(c);
     const int H_ = x->d->hidden;
+    if (x->wq) {
+      const long long n = i == 0 ? (3LL * H_ + 2LL * x->d->ffn) * H_ : (long long)H_ * (H_ + x->d->ffn);
+      return codes_bf16_launch(i == 0 ? x->wq->q1 : x->wq->q2, dst, n, s2);
+    }
     const int first = i == 0 ? 0 : 1, second = i == 0 ? 2 : 3;
     int n, k;
     linear_shape(x->d, first, &n, &k);
@@ -478,20 +484,27 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
     linear_shape(x->d, second, &n, &k);
     return dequant_int8_launch(x->w8->q[second], x->w8->s[second], dst2, n, k, s2);
   };
-  uint16_t* slots = w8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
-  WeightPrefetch pf(st, slots, w8 ? int8_parallel_slot0_bytes(d) : 0, dequant, &dctx, 2);
+  const bool slotted = w8 || wq;  // weights prepared into the slots after the block workspace
+  uint16_t* slots = slotted ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
+  WeightPrefetch pf(st, slots, slotted ? int8_parallel_slot0_bytes(d) : 0, dequant, &dctx, 2);
+  // W8A8: per-token scales of h and of [o | a], after the slots
+  float* sa1 = wq ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + b.bytes + int8_parallel_scratch_bytes(d))
+                  : nullptr;
+  float* sa2 = wq ? sa1 + round_up(size_t(R), 64) : nullptr;
   int rc;
-  if (w8 && (rc = pf.start()) != DIT_OK) return rc;
-  const float* norm = w8 ? w8->norm1 : w->norm1;
-  const float* qn = w8 ? w8->q_norm : w->q_norm;
-  const float* kn = w8 ? w8->k_norm : w->k_norm;
-  const uint16_t *wqkv = w8 ? nullptr : w->wqkv, *wup = w8 ? nullptr : w->wup;
-  const uint16_t *wout = w8 ? nullptr : w->wout, *wdown = w8 ? nullptr : w->wdown;
+  if (slotted && (rc = pf.start()) != DIT_OK) return rc;
+  const float* norm = wq ? wq->norm1 : w8 ? w8->norm1 : w->norm1;
+  const float* qn = wq ? wq->q_norm : w8 ? w8->q_norm : w->q_norm;
+  const float* kn = wq ? wq->k_norm : w8 ? w8->k_norm : w->k_norm;
+  const uint16_t *wqkv = slotted ? nullptr : w->wqkv, *wup = slotted ? nullptr : w->wup;
+  const uint16_t *wout = slotted ? nullptr : w->wout, *wdown = slotted ? nullptr : w->wdown;
+  long long ld_out = H, ld_down = F;  // row strides of the two halves of the second GEMM's weight
 
-  // 1. h = LayerNorm(x) * norm * (1 + scale) + shift
+  // 1. h = LayerNorm(x) * norm * (1 + scale) + shift (W8A8: then its per-token codes in place)
   ModNormParams mp{txt, img, L, R, H, H, H, norm, mod.rows, mod.rows + H, 3LL * H, mod.map, d->eps, b.h};
   mp.layernorm = 1;
   if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+  if (wq && (rc = quant_rows_launch(b.h, R, H, wq->smooth1, sa1, st)) != DIT_OK) return rc;
 
   // 2. q, k, vt (QK-norm + rope epilogue) and a (SwiGLU epilogue) from h [Wqkv ; Wup]^T
   GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, qn, kn, err);
@@ -499,17 +512,23 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
   g.out = b.a;
   g.ldo = F;
   g.n_split = 3 * H;
-  if (w8) {
+  if (slotted) {
     const uint16_t* s0;
     if ((rc = pf.use(0, &s0)) != DIT_OK) return rc;
     wqkv = s0;
     wup = s0 + size_t(3) * H * H;
+  }
+  if (wq) {
+    g.a_scale = sa1;
+    g.w_scale = wq->scale1;
   }
   if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wqkv, H, wup, H, kEpiQKVSwiGLU, g, st)) != DIT_OK) return rc;
 
   // 3. o = attention(q, k, v); q and k rows QK-normed
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, qn, kn, nullptr, nullptr};
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
+  // W8A8: codes of the joined rows [o | a] in place, one scale per row
+  if (wq && (rc = quant_rows_joint_launch(b.o, H, b.a, F, R, wq->smooth2, nullptr, R, sa2, st)) != DIT_OK) return rc;
 
   // 4. x += gate * ([o | a] [Wout | Wdown]^T)
   g = base_params(R, H, H + F, err);
@@ -520,13 +539,22 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
   g.map = mod.map;
   g.gate_stride = 3LL * H;
   g.k_split = H;
-  if (w8) {
+  if (slotted) {
     const uint16_t* s1;
     if ((rc = pf.use(1, &s1)) != DIT_OK) return rc;
-    wout = s1;
-    wdown = s1 + size_t(H) * H;
+    if (wq) {
+      // linear2's codes [H, H + F]: the first H columns multiply o, the rest a
+      wout = s1;
+      wdown = s1 + H;
+      ld_out = ld_down = H + F;
+      g.a_scale = sa2;
+      g.w_scale = wq->scale2;
+    } else {
+      wout = s1;
+      wdown = s1 + size_t(H) * H;
+    }
   }
-  return gemm_launch_cat(b.o, H, b.a, F, wout, H, wdown, F, kEpiGated, g, st);
+  return gemm_launch_cat(b.o, H, b.a, F, wout, ld_out, wdown, ld_down, kEpiGated, g, st);
 }
 
 // The double-stream block: the sequential block in which text rows [0, L) and image rows [L, R)
@@ -536,43 +564,69 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
 // int8lin weights: linear i's text and image weights are dequantised on the side stream into one
 // scratch slot (text first, none when L = 0), one linear ahead of their GEMM, whatever the row count.
 int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w* wi, const dit_block_w8* w8t,
-                     const dit_block_w8* w8i, float* txt, int L, float* img, int N, const float* tc, const float* ts,
-                     const float* ic, const float* is, const ModRef& mod, void* ws, cudaStream_t st) {
+                     const dit_block_w8* w8i, const dit_block_w8a8* wqt, const dit_block_w8a8* wqi, float* txt, int L,
+                     float* img, int N, const float* tc, const float* ts, const float* ic, const float* is,
+                     const ModRef& mod, void* ws, cudaStream_t st) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
   const BlockWs b = carve_block_ws(d, R, ws);
-  // int8lin: the weights each GEMM reads live in the prefetch slots; tw8 / iw8 point at them, linear
-  // by linear, once the side stream has written them
+  // int8lin / W8A8: the weights each GEMM reads live in the prefetch slots (dequantised, or codes
+  // widened to bf16); tw8 / iw8 point at them, linear by linear, once the side stream has written them
   struct DequantCtx {
     const dit_dims* d;
     const dit_block_w8* t;
     const dit_block_w8* i;
+    const dit_block_w8a8* qt;
+    const dit_block_w8a8* qi;
     int L;
-  } dctx{d, w8t, w8i, L};
+  } dctx{d, w8t, w8i, wqt, wqi, L};
   auto dequant = [](const void* c, int i, uint16_t* dst, cudaStream_t s2) -> int {
     const DequantCtx* x = static_cast<const DequantCtx*>(c);
     int n, k;
     linear_shape(x->d, i, &n, &k);
     if (x->L > 0) {
-      int r = dequant_int8_launch(x->t->q[i], x->t->s[i], dst, n, k, s2);
+      int r = x->qi ? codes_bf16_launch(x->qt->q[i], dst, (long long)n * k, s2)
+                    : dequant_int8_launch(x->t->q[i], x->t->s[i], dst, n, k, s2);
       if (r != DIT_OK) return r;
       dst += size_t(n) * k;
     }
-    return dequant_int8_launch(x->i->q[i], x->i->s[i], dst, n, k, s2);
+    return x->qi ? codes_bf16_launch(x->qi->q[i], dst, (long long)n * k, s2)
+                 : dequant_int8_launch(x->i->q[i], x->i->s[i], dst, n, k, s2);
   };
-  const bool q8 = w8i != nullptr;
+  const bool q8 = w8i != nullptr || wqi != nullptr;
   uint16_t* slots = q8 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes) : nullptr;
   WeightPrefetch pf(st, slots, q8 ? 2 * int8_slot_bytes(d) : 0, dequant, &dctx);
+  // W8A8: per-token scales of the activation being quantised, after the slots
+  float* sa = wqi ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + b.bytes + int8_double_scratch_bytes(d))
+                  : nullptr;
   dit_block_w tw8{}, iw8{};
   if (q8) {
-    if (L > 0) tw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, w8t->norm1, w8t->norm2, w8t->q_norm, w8t->k_norm};
-    iw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, w8i->norm1, w8i->norm2, w8i->q_norm, w8i->k_norm};
+    if (wqi) {
+      if (L > 0) tw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, wqt->norm1, wqt->norm2, wqt->q_norm, wqt->k_norm};
+      iw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, wqi->norm1, wqi->norm2, wqi->q_norm, wqi->k_norm};
+    } else {
+      if (L > 0) tw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, w8t->norm1, w8t->norm2, w8t->q_norm, w8t->k_norm};
+      iw8 = dit_block_w{nullptr, nullptr, nullptr, nullptr, w8i->norm1, w8i->norm2, w8i->q_norm, w8i->k_norm};
+    }
     wt = &tw8;
     wi = &iw8;
     const int r = pf.start();
     if (r != DIT_OK) return r;
   }
+  // W8A8: codes of activation x [R, K] in place before linear i, each stream's rows with its own
+  // divisors, and the GEMM's scales (the image rows form the second row group when both streams run;
+  // with L = 0 the image stream is the only one and takes every row)
+  auto w8a8 = [&](int i, uint16_t* x, int K, GemmParams& g) -> int {
+    if (!wqi) return DIT_OK;
+    const int r = quant_rows_joint_launch(x, K, nullptr, 0, R, L > 0 ? wqt->smooth[i] : nullptr, wqi->smooth[i], L,
+                                          sa, st);
+    if (r != DIT_OK) return r;
+    g.a_scale = sa;
+    g.w_scale = L > 0 ? wqt->scale[i] : wqi->scale[i];
+    g.w_scale2 = L > 0 ? wqi->scale[i] : nullptr;
+    return DIT_OK;
+  };
   // before linear i's GEMMs: its weights ready on the caller's stream; after them: the slot released
   auto before = [&](int i) -> int {
     if (!q8) return DIT_OK;
@@ -630,6 +684,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.q_norm2 = wi->q_norm;
     g.k_norm2 = wi->k_norm;
     g.m_split = L;
+    if ((rc = w8a8(0, b.h, H, g)) != DIT_OK) return rc;
     if ((rc = before(0)) != DIT_OK) return rc;
     if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wqkv, H, wi->wqkv, H, kEpiQKV, g, st)) != DIT_OK) return rc;
     if ((rc = after(0)) != DIT_OK) return rc;
@@ -638,6 +693,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, H, 2);
     g.m_split = L;
+    if ((rc = w8a8(1, b.o, H, g)) != DIT_OK) return rc;
     if ((rc = before(1)) != DIT_OK) return rc;
     if ((rc = gemm_launch_cat(b.o, H, nullptr, 0, wt->wout, H, wi->wout, H, kEpiGated, g, st)) != DIT_OK) return rc;
     if ((rc = after(1)) != DIT_OK) return rc;
@@ -646,11 +702,13 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.out = b.a;
     g.ldo = F;
     g.m_split = L;
+    if ((rc = w8a8(2, b.h, H, g)) != DIT_OK) return rc;
     if ((rc = before(2)) != DIT_OK) return rc;
     if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wup, H, wi->wup, H, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
     if ((rc = after(2)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, F, 5);
     g.m_split = L;
+    if ((rc = w8a8(3, b.a, F, g)) != DIT_OK) return rc;
     if ((rc = before(3)) != DIT_OK) return rc;
     return gemm_launch_cat(b.a, F, nullptr, 0, wt->wdown, F, wi->wdown, F, kEpiGated, g, st);
   }
@@ -665,6 +723,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     GemmParams g = qkv_params(d, s.n, R, L, b, tc, ts, ic, is, s.w->q_norm, s.w->k_norm, err);
     g.row_off = s.r0;
     g.R_total = R;
+    if ((rc = w8a8(0, b.h, H, g)) != DIT_OK) return rc;  // (one stream: it runs once)
     if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wqkv, nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
   }
   if ((rc = after(0)) != DIT_OK) return rc;
@@ -679,6 +738,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, H, 2);
+    if ((rc = w8a8(1, b.o, H, g)) != DIT_OK) return rc;
     if ((rc = gemm_launch(b.o + size_t(s.r0) * H, H, s.w->wout, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
   }
   if ((rc = after(1)) != DIT_OK) return rc;
@@ -692,6 +752,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     GemmParams g = base_params(s.n, 2 * F, H, err);
     g.out = b.a + size_t(s.r0) * F;
     g.ldo = F;
+    if ((rc = w8a8(2, b.h, H, g)) != DIT_OK) return rc;
     if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wup, nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
   }
   if ((rc = after(2)) != DIT_OK) return rc;
@@ -700,6 +761,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, F, 5);
+    if ((rc = w8a8(3, b.a, F, g)) != DIT_OK) return rc;
     if ((rc = gemm_launch(b.a + size_t(s.r0) * F, F, s.w->wdown, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
   }
   return DIT_OK;
@@ -797,12 +859,15 @@ const char* dit_status_string(int s) {
 }
 
 size_t dit_workspace_bytes(const dit_dims* d, int L, int N, int variant) {
-  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 6) return 0;
-  size_t bytes = carve_block_ws(d, L + N, nullptr).bytes;
+  if (!dims_ok(d) || L < 0 || N < 1 || variant < 0 || variant > 8) return 0;
+  const size_t R = size_t(L) + N;
+  size_t bytes = carve_block_ws(d, int(R), nullptr).bytes;
   if (variant == 1) bytes += int8_scratch_bytes(d);
-  if (variant == 4) bytes += w8a8_extra_bytes(d, L + N);
+  if (variant == 4) bytes += w8a8_extra_bytes(d, int(R));
   if (variant == 5) bytes += int8_parallel_scratch_bytes(d);
   if (variant == 6) bytes += int8_double_scratch_bytes(d);
+  if (variant == 7) bytes += int8_parallel_scratch_bytes(d) + 2 * round_up(R, 64) * sizeof(float);
+  if (variant == 8) bytes += int8_double_scratch_bytes(d) + round_up(R * sizeof(float), 256);
   return bytes;
 }
 
@@ -849,8 +914,8 @@ int dit_parallel_block_forward(const dit_dims* d, const dit_block_w* w, float* t
   if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
   if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
   if (d->hidden % 256 != 0 || d->ffn % 128 != 0) return DIT_EUNSUPPORTED;  // 256-wide tiles over 3H and 2F
-  return run_parallel_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
-                            reinterpret_cast<cudaStream_t>(stream));
+  return run_parallel_block(d, w, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
+                            ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dit_double_block_forward(const dit_dims* d, const dit_block_w* w_txt, const dit_block_w* w_img, float* txt, int L,
@@ -863,7 +928,7 @@ int dit_double_block_forward(const dit_dims* d, const dit_block_w* w_txt, const 
     if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
     if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
   }
-  return run_double_block(d, w_txt, w_img, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
+  return run_double_block(d, w_txt, w_img, nullptr, nullptr, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
                           ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -876,8 +941,8 @@ int dit_parallel_block_forward_int8(const dit_dims* d, const dit_block_w8* w, fl
   if (d->hidden % 256 != 0 || d->ffn % 256 != 0) return DIT_EUNSUPPORTED;
   for (int i = 0; i < 4; ++i)
     if (!w->q[i] || !w->s[i] || !al16(w->q[i]) || !al16(w->s[i])) return DIT_EINVAL;
-  return run_parallel_block(d, nullptr, w, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
-                            reinterpret_cast<cudaStream_t>(stream));
+  return run_parallel_block(d, nullptr, w, nullptr, txt, L, img, N, tc, ts, ic, is,
+                            ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dit_double_block_forward_int8(const dit_dims* d, const dit_block_w8* w_txt, const dit_block_w8* w_img, float* txt,
@@ -893,8 +958,37 @@ int dit_double_block_forward_int8(const dit_dims* d, const dit_block_w8* w_txt, 
     for (int i = 0; i < 4; ++i)
       if (!w->q[i] || !w->s[i] || !al16(w->q[i]) || !al16(w->s[i])) return DIT_EINVAL;
   }
-  return run_double_block(d, nullptr, nullptr, L > 0 ? w_txt : nullptr, w_img, txt, L, img, N, tc, ts, ic, is,
-                          ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
+  return run_double_block(d, nullptr, nullptr, L > 0 ? w_txt : nullptr, w_img, nullptr, nullptr, txt, L, img, N, tc, ts,
+                          ic, is, ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_parallel_block_forward_w8a8(const dit_dims* d, const dit_parallel_w8a8* w, float* txt, int L, float* img, int N,
+                                    const float* tc, const float* ts, const float* ic, const float* is,
+                                    const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 7);
+  if (rc != DIT_OK) return rc;
+  if (!w || !w->q1 || !w->scale1 || !w->q2 || !w->scale2) return DIT_EINVAL;
+  if (!al16(w->q1) || !al16(w->q2)) return DIT_EINVAL;
+  if (d->hidden % 256 != 0 || d->ffn % 256 != 0) return DIT_EUNSUPPORTED;
+  return run_parallel_block(d, nullptr, nullptr, w, txt, L, img, N, tc, ts, ic, is,
+                            ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dit_double_block_forward_w8a8(const dit_dims* d, const dit_block_w8a8* w_txt, const dit_block_w8a8* w_img,
+                                  float* txt, int L, float* img, int N, const float* tc, const float* ts,
+                                  const float* ic, const float* is, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                  dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 8);
+  if (rc != DIT_OK) return rc;
+  if (d->hidden % 256 != 0 || d->ffn % 256 != 0) return DIT_EUNSUPPORTED;
+  for (const dit_block_w8a8* w : {w_txt, w_img}) {
+    if (w == w_txt && L == 0) continue;
+    if (!w) return DIT_EINVAL;
+    for (int i = 0; i < 4; ++i)
+      if (!w->q[i] || !w->scale[i] || !al16(w->q[i])) return DIT_EINVAL;
+  }
+  return run_double_block(d, nullptr, nullptr, nullptr, nullptr, L > 0 ? w_txt : nullptr, w_img, txt, L, img, N, tc,
+                          ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dit_lora_merge(const uint16_t* W, int n_out, int n_in, const uint16_t* A, const uint16_t* B, int rank,

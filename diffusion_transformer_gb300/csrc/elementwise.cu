@@ -441,50 +441,56 @@ __device__ __forceinline__ float w8a8_code(float v, float scale) {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-// One CTA per row of x [rows, K] bf16 (K a multiple of 8): codes written over x as bf16 (exact small
-// integers: the bf16 MMA then multiplies them exactly), the row's scale to scale[row]. Two passes
-// over the row (it is re-read from L2 after the maximum).
-__global__ void __launch_bounds__(kNormThreads) quant_rows_kernel(uint16_t* x, int K, const float* smooth,
-                                                                  float* scale) {
+// One CTA per row. The row is x[r, 0:K] followed by x2[r, 0:K2] (K2 = 0: x alone; both multiples of
+// 8), quantised as one row: codes written over both as bf16 (exact small integers: the bf16 MMA then
+// multiplies them exactly), the row's scale to scale[r]. The SmoothQuant divisors run over the
+// joined row; rows from row_split on take smooth2 instead (the second stream's divisors; NULL: none).
+// Two passes over the row (it is re-read from L2 after the maximum).
+__global__ void __launch_bounds__(kNormThreads) quant_rows_kernel(uint16_t* x, int K, uint16_t* x2, int K2,
+                                                                  const float* smooth, const float* smooth2,
+                                                                  int row_split, float* scale) {
   pdl_wait();
   pdl_trigger();
   __shared__ float part[kNormThreads / 32];
   uint4* row = reinterpret_cast<uint4*>(x + size_t(blockIdx.x) * K);
-  const int n8 = K / 8;
+  uint4* row2 = x2 ? reinterpret_cast<uint4*>(x2 + size_t(blockIdx.x) * K2) : nullptr;
+  const int n8 = K / 8, n8_all = n8 + K2 / 8;
+  const float* sm = int(blockIdx.x) >= row_split ? smooth2 : smooth;
+  auto chunk = [&](int i) -> uint4* { return i < n8 ? row + i : row2 + (i - n8); };
   float m = 0.f;
-  for (int i = threadIdx.x; i < n8; i += kNormThreads) {
-    const uint4 u = row[i];
+  for (int i = threadIdx.x; i < n8_all; i += kNormThreads) {
+    const uint4 u = *chunk(i);
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-      if (smooth) {
-        a = __fdiv_rn(a, __ldg(smooth + 8 * i + 2 * j));
-        b = __fdiv_rn(b, __ldg(smooth + 8 * i + 2 * j + 1));
+      if (sm) {
+        a = __fdiv_rn(a, __ldg(sm + 8 * i + 2 * j));
+        b = __fdiv_rn(b, __ldg(sm + 8 * i + 2 * j + 1));
       }
       m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
     }
   }
   const float sc = __fdiv_rn(block_max(m, part), 127.f);
-  for (int i = threadIdx.x; i < n8; i += kNormThreads) {
-    const uint4 u = row[i];
+  for (int i = threadIdx.x; i < n8_all; i += kNormThreads) {
+    uint4* dst = chunk(i);
+    const uint4 u = *dst;
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-      if (smooth) {
-        a = __fdiv_rn(a, __ldg(smooth + 8 * i + 2 * j));
-        b = __fdiv_rn(b, __ldg(smooth + 8 * i + 2 * j + 1));
+      if (sm) {
+        a = __fdiv_rn(a, __ldg(sm + 8 * i + 2 * j));
+        b = __fdiv_rn(b, __ldg(sm + 8 * i + 2 * j + 1));
       }
       o[j] = pack_bf16x2(w8a8_code(a, sc), w8a8_code(b, sc));  // integers up to 127: exact in bf16
     }
-    row[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    *dst = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (threadIdx.x == 0) scale[blockIdx.x] = sc;
 }
 
-// One CTA per output channel of w [N, K] bf16: codes int8 [N, K], scale[n] (smooth folded first).
 __global__ void __launch_bounds__(kNormThreads) quant_weight_kernel(const uint16_t* w, int K, const float* smooth,
                                                                     int8_t* q, float* scale) {
   pdl_wait();
@@ -523,9 +529,15 @@ __global__ void codes_bf16_kernel(const int8_t* q, uint16_t* w, long long n16) {
 }
 
 int quant_rows_launch(uint16_t* x, int rows, int K, const float* smooth, float* scale, cudaStream_t stream) {
+  return quant_rows_joint_launch(x, K, nullptr, 0, rows, smooth, nullptr, rows, scale, stream);
+}
+
+int quant_rows_joint_launch(uint16_t* x, int K, uint16_t* x2, int K2, int rows, const float* smooth,
+                            const float* smooth2, int row_split, float* scale, cudaStream_t stream) {
   if (rows <= 0) return DIT_OK;
-  if (K % 8 != 0) return DIT_EUNSUPPORTED;
-  if (launch_pdl(quant_rows_kernel, dim3(rows), dim3(kNormThreads), 0, stream, 1, x, K, smooth, scale) != cudaSuccess)
+  if (K % 8 != 0 || K2 % 8 != 0 || (K2 > 0 && !x2)) return DIT_EUNSUPPORTED;
+  if (launch_pdl(quant_rows_kernel, dim3(rows), dim3(kNormThreads), 0, stream, 1, x, K, x2, K2, smooth, smooth2,
+                 row_split, scale) != cudaSuccess)
     return DIT_ECUDA;
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
 }

@@ -507,8 +507,8 @@ __device__ __forceinline__ void sk_store(uint32_t taddr, float* dst, int lane) {
 // `part(i)` is segment i's slot (this warp's rows). The loads of parts 0 and 1 of a chunk are issued
 // together (one L2 round trip for the usual two-part tile), a third part's after them.
 template <int BN, typename PartFn>
-__device__ __forceinline__ void sk_sum(const GemmParams& p, uint32_t taddr, PartFn part, int nparts, int lane, int row,
-                                       int row_end, int n0) {
+__device__ __forceinline__ void sk_sum(const GemmParams& p, const float* w_scale, uint32_t taddr, PartFn part,
+                                       int nparts, int lane, int row, int row_end, int n0) {
   static_assert(kSkMaxParts == 3, "parts 0 and 1 together, then part 2");
   const float sa = (p.a_scale && row < row_end) ? __ldg(p.a_scale + row) : 0.f;
   const float4* s0 = reinterpret_cast<const float4*>(part(0)) + lane;
@@ -549,7 +549,7 @@ __device__ __forceinline__ void sk_sum(const GemmParams& p, uint32_t taddr, Part
       v[4 * q + 3] = __float_as_uint(a[q].w);
     }
     if (p.a_scale) {
-      const float* sw = p.w_scale + n0 + c * 32;
+      const float* sw = w_scale + n0 + c * 32;
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sa * __ldg(sw + j));
     }
@@ -856,6 +856,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
         static_assert(B8 || Cfg::kEpiCols == BN, "one epilogue warp per TMEM lane quadrant");
         const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
         const int row = tr.base + rows_of + quad * 32 + lane;
+        const float* w_scale = (tr.g2 && p.w_scale2) ? p.w_scale2 : p.w_scale;  // this row group's
         bool scaled = false;
         if (w.part >= 0) {
           // stream-K segment: publish this warp's partial, count it, and if it was the quadrant's
@@ -881,7 +882,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
           auto part = [&](int i) -> const float* {
             return p.sk_part + (size_t(sk_slot(p, w.u_first + i, w.trel, KB)) * kSlabs + rank) * slab + warp_off;
           };
-          sk_sum<BN>(p, taddr, part, w.nparts, lane, row, tr.end, nb * BN);
+          sk_sum<BN>(p, w_scale, taddr, part, w.nparts, lane, row, tr.end, nb * BN);
           if (lane == 0) atomicExch(cnt, 0u);  // zero again for the next launch
           scaled = true;
         }
@@ -894,7 +895,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, B8, PAIR>::kThreads, 1)
             uint32_t v[32];
             tmem_ld32(taddr + c * 32, v);
             tmem_ld_wait();
-            const float* sw = p.w_scale + nb * BN + c * 32;
+            const float* sw = w_scale + nb * BN + c * 32;
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sa * __ldg(sw + j));
             tmem_st32(taddr + c * 32, v);

@@ -74,8 +74,9 @@ struct GemmParams {
   // set by the launcher for CTA-pair launches: a launch counter that picks the start-word set
   uint32_t pair_epoch;
   // W8A8 (both non-null): the accumulator is multiplied by a_scale[GEMM row] * w_scale[column]
-  // before the epilogue (per-token and per-output-channel scales of integer codes)
-  const float *a_scale, *w_scale;
+  // before the epilogue (per-token and per-output-channel scales of integer codes); rows of the
+  // second row group (m_split) take w_scale2 when it is given (the second stream's weight scales)
+  const float *a_scale, *w_scale, *w_scale2;
 };
 
 // B operand in int8 with one bf16 scale per 32 consecutive K elements (int8lin weights). For row
@@ -172,6 +173,10 @@ int dequant_int8_launch(const int8_t* q, const uint16_t* s, uint16_t* w, long lo
 // W8A8: per-token codes of x [rows, K] bf16 written over x (as bf16 integers) with scale[rows];
 // per-output-channel codes of a bf16 weight [N, K] (int8) with scale[N]; int8 codes to bf16 (n % 16 == 0)
 int quant_rows_launch(uint16_t* x, int rows, int K, const float* smooth, float* scale, cudaStream_t stream);
+// The same over joined rows x[r, 0:K] ++ x2[r, 0:K2] (one code scale per joined row, divisors over the
+// joined row), rows from row_split on taking the divisors smooth2 instead of smooth (NULL: none).
+int quant_rows_joint_launch(uint16_t* x, int K, uint16_t* x2, int K2, int rows, const float* smooth,
+                            const float* smooth2, int row_split, float* scale, cudaStream_t stream);
 int quant_weight_launch(const uint16_t* w, int N, int K, const float* smooth, int8_t* q, float* scale,
                         cudaStream_t stream);
 int codes_bf16_launch(const int8_t* q, uint16_t* w, long long n, cudaStream_t stream);

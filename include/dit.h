@@ -299,6 +299,48 @@ DIT_API int dit_double_block_forward_int8(const dit_dims* dims, const dit_block_
                                           const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
                                           dit_stream_t stream);
 
+/* W8A8 weights of the parallel block [klein, section 5 (int8 detail: a single block's linear1 and
+ * linear2) and its D4 / D5 entries]: linear1 = [Wqkv ; Wup] as one weight q1 [3H + 2F, H] (rows
+ * all-Q, all-K, all-V, then the gate/up rows interleaved) and linear2 = [Wout | Wdown] as one weight
+ * q2 [H, H + F] (inputs: the attention output's H, then the SwiGLU output's F), each quantised per
+ * output channel over its whole row (dit_w8a8_quantize_weight of the joined matrix, after the fold
+ * of its divisors), scale1 [3H + 2F] and scale2 [H] fp32; smooth1 [H] and smooth2 [H + F] fp32 the
+ * SmoothQuant divisors used for them, or NULL. norm1, q_norm, k_norm as in dit_block_w. */
+typedef struct {
+  const int8_t* q1;
+  const float* scale1;
+  const float* smooth1;
+  const int8_t* q2;
+  const float* scale2;
+  const float* smooth2;
+  const float* norm1;
+  const float* q_norm;
+  const float* k_norm;
+} dit_parallel_w8a8;
+
+/* The W8A8 forms of the parallel and the double-stream blocks (an opt-in lossy tier, as for
+ * dit_block_forward_w8a8) [klein, section 5 and its D4 / D5 entries]. Parallel: h (the modulated
+ * LayerNorm's bf16 rows) is quantised per token (after the division by smooth1) and multiplied with
+ * linear1's codes, the accumulator scaled by both scales before the QK-norm/rotary and SwiGLU
+ * epilogues; the attention output o and the SwiGLU output a are quantised per token as one joined
+ * row [o | a] (divisors smooth2) and multiplied with linear2's codes before the gated residual.
+ * Double-stream: each stream's four linears are W8A8 linears with that stream's weights, scales
+ * and divisors (w_txt for the text rows [0, L), w_img for the image rows; w_txt may be NULL when
+ * L = 0), each activation quantised per token with its own stream's divisors. Weight codes are
+ * widened to bf16 on the library's second stream one linear ahead; the integer dot products are
+ * exact on the bf16 tensor cores while every partial sum stays below 2^24 in magnitude.
+ * Workspace: dit_workspace_bytes(dims, L, N, 7) (parallel) and (dims, L, N, 8) (double-stream).
+ * Requires H % 256 == 0 and ffn % 256 == 0 besides the dims rules. Errors as dit_block_forward. */
+DIT_API int dit_parallel_block_forward_w8a8(const dit_dims* dims, const dit_parallel_w8a8* w, float* txt, int L,
+                                            float* img, int N, const float* txt_cos, const float* txt_sin,
+                                            const float* img_cos, const float* img_sin, const dit_mod* mod,
+                                            void* ws, size_t ws_bytes, dit_stream_t stream);
+DIT_API int dit_double_block_forward_w8a8(const dit_dims* dims, const dit_block_w8a8* w_txt,
+                                          const dit_block_w8a8* w_img, float* txt, int L, float* img, int N,
+                                          const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                          const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                          dit_stream_t stream);
+
 /* FlowMatch Euler step [host contract, section 6]: x[i] <- x[i] + (sigma_next - sigma) * vel[i],
  * each operation rounded separately in fp32 (no fused multiply-add). n >= 0. */
 DIT_API int dit_euler_step(float* x, const float* vel, int64_t n, float sigma, float sigma_next, dit_stream_t stream);
@@ -346,8 +388,8 @@ DIT_API int dit_denoise(const dit_model* model, float* img_tokens, int N, const 
                 const float* img_cos, const float* img_sin, void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* Workspace sizes. variant 0 = bf16 block, 1 = int8lin block, 2 = parallel block, 3 = double-stream
- * block, 4 = W8A8 block, 5 = int8lin parallel block, 6 = int8lin double-stream block. Returns 0 for
- * unsupported dims. */
+ * block, 4 = W8A8 block, 5 = int8lin parallel block, 6 = int8lin double-stream block, 7 = W8A8
+ * parallel block, 8 = W8A8 double-stream block. Returns 0 for unsupported dims. */
 DIT_API size_t dit_workspace_bytes(const dit_dims* dims, int L, int N, int variant);
 DIT_API size_t dit_denoise_workspace_bytes(const dit_model* model, int L, int N, int steps);
 

@@ -148,12 +148,15 @@ def parallel_block_forward_w8a8_rows(x, linear1, linear2, mod, mod_map, cos, sin
     rows = np.arange(R) if rows is None else np.asarray(rows)
     m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)]
     h = modulated_layernorm(x, norm, m[:, 0], m[:, 1], eps)
-    u = w8a8_linear_f(h, linear1[0], linear1[1], smooth1)
+    # linear1's output channels split at 3H (each channel's codes and scale are its own row, and each
+    # row of h has its own codes): the Q|K|V part for every row, the gate/up part for `rows` only
+    q1, s1 = np.asarray(linear1[0]), np.asarray(linear1[1])
+    u = w8a8_linear_f(h, q1[:3 * H], s1[:3 * H], smooth1)
     q = rotate(qk_rmsnorm(u[:, 0:H].reshape(R, nh, d), q_norm, qk_eps), cos, sin)
     k = rotate(qk_rmsnorm(u[:, H:2 * H].reshape(R, nh, d), k_norm, qk_eps), cos, sin)
     v = u[:, 2 * H:3 * H].reshape(R, nh, d)
     o = attention(q, k, v, rows)
-    a = swiglu_interleaved(u[rows, 3 * H:])
+    a = swiglu_interleaved(w8a8_linear_f(h[rows], q1[3 * H:], s1[3 * H:], smooth1))
     y = w8a8_linear_f(np.concatenate([o, a], axis=1), linear2[0], linear2[1], smooth2)
     return x[rows] + m[rows, 2] * y
 

@@ -90,11 +90,12 @@ def test_workspace_variants_host_only(libdit, H, nh, hd, F, L, N):
     block = (_ru(R * H * 2) + 2 * _ru(nh * R * hd * 2) + _ru(nh * hd * _ru(R, 8) * 2) + _ru(R * H * 2) +
              _ru(R * F * 2))
     slot = _ru(max(3 * H * H, H * H, 2 * F * H, H * F) * 2)
+    par = _ru((3 * H + 2 * F) * H * 2) + _ru(H * (H + F) * 2)
     expect = {0: block, 1: block + 2 * slot, 2: block, 3: block, 4: block + 2 * slot + _ru(R * 4),
-              5: block + _ru((3 * H + 2 * F) * H * 2) + _ru(H * (H + F) * 2), 6: block + 4 * slot}
+              5: block + par, 6: block + 4 * slot, 7: block + par + 2 * _ru(R, 64) * 4, 8: block + 4 * slot + _ru(R * 4)}
     for variant, want in expect.items():
         assert D.dit_workspace_bytes(d, L, N, variant) == want, variant
-    assert D.dit_workspace_bytes(d, L, N, 7) == 0 and D.dit_workspace_bytes(d, L, N, -1) == 0
+    assert D.dit_workspace_bytes(d, L, N, 9) == 0 and D.dit_workspace_bytes(d, L, N, -1) == 0
 
 
 def test_new_entries_reject_invalid_arguments_before_any_cuda_call(libdit):
@@ -109,6 +110,8 @@ def test_new_entries_reject_invalid_arguments_before_any_cuda_call(libdit):
     args = (None, 0, None, 1, None, None, None, None, None, None, 0, None)
     assert L.dit_parallel_block_forward_int8(None, None, *args) == -1
     assert L.dit_double_block_forward_int8(None, None, None, *args) == -1
+    assert L.dit_parallel_block_forward_w8a8(None, None, *args) == -1
+    assert L.dit_double_block_forward_w8a8(None, None, None, *args) == -1
     # no-allocation block: every argument is checked before the scratch address is looked up (that
     # lookup is the call's first CUDA call), so on this GPU-less host the errors are the argument
     # errors, never DIT_ECUDA
