@@ -614,6 +614,51 @@ def run_ours(args):
                "ms_per_block": msA, "tflops": tfA, "frac_of_peak": tfA / peaks["bf16_tflops"], "flop_per_block": flops,
                "launches_per_block": 11}
         del wA, wsA, wq, wsc
+        # the W8A8 parallel block: linear1 = [Wqkv ; Wup], linear2 = [Wout | Wdown] (one joined weight
+        # each, quantised per output channel over its whole row), per-row [R, 3, H] modulation
+        if not args.no_parallel:
+            inpP = DI.parallel_block_inputs(WORKLOAD)
+            modP = D.Modulation(_dev(torch, inpP.mod), _dev(torch, inpP.mod_map))
+            del inpP
+            W = st["w"].tensors
+            lin = []
+            for Wj in (torch.cat([W[0], W[2]], 0), torch.cat([W[1], W[3]], 1)):
+                qj = torch.empty(Wj.shape, dtype=torch.int8, device="cuda")
+                sj = torch.empty(Wj.shape[0], dtype=torch.float32, device="cuda")
+                D.dit_w8a8_quantize_weight(Wj.contiguous(), None, qj, sj)
+                lin += [qj, sj]
+            wPA = D.ParallelW8A8Weights(lin[0], lin[1], lin[2], lin[3])
+            wsPA = torch.empty(D.dit_workspace_bytes(st["dims"], sh.L, sh.N, 7), dtype=torch.uint8, device="cuda")
+            callPA = lambda t, i: D.dit_parallel_block_forward_w8a8(st["dims"], wPA, t, i, st["tc"], st["ts"],
+                                                                    st["ic"], st["is_"], modP, wsPA)
+            msPA = _time_blocks(torch, st, callPA, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            tfPA = flops / (msPA * 1e-3) / 1e12
+            w8a["parallel_block"] = {"ms_per_block": msPA, "tflops": tfPA, "frac_of_peak": tfPA / peaks["bf16_tflops"],
+                                     "launches_per_block": 6}
+            del wPA, wsPA, lin, modP
+        # the W8A8 double-stream block: each stream's four linears quantised on its own
+        if not args.no_double:
+            inpT = DI.block_inputs(WORKLOAD, seed=sh.seed + 50)
+            streams = []
+            for Ws in ((_dev_bf16(torch, inpT.wqkv), _dev_bf16(torch, inpT.wout), _dev_bf16(torch, inpT.wup),
+                        _dev_bf16(torch, inpT.wdown)), st["w"].tensors[:4]):
+                qs, ss = [], []
+                for Wj in Ws:
+                    qs.append(torch.empty(Wj.shape, dtype=torch.int8, device="cuda"))
+                    ss.append(torch.empty(Wj.shape[0], dtype=torch.float32, device="cuda"))
+                    D.dit_w8a8_quantize_weight(Wj, None, qs[-1], ss[-1])
+                streams.append(D.W8A8BlockWeights(qs, ss))
+            del inpT
+            wsDA = torch.empty(D.dit_workspace_bytes(st["dims"], sh.L, sh.N, 8), dtype=torch.uint8, device="cuda")
+            callDA = lambda t, i: D.dit_double_block_forward_w8a8(st["dims"], streams[0], streams[1], t, i, st["tc"],
+                                                                  st["ts"], st["ic"], st["is_"], st["mod"], wsDA)
+            msDA = _time_blocks(torch, st, callDA, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            tfDA = flops / (msDA * 1e-3) / 1e12
+            w8a["double_stream_block"] = {"ms_per_block": msDA, "tflops": tfDA,
+                                          "frac_of_peak": tfDA / peaks["bf16_tflops"], "launches_per_block": 11}
+            del streams, wsDA
 
     # end to end through host buffers
     e2e_ms, h2d, d2h = _e2e(torch, D, st, inp, max(3, args.steps // 2), 2)
