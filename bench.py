@@ -575,6 +575,28 @@ def run_ours(args):
         lor = {"workload": "1024sq block with rank-64 LoRA adapters on qkv, out, up and down", "ms_per_block": msL,
                "tflops": tfL, "frac_of_peak": tfL / peaks["bf16_tflops"], "flop_per_block": flL,
                "launches_per_block": 11}
+        # the parallel and double-stream blocks with the same adapters (double: on both streams)
+        if not args.no_parallel:
+            inpP = DI.parallel_block_inputs(WORKLOAD)
+            modP = D.Modulation(_dev(torch, inpP.mod), _dev(torch, inpP.mod_map))
+            del inpP
+            callLP = lambda t, i: D.dit_parallel_block_forward_lora(st["dims"], st["w"], loraW, t, i, st["tc"],
+                                                                    st["ts"], st["ic"], st["is_"], modP, wsL)
+            msLP = _time_blocks(torch, st, callLP, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            lor["parallel_block"] = {"ms_per_block": msLP, "tflops": flL / (msLP * 1e-3) / 1e12,
+                                     "frac_of_peak": flL / (msLP * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                     "launches_per_block": 10}
+            del modP
+        if not args.no_double:
+            callLD = lambda t, i: D.dit_double_block_forward_lora(st["dims"], st["w"], loraW, st["w"], loraW, t, i,
+                                                                  st["tc"], st["ts"], st["ic"], st["is_"], st["mod"],
+                                                                  wsL)
+            msLD = _time_blocks(torch, st, callLD, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            lor["double_stream_block"] = {"ms_per_block": msLD, "tflops": flL / (msLD * 1e-3) / 1e12,
+                                          "frac_of_peak": flL / (msLD * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                          "launches_per_block": 22}
         del loraW, wsL
 
     # the sandwich block: both branches RMS-normed (own weights) before their gates

@@ -21,6 +21,7 @@ __all__ = [
     "ParallelW8A8Weights", "dit_parallel_block_forward_w8a8", "dit_double_block_forward_w8a8",
     "dit_linear_w8a8", "dit_linear_w8a8_workspace_bytes",
     "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA", "dit_lora_merge",
+    "dit_parallel_block_forward_lora", "dit_double_block_forward_lora",
     "dit_block_forward_sandwich", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
@@ -93,6 +94,13 @@ _SIGNATURES = {
                                        c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod),
                                        c_void_p, c_size_t, c_void_p]),
     "dit_lora_workspace_bytes": (c_size_t, [POINTER(dit_dims), c_int, c_int, c_int]),
+    "dit_parallel_block_forward_lora": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), POINTER(dit_lora), c_void_p,
+                                                c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
+    "dit_double_block_forward_lora": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), POINTER(dit_lora),
+                                              POINTER(dit_block_w), POINTER(dit_lora), c_void_p, c_int, c_void_p,
+                                              c_int, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod),
+                                              c_void_p, c_size_t, c_void_p]),
     "dit_block_forward_sandwich": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_void_p, c_void_p,
                                            c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                                            POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
@@ -366,6 +374,36 @@ def dit_block_forward_lora(dims: DitDims, w: BlockWeights, lora: "LoRA", txt, im
                                      _ptr(txt_cos, f32), _ptr(txt_sin, f32), _ptr(img_cos, f32), _ptr(img_sin, f32),
                                      ctypes.byref(mod.c), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                      _stream(stream)), "dit_block_forward_lora")
+
+
+def dit_parallel_block_forward_lora(dims: DitDims, w: BlockWeights, lora: "LoRA", txt, img, txt_cos, txt_sin,
+                                    img_cos, img_sin, mod: Modulation, ws, stream=None):
+    """The parallel block with LoRA adapters; mod rows are [M, 3, H] (shift, scale, gate)."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_parallel_block_forward_lora(ctypes.byref(dims.c), ctypes.byref(w.c), ctypes.byref(lora.c),
+                                              _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"), img.shape[0],
+                                              _ptr(txt_cos, f32), _ptr(txt_sin, f32), _ptr(img_cos, f32),
+                                              _ptr(img_sin, f32), ctypes.byref(mod.c), _ptr(ws, None, "ws"),
+                                              ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_parallel_block_forward_lora")
+
+
+def dit_double_block_forward_lora(dims: DitDims, w_txt: Optional[BlockWeights], lora_txt: Optional["LoRA"],
+                                  w_img: BlockWeights, lora_img: Optional["LoRA"], txt, img, txt_cos, txt_sin,
+                                  img_cos, img_sin, mod: Modulation, ws, stream=None):
+    """The double-stream block with per-stream LoRA adapters (either set may be None, not both)."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    ref = lambda x: None if x is None else ctypes.byref(x.c)
+    _ok(lib().dit_double_block_forward_lora(ctypes.byref(dims.c), ref(w_txt), ref(lora_txt), ctypes.byref(w_img.c),
+                                            ref(lora_img), _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"),
+                                            img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32), _ptr(img_cos, f32),
+                                            _ptr(img_sin, f32), ctypes.byref(mod.c), _ptr(ws, None, "ws"),
+                                            ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_double_block_forward_lora")
 
 
 def dit_block_forward_sandwich(dims: DitDims, w: BlockWeights, post_attn, post_mlp, txt, img, txt_cos, txt_sin,

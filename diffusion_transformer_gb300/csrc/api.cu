@@ -239,6 +239,26 @@ struct ModRef {
 // One whole block on already-validated arguments. `w8` selects the int8lin path.
 int lora_rank_pad(int rank) { return (rank + 63) / 64 * 64; }
 
+// Linear i over the rows x [g.M, K] (bf16) with its LoRA adapter beside it when `lora` has factors
+// for linear i [gizai:dit, loraOf, withLora]: down = x A_i^T into `down` ([g.M, rank padded to 64];
+// the B operand's TMA map ends at the rank, so the padding columns come out as zeros), then one GEMM
+// over [x | down] [W | B_i]^T through the linear's own epilogue. Without an adapter, the plain GEMM.
+int gemm_with_lora(const dit_lora* lora, int i, const uint16_t* x, int K, const uint16_t* W, int epi, GemmParams g,
+                   uint16_t* down, int* err, cudaStream_t st) {
+  if (!lora || !lora->A[i]) return gemm_launch(x, K, W, nullptr, epi, g, st);
+  const int rp = lora_rank_pad(lora->rank);
+  GemmParams gd = base_params(g.M, rp, K, err);
+  gd.out = down;
+  gd.ldo = rp;
+  gd.b_rows = lora->rank;
+  int rc = gemm_launch(x, K, lora->A[i], nullptr, kEpiStoreBF16, gd, st);
+  if (rc != DIT_OK) return rc;
+  g.K = K + rp;
+  g.k_split = K;
+  g.b2_inner = lora->rank;
+  return gemm_launch_cat(x, K, down, rp, W, K, lora->B[i], lora->rank, epi, g, st);
+}
+
 int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, float* txt, int L, float* img, int N,
               const float* tc, const float* ts, const float* ic, const float* is, const ModRef& mod, void* ws,
               cudaStream_t st, const dit_lora* lora = nullptr, const float* post_attn = nullptr,
@@ -254,17 +274,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
   auto linear = [&](int i, const uint16_t* x, int K, const uint16_t* W, const GemmInt8B* w8b, int epi,
                     GemmParams g) -> int {
     if (!lora || !lora->A[i]) return gemm_launch(x, K, W, w8b, epi, g, st);
-    const int rp = lora_rank_pad(lora->rank);
-    GemmParams gd = base_params(R, rp, K, err);
-    gd.out = lora_down;
-    gd.ldo = rp;
-    gd.b_rows = lora->rank;
-    int rc = gemm_launch(x, K, lora->A[i], nullptr, kEpiStoreBF16, gd, st);
-    if (rc != DIT_OK) return rc;
-    g.K = K + rp;
-    g.k_split = K;
-    g.b2_inner = lora->rank;
-    return gemm_launch_cat(x, K, lora_down, rp, W, K, lora->B[i], lora->rank, epi, g, st);
+    return gemm_with_lora(lora, i, x, K, W, epi, g, lora_down, err, st);
   };
   // a gated linear; with a post-norm weight (sandwich block) its output y goes to the h..vt span as
   // fp32 (consumed by then, and at least R * H * 4 bytes) and the sandwich kernel adds
@@ -456,11 +466,43 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
 // row count; the GEMMs are then the bf16 ones on the slots.
 int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, const dit_parallel_w8a8* wq,
                        float* txt, int L, float* img, int N, const float* tc, const float* ts, const float* ic,
-                       const float* is, const ModRef& mod, void* ws, cudaStream_t st) {
+                       const float* is, const ModRef& mod, void* ws, cudaStream_t st, const dit_lora* lora = nullptr) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
   const BlockWs b = carve_block_ws(d, R, ws);
+  if (lora) {
+    // Adapters beside the linears: the fused GEMMs cannot take a second K-concatenated factor per
+    // fused part, so the four linears run one by one, each with its adapter (gemm_with_lora), the
+    // two output linears both adding gate * (their product) to x.
+    uint16_t* down = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes);
+    int rc;
+    ModNormParams mp{txt, img, L, R, H, H, H, w->norm1, mod.rows, mod.rows + H, 3LL * H, mod.map, d->eps, b.h};
+    mp.layernorm = 1;
+    if ((rc = modnorm_launch(mp, st)) != DIT_OK) return rc;
+    GemmParams g = qkv_params(d, R, R, L, b, tc, ts, ic, is, w->q_norm, w->k_norm, err);
+    if ((rc = gemm_with_lora(lora, 0, b.h, H, w->wqkv, kEpiQKV, g, down, err, st)) != DIT_OK) return rc;
+    g = base_params(R, 2 * F, H, err);
+    g.out = b.a;
+    g.ldo = F;
+    if ((rc = gemm_with_lora(lora, 2, b.h, H, w->wup, kEpiSwiGLU, g, down, err, st)) != DIT_OK) return rc;
+    AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, w->q_norm, w->k_norm, nullptr,
+                  nullptr};
+    if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
+    for (int i : {1, 3}) {
+      g = base_params(R, H, i == 1 ? H : F, err);
+      g.txt = txt;
+      g.img = img;
+      g.L = L;
+      g.gate = mod.rows + 2LL * H;
+      g.map = mod.map;
+      g.gate_stride = 3LL * H;
+      if ((rc = gemm_with_lora(lora, i, i == 1 ? b.o : b.a, i == 1 ? H : F, i == 1 ? w->wout : w->wdown, kEpiGated,
+                               g, down, err, st)) != DIT_OK)
+        return rc;
+    }
+    return DIT_OK;
+  }
   struct DequantCtx {
     const dit_dims* d;
     const dit_block_w8* w8;
@@ -566,7 +608,8 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
 int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w* wi, const dit_block_w8* w8t,
                      const dit_block_w8* w8i, const dit_block_w8a8* wqt, const dit_block_w8a8* wqi, float* txt, int L,
                      float* img, int N, const float* tc, const float* ts, const float* ic, const float* is,
-                     const ModRef& mod, void* ws, cudaStream_t st) {
+                     const ModRef& mod, void* ws, cudaStream_t st, const dit_lora* lora_t = nullptr,
+                     const dit_lora* lora_i = nullptr) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
@@ -646,8 +689,10 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     const dit_block_w* w;
     int r0, n;
     bool text;
+    const dit_lora* lora;  // adapters beside this stream's linears (per-stream launches), or null
   };
-  const Stream S[2] = {{wt, 0, L, true}, {wi, L, N, false}};
+  const Stream S[2] = {{wt, 0, L, true, lora_t}, {wi, L, N, false, lora_i}};
+  uint16_t* lora_down = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes);
   int rc;
   // the text stream's rows are txt[0, L) (all below L); the image stream's img[0, N) (L = 0 here)
   auto norm = [&](const Stream& s, const float* w, long long shift_row) {
@@ -668,7 +713,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     return g;
   };
 
-  if (L > 0 && N > 0) {
+  if (L > 0 && N > 0 && !lora_t && !lora_i) {
     // Every norm and linear runs once over all rows, the GEMMs taking the image weights from row L on
     // (m_split; when L is not on a row-tile boundary each stream's rows are padded to whole tiles, so
     // no tile mixes the streams) and the norms the image norm weights.
@@ -724,7 +769,9 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.row_off = s.r0;
     g.R_total = R;
     if ((rc = w8a8(0, b.h, H, g)) != DIT_OK) return rc;  // (one stream: it runs once)
-    if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wqkv, nullptr, kEpiQKV, g, st)) != DIT_OK) return rc;
+    if ((rc = gemm_with_lora(s.lora, 0, b.h + size_t(s.r0) * H, H, s.w->wqkv, kEpiQKV, g, lora_down, err, st)) !=
+        DIT_OK)
+      return rc;
   }
   if ((rc = after(0)) != DIT_OK) return rc;
   // 3. o = attention over all rows (q and k QK-normed with the weights of the streams that have rows)
@@ -739,7 +786,9 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if (s.n == 0) continue;
     GemmParams g = gated(s, H, 2);
     if ((rc = w8a8(1, b.o, H, g)) != DIT_OK) return rc;
-    if ((rc = gemm_launch(b.o + size_t(s.r0) * H, H, s.w->wout, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
+    if ((rc = gemm_with_lora(s.lora, 1, b.o + size_t(s.r0) * H, H, s.w->wout, kEpiGated, g, lora_down, err, st)) !=
+        DIT_OK)
+      return rc;
   }
   if ((rc = after(1)) != DIT_OK) return rc;
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m), per stream
@@ -753,7 +802,9 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     g.out = b.a + size_t(s.r0) * F;
     g.ldo = F;
     if ((rc = w8a8(2, b.h, H, g)) != DIT_OK) return rc;
-    if ((rc = gemm_launch(b.h + size_t(s.r0) * H, H, s.w->wup, nullptr, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
+    if ((rc = gemm_with_lora(s.lora, 2, b.h + size_t(s.r0) * H, H, s.w->wup, kEpiSwiGLU, g, lora_down, err, st)) !=
+        DIT_OK)
+      return rc;
   }
   if ((rc = after(2)) != DIT_OK) return rc;
   // 7. x += gate_m * (a Wdown^T), per stream
@@ -762,7 +813,9 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if (s.n == 0) continue;
     GemmParams g = gated(s, F, 5);
     if ((rc = w8a8(3, b.a, F, g)) != DIT_OK) return rc;
-    if ((rc = gemm_launch(b.a + size_t(s.r0) * F, F, s.w->wdown, nullptr, kEpiGated, g, st)) != DIT_OK) return rc;
+    if ((rc = gemm_with_lora(s.lora, 3, b.a + size_t(s.r0) * F, F, s.w->wdown, kEpiGated, g, lora_down, err, st)) !=
+        DIT_OK)
+      return rc;
   }
   return DIT_OK;
 }
@@ -1019,6 +1072,59 @@ int dit_block_forward_lora(const dit_dims* d, const dit_block_w* w, const dit_lo
   if (ws_bytes < dit_lora_workspace_bytes(d, L, N, lora->rank)) return DIT_EWORKSPACE;
   return run_block(d, w, nullptr, txt, L, img, N, tc, ts, ic, is, ModRef{mod->rows, mod->map, mod->M}, ws,
                    reinterpret_cast<cudaStream_t>(stream), lora);
+}
+
+namespace {
+// Pre-launch checks of a LoRA adapter set: rank within [8, 1024], a multiple of 8; each linear's two
+// factors both given or both absent, 16-byte aligned.
+int check_lora(const dit_lora* lora) {
+  if (!lora) return DIT_EINVAL;
+  if (lora->rank < 8 || lora->rank > 1024 || lora->rank % 8 != 0) return DIT_EUNSUPPORTED;
+  for (int i = 0; i < 4; ++i) {
+    if ((lora->A[i] == nullptr) != (lora->B[i] == nullptr)) return DIT_EINVAL;
+    if (lora->A[i] && (!al16(lora->A[i]) || !al16(lora->B[i]))) return DIT_EINVAL;
+  }
+  return DIT_OK;
+}
+}  // namespace
+
+int dit_parallel_block_forward_lora(const dit_dims* d, const dit_block_w* w, const dit_lora* lora, float* txt, int L,
+                                    float* img, int N, const float* tc, const float* ts, const float* ic,
+                                    const float* is, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                    dit_stream_t stream) {
+  if (!lora) return DIT_EINVAL;
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 2);
+  if (rc != DIT_OK) return rc;
+  if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+  if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  if ((rc = check_lora(lora)) != DIT_OK) return rc;
+  if (ws_bytes < dit_lora_workspace_bytes(d, L, N, lora->rank)) return DIT_EWORKSPACE;
+  return run_parallel_block(d, w, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
+                            ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream), lora);
+}
+
+int dit_double_block_forward_lora(const dit_dims* d, const dit_block_w* w_txt, const dit_lora* lora_txt,
+                                  const dit_block_w* w_img, const dit_lora* lora_img, float* txt, int L, float* img,
+                                  int N, const float* tc, const float* ts, const float* ic, const float* is,
+                                  const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 3);
+  if (rc != DIT_OK) return rc;
+  if (!lora_img && (L == 0 || !lora_txt)) return DIT_EINVAL;  // at least one adapter set
+  int rank = 0;
+  for (const dit_lora* lr : {L > 0 ? lora_txt : nullptr, lora_img}) {
+    if (!lr) continue;
+    if ((rc = check_lora(lr)) != DIT_OK) return rc;
+    rank = std::max(rank, lr->rank);
+  }
+  for (const dit_block_w* w : {w_txt, w_img}) {
+    if (w == w_txt && L == 0) continue;
+    if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+    if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  }
+  if (ws_bytes < dit_lora_workspace_bytes(d, L, N, rank)) return DIT_EWORKSPACE;
+  return run_double_block(d, w_txt, w_img, nullptr, nullptr, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
+                          ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream),
+                          L > 0 ? lora_txt : nullptr, lora_img);
 }
 
 int dit_block_forward_sandwich(const dit_dims* d, const dit_block_w* w, const float* post_attn, const float* post_mlp,

@@ -182,6 +182,26 @@ DIT_API int dit_block_forward_lora(const dit_dims* dims, const dit_block_w* w, c
                                    int L, float* img, int N, const float* txt_cos, const float* txt_sin,
                                    const float* img_cos, const float* img_sin, const dit_mod* mod, void* ws,
                                    size_t ws_bytes, dit_stream_t stream);
+
+/* The parallel and the double-stream blocks with LoRA adapters beside their linears [gizai:dit,
+ * Block.parallel; withLora, loraOf, weightAt; klein article, sections 4.3-4.4 (double blocks)]:
+ * each adapted linear runs as in dit_block_forward_lora (down = x A^T, then [x | down] [W | B]^T with
+ * its usual epilogue). The parallel block then runs its four linears one by one (its fused GEMMs take
+ * no per-part adapter factor), both output linears adding gate * (their product) to x; mod rows
+ * [M, 3, H] as dit_parallel_block_forward. The double-stream block runs per stream, the text rows'
+ * linears with lora_txt and the image rows' with lora_img (either may be NULL: no adapters on that
+ * stream, but not both; lora_txt is ignored when L = 0). Workspace: dit_lora_workspace_bytes(dims,
+ * L, N, rank) with the larger rank of the two sets. Otherwise as dit_parallel_block_forward and
+ * dit_double_block_forward. */
+DIT_API int dit_parallel_block_forward_lora(const dit_dims* dims, const dit_block_w* w, const dit_lora* lora,
+                                            float* txt, int L, float* img, int N, const float* txt_cos,
+                                            const float* txt_sin, const float* img_cos, const float* img_sin,
+                                            const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream);
+DIT_API int dit_double_block_forward_lora(const dit_dims* dims, const dit_block_w* w_txt, const dit_lora* lora_txt,
+                                          const dit_block_w* w_img, const dit_lora* lora_img, float* txt, int L,
+                                          float* img, int N, const float* txt_cos, const float* txt_sin,
+                                          const float* img_cos, const float* img_sin, const dit_mod* mod, void* ws,
+                                          size_t ws_bytes, dit_stream_t stream);
 DIT_API size_t dit_lora_workspace_bytes(const dit_dims* dims, int L, int N, int rank);
 
 /* The sandwich block [gizai:dit, POST_ATTN, POST_MLP]: dit_block_forward whose attention and MLP
