@@ -319,7 +319,7 @@ def modulated_layernorm(x, w, shift, scale, eps):
 
 def parallel_block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_dim,
                                 rows: Optional[np.ndarray] = None, norm=None, q_norm=None, k_norm=None,
-                                eps=1e-6, qk_eps=1e-6):
+                                eps=1e-6, qk_eps=1e-6, post_attn=None, post_mlp=None):
     """The parallel block over the packed rows x [R, H]: both branches read one modulated norm.
 
     1. h = modulated LayerNorm(x; norm, shift, scale)         mod rows [M, 3, H] = shift, scale, gate
@@ -329,6 +329,11 @@ def parallel_block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_
     5. x + gate * (o Wout^T + a Wdown^T)
 
     Steps 1-2 run for every row, 3-5 for ``rows`` (all by default).
+    With post_attn / post_mlp ([H] norm weights, a sandwich block) each branch's output is RMS-normed
+    with its own weight before the shared gate: x + gate * (rmsnorm(o Wout^T) post_attn +
+    rmsnorm(a Wdown^T) post_mlp). The pages name the post-norm weights of a block and norm its outputs
+    before their gates (gizai:dit, POST_ATTN / POST_MLP) without showing them in the parallel form;
+    this is the reading with one gate over both normed branches.
     [gizai:dit, Block.parallel; weightAt, prepOf and gluRows for the shared pieces]"""
     x = np.asarray(x, dtype=np.float64)
     R, H = x.shape
@@ -343,10 +348,11 @@ def parallel_block_forward_rows(x, weights, mod, mod_map, cos, sin, heads, head_
     v = qkv[:, 2 * H:3 * H].reshape(R, nh, d)
     o = attention(q, k, v, rows)
     a = swiglu_interleaved(h[rows] @ Wup.T)
-    return x[rows] + m[rows, 2] * (o @ Wout.T + a @ Wdown.T)
+    post = lambda y, w: y if w is None else modulated_rmsnorm(y, w, 0.0, 0.0, eps)
+    return x[rows] + m[rows, 2] * (post(o @ Wout.T, post_attn) + post(a @ Wdown.T, post_mlp))
 
 
-def parallel_block_forward(inp, weights=None, rows=None):
+def parallel_block_forward(inp, weights=None, rows=None, post_attn=None, post_mlp=None):
     """Parallel block on ``dit_inputs.parallel_block_inputs``: (txt_out, img_out) float64, or the
     packed output rows ``rows`` when given."""
     sh = inp.shape
@@ -355,7 +361,7 @@ def parallel_block_forward(inp, weights=None, rows=None):
     W = block_weights_f64(inp) if weights is None else weights
     y = parallel_block_forward_rows(x, W, inp.mod, inp.mod_map, cos, sin, sh.heads, sh.head_dim, rows=rows,
                                     norm=inp.norm1, q_norm=inp.q_norm, k_norm=inp.k_norm, eps=sh.eps,
-                                    qk_eps=sh.qk_eps)
+                                    qk_eps=sh.qk_eps, post_attn=post_attn, post_mlp=post_mlp)
     if rows is not None:
         return y
     return y[:sh.L], y[sh.L:]
@@ -367,18 +373,23 @@ def parallel_block_forward(inp, weights=None, rows=None):
 
 def double_block_forward_rows(x, weights_txt, weights_img, mod, mod_map, cos, sin, heads, head_dim, L,
                               rows: Optional[np.ndarray] = None, norms_txt=(None, None, None, None),
-                              norms_img=(None, None, None, None), eps=1e-6, qk_eps=1e-6):
+                              norms_img=(None, None, None, None), eps=1e-6, qk_eps=1e-6, post_txt=(None, None),
+                              post_img=(None, None)):
     """The double-stream block over the packed rows x [R, H] (text rows 0..L-1, image rows L..R-1):
     the sequential block of ``block_forward_rows`` in which each stream has its own four linears
     and its own norm weights (norm1, norm2, q_norm, k_norm), while the attention is one softmax over
     the concatenated text and image keys. Modulation rows come through ``mod_map`` as for the
-    sequential block, so each stream's rows pick their own rows of ``mod`` [M, 6, H]."""
+    sequential block, so each stream's rows pick their own rows of ``mod`` [M, 6, H]. post_txt /
+    post_img are each stream's sandwich post-norm weights (post_attn, post_mlp; None: that branch
+    un-normed), as in ``block_forward_rows``."""
     x = np.asarray(x, dtype=np.float64)
     R, H = x.shape
     nh, d = heads, head_dim
     rows = np.arange(R) if rows is None else np.asarray(rows)
     m = np.asarray(mod, dtype=np.float64)[np.asarray(mod_map)]
     streams = [(np.arange(0, L), weights_txt, norms_txt), (np.arange(L, R), weights_img, norms_img)]
+    posts = [post_txt, post_img]
+    post = lambda y, w: y if w is None else modulated_rmsnorm(y, w, 0.0, 0.0, eps)
     q = np.empty((R, nh, d))
     k = np.empty((R, nh, d))
     v = np.empty((R, nh, d))
@@ -392,14 +403,14 @@ def double_block_forward_rows(x, weights_txt, weights_img, mod, mod_map, cos, si
         v[idx] = qkv[:, 2 * H:3 * H].reshape(-1, nh, d)
     o = attention(q, k, v, rows)
     out = np.empty((rows.size, H))
-    for idx, W, nrm in streams:
+    for (idx, W, nrm), pw in zip(streams, posts):
         sel = np.isin(rows, idx)
         if not sel.any():
             continue
         r = rows[sel]
-        xr = x[r] + m[r, 2] * (o[sel] @ W[1].T)
+        xr = x[r] + m[r, 2] * post(o[sel] @ W[1].T, pw[0])
         h2 = modulated_rmsnorm(xr, nrm[1], m[r, 3], m[r, 4], eps)
-        out[sel] = xr + m[r, 5] * (swiglu_interleaved(h2 @ W[2].T) @ W[3].T)
+        out[sel] = xr + m[r, 5] * post(swiglu_interleaved(h2 @ W[2].T) @ W[3].T, pw[1])
     return out
 
 

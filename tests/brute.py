@@ -97,11 +97,23 @@ def layernorm_row(x, eps):
 
 
 def parallel_block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, eps, qk_eps,
-                   norm=None, qn=None, kn=None, linear=None, linear2=None):
+                   norm=None, qn=None, kn=None, linear=None, linear2=None, post_attn=None, post_mlp=None):
     """The parallel block: x + gate * (attention + SwiGLU MLP), both branches reading one modulated
     LayerNorm. mod_rows[r] = 3 lists of H (shift, scale, gate) for row r. Returns new rows.
     linear(W, row) replaces the products of Wq, Wk, Wv, Wg and Wu when given; linear2(o, a) replaces
-    the sum of the two output products Wo o + Wd a (one linear over the joined input [o | a])."""
+    the sum of the two output products Wo o + Wd a (one linear over the joined input [o | a]).
+    post_attn / post_mlp: each branch's output RMS-normed times its weight before the shared gate."""
+    if post_attn is not None or post_mlp is not None:
+        assert linear2 is None, "post norms need the two output products apart"
+
+        def joint(o, a):
+            att, mlp = matvec(Wo, o), matvec(Wd, a)
+            if post_attn is not None:
+                att = [v * w for v, w in zip(rmsnorm_row(att, eps), post_attn)]
+            if post_mlp is not None:
+                mlp = [v * w for v, w in zip(rmsnorm_row(mlp, eps), post_mlp)]
+            return [u + v for u, v in zip(att, mlp)]
+        linear2 = joint
     matvec_ = linear or matvec
     joint = linear2 or (lambda o, a: [u + v for u, v in zip(matvec(Wo, o), matvec(Wd, a))])
     R, H = len(x), len(x[0])
@@ -151,11 +163,16 @@ def parallel_block(x, Wq, Wk, Wv, Wo, Wg, Wu, Wd, mod_rows, cos, sin, heads, d, 
 
 
 def double_block(x, L, Wt, Wi, mod_rows, cos, sin, heads, d, eps, qk_eps, norms_t=None, norms_i=None,
-                 linear=None):
+                 linear=None, post_t=None, post_i=None):
     """The sequential block with per-stream weights: rows r < L use Wt = (Wq, Wk, Wv, Wo, Wg, Wu, Wd)
     and norms_t = (norm1, norm2, qn, kn), the others Wi / norms_i; one attention over all rows.
-    linear(W, row) replaces the plain W row products when given (one call per weight matrix)."""
+    linear(W, row) replaces the plain W row products when given (one call per weight matrix).
+    post_t / post_i: each stream's (post_attn, post_mlp) sandwich weights (None: un-normed)."""
     matvec = linear or globals()["matvec"]
+    posts = (post_t or (None, None), post_i or (None, None))
+
+    def post(y, w):
+        return y if w is None else [v * c for v, c in zip(rmsnorm_row(y, eps), w)]
     R, H = len(x), len(x[0])
     one = lambda n: [1.0] * n
     nt = norms_t or (None, None, None, None)
@@ -200,11 +217,12 @@ def double_block(x, L, Wt, Wi, mod_rows, cos, sin, heads, d, eps, qk_eps, norms_
             z = sum(e)
             for j in range(d):
                 o.append(sum(e[c] / z * V[c][n][j] for c in range(R)))
-        att = matvec(W[3], o)
+        pw = posts[0] if r < L else posts[1]
+        att = post(matvec(W[3], o), pw[0])
         xr = [x[r][i] + mod_rows[r][2][i] * att[i] for i in range(H)]
         h2 = modnorm(xr, nr[1], mod_rows[r][3], mod_rows[r][4])
         g, u = matvec(W[4], h2), matvec(W[5], h2)
         a = [g[j] / (1.0 + math.exp(-g[j])) * u[j] for j in range(len(g))]
-        mlp = matvec(W[6], a)
+        mlp = post(matvec(W[6], a), pw[1])
         out.append([xr[i] + mod_rows[r][5][i] * mlp[i] for i in range(H)])
     return out
