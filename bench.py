@@ -613,6 +613,28 @@ def run_ours(args):
         swb = {"workload": "1024sq sandwich block: attention and MLP outputs RMS-normed before their gates",
                "ms_per_block": msW, "tflops": tfW, "frac_of_peak": tfW / peaks["bf16_tflops"], "flop_per_block": flops,
                "launches_per_block": 9}
+        # the parallel and double-stream sandwich blocks (double: the same post weights on both streams)
+        if not args.no_parallel:
+            inpP = DI.parallel_block_inputs(WORKLOAD)
+            modP = D.Modulation(_dev(torch, inpP.mod), _dev(torch, inpP.mod_map))
+            del inpP
+            callWP = lambda t, i: D.dit_parallel_block_forward_sandwich(st["dims"], st["w"], pa, pm, t, i, st["tc"],
+                                                                        st["ts"], st["ic"], st["is_"], modP, st["ws"])
+            msWP = _time_blocks(torch, st, callWP, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            swb["parallel_block"] = {"ms_per_block": msWP, "tflops": flops / (msWP * 1e-3) / 1e12,
+                                     "frac_of_peak": flops / (msWP * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                     "launches_per_block": 6}
+            del modP
+        if not args.no_double:
+            callWD = lambda t, i: D.dit_double_block_forward_sandwich(st["dims"], st["w"], (pa, pm), st["w"], (pa, pm),
+                                                                      t, i, st["tc"], st["ts"], st["ic"], st["is_"],
+                                                                      st["mod"], st["ws"])
+            msWD = _time_blocks(torch, st, callWD, args.steps, args.warmup, dist) / args.steps
+            D.dit_check()
+            swb["double_stream_block"] = {"ms_per_block": msWD, "tflops": flops / (msWD * 1e-3) / 1e12,
+                                          "frac_of_peak": flops / (msWD * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                          "launches_per_block": 9}
         del pa, pm
 
     # the W8A8 block (opt-in lossy tier): the block's bf16 weights quantised per output channel

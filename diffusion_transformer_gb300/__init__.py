@@ -21,7 +21,8 @@ __all__ = [
     "ParallelW8A8Weights", "dit_parallel_block_forward_w8a8", "dit_double_block_forward_w8a8",
     "dit_linear_w8a8", "dit_linear_w8a8_workspace_bytes",
     "dit_double_block_forward", "dit_block_forward_lora", "dit_lora_workspace_bytes", "LoRA", "dit_lora_merge",
-    "dit_parallel_block_forward_lora", "dit_double_block_forward_lora",
+    "dit_parallel_block_forward_lora", "dit_double_block_forward_lora", "dit_parallel_block_forward_sandwich",
+    "dit_double_block_forward_sandwich",
     "dit_block_forward_sandwich", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
@@ -94,6 +95,13 @@ _SIGNATURES = {
                                        c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod),
                                        c_void_p, c_size_t, c_void_p]),
     "dit_lora_workspace_bytes": (c_size_t, [POINTER(dit_dims), c_int, c_int, c_int]),
+    "dit_parallel_block_forward_sandwich": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_void_p,
+                                                    c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
+                                                    c_void_p, POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
+    "dit_double_block_forward_sandwich": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), c_void_p, c_void_p,
+                                                  POINTER(dit_block_w), c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+                                                  c_int, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(dit_mod),
+                                                  c_void_p, c_size_t, c_void_p]),
     "dit_parallel_block_forward_lora": (c_int, [POINTER(dit_dims), POINTER(dit_block_w), POINTER(dit_lora), c_void_p,
                                                 c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                                                 POINTER(dit_mod), c_void_p, c_size_t, c_void_p]),
@@ -404,6 +412,40 @@ def dit_double_block_forward_lora(dims: DitDims, w_txt: Optional[BlockWeights], 
                                             _ptr(img_sin, f32), ctypes.byref(mod.c), _ptr(ws, None, "ws"),
                                             ws.numel() * ws.element_size(), _stream(stream)),
         "dit_double_block_forward_lora")
+
+
+def dit_parallel_block_forward_sandwich(dims: DitDims, w: BlockWeights, post_attn, post_mlp, txt, img, txt_cos,
+                                        txt_sin, img_cos, img_sin, mod: Modulation, ws, stream=None):
+    """The parallel sandwich block; post_attn / post_mlp [H] fp32 (None: that branch un-normed)."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    _ok(lib().dit_parallel_block_forward_sandwich(ctypes.byref(dims.c), ctypes.byref(w.c), _ptr(post_attn, f32),
+                                                  _ptr(post_mlp, f32), _ptr(txt, f32, "txt"), L, _ptr(img, f32, "img"),
+                                                  img.shape[0], _ptr(txt_cos, f32), _ptr(txt_sin, f32),
+                                                  _ptr(img_cos, f32), _ptr(img_sin, f32), ctypes.byref(mod.c),
+                                                  _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                                  _stream(stream)),
+        "dit_parallel_block_forward_sandwich")
+
+
+def dit_double_block_forward_sandwich(dims: DitDims, w_txt: Optional[BlockWeights], post_txt, w_img: BlockWeights,
+                                      post_img, txt, img, txt_cos, txt_sin, img_cos, img_sin, mod: Modulation, ws,
+                                      stream=None):
+    """The double-stream sandwich block; post_txt / post_img = (post_attn, post_mlp) [H] fp32 or None each."""
+    import torch
+    f32 = torch.float32
+    L = 0 if txt is None else txt.shape[0]
+    pt = post_txt if post_txt is not None else (None, None)
+    pi = post_img if post_img is not None else (None, None)
+    _ok(lib().dit_double_block_forward_sandwich(ctypes.byref(dims.c), None if w_txt is None else ctypes.byref(w_txt.c),
+                                                _ptr(pt[0], f32), _ptr(pt[1], f32), ctypes.byref(w_img.c),
+                                                _ptr(pi[0], f32), _ptr(pi[1], f32), _ptr(txt, f32, "txt"), L,
+                                                _ptr(img, f32, "img"), img.shape[0], _ptr(txt_cos, f32),
+                                                _ptr(txt_sin, f32), _ptr(img_cos, f32), _ptr(img_sin, f32),
+                                                ctypes.byref(mod.c), _ptr(ws, None, "ws"),
+                                                ws.numel() * ws.element_size(), _stream(stream)),
+        "dit_double_block_forward_sandwich")
 
 
 def dit_block_forward_sandwich(dims: DitDims, w: BlockWeights, post_attn, post_mlp, txt, img, txt_cos, txt_sin,

@@ -288,7 +288,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
     gy.ldo = H;
     int rc = linear(i, x, K, W, w8b, kEpiStoreF32, gy);
     if (rc != DIT_OK) return rc;
-    SandwichParams sp{txt, img, L, R, H, y, mod.rows + gate_row * H, 6LL * H, mod.map, post, d->eps};
+    SandwichParams sp{txt, img, L, R, H, y, mod.rows + gate_row * H, 6LL * H, mod.map, post, d->eps, 1, 1, post};
     return sandwich_launch(sp, st);
   };
   // int8lin scratch after the block workspace: two slots of dequantised weights
@@ -466,7 +466,8 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
 // row count; the GEMMs are then the bf16 ones on the slots.
 int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, const dit_parallel_w8a8* wq,
                        float* txt, int L, float* img, int N, const float* tc, const float* ts, const float* ic,
-                       const float* is, const ModRef& mod, void* ws, cudaStream_t st, const dit_lora* lora = nullptr) {
+                       const float* is, const ModRef& mod, void* ws, cudaStream_t st, const dit_lora* lora = nullptr,
+                       const float* post_attn = nullptr, const float* post_mlp = nullptr) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
@@ -572,7 +573,24 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
   // W8A8: codes of the joined rows [o | a] in place, one scale per row
   if (wq && (rc = quant_rows_joint_launch(b.o, H, b.a, F, R, wq->smooth2, nullptr, R, sa2, st)) != DIT_OK) return rc;
 
-  // 4. x += gate * ([o | a] [Wout | Wdown]^T)
+  // 4. x += gate * ([o | a] [Wout | Wdown]^T); with post-norm weights (a sandwich block) each output
+  // product is stored in fp32 (o Wout^T over h and q, a Wdown^T over k and vt, consumed by now) and
+  // the sandwich kernel adds gate * (rmsnorm(y1) post_attn + rmsnorm(y2) post_mlp) to x
+  if (post_attn || post_mlp) {
+    float* y1 = reinterpret_cast<float*>(b.h);
+    float* y2 = reinterpret_cast<float*>(b.k);
+    for (int i : {1, 3}) {
+      g = base_params(R, H, i == 1 ? H : F, err);
+      g.out = i == 1 ? y1 : y2;
+      g.ldo = H;
+      if ((rc = gemm_launch(i == 1 ? b.o : b.a, i == 1 ? H : F, i == 1 ? wout : wdown, nullptr, kEpiStoreF32, g, st)) !=
+          DIT_OK)
+        return rc;
+    }
+    SandwichParams sp{txt, img, L, R, H, y1, mod.rows + 2LL * H, 3LL * H, mod.map, post_attn, d->eps,
+                      post_attn != nullptr, post_attn != nullptr, post_attn, y2, post_mlp, post_mlp != nullptr};
+    return sandwich_launch(sp, st);
+  }
   g = base_params(R, H, H + F, err);
   g.txt = txt;
   g.img = img;
@@ -609,7 +627,8 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
                      const dit_block_w8* w8i, const dit_block_w8a8* wqt, const dit_block_w8a8* wqi, float* txt, int L,
                      float* img, int N, const float* tc, const float* ts, const float* ic, const float* is,
                      const ModRef& mod, void* ws, cudaStream_t st, const dit_lora* lora_t = nullptr,
-                     const dit_lora* lora_i = nullptr) {
+                     const dit_lora* lora_i = nullptr, const float* const* post_t = nullptr,
+                     const float* const* post_i = nullptr) {
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   const int R = L + N, H = d->hidden, F = d->ffn;
@@ -693,6 +712,20 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   };
   const Stream S[2] = {{wt, 0, L, true, lora_t}, {wi, L, N, false, lora_i}};
   uint16_t* lora_down = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + b.bytes);
+  // Sandwich post-norms per stream: post_t / post_i = {attention, MLP} weights of the text / image
+  // stream (null entries: that stream's branch un-normed). A branch with a post weight on either
+  // stream stores its linear's output in fp32 over h and q (consumed by then), then the sandwich
+  // kernel adds gate * f(y) to x, f normalising the rows of the streams that have a weight.
+  auto post_of = [&](const float* const* pw, int br) -> const float* { return pw ? pw[br] : nullptr; };
+  auto has_post = [&](int br) { return (L > 0 && post_of(post_t, br)) || post_of(post_i, br); };
+  float* ybuf = reinterpret_cast<float*>(b.h);
+  auto sandwich = [&](int br, long long gate_row) {
+    const float* wtx = L > 0 ? post_of(post_t, br) : nullptr;
+    const float* wim = post_of(post_i, br);
+    SandwichParams sp{txt, img, L, R, H, ybuf, mod.rows + gate_row * H, 6LL * H, mod.map, wtx, d->eps,
+                      wtx != nullptr, wim != nullptr, wim};
+    return sandwich_launch(sp, st);
+  };
   int rc;
   // the text stream's rows are txt[0, L) (all below L); the image stream's img[0, N) (L = 0 here)
   auto norm = [&](const Stream& s, const float* w, long long shift_row) {
@@ -737,11 +770,19 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
                   wi->q_norm, wi->k_norm};
     if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, H, 2);
+    if (has_post(0)) {
+      g = base_params(R, H, H, err);
+      g.out = ybuf;
+      g.ldo = H;
+    }
     g.m_split = L;
     if ((rc = w8a8(1, b.o, H, g)) != DIT_OK) return rc;
     if ((rc = before(1)) != DIT_OK) return rc;
-    if ((rc = gemm_launch_cat(b.o, H, nullptr, 0, wt->wout, H, wi->wout, H, kEpiGated, g, st)) != DIT_OK) return rc;
+    if ((rc = gemm_launch_cat(b.o, H, nullptr, 0, wt->wout, H, wi->wout, H, has_post(0) ? kEpiStoreF32 : kEpiGated, g,
+                              st)) != DIT_OK)
+      return rc;
     if ((rc = after(1)) != DIT_OK) return rc;
+    if (has_post(0) && (rc = sandwich(0, 2)) != DIT_OK) return rc;
     if ((rc = norm_all(wt->norm2, wi->norm2, 3)) != DIT_OK) return rc;
     g = base_params(R, 2 * F, H, err);
     g.out = b.a;
@@ -752,10 +793,18 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if ((rc = gemm_launch_cat(b.h, H, nullptr, 0, wt->wup, H, wi->wup, H, kEpiSwiGLU, g, st)) != DIT_OK) return rc;
     if ((rc = after(2)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, F, 5);
+    if (has_post(1)) {
+      g = base_params(R, H, F, err);
+      g.out = ybuf;
+      g.ldo = H;
+    }
     g.m_split = L;
     if ((rc = w8a8(3, b.a, F, g)) != DIT_OK) return rc;
     if ((rc = before(3)) != DIT_OK) return rc;
-    return gemm_launch_cat(b.a, F, nullptr, 0, wt->wdown, F, wi->wdown, F, kEpiGated, g, st);
+    if ((rc = gemm_launch_cat(b.a, F, nullptr, 0, wt->wdown, F, wi->wdown, F, has_post(1) ? kEpiStoreF32 : kEpiGated,
+                              g, st)) != DIT_OK)
+      return rc;
+    return has_post(1) ? sandwich(1, 5) : DIT_OK;
   }
 
   // 1. h = modnorm(x; norm1, shift_a, scale_a), per stream
@@ -785,12 +834,18 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, H, 2);
+    if (has_post(0)) {
+      g = base_params(s.n, H, H, err);
+      g.out = ybuf + size_t(s.r0) * H;
+      g.ldo = H;
+    }
     if ((rc = w8a8(1, b.o, H, g)) != DIT_OK) return rc;
-    if ((rc = gemm_with_lora(s.lora, 1, b.o + size_t(s.r0) * H, H, s.w->wout, kEpiGated, g, lora_down, err, st)) !=
-        DIT_OK)
+    if ((rc = gemm_with_lora(s.lora, 1, b.o + size_t(s.r0) * H, H, s.w->wout, has_post(0) ? kEpiStoreF32 : kEpiGated,
+                             g, lora_down, err, st)) != DIT_OK)
       return rc;
   }
   if ((rc = after(1)) != DIT_OK) return rc;
+  if (has_post(0) && (rc = sandwich(0, 2)) != DIT_OK) return rc;
   // 5. h2 = modnorm(x; norm2, shift_m, scale_m), per stream
   for (const Stream& s : S)
     if (s.n > 0 && (rc = norm(s, s.w->norm2, 3)) != DIT_OK) return rc;
@@ -812,12 +867,17 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   for (const Stream& s : S) {
     if (s.n == 0) continue;
     GemmParams g = gated(s, F, 5);
+    if (has_post(1)) {
+      g = base_params(s.n, H, F, err);
+      g.out = ybuf + size_t(s.r0) * H;
+      g.ldo = H;
+    }
     if ((rc = w8a8(3, b.a, F, g)) != DIT_OK) return rc;
-    if ((rc = gemm_with_lora(s.lora, 3, b.a + size_t(s.r0) * F, F, s.w->wdown, kEpiGated, g, lora_down, err, st)) !=
-        DIT_OK)
+    if ((rc = gemm_with_lora(s.lora, 3, b.a + size_t(s.r0) * F, F, s.w->wdown, has_post(1) ? kEpiStoreF32 : kEpiGated,
+                             g, lora_down, err, st)) != DIT_OK)
       return rc;
   }
-  return DIT_OK;
+  return has_post(1) ? sandwich(1, 5) : DIT_OK;
 }
 
 int check_block_args(const dit_dims* d, const float* txt, int L, const float* img, int N, const float* tc,
@@ -1125,6 +1185,41 @@ int dit_double_block_forward_lora(const dit_dims* d, const dit_block_w* w_txt, c
   return run_double_block(d, w_txt, w_img, nullptr, nullptr, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
                           ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream),
                           L > 0 ? lora_txt : nullptr, lora_img);
+}
+
+int dit_parallel_block_forward_sandwich(const dit_dims* d, const dit_block_w* w, const float* post_attn,
+                                        const float* post_mlp, float* txt, int L, float* img, int N, const float* tc,
+                                        const float* ts, const float* ic, const float* is, const dit_mod* mod,
+                                        void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 2);
+  if (rc != DIT_OK) return rc;
+  if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+  if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  if ((post_attn && !al16(post_attn)) || (post_mlp && !al16(post_mlp))) return DIT_EINVAL;
+  return run_parallel_block(d, w, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
+                            ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                            post_attn, post_mlp);
+}
+
+int dit_double_block_forward_sandwich(const dit_dims* d, const dit_block_w* w_txt, const float* post_attn_txt,
+                                      const float* post_mlp_txt, const dit_block_w* w_img, const float* post_attn_img,
+                                      const float* post_mlp_img, float* txt, int L, float* img, int N,
+                                      const float* tc, const float* ts, const float* ic, const float* is,
+                                      const dit_mod* mod, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  int rc = check_block_args(d, txt, L, img, N, tc, ts, ic, is, mod, ws, ws_bytes, 3);
+  if (rc != DIT_OK) return rc;
+  for (const dit_block_w* w : {w_txt, w_img}) {
+    if (w == w_txt && L == 0) continue;
+    if (!w || !w->wqkv || !w->wout || !w->wup || !w->wdown) return DIT_EINVAL;
+    if (!al16(w->wqkv) || !al16(w->wout) || !al16(w->wup) || !al16(w->wdown)) return DIT_EINVAL;
+  }
+  for (const float* p : {post_attn_txt, post_mlp_txt, post_attn_img, post_mlp_img})
+    if (p && !al16(p)) return DIT_EINVAL;
+  const float* pt[2] = {post_attn_txt, post_mlp_txt};
+  const float* pi[2] = {post_attn_img, post_mlp_img};
+  return run_double_block(d, w_txt, w_img, nullptr, nullptr, nullptr, nullptr, txt, L, img, N, tc, ts, ic, is,
+                          ModRef{mod->rows, mod->map, mod->M}, ws, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                          nullptr, pt, pi);
 }
 
 int dit_block_forward_sandwich(const dit_dims* d, const dit_block_w* w, const float* post_attn, const float* post_mlp,

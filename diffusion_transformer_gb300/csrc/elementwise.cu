@@ -253,59 +253,84 @@ __global__ void dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __r
   }
 }
 
-// Sandwich residual (a branch normed before its gate): one CTA per row, H/1024 float4 chunks per
-// thread loaded before the reduction, then x += gate * y * rstd * w.
+// Sandwich residual (branch outputs normed before their gate): one CTA per row, H/1024 float4
+// chunks per thread of y (and y2) loaded before the reductions, then
+// x += gate * (y * rstd * w + y2 * rstd2 * w2) with rstd = 1 and w = 1 for an un-normed branch.
 template <int NC>
 __global__ void __launch_bounds__(kNormThreads) sandwich_kernel(const SandwichParams p) {
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.x;
-  float* x = r < p.L ? p.txt + size_t(r) * p.H : p.img + size_t(r - p.L) * p.H;
+  const bool text = r < p.L;
+  float* x = text ? p.txt + size_t(r) * p.H : p.img + size_t(r - p.L) * p.H;
   const int m = p.map ? __ldg(p.map + r) : 0;
+  const bool n1 = text ? p.norm_txt != 0 : p.norm_img != 0;  // the same for the whole CTA
+  const bool two = p.y2 != nullptr;
+  const bool n2 = two && p.norm2 != 0;
   const float4* y4 = reinterpret_cast<const float4*>(p.y + size_t(r) * p.H);
+  const float4* z4 = two ? reinterpret_cast<const float4*>(p.y2 + size_t(r) * p.H) : nullptr;
   const float4* g4 = reinterpret_cast<const float4*>(p.gate + size_t(m) * p.mod_stride);
-  const float4* w4 = reinterpret_cast<const float4*>(p.w);
+  const float4* w4 = n1 ? reinterpret_cast<const float4*>(text ? p.w : p.w_img) : nullptr;
+  const float4* w24 = n2 ? reinterpret_cast<const float4*>(p.w2) : nullptr;
   float4* x4 = reinterpret_cast<float4*>(x);
   __shared__ float part[kNormThreads / 32];
   const int n4 = p.H >> 2;
   constexpr int K = NC > 0 ? NC : 1;
-  float4 yv[K];
-  float ss = 0.f;
+  float4 yv[K], zv[K];
+  float ss = 0.f, ss2 = 0.f;
+  auto acc = [](float s, float4 v) {
+    s = fmaf(v.x, v.x, s);
+    s = fmaf(v.y, v.y, s);
+    s = fmaf(v.z, v.z, s);
+    return fmaf(v.w, v.w, s);
+  };
   if constexpr (NC > 0) {
 #pragma unroll
-    for (int k = 0; k < NC; ++k) yv[k] = y4[threadIdx.x + k * kNormThreads];
+    for (int k = 0; k < NC; ++k) {
+      yv[k] = y4[threadIdx.x + k * kNormThreads];
+      if (two) zv[k] = z4[threadIdx.x + k * kNormThreads];
+    }
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
-      ss = fmaf(yv[k].x, yv[k].x, ss);
-      ss = fmaf(yv[k].y, yv[k].y, ss);
-      ss = fmaf(yv[k].z, yv[k].z, ss);
-      ss = fmaf(yv[k].w, yv[k].w, ss);
+      ss = acc(ss, yv[k]);
+      if (two) ss2 = acc(ss2, zv[k]);
     }
   } else {
     for (int i = threadIdx.x; i < n4; i += kNormThreads) {
-      const float4 v = y4[i];
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
+      ss = acc(ss, y4[i]);
+      if (two) ss2 = acc(ss2, z4[i]);
     }
   }
-  const float rstd = rsqrtf(block_sum(ss, part) / float(p.H) + p.eps);
-  auto apply = [&](int i, float4 v) {
+  const float rstd = n1 ? rsqrtf(block_sum(ss, part) / float(p.H) + p.eps) : 1.f;
+  const float rstd2 = n2 ? rsqrtf(block_sum(ss2, part) / float(p.H) + p.eps) : 1.f;
+  const float4 ones = make_float4(1.f, 1.f, 1.f, 1.f);
+  auto apply = [&](int i, float4 v, float4 u) {
     const float4 g = __ldg(g4 + i);
-    const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
+    const float4 w = w4 ? __ldg(w4 + i) : ones;
+    float4 b;  // the gated branches' sum before the gate
+    b.x = v.x * rstd * w.x;
+    b.y = v.y * rstd * w.y;
+    b.z = v.z * rstd * w.z;
+    b.w = v.w * rstd * w.w;
+    if (two) {
+      const float4 w2 = w24 ? __ldg(w24 + i) : ones;
+      b.x += u.x * rstd2 * w2.x;
+      b.y += u.y * rstd2 * w2.y;
+      b.z += u.z * rstd2 * w2.z;
+      b.w += u.w * rstd2 * w2.w;
+    }
     float4 xv = x4[i];
-    xv.x = fmaf(g.x, v.x * rstd * w.x, xv.x);
-    xv.y = fmaf(g.y, v.y * rstd * w.y, xv.y);
-    xv.z = fmaf(g.z, v.z * rstd * w.z, xv.z);
-    xv.w = fmaf(g.w, v.w * rstd * w.w, xv.w);
+    xv.x = fmaf(g.x, b.x, xv.x);
+    xv.y = fmaf(g.y, b.y, xv.y);
+    xv.z = fmaf(g.z, b.z, xv.z);
+    xv.w = fmaf(g.w, b.w, xv.w);
     x4[i] = xv;
   };
   if constexpr (NC > 0) {
 #pragma unroll
-    for (int k = 0; k < NC; ++k) apply(threadIdx.x + k * kNormThreads, yv[k]);
+    for (int k = 0; k < NC; ++k) apply(threadIdx.x + k * kNormThreads, yv[k], two ? zv[k] : ones);
   } else {
-    for (int i = threadIdx.x; i < n4; i += kNormThreads) apply(i, y4[i]);
+    for (int i = threadIdx.x; i < n4; i += kNormThreads) apply(i, y4[i], two ? z4[i] : ones);
   }
 }
 

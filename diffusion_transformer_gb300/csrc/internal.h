@@ -144,8 +144,11 @@ struct ModNormParams {
 };
 int modnorm_launch(const ModNormParams& p, cudaStream_t stream);
 
-// Sandwich residual: x[r] += gate[map[r]] * y[r] * rsqrt(mean(y[r]^2) + eps) * w, y [R, H] fp32 (the
-// branch's linear output), x rows < L in txt, others in img (row stride H).
+// Sandwich residual: x[r] += gate[map[r]] * (f(y[r]) + f2(y2[r])), y [R, H] fp32 (a branch's linear
+// output), f(y) = y * rsqrt(mean(y^2) + eps) * w for a normed row, y for an un-normed one; x rows < L
+// in txt, others in img (row stride H). Text rows take (norm_txt, w), image rows (norm_img, w_img)
+// (the double-stream block's per-stream post weights); the optional second branch y2 (the parallel
+// block's MLP output under the same gate) is normed when norm2, with weight w2.
 struct SandwichParams {
   float* txt;
   float* img;
@@ -154,8 +157,13 @@ struct SandwichParams {
   const float* gate;       // row m at gate + m * mod_stride
   long long mod_stride;
   const int32_t* map;      // [R] or null
-  const float* w;          // [H] post-norm weight or null (ones)
+  const float* w;          // [H] post-norm weight of the text rows or null (ones)
   float eps;
+  int norm_txt, norm_img;  // text / image rows of y normed (1) or added as they are (0)
+  const float* w_img;      // [H] post-norm weight of the image rows or null (ones)
+  const float* y2;         // [R, H] second branch or null
+  const float* w2;         // its post-norm weight or null (ones)
+  int norm2;
 };
 int sandwich_launch(const SandwichParams& p, cudaStream_t stream);
 // bounded-wait diagnostic (see dit_selftest_bounded_wait)

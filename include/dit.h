@@ -216,6 +216,28 @@ DIT_API int dit_block_forward_sandwich(const dit_dims* dims, const dit_block_w* 
                                        const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
                                        dit_stream_t stream);
 
+/* The parallel and the double-stream sandwich blocks [gizai:dit, POST_ATTN, POST_MLP; Block.parallel;
+ * klein article, sections 4.3-4.4]: branch outputs RMS-normed (the block's eps) times their post
+ * weights ([H] fp32) before their gates. Parallel: x += gate * (rmsnorm(o Wout^T) post_attn +
+ * rmsnorm(a Wdown^T) post_mlp), the one gate over both normed branches (a NULL weight leaves that
+ * branch un-normed); the two output products are stored in fp32 and a row kernel applies the norms,
+ * gate and residual. Double-stream: each stream's branches normed with that stream's weights
+ * (post_*_txt for the text rows, post_*_img for the image rows; NULL: that stream's branch
+ * un-normed). Workspace and other arguments as dit_parallel_block_forward / dit_double_block_forward
+ * (variants 2 / 3). */
+DIT_API int dit_parallel_block_forward_sandwich(const dit_dims* dims, const dit_block_w* w, const float* post_attn,
+                                                const float* post_mlp, float* txt, int L, float* img, int N,
+                                                const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                                const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                                dit_stream_t stream);
+DIT_API int dit_double_block_forward_sandwich(const dit_dims* dims, const dit_block_w* w_txt,
+                                              const float* post_attn_txt, const float* post_mlp_txt,
+                                              const dit_block_w* w_img, const float* post_attn_img,
+                                              const float* post_mlp_img, float* txt, int L, float* img, int N,
+                                              const float* txt_cos, const float* txt_sin, const float* img_cos,
+                                              const float* img_sin, const dit_mod* mod, void* ws, size_t ws_bytes,
+                                              dit_stream_t stream);
+
 /* The same block with int8lin weights [host contract, section 1]: W = bf16_rne(q * s), then the
  * bf16 MMA. With at most 512 rows the GEMM's converter warps dequantize each weight k-block inside
  * the mainloop; with more rows (many M tiles per weight tile) each linear's weight is dequantized
