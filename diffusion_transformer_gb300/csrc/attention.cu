@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
       mbar_init(smem_u32(&k_empty[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
       mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&p_full[s]), fixed ? 128 * AttnSplit<D, MODE>::kParts : 128);  // softmax threads per tile
+      // one arrival per softmax warp of the tile (each after its lanes' TMEM stores, fence and warp sync)
+      mbar_init(smem_u32(&p_full[s]), fixed ? 4 * AttnSplit<D, MODE>::kParts : 4);
       mbar_init(smem_u32(&o_done[s]), 1);
     }
     mbar_init(smem_u32(drain), 1);
@@ -201,30 +202,33 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128);
       constexpr uint32_t idesc_o = idesc_bf16(128, D);
       bool ok = mbar_wait(smem_u32(q_full), 0, p.err, kErrTimeoutMma);
+      // descriptor low words of the three 1024-byte-aligned operand regions; tiles inside them add
+      // their byte offset >> 4 (umma_bf16_lo), so each MMA costs two 32-bit adds besides itself
+      const uint64_t dq = sw128_desc(smem_u32(sQ));
+      const uint32_t q_lo = uint32_t(dq), d_hi = uint32_t(dq >> 32);
+      const uint32_t k_lo = uint32_t(sw128_desc(smem_u32(sK))), v_lo = uint32_t(sw128_desc(smem_u32(sV)));
       auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T into columns [128 t, 128 t + 128)
-        const int s = j & 1;
         const uint32_t dS = tmem_base + uint32_t(t * 128);
+        const uint32_t qt = q_lo + uint32_t(t * (Cfg::kQBytes >> 4));
+        const uint32_t ks = k_lo + uint32_t((j & 1) * (Cfg::kKBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t a = kk >> 2, off = uint32_t(2 * (kk & 3));
-          const uint64_t ad = sw128_desc(smem_u32(sQ + t * Cfg::kQBytes + a * Cfg::kAtom)) + off;
-          const uint64_t bd = sw128_desc(smem_u32(sK + s * Cfg::kKBytes + a * Cfg::kAtom)) + off;
-          umma_bf16(dS, ad, bd, idesc_s, kk != 0);
+          const uint32_t c = uint32_t((kk >> 2) * (Cfg::kAtom >> 4) + 2 * (kk & 3));
+          umma_bf16_lo(dS, qt + c, ks + c, d_hi, idesc_s, kk != 0);
         }
         umma_commit(smem_u32(&s_full[t]));
       };
       // O_t += P_t V_j; P_t in TMEM: keys 16 kk .. 16 kk + 15 at column 128 t + 8 kk (running max), or
       // inside their part's own S columns (fixed maximum: part p of KP keys at 128 t + KP p)
       auto issue_pv = [&](int t, int j) {
-        const int s = j & 1;
         const uint32_t dO = tmem_base + 256u + uint32_t(t * D);
+        const uint32_t vs = v_lo + uint32_t((j & 1) * (Cfg::kVBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t b = kk >> 2, off = uint32_t(2 * (kk & 3));
-          const uint64_t bd = sw128_desc(smem_u32(sV + s * Cfg::kVBytes + b * Cfg::kVAtom)) + off;
+          const uint32_t c = uint32_t((kk >> 2) * (Cfg::kVAtom >> 4) + 2 * (kk & 3));
           constexpr int KP = 128 / AttnSplit<D, MODE>::kParts;  // keys per part (fixed maximum)
           const uint32_t pcol = fixed ? uint32_t(t * 128 + (kk * 16 / KP) * KP + (kk * 16 % KP) / 2) : uint32_t(t * 128 + kk * 8);
-          umma_bf16_ts(dO, tmem_base + pcol, bd, idesc_o, (j | kk) != 0);
+          umma_bf16_ts_lo(dO, tmem_base + pcol, vs + c, d_hi, idesc_o, (j | kk) != 0);
         }
       };
       if (ok) ok = mbar_wait(smem_u32(&k_full[0]), 0, p.err, kErrTimeoutMma);
@@ -238,16 +242,16 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
         const int s = j & 1;
         const bool last = j + 1 == nkv;
         if (!mbar_wait(smem_u32(&v_full[s]), (j >> 1) & 1, p.err, kErrTimeoutMma)) break;
+        // K(j+1) is loaded long before the softmax of S(j) ends: wait for it first, so that P V(j) and
+        // S(j+1) go out back to back once P(j) is ready (its stage was freed by S1(j), which needs
+        // nothing from the softmax)
+        if (!last && !mbar_wait(smem_u32(&k_full[(j + 1) & 1]), ((j + 1) >> 1) & 1, p.err, kErrTimeoutMma)) break;
         // tile 0: P V(j), then S(j+1) over the same columns
         if (!mbar_wait(smem_u32(&p_full[0]), j & 1, p.err, kErrTimeoutMma)) break;
         tc_fence_after();
         issue_pv(0, j);
         if (last) umma_commit(smem_u32(&o_done[0]));
-        if (!last) {
-          if (!mbar_wait(smem_u32(&k_full[(j + 1) & 1]), ((j + 1) >> 1) & 1, p.err, kErrTimeoutMma)) break;
-          tc_fence_after();
-          issue_s(0, j + 1);
-        }
+        if (!last) issue_s(0, j + 1);
         // tile 1
         if (!mbar_wait(smem_u32(&p_full[1]), j & 1, p.err, kErrTimeoutMma)) break;
         tc_fence_after();
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = uint32_t(quad * 32) << 16;
-    float l[2] = {0.f, 0.f};
+    float l0 = 0.f, l1 = 0.f;  // row sums of the two tiles (scalars: an array indexed by t would sit in local memory)
     bool ok = true;
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     const uint64_t negm2 = f2_pack(-m_fixed, -m_fixed);
@@ -307,10 +311,12 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
         }
         const uint64_t s01 = f2_add(sum2[0], sum2[1]), s23 = f2_add(sum2[2], sum2[3]);
         const uint64_t s4 = f2_add(s01, s23);
-        l[t] += f2_lo(s4) + f2_hi(s4);
+        const float ls = f2_lo(s4) + f2_hi(s4);
+        if (t == 0) l0 += ls; else l1 += ls;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(smem_u32(&p_full[t]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
       }
     }
     // Both tiles' last P V done: every MMA has completed, so the Q tiles' shared memory is free and
@@ -320,8 +326,8 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
       done = done && mbar_wait_warp(smem_u32(&o_done[t]), 0, p.err, kErrTimeoutSoftmax);
     float* lsum = reinterpret_cast<float*>(sQ);  // [tile][part][128 rows]
     if (done) {
-      lsum[(0 * KS + part) * 128 + row] = l[0];
-      lsum[(1 * KS + part) * 128 + row] = l[1];
+      lsum[(0 * KS + part) * 128 + row] = l0;
+      lsum[(1 * KS + part) * 128 + row] = l1;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(128 * KS) : "memory");  // the softmax warps
     if (done) {
@@ -439,7 +445,8 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&p_full[t]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
     }
     if (ok && mbar_wait_warp(smem_u32(&o_done[t]), 0, p.err, kErrTimeoutSoftmax)) {
       tc_fence_after();

@@ -205,6 +205,38 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// The two MMAs above with each shared-memory descriptor given as its low word over a common high
+// word (sw128_desc: the high word holds only fixed fields). A tile at byte offset o from a
+// 1024-byte-aligned base below 256 KB has the base's low word plus o >> 4, without carry, so an
+// issuing loop adds one 32-bit constant per operand instead of rebuilding 64-bit descriptors.
+__device__ __forceinline__ void umma_bf16_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t desc_hi,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred P;\n"
+      ".reg .b64 A, B;\n"
+      "setp.ne.b32 P, %5, 0;\n"
+      "mov.b64 A, {%1, %3};\n"
+      "mov.b64 B, {%2, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], A, B, %4, P;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t desc_hi,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred P;\n"
+      ".reg .b64 B;\n"
+      "setp.ne.b32 P, %5, 0;\n"
+      "mov.b64 B, {%2, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], B, %4, P;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
