@@ -74,6 +74,33 @@ struct AttnSplit {
   static constexpr int kThreads = 64 + 128 * kParts;
 };
 
+// Output staging. The thread that owns row r of a query tile writes its 16-byte chunks of the
+// normalised bf16 row into shared memory at r * 2D + ((c ^ (r & 7)) << 4): eight consecutive rows
+// writing the same chunk c land on distinct banks. The tile then leaves by whole rows, consecutive
+// threads taking consecutive chunks (a warp stores two full 256-byte rows of o per instruction
+// instead of one 16-byte piece of 32 rows).
+template <int D>
+__device__ __forceinline__ void stage_chunk(uint8_t* stage, int r, int c, uint4 v) {
+  *reinterpret_cast<uint4*>(stage + r * (2 * D) + ((c ^ (r & 7)) << 4)) = v;
+}
+template <int D>
+__device__ __forceinline__ void copy_out(const uint8_t* stage, uint16_t* o, int row0, int R, int H, int col0, int tid,
+                                         int nthreads) {
+  constexpr int kChunks = 2 * D / 16;  // 16-byte chunks per row
+  for (int i = tid; i < 128 * kChunks; i += nthreads) {
+    const int r = i / kChunks, c = i % kChunks;
+    if (row0 + r < R)
+      *reinterpret_cast<uint4*>(o + size_t(row0 + r) * H + col0 + c * 8) =
+          *reinterpret_cast<const uint4*>(stage + r * (2 * D) + ((c ^ (r & 7)) << 4));
+  }
+}
+__device__ __forceinline__ uint4 pack8_scaled(const uint32_t* r, float s) {
+  return make_uint4(pack_bf16x2(__uint_as_float(r[0]) * s, __uint_as_float(r[1]) * s),
+                    pack_bf16x2(__uint_as_float(r[2]) * s, __uint_as_float(r[3]) * s),
+                    pack_bf16x2(__uint_as_float(r[4]) * s, __uint_as_float(r[5]) * s),
+                    pack_bf16x2(__uint_as_float(r[6]) * s, __uint_as_float(r[7]) * s));
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -319,25 +346,25 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
       }
     }
-    // Both tiles' last P V done: every MMA has completed, so the Q tiles' shared memory is free and
-    // holds the parts' row sums.
-    bool done = ok;
-    for (int t = 0; t < 2; ++t)
-      done = done && mbar_wait_warp(smem_u32(&o_done[t]), 0, p.err, kErrTimeoutSoftmax);
-    float* lsum = reinterpret_cast<float*>(sQ);  // [tile][part][128 rows]
+    // MMAs complete in issue order, so once tile 0's last P V is done only tile 1's is left: the Q
+    // tiles' shared memory is free for the output staging and the K stages' for the parts' row sums.
+    bool done = ok && mbar_wait_warp(smem_u32(&o_done[0]), 0, p.err, kErrTimeoutSoftmax);
+    float* lsum = reinterpret_cast<float*>(sK);  // [tile][part][128 rows]
     if (done) {
       lsum[(0 * KS + part) * 128 + row] = l0;
       lsum[(1 * KS + part) * 128 + row] = l1;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(128 * KS) : "memory");  // the softmax warps
-    if (done) {
-      tc_fence_after();
-      const int H = p.heads * D;
-      constexpr int DC = D / KS;  // output columns of this warp
+    const int H = p.heads * D;
+    constexpr int DC = D / KS;  // output columns of this warp
 #pragma unroll 1
-      for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < 2; ++t) {
+      // tile 0 is staged and stored while tile 1's last P V runs
+      if (t == 1) done = done && mbar_wait_warp(smem_u32(&o_done[1]), 0, p.err, kErrTimeoutSoftmax);
+      uint8_t* stage = sQ + t * Cfg::kQBytes;
+      if (done) {
+        tc_fence_after();
         const uint32_t tO = tmem_base + lane_off + 256u + uint32_t(t * D + part * DC);
-        const int grow = (2 * qp + t) * 128 + row;
         float lt = 0.f;
 #pragma unroll
         for (int q = 0; q < KS; ++q) lt += lsum[(t * KS + q) * 128 + row];
@@ -347,17 +374,12 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
           uint32_t r[32];
           tmem_ld32(tO + uint32_t(c * 32), r);
           tmem_ld_wait();
-          if (grow < R) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + size_t(grow) * H + head * D + part * DC + c * 32);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv_l, __uint_as_float(r[8 * q + 1]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv_l, __uint_as_float(r[8 * q + 3]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv_l, __uint_as_float(r[8 * q + 5]) * inv_l),
-                                  pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv_l, __uint_as_float(r[8 * q + 7]) * inv_l));
-          }
+          for (int q = 0; q < 4; ++q) stage_chunk<D>(stage, row, (part * DC + c * 32) / 8 + q, pack8_scaled(&r[8 * q], inv_l));
         }
       }
+      asm volatile("bar.sync 1, %0;" ::"n"(128 * KS) : "memory");
+      if (done) copy_out<D>(stage, p.o, (2 * qp + t) * 128, R, H, head * D, int(threadIdx.x) - 64, 128 * KS);
     }
   } else {
     // ------------------------------------------------------------------ softmax warps 2..9, running max
@@ -448,27 +470,25 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
     }
-    if (ok && mbar_wait_warp(smem_u32(&o_done[t]), 0, p.err, kErrTimeoutSoftmax)) {
+    // after tile t's last P V the Q tiles are free (the last S of both tiles completed before it)
+    const bool done = ok && mbar_wait_warp(smem_u32(&o_done[t]), 0, p.err, kErrTimeoutSoftmax);
+    uint8_t* stage = sQ + t * Cfg::kQBytes;
+    if (done) {
       tc_fence_after();
-      const int grow = (2 * qp + t) * 128 + row;
       const float inv_l = 1.0f / l;
-      const int H = p.heads * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tO + uint32_t(c * 32), r);
         tmem_ld_wait();
-        if (grow < R) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + size_t(grow) * H + head * D + c * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv_l, __uint_as_float(r[8 * q + 1]) * inv_l),
-                                pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv_l, __uint_as_float(r[8 * q + 3]) * inv_l),
-                                pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv_l, __uint_as_float(r[8 * q + 5]) * inv_l),
-                                pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv_l, __uint_as_float(r[8 * q + 7]) * inv_l));
-        }
+        for (int q = 0; q < 4; ++q) stage_chunk<D>(stage, row, c * 4 + q, pack8_scaled(&r[8 * q], inv_l));
       }
     }
+    // the tile's four warps
+    if (t == 0) asm volatile("bar.sync 2, 128;" ::: "memory");
+    else asm volatile("bar.sync 3, 128;" ::: "memory");
+    if (done) copy_out<D>(stage, p.o, (2 * qp + t) * 128, R, p.heads * D, head * D, int(threadIdx.x) - 64 - 128 * t, 128);
   }
 
   tc_fence_before();
