@@ -272,8 +272,10 @@ def _kernel_breakdown(torch, D, st, inp, steps):
         ("gemm_qkv_rope", lambda: D.dit_qkv_rope(dims, h, sh.L, sh.N, w[0], None, None, st["tc"], st["ts"], st["ic"],
                                                  st["is_"], q, k, vt, ws=split_ws), 2.0 * R * 3 * H * H,
          R * H * 2 + 3 * H * H * 2 + 3 * R * H * 2),
-        # q and k from the QK-norm epilogue above (unit norm weights), as in the block
-        ("attention", lambda: D.dit_attention_qknorm(dims, R, q, k, vt, None, None, o), 4.0 * R * R * H, 4 * R * H * 2),
+        # q and k from the QK-norm epilogue above (unit norm weights), as in the block; the block lends
+        # its h rows as the persistent schedule's scratch, and so does this call
+        ("attention", lambda: D.dit_attention_qknorm(dims, R, q, k, vt, None, None, o, ws=h), 4.0 * R * R * H,
+         4 * R * H * 2),
         ("gemm_out_gated", lambda: D.dit_linear_gated(dims, o, sh.L, sh.N, w[1], st["mod"], 0, st["txt"], st["img"],
                                                   split_ws),
          2.0 * R * H * H, gated_bytes(H)),

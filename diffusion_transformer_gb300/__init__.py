@@ -26,7 +26,7 @@ __all__ = [
     "dit_block_forward_sandwich", "dit_euler_step",
     "dit_rope_tables",
     "dit_denoise", "dit_block_forward_noalloc", "dit_block_noalloc_max_bytes", "dit_workspace_bytes", "dit_denoise_workspace_bytes", "dit_modnorm", "dit_qkv_rope",
-    "dit_vt_stride", "dit_stream_k_workspace_bytes", "dit_attention", "dit_attention_qknorm", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
+    "dit_vt_stride", "dit_stream_k_workspace_bytes", "dit_attention", "dit_attention_qknorm", "dit_attention_workspace_bytes", "dit_linear_gated", "dit_linear_swiglu", "dit_linear",
     "dit_dequant_int8", "dit_linear_int8", "dit_linear_int8_workspace_bytes", "dit_check", "dit_selftest_bounded_wait", "dit_status_string", "dit_version",
 ]
 
@@ -155,9 +155,11 @@ _SIGNATURES = {
                              c_void_p]),
     "dit_stream_k_workspace_bytes": (c_size_t, []),
     "dit_vt_stride": (c_int, [c_int]),
-    "dit_attention": (c_int, [POINTER(dit_dims), c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "dit_attention": (c_int, [POINTER(dit_dims), c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                              c_void_p]),
+    "dit_attention_workspace_bytes": (c_size_t, [POINTER(dit_dims), c_int]),
     "dit_attention_qknorm": (c_int, [POINTER(dit_dims), c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                     c_void_p, c_void_p]),
+                                     c_void_p, c_void_p, c_size_t, c_void_p]),
     "dit_linear_gated": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_int, c_void_p, POINTER(dit_mod), c_int,
                                  c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "dit_linear_swiglu": (c_int, [POINTER(dit_dims), c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_size_t,
@@ -601,19 +603,25 @@ def dit_qkv_rope(dims: DitDims, h, L: int, N: int, wqkv, q_norm, k_norm, txt_cos
                            _ptr(vt, bf, "vt"), _ptr(ws), _ws_bytes(ws), _stream(stream)), "dit_qkv_rope")
 
 
-def dit_attention(dims: DitDims, R: int, q, k, vt, o, stream=None):
+def dit_attention_workspace_bytes(dims: DitDims, R: int) -> int:
+    return int(lib().dit_attention_workspace_bytes(ctypes.byref(dims.c), R))
+
+
+def dit_attention(dims: DitDims, R: int, q, k, vt, o, ws=None, stream=None):
+    """ws: optional scratch of dit_attention_workspace_bytes (persistent schedule)."""
     bf = _bf16()
     _ok(lib().dit_attention(ctypes.byref(dims.c), R, _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(vt, bf, "vt"),
-                            _ptr(o, bf, "o"), _stream(stream)), "dit_attention")
+                            _ptr(o, bf, "o"), _ptr(ws), _ws_bytes(ws), _stream(stream)), "dit_attention")
 
 
-def dit_attention_qknorm(dims: DitDims, R: int, q, k, vt, q_norm, k_norm, o, stream=None):
+def dit_attention_qknorm(dims: DitDims, R: int, q, k, vt, q_norm, k_norm, o, ws=None, stream=None):
     """dit_attention for q and k rows that are QK-RMS-normalised with q_norm / k_norm (None = ones)."""
     import torch
     bf = _bf16()
     f32 = torch.float32
     _ok(lib().dit_attention_qknorm(ctypes.byref(dims.c), R, _ptr(q, bf, "q"), _ptr(k, bf, "k"), _ptr(vt, bf, "vt"),
-                                   _ptr(q_norm, f32), _ptr(k_norm, f32), _ptr(o, bf, "o"), _stream(stream)),
+                                   _ptr(q_norm, f32), _ptr(k_norm, f32), _ptr(o, bf, "o"), _ptr(ws), _ws_bytes(ws),
+                                   _stream(stream)),
         "dit_attention_qknorm")
 
 

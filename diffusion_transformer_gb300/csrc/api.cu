@@ -90,6 +90,13 @@ BlockWs carve_block_ws(const dit_dims* d, int R, void* base) {
   return w;
 }
 
+// Every block reads h (or its codes) only in the linears before attention and rewrites it only
+// after: attention borrows the h rows as scratch for the partials of its persistent schedule.
+void lend_h(AttnParams& ap, const BlockWs& b, int R, int H) {
+  ap.part = b.h;
+  ap.part_bytes = size_t(R) * H * 2;
+}
+
 // int8lin scratch of a block: two slots, each the dequantised weight of its largest linear (the
 // weights are dequantised one linear ahead of their use, alternating slots)
 size_t int8_slot_bytes(const dit_dims* d) {
@@ -336,6 +343,7 @@ int run_block(const dit_dims* d, const dit_block_w* w, const dit_block_w8* w8, f
 
   // 3. o = attention(q, k, v); q and k rows QK-normed with qn, kn
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, qn, kn, nullptr, nullptr};
+  lend_h(ap, b, R, H);
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
 
   // 4. x += gate_a * (o Wout^T)
@@ -440,6 +448,7 @@ int run_block_w8a8(const dit_dims* d, const dit_block_w8a8* w, float* txt, int L
   // 3. o = attention(q, k, v)
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, w->q_norm, w->k_norm, nullptr,
                 nullptr};
+  lend_h(ap, b, R, H);
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
   // 4. x += gate_a * W8A8(o, Wout)
   if ((rc = linear(1, b.o, H, kEpiGated, gated(H, 2))) != DIT_OK) return rc;
@@ -489,6 +498,7 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
     if ((rc = gemm_with_lora(lora, 2, b.h, H, w->wup, kEpiSwiGLU, g, down, err, st)) != DIT_OK) return rc;
     AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, w->q_norm, w->k_norm, nullptr,
                   nullptr};
+    lend_h(ap, b, R, H);
     if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
     for (int i : {1, 3}) {
       g = base_params(R, H, i == 1 ? H : F, err);
@@ -569,6 +579,7 @@ int run_parallel_block(const dit_dims* d, const dit_block_w* w, const dit_block_
 
   // 3. o = attention(q, k, v); q and k rows QK-normed
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 1, qn, kn, nullptr, nullptr};
+  lend_h(ap, b, R, H);
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
   // W8A8: codes of the joined rows [o | a] in place, one scale per row
   if (wq && (rc = quant_rows_joint_launch(b.o, H, b.a, F, R, wq->smooth2, nullptr, R, sa2, st)) != DIT_OK) return rc;
@@ -768,6 +779,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
     if ((rc = after(0)) != DIT_OK) return rc;
     AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, 2, wt->q_norm, wt->k_norm,
                   wi->q_norm, wi->k_norm};
+    lend_h(ap, b, R, H);
     if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
     g = gated(Stream{nullptr, 0, R, false}, H, 2);
     if (has_post(0)) {
@@ -828,6 +840,7 @@ int run_double_block(const dit_dims* d, const dit_block_w* wt, const dit_block_w
   const Stream* s1 = (S[0].n > 0 && S[1].n > 0) ? &S[1] : nullptr;
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), b.q, b.k, b.vt, b.o, err, s1 ? 2 : 1, s0->w->q_norm,
                 s0->w->k_norm, s1 ? s1->w->q_norm : nullptr, s1 ? s1->w->k_norm : nullptr};
+  lend_h(ap, b, R, H);
   if ((rc = attention_launch(ap, st)) != DIT_OK) return rc;
   // 4. x += gate_a * (o Wout^T), per stream
   if ((rc = before(1)) != DIT_OK) return rc;
@@ -1364,25 +1377,35 @@ int dit_qkv_rope(const dit_dims* d, const uint16_t* h, int L, int N, const uint1
   return gemm_launch(h, H, wqkv, nullptr, kEpiQKV, g, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t dit_attention_workspace_bytes(const dit_dims* d, int R) {
+  if (!d || R < 1 || !dims_ok(d)) return 0;
+  return attention_part_bytes(R, d->heads, d->head_dim);
+}
+
 int dit_attention(const dit_dims* d, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt, uint16_t* o,
-                  dit_stream_t stream) {
+                  void* ws, size_t ws_bytes, dit_stream_t stream) {
   if (!d || R < 1 || !q || !k || !vt || !o) return DIT_EINVAL;
   if (!dims_ok(d)) return DIT_EUNSUPPORTED;
-  if (!al16(q) || !al16(k) || !al16(vt) || !al16(o)) return DIT_EINVAL;
+  if (!al16(q) || !al16(k) || !al16(vt) || !al16(o) || (ws && !al16(ws))) return DIT_EINVAL;
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), q, k, vt, o, err};
+  ap.part = ws_bytes ? ws : nullptr;
+  ap.part_bytes = ws ? ws_bytes : 0;
   return attention_launch(ap, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dit_attention_qknorm(const dit_dims* d, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
-                         const float* q_norm, const float* k_norm, uint16_t* o, dit_stream_t stream) {
+                         const float* q_norm, const float* k_norm, uint16_t* o, void* ws, size_t ws_bytes,
+                         dit_stream_t stream) {
   if (!d || R < 1 || !q || !k || !vt || !o) return DIT_EINVAL;
   if (!dims_ok(d)) return DIT_EUNSUPPORTED;
-  if (!al16(q) || !al16(k) || !al16(vt) || !al16(o)) return DIT_EINVAL;
+  if (!al16(q) || !al16(k) || !al16(vt) || !al16(o) || (ws && !al16(ws))) return DIT_EINVAL;
   int* err = err_word();
   if (!err) return DIT_ECUDA;
   AttnParams ap{R, d->heads, d->head_dim, vt_stride(R), q, k, vt, o, err, 1, q_norm, k_norm, nullptr, nullptr};
+  ap.part = ws_bytes ? ws : nullptr;
+  ap.part_bytes = ws ? ws_bytes : 0;
   return attention_launch(ap, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -119,8 +119,17 @@ struct AttnParams {
   // epilogue does. The softmax may then subtract a fixed maximum (see attention.cu).
   int qk_normed;
   const float *qn0, *kn0, *qn1, *kn1;
+  // optional scratch (16-byte aligned) for the persistent schedule: the unnormalised partials of
+  // units split between two CTAs, 133 KB per CTA at d = 128; without it one CTA per unit
+  void* part = nullptr;
+  size_t part_bytes = 0;
+  // set by attention_launch: key-tile steps per CTA, launch epoch of the ready words
+  int work = 0;
+  uint32_t epoch = 0;
 };
 int attention_launch(const AttnParams& p, cudaStream_t stream);
+// Scratch the persistent schedule wants for R rows (0: it is not used for this shape).
+size_t attention_part_bytes(int R, int heads, int head_dim);
 
 // ------------------------------------------------------------------------------------------
 // elementwise / row kernels

@@ -469,9 +469,20 @@ DIT_API int dit_qkv_rope(const dit_dims* dims, const uint16_t* h, int L, int N, 
 DIT_API int dit_vt_stride(int R);
 
 /* Joint attention [klein, section 4.3]: o[r, n*d + j] = sum_c softmax_c(q_n[r] . k_n[c] / sqrt(d))
- * vt_n[j, c] over all R rows, bf16 out [R, heads * d]. Layouts as dit_qkv_rope writes them. */
+ * vt_n[j, c] over all R rows, bf16 out [R, heads * d]. Layouts as dit_qkv_rope writes them.
+ * ws / ws_bytes: optional scratch (16-byte aligned, not overlapping the other buffers) of at least
+ * dit_attention_workspace_bytes(dims, R); NULL = one CTA per (pair of 128-row query tiles, head). */
 DIT_API int dit_attention(const dit_dims* dims, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
-                  uint16_t* o, dit_stream_t stream);
+                  uint16_t* o, void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* Scratch for the persistent attention schedule (no counterpart on the pages: a scheduling device of
+ * this library), 0 when it is not used for this shape. When the (query-tile pair, head) units leave
+ * the last wave over the SMs part-empty, one CTA per SM takes an equal share of all the units' key
+ * tiles; a unit cut between two CTAs is finished by the one holding its first key tiles, which adds
+ * the unnormalised output, row sum (and running maximum) the other left in the scratch (133 KB per
+ * CTA at d = 128). The result differs from the unscheduled one by the order of fp32 additions in
+ * the cut units only. The block calls lend their h rows for it. */
+DIT_API size_t dit_attention_workspace_bytes(const dit_dims* dims, int R);
 
 /* The same attention for q and k rows as dit_qkv_rope writes them: RMS-normalised per head and
  * scaled by q_norm / k_norm ([d] fp32 each, NULL = ones; the caller vouches for this, the kernel
@@ -482,7 +493,8 @@ DIT_API int dit_attention(const dit_dims* dims, int R, const uint16_t* q, const 
  * at d = 128; the result differs from dit_attention by rounding only); otherwise it is
  * dit_attention. */
 DIT_API int dit_attention_qknorm(const dit_dims* dims, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
-                                 const float* q_norm, const float* k_norm, uint16_t* o, dit_stream_t stream);
+                                 const float* q_norm, const float* k_norm, uint16_t* o, void* ws, size_t ws_bytes,
+                                 dit_stream_t stream);
 
 /* Linear with gated residual [gizai:dit, gatedInto]: x[r] += gate[map[r]] * (a[r] W^T) for the
  * attention (which = 0, W = wout [H, H], a [R, H]) or the MLP (which = 1, W = wdown [H, F],
