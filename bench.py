@@ -59,7 +59,7 @@ KERNEL_FAMILY = {"modnorm": "modnorm", "attention": "attention", "gemm_qkv_rope"
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, sha256 of its sources at capture)
     "gemm_up_swiglu": (261_856_768, "53337c935326b9674bb0a3729f42bdb96a09fa8f79159160ef562d4199a954f2"),
-    "attention": (107_648_000, "fce7ca868e6dd40225ca73b15c0195b4c58df552bb932c6a6ef53ba60013a0b4"),
+    "attention": (107_648_000, "89a3a92caa08a4fb695414b4b223d8d9014d2e6f4cf36236f68f563b2a96f65b"),
 }
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of a kernel from the same kind of
 # capture, with the same source check: a counter-based view of tensor utilisation beside the
@@ -67,7 +67,7 @@ NCU_TRAFFIC = {
 # can flatter).
 NCU_TENSOR_ACTIVE = {
     "gemm_up_swiglu": (0.9048, "53337c935326b9674bb0a3729f42bdb96a09fa8f79159160ef562d4199a954f2"),
-    "attention": (0.6698, "fce7ca868e6dd40225ca73b15c0195b4c58df552bb932c6a6ef53ba60013a0b4"),
+    "attention": (0.6698, "89a3a92caa08a4fb695414b4b223d8d9014d2e6f4cf36236f68f563b2a96f65b"),
 }
 
 

@@ -6,11 +6,17 @@
 // through on-chip memory and keep a running row max m and sum l, rescaling the accumulator by
 // exp(m_old - m_new) ("online softmax", exact up to rounding order), applying 1/sqrt(d) in fp32.
 //
-// GB300 mapping. One CTA per (pair of 128-query tiles, head). Warp 0 loads Q0, Q1 once and the
-// K/V tiles (128 keys) with TMA into a 2-deep ring; warp 1 issues every MMA; warps 2-5 run the
-// softmax of query tile 0 and warps 6-9 that of tile 1, one query row per thread. While one
-// softmax group works, the tensor core runs the other tile's S = Q K^T and O += P V, so the
-// exponentials and the MMAs of the two tiles overlap. Tensor memory (512 columns):
+// GB300 mapping. A unit is (pair of 128-query tiles, head), its steps are its 128-key tiles. A CTA
+// works through a range of steps: one whole unit, or (persistent schedule) an equal share of all
+// units' steps per SM, a unit cut between two CTAs being finished by the one holding its first key
+// tiles, which starts from the partial O, l (and m) the other left in the caller's scratch. Warp 0
+// loads Q0, Q1 per unit and the K/V tiles with TMA into a 2-deep ring; warp 1 issues every MMA; the
+// softmax warps turn S into P (running maximum: warps 2-5 tile 0, warps 6-9 tile 1, one query row
+// per thread; fixed maximum: all of them on each tile in turn). While one tile's softmax runs, the
+// tensor core runs the other tile's S = Q K^T and O += P V, so the exponentials and the MMAs of the
+// two tiles overlap; under the fixed maximum the first half of each key part's P is announced
+// early and half of the P V runs while the softmax finishes. Output tiles are normalised into a
+// 128B-swizzled staging buffer and leave by TMA tensor stores. Tensor memory (512 columns):
 //   [0, 128) S0, overwritten by P0   [128, 256) S1 / P1   [256, 256 + d) O0   [256 + d, 256 + 2d) O1
 // The softmax reads S from TMEM, writes P (bf16, two keys per 32-bit column) back over the columns
 // it has consumed, and the P V MMA reads A straight from TMEM. MMAs issued by one thread complete
