@@ -79,14 +79,16 @@ struct AttnCfg {
   static constexpr size_t kPartBytes = size_t(2) * 128 * D * 4 + 2 * 2 * 128 * 4;
 };
 
-// Softmax modes: running maximum; fixed maximum (QK-normed rows, unit weights: the bound is known);
-// decided per launch from the norm weights (both paths compiled, so kept apart from the other two,
-// whose register allocation it would otherwise share).
-enum AttnMode : int { kAttnRunning = 0, kAttnFixed = 1, kAttnAuto = 2 };
+// Softmax modes: running maximum, or fixed maximum (QK-normed rows whose bound B is below 60). With
+// norm weights other than ones the bound is known only on the device: both kernels are launched
+// one after the other (AttnParams::select), each computes B from the weights, and the one not
+// chosen returns before its set-up (one kernel with both paths would take the running path's
+// register allocation, and with it fewer softmax warps, for the common fixed case).
+enum AttnMode : int { kAttnRunning = 0, kAttnFixed = 1 };
 // Key parts per softmax row under the fixed maximum: four (sixteen softmax warps, four per SM
-// sub-partition, 32 keys each) in the fixed kernel at d = 128, whose path needs about 100 registers;
-// two where the running path (168 registers) shares the kernel, or at d = 64 (d / 4 output columns
-// would be narrower than one TMEM load).
+// sub-partition, 32 keys each) at d = 128, whose path needs about 100 registers; two at d = 64
+// (d / 4 output columns would be narrower than one TMEM load). The running path keeps whole rows
+// (168 registers) in two groups of four warps.
 template <int D, int MODE>
 struct AttnSplit {
   static constexpr int kParts = (MODE == kAttnFixed && D == 128) ? 4 : 2;
@@ -107,6 +109,31 @@ __device__ __forceinline__ uint4 pack8_scaled(const uint32_t* r, float s) {
                     pack_bf16x2(__uint_as_float(r[2]) * s, __uint_as_float(r[3]) * s),
                     pack_bf16x2(__uint_as_float(r[4]) * s, __uint_as_float(r[5]) * s),
                     pack_bf16x2(__uint_as_float(r[6]) * s, __uint_as_float(r[7]) * s));
+}
+
+// B = (1 + 2^-6)^2 d max|w_q| max|w_k| scale (log2 units) over the norm weights of every stream:
+// every scaled score of QK-normed rows lies in [-B, B]. The margin per factor covers the bf16
+// rounding of q and k and the fp32 normalisation. Computed by every warp (lane-strided max, then a
+// butterfly), exactly the same in every warp and in both kernels of a pair of launches.
+template <int D>
+__device__ __noinline__ float qk_bound(const float* qn0, const float* kn0, const float* qn1, const float* kn1,
+                                       int streams, float scale_log2) {
+  const int lane = lane_id();
+  float mq = 0.f, mk = 0.f;
+  for (int i = lane; i < D; i += 32) {
+    mq = fmaxf(mq, qn0 ? fabsf(qn0[i]) : 1.f);
+    mk = fmaxf(mk, kn0 ? fabsf(kn0[i]) : 1.f);
+    if (streams > 1) {
+      mq = fmaxf(mq, qn1 ? fabsf(qn1[i]) : 1.f);
+      mk = fmaxf(mk, kn1 ? fabsf(kn1[i]) : 1.f);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+    mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+  }
+  return 1.015625f * mq * 1.015625f * mk * float(D) * scale_log2;
 }
 
 // Wait (bounded) until the ready word holds this launch's epoch; false after the limit or an error.
@@ -167,35 +194,17 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
   auto slot_ptr = [&](int slot) { return reinterpret_cast<uint8_t*>(p.part) + size_t(slot) * Cfg::kPartBytes; };
   uint32_t* ready = g_attn_ready + (p.epoch % kAttnSlots) * kAttnMaxCtas;
 
-  // fixed-maximum mode (the same verdict in every warp: an exact max over the same values); the
-  // norm weights are read after pdl_wait, before the barriers' set-up when they decide its counts
-  float m_fixed = 0.f;
-  bool auto_fixed = false;  // kAttnAuto: the bound's verdict
-  auto fixed_bound = [&]() {
-    float mq = 0.f, mk = 0.f;
-    for (int i = lane; i < D; i += 32) {
-      mq = fmaxf(mq, p.qn0 ? fabsf(p.qn0[i]) : 1.f);
-      mk = fmaxf(mk, p.kn0 ? fabsf(p.kn0[i]) : 1.f);
-      if (p.qk_normed > 1) {
-        mq = fmaxf(mq, p.qn1 ? fabsf(p.qn1[i]) : 1.f);
-        mk = fmaxf(mk, p.kn1 ? fabsf(p.kn1[i]) : 1.f);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
-      mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
-    }
-    // margin 2^-6 per factor: bf16 rounding of q and k, fp32 normalisation
-    m_fixed = 1.015625f * mq * 1.015625f * mk * float(D) * scale_log2;
-    auto_fixed = m_fixed < 60.f;
-  };
-  if constexpr (MODE == kAttnAuto) {
+  // the fixed maximum B from the norm weights (the same value in every warp and in either kernel of a
+  // pair of launches)
+  if (p.select != 0) {
+    // one of a pair of launches over the same call (norm weights other than ones): the fixed kernel
+    // works when B < 60, the running one otherwise; the other returns here, before any set-up
+    // (the weights may come from the previous kernel in the stream, hence after its completion)
     pdl_wait();
-    fixed_bound();
+    if ((p.select == 1) != (qk_bound<D>(p.qn0, p.kn0, p.qn1, p.kn1, p.qk_normed, scale_log2) < 60.f)) return;
   }
-  // a compile-time constant in the fixed and running kernels (their issue loops fold it away)
-  const bool fixed = MODE == kAttnFixed ? true : MODE == kAttnRunning ? false : auto_fixed;
+  float m_fixed = 0.f;
+  constexpr bool fixed = MODE == kAttnFixed;
   constexpr int KS = AttnSplit<D, MODE>::kParts;
   const uint32_t softmax_warps = fixed ? 4 * KS : 8;
 
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(AttnSplit<D, MODE>::kThreads, 1)
   // the set-up above may overlap the previous kernel in the stream; its results only from here
   pdl_wait();
   pdl_trigger();
-  if constexpr (MODE == kAttnFixed) fixed_bound();
+  if constexpr (MODE == kAttnFixed) m_fixed = qk_bound<D>(p.qn0, p.kn0, p.qn1, p.kn1, p.qk_normed, scale_log2);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -796,27 +805,33 @@ int launch_d(const AttnParams& p0, cudaStream_t stream) {
     return DIT_ECUDA;
   // unit norm weights give B = 1.0157^2 d scale = 16.8 (d = 128) or 11.9 (d = 64): always fixed
   const bool unit = !p.qn0 && !p.kn0 && (p.qk_normed < 2 || (!p.qn1 && !p.kn1));
-  auto kern = p.qk_normed <= 0 ? attn_kernel<D, kAttnRunning> : unit ? attn_kernel<D, kAttnFixed> : attn_kernel<D, kAttnAuto>;
-  if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
   const float scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
-  const int threads = p.qk_normed <= 0 ? AttnSplit<D, kAttnRunning>::kThreads
-                      : unit             ? AttnSplit<D, kAttnFixed>::kThreads
-                                         : AttnSplit<D, kAttnAuto>::kThreads;
   // one CTA per (query-tile pair, head); or, when that leaves the last wave part-empty and the
   // caller lent scratch for the partials, one CTA per SM over an equal share of the key tiles
   const AttnPlan pl = attn_plan(p.R, p.heads);
-  dim3 grid = dim3(unsigned((p.R + 255) / 256), unsigned(p.heads));
-  p.work = (p.R + 127) / 128;
-  p.epoch = 0;
-  if (pl.ctas > 0 && p.part && size_t(pl.ctas) * Cfg::kPartBytes <= p.part_bytes &&
-      (reinterpret_cast<uintptr_t>(p.part) & 15) == 0) {
-    grid = dim3(unsigned(pl.ctas));
-    p.work = pl.work;
-    p.epoch = next_epoch();
-  }
-  if (launch_pdl(kern, grid, dim3(threads), Cfg::kSmemBytes, stream, 1, tq, tk, tv, to, p, scale_log2) != cudaSuccess)
-    return DIT_ECUDA;
-  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  auto launch = [&](auto kern, int threads, int select) -> int {
+    if (!smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmemBytes)) return DIT_ECUDA;
+    AttnParams q = p;
+    q.select = select;
+    dim3 grid = dim3(unsigned((q.R + 255) / 256), unsigned(q.heads));
+    q.work = (q.R + 127) / 128;
+    q.epoch = 0;
+    if (pl.ctas > 0 && q.part && size_t(pl.ctas) * Cfg::kPartBytes <= q.part_bytes &&
+        (reinterpret_cast<uintptr_t>(q.part) & 15) == 0) {
+      grid = dim3(unsigned(pl.ctas));
+      q.work = pl.work;
+      q.epoch = next_epoch();
+    }
+    if (launch_pdl(kern, grid, dim3(threads), Cfg::kSmemBytes, stream, 1, tq, tk, tv, to, q, scale_log2) != cudaSuccess)
+      return DIT_ECUDA;
+    return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ECUDA;
+  };
+  constexpr int kRunThreads = AttnSplit<D, kAttnRunning>::kThreads, kFixThreads = AttnSplit<D, kAttnFixed>::kThreads;
+  if (p.qk_normed <= 0) return launch(attn_kernel<D, kAttnRunning>, kRunThreads, 0);
+  if (unit) return launch(attn_kernel<D, kAttnFixed>, kFixThreads, 0);
+  // the rare running case first, so that the common fixed kernel runs last and hands on directly
+  const int rc = launch(attn_kernel<D, kAttnRunning>, kRunThreads, 2);
+  return rc != DIT_OK ? rc : launch(attn_kernel<D, kAttnFixed>, kFixThreads, 1);
 }
 
 }  // namespace

@@ -123,9 +123,12 @@ struct AttnParams {
   // units split between two CTAs, 133 KB per CTA at d = 128; without it one CTA per unit
   void* part = nullptr;
   size_t part_bytes = 0;
-  // set by attention_launch: key-tile steps per CTA, launch epoch of the ready words
+  // set by attention_launch: key-tile steps per CTA, launch epoch of the ready words, and which of
+  // a pair of launches this is (0: the only one; 1: fixed maximum, works when B < 60; 2: running
+  // maximum, works when B >= 60)
   int work = 0;
   uint32_t epoch = 0;
+  int select = 0;
 };
 int attention_launch(const AttnParams& p, cudaStream_t stream);
 // Scratch the persistent schedule wants for R rows (0: it is not used for this shape).
