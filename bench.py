@@ -58,16 +58,16 @@ KERNEL_FAMILY = {"modnorm": "modnorm", "attention": "attention", "gemm_qkv_rope"
                  "gemm_up_swiglu": "gemm", "gemm_down_gated": "gemm"}
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, sha256 of its sources at capture)
-    "gemm_up_swiglu": (261_856_768, "53337c935326b9674bb0a3729f42bdb96a09fa8f79159160ef562d4199a954f2"),
-    "attention": (107_648_000, "89a3a92caa08a4fb695414b4b223d8d9014d2e6f4cf36236f68f563b2a96f65b"),
+    "gemm_up_swiglu": (261_929_728, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
+    "attention": (107_756_032, "805f1adc0ddf899bbdd0b75bac8728963dfd7c35bd943a2fa1a0c4cbded26ab1"),
 }
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of a kernel from the same kind of
 # capture, with the same source check: a counter-based view of tensor utilisation beside the
 # event-timed fraction of the measured peak (which a cuBLAS burst figure taken at a lower clock
 # can flatter).
 NCU_TENSOR_ACTIVE = {
-    "gemm_up_swiglu": (0.9048, "53337c935326b9674bb0a3729f42bdb96a09fa8f79159160ef562d4199a954f2"),
-    "attention": (0.6698, "89a3a92caa08a4fb695414b4b223d8d9014d2e6f4cf36236f68f563b2a96f65b"),
+    "gemm_up_swiglu": (0.9094, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
+    "attention": (0.6636, "805f1adc0ddf899bbdd0b75bac8728963dfd7c35bd943a2fa1a0c4cbded26ab1"),
 }
 
 
