@@ -478,10 +478,13 @@ DIT_API int dit_attention(const dit_dims* dims, int R, const uint16_t* q, const 
 /* Scratch for the persistent attention schedule (no counterpart on the pages: a scheduling device of
  * this library), 0 when it is not used for this shape. When the (query-tile pair, head) units leave
  * the last wave over the SMs part-empty, one CTA per SM takes an equal share of all the units' key
- * tiles; a unit cut between two CTAs is finished by the one holding its first key tiles, which adds
- * the unnormalised output, row sum (and running maximum) the other left in the scratch (133 KB per
- * CTA at d = 128). The result differs from the unscheduled one by the order of fp32 additions in
- * the cut units only. The block calls lend their h rows for it. */
+ * tiles; a unit cut between two CTAs is finished by the one holding its first key tiles, which
+ * starts from the unnormalised output, row sum (and running maximum) the other left in the scratch
+ * (133 KB per CTA at d = 128). The result does not depend on timing; it differs from the unscheduled
+ * one in the cut units only: by the order of fp32 additions under the fixed maximum (within one bf16
+ * step), by the bf16 rounding of each part's weights against its own maximum under a running one.
+ * The block calls lend their h rows for it. Requires dims and R valid (else 0); reads the SM count
+ * of the current device. */
 DIT_API size_t dit_attention_workspace_bytes(const dit_dims* dims, int R);
 
 /* The same attention for q and k rows as dit_qkv_rope writes them: RMS-normalised per head and
@@ -491,6 +494,8 @@ DIT_API size_t dit_attention_workspace_bytes(const dit_dims* dims, int R);
  * bf16 rounding of q and k; 16.8 at d = 128 with unit weights); when B < 60 the softmax subtracts B
  * instead of a running row maximum, which lets it split each row over several warps (two, or four
  * at d = 128; the result differs from dit_attention by rounding only); otherwise it is
+ * dit_attention. With weights other than ones (NULL counts as ones) B is computed on the device:
+ * two kernels are launched and the one B does not choose returns at once. ws / ws_bytes as for
  * dit_attention. */
 DIT_API int dit_attention_qknorm(const dit_dims* dims, int R, const uint16_t* q, const uint16_t* k, const uint16_t* vt,
                                  const float* q_norm, const float* k_norm, uint16_t* o, void* ws, size_t ws_bytes,
