@@ -59,7 +59,7 @@ KERNEL_FAMILY = {"modnorm": "modnorm", "attention": "attention", "gemm_qkv_rope"
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, sha256 of its sources at capture)
     "gemm_up_swiglu": (261_929_728, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
-    "attention": (107_756_032, "805f1adc0ddf899bbdd0b75bac8728963dfd7c35bd943a2fa1a0c4cbded26ab1"),
+    "attention": (107_756_032, "c8ac37b57df01d0baf34c74726deda384d97c2a0d5c71ab5ec271114adb9419a"),
 }
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of a kernel from the same kind of
 # capture, with the same source check: a counter-based view of tensor utilisation beside the
@@ -67,7 +67,7 @@ NCU_TRAFFIC = {
 # can flatter).
 NCU_TENSOR_ACTIVE = {
     "gemm_up_swiglu": (0.9094, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
-    "attention": (0.6636, "805f1adc0ddf899bbdd0b75bac8728963dfd7c35bd943a2fa1a0c4cbded26ab1"),
+    "attention": (0.6636, "c8ac37b57df01d0baf34c74726deda384d97c2a0d5c71ab5ec271114adb9419a"),
 }
 
 

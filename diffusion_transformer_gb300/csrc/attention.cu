@@ -31,8 +31,8 @@
 // rounding). For B below 60 the softmax subtracts m = B throughout: the weights exp2(s - B) lie in
 // [2^-120, 1], normal in fp32 and bf16, the same relative rounding as with a running max, and no row
 // max is needed. Then no thread needs a whole row, and all the softmax warps work on each query
-// tile in turn, warp (quadrant, part) taking 32 rows and 128 / parts of the keys (two parts and
-// eight warps, or four parts and sixteen warps in the fixed kernel at d = 128): several warps per SM
+// tile in turn, warp (quadrant, part) taking 32 rows and 128 / parts of the keys (four parts and
+// sixteen warps at d = 128, two parts and eight warps at d = 64): several warps per SM
 // sub-partition share every softmax, so its latency drops and the next S no longer waits on it.
 // P of key part p goes to the first half of that part's own S columns (inside what that warp has
 // consumed), and the P V MMA reads it from there.
