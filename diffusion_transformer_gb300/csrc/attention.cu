@@ -137,13 +137,17 @@ __device__ __noinline__ float qk_bound(const float* qn0, const float* kn0, const
 }
 
 // Wait (bounded) until the ready word holds this launch's epoch; false after the limit or an error.
-__device__ __forceinline__ bool wait_ready(const uint32_t* w, uint32_t epoch, int* err) {
+// The finisher is the word's only reader: it clears the word once seen, so that every launch starts
+// from cleared words even when a captured graph replays the same epoch (the word's next writer is
+// a later kernel in the stream).
+__device__ __forceinline__ bool wait_ready(uint32_t* w, uint32_t epoch, int* err) {
   const uint64_t t0 = globaltimer_ns();
   while (ld_acquire_gpu(w) != epoch)
     if (aborted(err) || globaltimer_ns() - t0 > 4 * kWaitLimitNs) {
       atomicCAS(err, 0, int(kErrTimeoutSoftmax));
       return false;
     }
+  *w = 0u;
   return true;
 }
 

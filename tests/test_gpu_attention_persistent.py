@@ -149,3 +149,37 @@ def test_persistent_attention_scratch_too_small_runs_one_cta_per_unit():
     qd, kd, vtd = dev_bf16(q), dev_bf16(k), dev_bf16(vt)
     small = torch.zeros(D.dit_attention_workspace_bytes(dims, R) - 16, dtype=torch.uint8, device="cuda")
     assert torch.equal(_run(dims, R, qd, kd, vtd, w, "fixed", small), _run(dims, R, qd, kd, vtd, w, "fixed", None))
+
+
+def test_persistent_attention_replayed_in_a_cuda_graph():
+    # a captured launch keeps its epoch across replays: every replay must still wait for the partials
+    # of its own run (the finisher clears the ready word it consumed), so each replay on fresh inputs
+    # equals a direct call on them bit for bit
+    R, nh, d = 2000, 24, 128
+    if _cut_units(R, nh) is None:
+        pytest.skip("this GPU's SM count fills the last wave")
+    dims = D.DitDims(nh * d, nh, d, 256)
+    q0, k0, v0, vt0, w = _case(R, nh, d, "fixed", 11)
+    qd, kd, vtd = dev_bf16(q0), dev_bf16(k0), dev_bf16(vt0)
+    ws = torch.zeros(D.dit_attention_workspace_bytes(dims, R), dtype=torch.uint8, device="cuda")
+    o = torch.empty(R, nh * d, dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        D.dit_attention_qknorm(dims, R, qd, kd, vtd, None, None, o, ws=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        D.dit_attention_qknorm(dims, R, qd, kd, vtd, None, None, o, ws=ws)
+    for seed in (12, 13, 14, 15):
+        q, k, v, vt, _ = _case(R, nh, d, "fixed", seed)
+        qd.copy_(dev_bf16(q))
+        kd.copy_(dev_bf16(k))
+        vtd.copy_(dev_bf16(vt))
+        graph.replay()
+        torch.cuda.synchronize()
+        direct = _run(dims, R, dev_bf16(q), dev_bf16(k), dev_bf16(vt), None, "fixed",
+                      torch.zeros_like(ws))
+        assert torch.equal(o, direct), seed
+    D.dit_check()
