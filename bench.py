@@ -58,16 +58,16 @@ KERNEL_FAMILY = {"modnorm": "modnorm", "attention": "attention", "gemm_qkv_rope"
                  "gemm_up_swiglu": "gemm", "gemm_down_gated": "gemm"}
 NCU_TRAFFIC = {
     # kernel: (bytes per launch, sha256 of its sources at capture)
-    "gemm_up_swiglu": (261_929_728, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
-    "attention": (107_756_032, "c8ac37b57df01d0baf34c74726deda384d97c2a0d5c71ab5ec271114adb9419a"),
+    "gemm_up_swiglu": (261_899_520, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
+    "attention": (107_785_984, "d832fc99513b6acabf10c5f26f19dc32976c8a54ebf42cc9e76305b3e72725e9"),
 }
 # sm__pipe_tensor_cycles_active (fraction of elapsed cycles) of a kernel from the same kind of
 # capture, with the same source check: a counter-based view of tensor utilisation beside the
 # event-timed fraction of the measured peak (which a cuBLAS burst figure taken at a lower clock
 # can flatter).
 NCU_TENSOR_ACTIVE = {
-    "gemm_up_swiglu": (0.9094, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
-    "attention": (0.6636, "c8ac37b57df01d0baf34c74726deda384d97c2a0d5c71ab5ec271114adb9419a"),
+    "gemm_up_swiglu": (0.9070, "fe5db7d96330e499ed0ac2b712c894672b47cfb5d56e55e85a7c21ce6e37714d"),
+    "attention": (0.6653, "d832fc99513b6acabf10c5f26f19dc32976c8a54ebf42cc9e76305b3e72725e9"),
 }
 
 
